@@ -1,0 +1,93 @@
+"""Algorithmic bytes of one decode step: what the method must move per token.
+
+A batch-1 decode step streams every weight it uses once, reads and writes the
+recurrent state once, and reads the KV cache once, so its roofline is
+tokens/s = bandwidth / bytes per token ("Beating llama.cpp from Scratch on
+Consumer AMD", Act 6: theoretical max tok/s = memory bandwidth / model size).
+MoE counts only the experts a token selects; the embedding counts one row.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+BF16 = 2
+F32 = 4
+
+
+@dataclass
+class StepBytes:
+    weights: int
+    state: int
+    kv_read: int
+    kv_write: int
+    activations: int
+
+    @property
+    def total(self) -> int:
+        return self.weights + self.state + self.kv_read + self.kv_write + self.activations
+
+
+def gdn_state_bytes_per_layer(nh: int, dk: int, dv: int) -> int:
+    """FP32 recurrent state of one Gated DeltaNet layer."""
+    return nh * dv * dk * F32
+
+
+def kv_bytes_per_token(n_attn: int, nkv: int, hd: int, elem: int = BF16) -> int:
+    """K and V of one position over all attention layers."""
+    return n_attn * 2 * nkv * hd * elem
+
+
+def roofline_tokens_per_s(bandwidth_gbs: float, bytes_per_token: float) -> float:
+    return bandwidth_gbs * 1e9 / bytes_per_token
+
+
+def linear_bytes(rows: int, cols: int, weight_format: int) -> int:
+    if weight_format == 1:  # 4-bit blocks of 32: 16 bytes of nibbles + a 2-byte scale per block
+        return rows * cols // 2 + rows * (cols // 32) * 2
+    return rows * cols * BF16
+
+
+def step_bytes(shape, context: int, experts_touched: int | None = None) -> StepBytes:
+    """Bytes one decode step at position ``context`` must move.
+
+    ``shape`` has the model-shape attributes; ``experts_touched`` (MoE) is
+    the number of distinct routed experts read per layer (top_k at batch 1).
+    """
+    s = shape
+    H = s.hidden
+    fmt = getattr(s, "weight_format", 0)
+    n_attn = sum(1 for l in range(s.n_layers) if s.is_attn(l))
+    n_gdn = s.n_layers - n_attn
+    CC = 2 * s.gdn_heads * s.gdn_dk + s.gdn_heads * s.gdn_dv
+    w = 0
+    w += n_gdn * (linear_bytes(CC + 2 * s.gdn_heads, H, fmt) + linear_bytes(H, s.gdn_heads * s.gdn_dv, fmt)
+                  + CC * s.conv_k * BF16)
+    w += n_attn * (linear_bytes((s.attn_q_heads + 2 * s.attn_kv_heads) * s.head_dim, H, fmt)
+                   + linear_bytes(H, s.attn_q_heads * s.head_dim, fmt))
+    w += s.n_layers * 2 * H * F32  # norm gains
+    if s.ffn > 0:
+        w += s.n_layers * (2 * linear_bytes(s.ffn, H, fmt) + linear_bytes(H, s.ffn, fmt))
+    else:
+        e = s.top_k if experts_touched is None else experts_touched
+        w += s.n_layers * ((s.n_experts + 1) * H * BF16
+                           + e * (2 * linear_bytes(s.expert_ffn, H, fmt) + linear_bytes(H, s.expert_ffn, fmt))
+                           + 2 * linear_bytes(s.shared_ffn, H, fmt) + linear_bytes(H, s.shared_ffn, fmt))
+    w += H * BF16 + H * F32 + linear_bytes(s.vocab, H, fmt)  # embedding row, final norm, LM head
+    state = n_gdn * (2 * gdn_state_bytes_per_layer(s.gdn_heads, s.gdn_dk, s.gdn_dv) + s.conv_k * CC * F32)
+    kv_read = kv_bytes_per_token(n_attn, s.attn_kv_heads, s.head_dim) * context
+    kv_write = kv_bytes_per_token(n_attn, s.attn_kv_heads, s.head_dim)
+    return StepBytes(weights=w, state=state, kv_read=kv_read, kv_write=kv_write, activations=0)
+
+
+def gemv_swiglu_bytes(rows: int, cols: int) -> int:
+    """One gate/up SwiGLU GEMV launch: two bf16 [rows][cols] matrices, the FP32
+    input vector and the FP32 output."""
+    return 2 * rows * cols * BF16 + cols * F32 + rows * F32
+
+
+def kernels_per_step(shape, debug: bool = False) -> int:
+    """Kernel launches of one batch-1 decode step (each layer: input
+    projection, mixer, output projection, 2 dense or 3 MoE FFN kernels; then
+    the LM head)."""
+    per = 3 + (2 if shape.ffn > 0 else 3) + (1 if debug else 0)
+    return shape.n_layers * per + 1

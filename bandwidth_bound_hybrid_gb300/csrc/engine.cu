@@ -1,0 +1,853 @@
+// The decode-step engine behind include/hybrid.h: model and cache objects,
+// the per-step kernel plan, CUDA-graph capture and replay, and the C ABI.
+//
+// One decode step is ~5 kernels per layer plus the head, all launched with
+// programmatic dependent launch so each kernel's weight stream starts while
+// its predecessor drains, and captured once into a CUDA graph that is
+// replayed per token with its positions read from device memory ("Beating
+// llama.cpp from Scratch on Consumer AMD", Act 0 pass 3: the whole decode
+// iteration captured once and replayed; argmax on the device, a 4-byte id
+// back).
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/hybrid.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace hy;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+#define HY_CK(call)                                                                         \
+  do {                                                                                      \
+    cudaError_t e_ = (call);                                                                \
+    if (e_ != cudaSuccess) return fail(HY_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+
+std::mutex g_init_mu;
+std::map<int, bool> g_inited;
+std::map<int, unsigned*> g_op_guard;
+
+int ensure_init(int dev) {
+  std::lock_guard<std::mutex> lk(g_init_mu);
+  if (g_inited[dev]) return HY_OK;
+  HY_CK(gemv::init());
+  HY_CK(attn::init());
+  g_inited[dev] = true;
+  return HY_OK;
+}
+
+int current_device(int* dev, int* nsm) {
+  HY_CK(cudaGetDevice(dev));
+  HY_CK(cudaDeviceGetAttribute(nsm, cudaDevAttrMultiProcessorCount, *dev));
+  return HY_OK;
+}
+
+__global__ void k_copy_f32(const float* __restrict__ src, float* __restrict__ dst, int n) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) dst[i] = src[i];
+}
+
+}  // namespace
+
+// ====================================================================== model
+
+struct hy_model {
+  hy_config cfg;
+  std::vector<hy_layer_weights> layers;
+  hy_weights w;
+  int device = 0, nsm = 0;
+  int n_gdn = 0, n_attn = 0;
+  std::vector<int> sub;      // index of a layer among layers of its kind
+  std::vector<bool> is_attn;
+  int CC = 0, gdn_rows = 0, attn_rows = 0;
+  int y_len = 0, o_len = 0, h_len = 0;
+  int splits = 1;
+  bool moe = false, pdl = true, graphs = true, debug = false;
+};
+
+struct hy_cache {
+  hy_model* m = nullptr;
+  int max_seqs = 0;
+  std::vector<int> cap, len;
+  std::vector<uint8_t*> mem;
+  std::vector<size_t> off_kv;
+  size_t off_conv = 0;
+  int* d_len = nullptr;
+  // scratch
+  float *x = nullptr, *y = nullptr, *o = nullptr, *h = nullptr, *part = nullptr, *am_val = nullptr;
+  float *rlog = nullptr, *moe_w = nullptr, *logits_buf = nullptr;
+  int *am_idx = nullptr, *tok = nullptr, *ids = nullptr, *moe_ids = nullptr;
+  unsigned *cnt_attn = nullptr, *cnt_am = nullptr, *cnt_router = nullptr, *guard = nullptr;
+  float2* rope = nullptr;
+  float *dbg_hidden = nullptr, *dbg_rlog = nullptr;
+  int* dbg_rids = nullptr;
+  std::vector<void*> allocs;
+  cudaStream_t cap_stream = nullptr;
+  struct Graph {
+    int seq;
+    float* logits;
+    int* ids;
+    cudaGraphExec_t exec;
+  };
+  std::vector<Graph> graphs;
+};
+
+namespace {
+
+float* gdn_state(hy_cache* c, int seq, int gi) {
+  const hy_model* m = c->m;
+  return reinterpret_cast<float*>(c->mem[seq]) + (size_t)gi * m->cfg.gdn_heads * m->cfg.gdn_dv * m->cfg.gdn_dk;
+}
+float* conv_state(hy_cache* c, int seq, int gi) {
+  const hy_model* m = c->m;
+  return reinterpret_cast<float*>(c->mem[seq] + c->off_conv) + (size_t)gi * m->cfg.conv_k * m->CC;
+}
+uint16_t* kv_cache(hy_cache* c, int seq, int ai, int which) {
+  const hy_model* m = c->m;
+  const size_t per = (size_t)m->cfg.attn_kv_heads * c->cap[seq] * m->cfg.head_dim;
+  return reinterpret_cast<uint16_t*>(c->mem[seq] + c->off_kv[seq]) + ((size_t)ai * 2 + which) * per;
+}
+
+// Issue every kernel of one decode step for sequence `seq` on `st`.
+int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) {
+  hy_model* m = c->m;
+  const hy_config& cf = m->cfg;
+  const int H = cf.hidden;
+  const bool pdl = m->pdl;
+  int* pos = c->d_len + seq;
+
+  auto gemv_base = [&]() {
+    gemv::Params p;
+    memset(&p, 0, sizeof(p));
+    p.guard = c->guard;
+    p.eps = cf.rms_eps;
+    return p;
+  };
+  auto run = [&](gemv::Params& p, int src, int in, int epi, const char* what) -> int {
+    const int npair = (epi == gemv::kEpiSwiglu) ? 2 : 1;
+    const gemv::Plan pl = gemv::plan(p.R, p.C, npair, m->nsm);
+    if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no GEMV plan for %s (%d x %d)", what, p.R, p.C);
+    cudaError_t e = gemv::launch(p, pl, src, in, epi, st, pdl);
+    if (e != cudaSuccess) return fail(HY_ERR_CUDA, "GEMV %s launch: %s", what, cudaGetErrorString(e));
+    return HY_OK;
+  };
+
+  for (int l = 0; l < cf.n_layers; ++l) {
+    const hy_layer_weights& L = m->layers[l];
+    const bool attn_l = m->is_attn[l];
+    int rc;
+    {  // RMSNorm + input projection (layer 0 also gathers the embedding row)
+      gemv::Params p = gemv_base();
+      p.W[0] = (const uint8_t*)L.w_in.w;
+      p.R = attn_l ? m->attn_rows : m->gdn_rows;
+      p.C = H;
+      p.x = c->x;
+      p.norm_g = L.norm1;
+      p.y = c->y;
+      int in = gemv::kInX;
+      if (l == 0) {
+        in = gemv::kInEmbed;
+        p.embed = (const uint16_t*)m->w.embed;
+        p.tok = c->tok;
+        p.vocab = cf.vocab;
+        p.x_out = c->x;
+      }
+      if ((rc = run(p, gemv::kSrcDense, in, gemv::kEpiStore, "in-proj")) != HY_OK) return rc;
+    }
+    if (attn_l) {
+      attn::Params a;
+      memset(&a, 0, sizeof(a));
+      a.y = c->y;
+      a.K = kv_cache(c, seq, m->sub[l], 0);
+      a.V = kv_cache(c, seq, m->sub[l], 1);
+      a.len = pos;
+      a.rope = c->rope;
+      a.cap = c->cap[seq];
+      a.nq = cf.attn_q_heads;
+      a.nkv = cf.attn_kv_heads;
+      a.hd = cf.head_dim;
+      a.nsplit = m->splits;
+      a.scale = 1.0f / sqrtf((float)cf.head_dim);
+      a.part = c->part;
+      a.counter = c->cnt_attn;
+      a.o = c->o;
+      a.guard = c->guard;
+      cudaError_t e = attn::launch(a, st, pdl);
+      if (e != cudaSuccess) return fail(HY_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+    } else {
+      gdn::Params g;
+      memset(&g, 0, sizeof(g));
+      g.y = c->y;
+      g.conv_w = (const uint16_t*)L.conv_w;
+      g.conv_state = conv_state(c, seq, m->sub[l]);
+      g.S = gdn_state(c, seq, m->sub[l]);
+      g.o = c->o;
+      g.nh = cf.gdn_heads;
+      g.dk = cf.gdn_dk;
+      g.dv = cf.gdn_dv;
+      g.conv_k = cf.conv_k;
+      g.pos = pos;
+      g.guard = c->guard;
+      cudaError_t e = gdn::launch(g, st, pdl);
+      if (e != cudaSuccess) return fail(HY_ERR_CUDA, "GDN launch: %s", cudaGetErrorString(e));
+    }
+    {  // output projection + residual
+      gemv::Params p = gemv_base();
+      p.W[0] = (const uint8_t*)L.w_o.w;
+      p.R = H;
+      p.C = attn_l ? cf.attn_q_heads * cf.head_dim : cf.gdn_heads * cf.gdn_dv;
+      p.x = c->o;
+      p.y = c->x;
+      if ((rc = run(p, gemv::kSrcDense, gemv::kInX, gemv::kEpiResid, "out-proj")) != HY_OK) return rc;
+    }
+    if (!m->moe) {
+      gemv::Params p = gemv_base();
+      p.W[0] = (const uint8_t*)L.w_gate.w;
+      p.W[1] = (const uint8_t*)L.w_up.w;
+      p.R = cf.ffn;
+      p.C = H;
+      p.x = c->x;
+      p.norm_g = L.norm2;
+      p.y = c->h;
+      if ((rc = run(p, gemv::kSrcDense, gemv::kInX, gemv::kEpiSwiglu, "gate/up")) != HY_OK) return rc;
+      gemv::Params d = gemv_base();
+      d.W[0] = (const uint8_t*)L.w_down.w;
+      d.R = H;
+      d.C = cf.ffn;
+      d.x = c->h;
+      d.y = c->x;
+      if ((rc = run(d, gemv::kSrcDense, gemv::kInX, gemv::kEpiResid, "down")) != HY_OK) return rc;
+    } else {
+      const int E = cf.n_experts, K = cf.top_k, Fe = cf.expert_ffn;
+      gemv::Params r = gemv_base();
+      r.W[0] = (const uint8_t*)L.router;
+      r.R = E + 1;
+      r.C = H;
+      r.x = c->x;
+      r.norm_g = L.norm2;
+      r.router_logits = c->rlog;
+      r.out_ids = c->moe_ids;
+      r.out_w = c->moe_w;
+      r.counter = c->cnt_router;
+      r.n_experts = E;
+      r.top_k = K;
+      if (m->debug) {
+        r.dbg_ids = c->dbg_rids + (size_t)l * K;
+        r.dbg_logits = c->dbg_rlog + (size_t)l * (E + 1);
+      }
+      if ((rc = run(r, gemv::kSrcDense, gemv::kInX, gemv::kEpiRouter, "router")) != HY_OK) return rc;
+      gemv::Params gu = gemv_base();
+      gu.exp_base[0] = (const uint8_t*)L.exp_gate.w;
+      gu.exp_base[1] = (const uint8_t*)L.exp_up.w;
+      gu.sh_base[0] = (const uint8_t*)L.sh_gate.w;
+      gu.sh_base[1] = (const uint8_t*)L.sh_up.w;
+      gu.exp_stride = (long long)Fe * H * 2;
+      gu.moe_ids = c->moe_ids;
+      gu.top_k = K;
+      gu.n_experts = E;
+      gu.slot_rows = Fe;
+      gu.sh_rows = cf.shared_ffn;
+      gu.R = K * Fe + cf.shared_ffn;
+      gu.C = H;
+      gu.x = c->x;
+      gu.norm_g = L.norm2;
+      gu.y = c->h;
+      if ((rc = run(gu, gemv::kSrcExpertRows, gemv::kInX, gemv::kEpiSwiglu, "expert gate/up")) != HY_OK) return rc;
+      gemv::Params dn = gemv_base();
+      dn.exp_base[0] = (const uint8_t*)L.exp_down.w;
+      dn.sh_base[0] = (const uint8_t*)L.sh_down.w;
+      dn.exp_stride = (long long)H * Fe * 2;
+      dn.moe_ids = c->moe_ids;
+      dn.moe_w = c->moe_w;
+      dn.top_k = K;
+      dn.n_experts = E;
+      dn.seg_cols = Fe;
+      dn.R = H;
+      dn.C = (K + 1) * Fe;
+      dn.x = c->h;
+      dn.y = c->x;
+      if ((rc = run(dn, gemv::kSrcExpertSegs, gemv::kInMoeZ, gemv::kEpiResid, "expert down")) != HY_OK) return rc;
+    }
+    if (m->debug) {
+      cudaError_t e = launch_k(k_copy_f32, dim3((H + 255) / 256), dim3(256), 0, st, pdl, (const float*)c->x,
+                               c->dbg_hidden + (size_t)l * H, H);
+      if (e != cudaSuccess) return fail(HY_ERR_CUDA, "debug copy: %s", cudaGetErrorString(e));
+    }
+  }
+  {  // final RMSNorm + LM head + argmax; the last CTA advances the position
+    gemv::Params p = gemv_base();
+    p.W[0] = (const uint8_t*)m->w.lm_head.w;
+    p.R = cf.vocab;
+    p.C = H;
+    p.x = c->x;
+    p.norm_g = m->w.final_norm;
+    p.y = logits;
+    p.part_val = c->am_val;
+    p.part_idx = c->am_idx;
+    p.counter = c->cnt_am;
+    p.ids_out = ids;
+    p.len_inc = pos;
+    int rc = run(p, gemv::kSrcDense, gemv::kInX, gemv::kEpiArgmax, "lm-head");
+    if (rc != HY_OK) return rc;
+  }
+  return HY_OK;
+}
+
+int get_graph(hy_cache* c, int seq, float* logits, int* ids, cudaGraphExec_t* out) {
+  for (auto& g : c->graphs)
+    if (g.seq == seq && g.logits == logits && g.ids == ids) {
+      *out = g.exec;
+      return HY_OK;
+    }
+  if (c->graphs.size() >= 16) {
+    cudaGraphExecDestroy(c->graphs.front().exec);
+    c->graphs.erase(c->graphs.begin());
+  }
+  HY_CK(cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
+  int rc = record_step(c, seq, logits, ids, c->cap_stream);
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(c->cap_stream, &graph);
+  if (rc != HY_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e));
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+  c->graphs.push_back({seq, logits, ids, exec});
+  *out = exec;
+  return HY_OK;
+}
+
+// one step of sequence `seq` whose token id is already in c->tok
+int run_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) {
+  if (!c->m->graphs) return record_step(c, seq, logits, ids, st);
+  cudaGraphExec_t exec;
+  int rc = get_graph(c, seq, logits, ids, &exec);
+  if (rc != HY_OK) return rc;
+  HY_CK(cudaGraphLaunch(exec, st));
+  return HY_OK;
+}
+
+int check_model_cfg(const hy_config* c) {
+  if (c->n_layers < 1 || c->n_layers > 64) return fail(HY_ERR_ARG, "n_layers must be in 1..64");
+  if (c->hidden <= 0 || c->hidden % 8 || c->vocab <= 0) return fail(HY_ERR_ARG, "hidden must be a positive multiple of 8");
+  if (c->weight_format != 0) return fail(HY_ERR_UNSUPPORTED, "only bf16 weights (weight_format 0) in this build");
+  const uint64_t mask = c->n_layers == 64 ? c->attn_layer_mask : (c->attn_layer_mask & ((1ull << c->n_layers) - 1));
+  const bool any_attn = mask != 0, any_gdn = (uint64_t)__builtin_popcountll(mask) < (uint64_t)c->n_layers;
+  if (any_gdn) {
+    if (c->gdn_heads <= 0 || (c->gdn_dk != 64 && c->gdn_dk != 128 && c->gdn_dk != 256) || c->gdn_dv <= 0 ||
+        c->gdn_dv % 8)
+      return fail(HY_ERR_UNSUPPORTED, "GDN shape: dk must be 64/128/256, dv a multiple of 8");
+    if (c->conv_k < 1 || c->conv_k > 8) return fail(HY_ERR_ARG, "conv_k must be in 1..8");
+  }
+  if (any_attn) {
+    if (c->attn_kv_heads <= 0 || c->attn_q_heads % c->attn_kv_heads || c->attn_q_heads / c->attn_kv_heads > 8)
+      return fail(HY_ERR_UNSUPPORTED, "attention: nq must be a multiple of nkv with nq/nkv <= 8");
+    const int G = c->attn_q_heads / c->attn_kv_heads;
+    if ((c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) || (G != 1 && G != 2 && G != 4 && G != 8))
+      return fail(HY_ERR_UNSUPPORTED, "attention: head_dim must be 64/128/256 and nq/nkv in {1,2,4,8}");
+  }
+  if (c->ffn < 0) return fail(HY_ERR_ARG, "ffn < 0");
+  if (c->ffn == 0) {
+    if (c->n_experts <= 0 || c->top_k <= 0 || c->top_k > 16 || c->top_k > c->n_experts || c->expert_ffn <= 0 ||
+        c->expert_ffn % 8)
+      return fail(HY_ERR_ARG, "MoE shape");
+    if (c->shared_ffn != c->expert_ffn) return fail(HY_ERR_UNSUPPORTED, "MoE: shared_ffn must equal expert_ffn");
+  } else if (c->ffn % 8) {
+    return fail(HY_ERR_ARG, "ffn must be a multiple of 8");
+  }
+  return HY_OK;
+}
+
+void free_cache_mem(hy_cache* c) {
+  for (auto& g : c->graphs) cudaGraphExecDestroy(g.exec);
+  c->graphs.clear();
+  for (void* p : c->allocs) cudaFree(p);
+  c->allocs.clear();
+  for (uint8_t* p : c->mem) cudaFree(p);
+  c->mem.clear();
+  if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+  c->cap_stream = nullptr;
+}
+
+template <typename T>
+int dalloc(hy_cache* c, T** p, size_t count) {
+  void* q = nullptr;
+  cudaError_t e = cudaMalloc(&q, count * sizeof(T) > 0 ? count * sizeof(T) : 16);
+  if (e != cudaSuccess) return fail(HY_ERR_NOMEM, "cudaMalloc of %zu bytes: %s", count * sizeof(T), cudaGetErrorString(e));
+  c->allocs.push_back(q);
+  *p = reinterpret_cast<T*>(q);
+  e = cudaMemset(q, 0, count * sizeof(T) > 0 ? count * sizeof(T) : 16);
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "cudaMemset: %s", cudaGetErrorString(e));
+  return HY_OK;
+}
+
+int valid_seq(const hy_cache* c, int seq) { return c && seq >= 0 && seq < c->max_seqs; }
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* hy_last_error(void) { return g_err.c_str(); }
+
+int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
+  if (!cfg || !w || !out) return fail(HY_ERR_ARG, "null argument");
+  *out = nullptr;
+  int rc = check_model_cfg(cfg);
+  if (rc != HY_OK) return rc;
+  if (!w->layers) return fail(HY_ERR_ARG, "weights.layers is null");
+  const hy_config& c = *cfg;
+  const int H = c.hidden;
+  auto need = [&](const void* p, const char* name, int l) -> int {
+    if (!aligned16(p)) return fail(HY_ERR_ARG, "weight %s of layer %d is null or not 16-byte aligned", name, l);
+    return HY_OK;
+  };
+  if ((rc = need(w->embed, "embed", -1)) || (rc = need(w->final_norm, "final_norm", -1)) ||
+      (rc = need(w->lm_head.w, "lm_head", -1)))
+    return rc;
+  auto* m = new hy_model();
+  m->cfg = c;
+  m->w = *w;
+  m->layers.assign(w->layers, w->layers + c.n_layers);
+  m->w.layers = nullptr;
+  m->is_attn.resize(c.n_layers);
+  m->sub.resize(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    m->is_attn[l] = (c.attn_layer_mask >> l) & 1ull;
+    m->sub[l] = m->is_attn[l] ? m->n_attn++ : m->n_gdn++;
+    const hy_layer_weights& L = m->layers[l];
+    if ((rc = need(L.norm1, "norm1", l)) || (rc = need(L.w_in.w, "w_in", l)) || (rc = need(L.w_o.w, "w_o", l)) ||
+        (rc = need(L.norm2, "norm2", l)))
+      break;
+    if (!m->is_attn[l] && !L.conv_w) { rc = fail(HY_ERR_ARG, "conv_w of layer %d is null", l); break; }
+    if (c.ffn > 0) {
+      if ((rc = need(L.w_gate.w, "w_gate", l)) || (rc = need(L.w_up.w, "w_up", l)) || (rc = need(L.w_down.w, "w_down", l)))
+        break;
+    } else {
+      if ((rc = need(L.router, "router", l)) || (rc = need(L.exp_gate.w, "exp_gate", l)) ||
+          (rc = need(L.exp_up.w, "exp_up", l)) || (rc = need(L.exp_down.w, "exp_down", l)) ||
+          (rc = need(L.sh_gate.w, "sh_gate", l)) || (rc = need(L.sh_up.w, "sh_up", l)) ||
+          (rc = need(L.sh_down.w, "sh_down", l)))
+        break;
+    }
+  }
+  if (rc != HY_OK) {
+    delete m;
+    return rc;
+  }
+  if ((rc = current_device(&m->device, &m->nsm)) != HY_OK || (rc = ensure_init(m->device)) != HY_OK) {
+    delete m;
+    return rc;
+  }
+  m->CC = 2 * c.gdn_heads * c.gdn_dk + c.gdn_heads * c.gdn_dv;
+  m->gdn_rows = m->CC + 2 * c.gdn_heads;
+  m->attn_rows = (c.attn_q_heads + 2 * c.attn_kv_heads) * c.head_dim;
+  m->moe = c.ffn == 0;
+  int y = H;
+  if (m->n_gdn) y = std::max(y, m->gdn_rows);
+  if (m->n_attn) y = std::max(y, m->attn_rows);
+  m->y_len = y;
+  m->o_len = std::max(m->n_gdn ? c.gdn_heads * c.gdn_dv : 0, m->n_attn ? c.attn_q_heads * c.head_dim : 0);
+  m->h_len = m->moe ? (c.top_k + 1) * c.expert_ffn : c.ffn;
+  m->splits = c.attn_splits > 0 ? c.attn_splits : attn::auto_splits(c.attn_kv_heads, m->nsm);
+  m->pdl = !(c.flags & HY_FLAG_NO_PDL);
+  m->graphs = !(c.flags & HY_FLAG_NO_GRAPH);
+  m->debug = (c.flags & HY_FLAG_DEBUG) != 0;
+  *out = m;
+  g_err.clear();
+  return HY_OK;
+}
+
+void hy_model_free(hy_model* m) { delete m; }
+
+int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, hy_cache** out) {
+  if (!m || !out || max_seqs <= 0 || !capacity_host) return fail(HY_ERR_ARG, "bad argument");
+  *out = nullptr;
+  const hy_config& cf = m->cfg;
+  auto* c = new hy_cache();
+  c->m = m;
+  c->max_seqs = max_seqs;
+  c->cap.assign(capacity_host, capacity_host + max_seqs);
+  c->len.assign(max_seqs, 0);
+  int rc = HY_OK;
+  int max_cap = 1;
+  for (int s = 0; s < max_seqs; ++s) {
+    if (c->cap[s] <= 0) { delete c; return fail(HY_ERR_ARG, "capacity of sequence %d must be positive", s); }
+    max_cap = std::max(max_cap, c->cap[s]);
+  }
+  const size_t state_b = (size_t)m->n_gdn * cf.gdn_heads * cf.gdn_dv * cf.gdn_dk * 4;
+  const size_t conv_b = (size_t)m->n_gdn * std::max(cf.conv_k, 1) * m->CC * 4;
+  c->off_conv = (state_b + 255) & ~(size_t)255;
+  const size_t off_kv = (c->off_conv + conv_b + 255) & ~(size_t)255;
+  for (int s = 0; s < max_seqs; ++s) {
+    const size_t kv_b = (size_t)m->n_attn * 2 * cf.attn_kv_heads * c->cap[s] * cf.head_dim * 2;
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, off_kv + kv_b + 256);
+    if (e != cudaSuccess) {
+      free_cache_mem(c);
+      delete c;
+      return fail(HY_ERR_NOMEM, "cache of sequence %d (%zu bytes): %s", s, off_kv + kv_b, cudaGetErrorString(e));
+    }
+    c->mem.push_back((uint8_t*)p);
+    c->off_kv.push_back(off_kv);
+    if ((e = cudaMemset(p, 0, off_kv)) != cudaSuccess) {
+      free_cache_mem(c);
+      delete c;
+      return fail(HY_ERR_CUDA, "cudaMemset: %s", cudaGetErrorString(e));
+    }
+  }
+  const int G = cf.attn_kv_heads > 0 ? cf.attn_q_heads / cf.attn_kv_heads : 1;
+  const size_t part = m->n_attn ? attn::part_floats(cf.attn_q_heads, cf.attn_kv_heads, cf.head_dim, m->splits) : 1;
+  (void)G;
+  if ((rc = dalloc(c, &c->d_len, max_seqs)) || (rc = dalloc(c, &c->x, cf.hidden)) ||
+      (rc = dalloc(c, &c->y, m->y_len)) || (rc = dalloc(c, &c->o, std::max(m->o_len, 1))) ||
+      (rc = dalloc(c, &c->h, std::max(m->h_len, 1))) || (rc = dalloc(c, &c->part, part)) ||
+      (rc = dalloc(c, &c->am_val, 1024)) || (rc = dalloc(c, &c->am_idx, 1024)) ||
+      (rc = dalloc(c, &c->rlog, std::max(cf.n_experts + 1, 1))) || (rc = dalloc(c, &c->moe_w, 17)) ||
+      (rc = dalloc(c, &c->moe_ids, 16)) || (rc = dalloc(c, &c->tok, max_seqs)) || (rc = dalloc(c, &c->ids, max_seqs)) ||
+      (rc = dalloc(c, &c->cnt_attn, std::max(cf.attn_kv_heads, 1))) || (rc = dalloc(c, &c->cnt_am, 1)) ||
+      (rc = dalloc(c, &c->cnt_router, 1)) || (rc = dalloc(c, &c->guard, 1)) ||
+      (rc = dalloc(c, &c->logits_buf, (size_t)cf.vocab))) {
+    free_cache_mem(c);
+    delete c;
+    return rc;
+  }
+  if (m->n_attn) {
+    if ((rc = dalloc(c, &c->rope, (size_t)max_cap * (cf.head_dim / 2)))) {
+      free_cache_mem(c);
+      delete c;
+      return rc;
+    }
+    cudaError_t e = attn::rope_table(c->rope, max_cap, cf.head_dim, (double)cf.rope_theta, 0);
+    if (e != cudaSuccess) {
+      free_cache_mem(c);
+      delete c;
+      return fail(HY_ERR_CUDA, "rope table: %s", cudaGetErrorString(e));
+    }
+  }
+  if (m->debug) {
+    if ((rc = dalloc(c, &c->dbg_hidden, (size_t)cf.n_layers * cf.hidden)) ||
+        (rc = dalloc(c, &c->dbg_rlog, (size_t)cf.n_layers * std::max(cf.n_experts + 1, 1))) ||
+        (rc = dalloc(c, &c->dbg_rids, (size_t)cf.n_layers * std::max(cf.top_k, 1)))) {
+      free_cache_mem(c);
+      delete c;
+      return rc;
+    }
+  }
+  cudaError_t e = cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    free_cache_mem(c);
+    delete c;
+    return fail(HY_ERR_CUDA, "cache setup: %s", cudaGetErrorString(e));
+  }
+  *out = c;
+  g_err.clear();
+  return HY_OK;
+}
+
+void hy_cache_free(hy_cache* c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  free_cache_mem(c);
+  delete c;
+}
+
+int hy_seq_reset(hy_cache* c, int32_t seq, void* stream) {
+  if (!valid_seq(c, seq)) return fail(HY_ERR_ARG, "bad sequence handle %d", seq);
+  cudaStream_t st = (cudaStream_t)stream;
+  HY_CK(cudaMemsetAsync(c->mem[seq], 0, c->off_kv[seq], st));
+  HY_CK(cudaMemsetAsync(c->d_len + seq, 0, sizeof(int), st));
+  c->len[seq] = 0;
+  return HY_OK;
+}
+
+int32_t hy_seq_len(const hy_cache* c, int32_t seq) { return valid_seq(c, seq) ? c->len[seq] : -1; }
+int32_t hy_seq_capacity(const hy_cache* c, int32_t seq) { return valid_seq(c, seq) ? c->cap[seq] : -1; }
+
+int hy_prefill(hy_model* m, hy_cache* c, int32_t seq, const int32_t* tokens_dev, int32_t n, float* logits_dev,
+               void* stream) {
+  if (!m || !c || c->m != m || !valid_seq(c, seq) || (n > 0 && !tokens_dev) || n < 0)
+    return fail(HY_ERR_ARG, "bad argument");
+  if ((long long)c->len[seq] + n > c->cap[seq])
+    return fail(HY_ERR_CAPACITY, "sequence %d: %d + %d tokens exceed capacity %d", seq, c->len[seq], n, c->cap[seq]);
+  cudaStream_t st = (cudaStream_t)stream;
+  for (int i = 0; i < n; ++i) {
+    HY_CK(cudaMemcpyAsync(c->tok, tokens_dev + i, sizeof(int), cudaMemcpyDeviceToDevice, st));
+    int rc = run_step(c, seq, (i == n - 1) ? logits_dev : nullptr, c->ids, st);
+    if (rc != HY_OK) return rc;
+    c->len[seq] += 1;
+  }
+  return HY_OK;
+}
+
+int hy_decode_step(hy_model* m, hy_cache* c, const int32_t* seqs_host, int32_t nseq, const int32_t* tokens_dev,
+                   float* logits_dev, int32_t* ids_dev, void* stream) {
+  if (!m || !c || c->m != m || !seqs_host || !tokens_dev || !ids_dev) return fail(HY_ERR_ARG, "null argument");
+  if (nseq != 1) return fail(HY_ERR_UNSUPPORTED, "this build decodes one sequence per step (nseq == 1)");
+  const int seq = seqs_host[0];
+  if (!valid_seq(c, seq)) return fail(HY_ERR_ARG, "bad sequence handle %d", seq);
+  if (c->len[seq] >= c->cap[seq]) return fail(HY_ERR_CAPACITY, "sequence %d is at its capacity %d", seq, c->cap[seq]);
+  cudaStream_t st = (cudaStream_t)stream;
+  HY_CK(cudaMemcpyAsync(c->tok, tokens_dev, sizeof(int), cudaMemcpyDeviceToDevice, st));
+  int rc = run_step(c, seq, logits_dev, ids_dev, st);
+  if (rc != HY_OK) return rc;
+  c->len[seq] += 1;
+  return HY_OK;
+}
+
+int hy_decode_step_host(hy_model* m, hy_cache* c, const int32_t* seqs_host, int32_t nseq, const int32_t* tokens_host,
+                        float* logits_host, int32_t* ids_host, void* stream) {
+  if (!m || !c || c->m != m || !seqs_host || !tokens_host || !ids_host) return fail(HY_ERR_ARG, "null argument");
+  if (nseq != 1) return fail(HY_ERR_UNSUPPORTED, "this build decodes one sequence per step (nseq == 1)");
+  const int seq = seqs_host[0];
+  if (!valid_seq(c, seq)) return fail(HY_ERR_ARG, "bad sequence handle %d", seq);
+  if (c->len[seq] >= c->cap[seq]) return fail(HY_ERR_CAPACITY, "sequence %d is at its capacity %d", seq, c->cap[seq]);
+  cudaStream_t st = (cudaStream_t)stream;
+  HY_CK(cudaMemcpyAsync(c->tok, tokens_host, sizeof(int), cudaMemcpyHostToDevice, st));
+  float* lg = logits_host ? c->logits_buf : nullptr;
+  int rc = run_step(c, seq, lg, c->ids, st);
+  if (rc != HY_OK) return rc;
+  c->len[seq] += 1;
+  HY_CK(cudaMemcpyAsync(ids_host, c->ids, sizeof(int), cudaMemcpyDeviceToHost, st));
+  if (logits_host)
+    HY_CK(cudaMemcpyAsync(logits_host, c->logits_buf, sizeof(float) * (size_t)m->cfg.vocab, cudaMemcpyDeviceToHost, st));
+  HY_CK(cudaStreamSynchronize(st));
+  return HY_OK;
+}
+
+int hy_check_device(hy_cache* c, void* stream, uint32_t* bits_out) {
+  if (!c) return fail(HY_ERR_ARG, "null cache");
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned bits = 0;
+  HY_CK(cudaMemcpyAsync(&bits, c->guard, sizeof(unsigned), cudaMemcpyDeviceToHost, st));
+  HY_CK(cudaStreamSynchronize(st));
+  if (bits_out) *bits_out = bits;
+  if (bits) {
+    HY_CK(cudaMemsetAsync(c->guard, 0, sizeof(unsigned), st));
+    HY_CK(cudaStreamSynchronize(st));
+    return fail(HY_ERR_DEVICE_GUARD, "device guard bits 0x%x", bits);
+  }
+  return HY_OK;
+}
+
+int hy_debug_hidden(hy_cache* c, int32_t layer, float* dst_dev, void* stream) {
+  if (!c || !dst_dev || layer < 0 || layer >= c->m->cfg.n_layers) return fail(HY_ERR_ARG, "bad argument");
+  if (!c->m->debug) return fail(HY_ERR_ARG, "model was created without HY_FLAG_DEBUG");
+  HY_CK(cudaMemcpyAsync(dst_dev, c->dbg_hidden + (size_t)layer * c->m->cfg.hidden, sizeof(float) * c->m->cfg.hidden,
+                        cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+  return HY_OK;
+}
+
+int hy_debug_router(hy_cache* c, int32_t layer, float* logits_dev, int32_t* ids_dev, void* stream) {
+  if (!c || layer < 0 || layer >= c->m->cfg.n_layers) return fail(HY_ERR_ARG, "bad argument");
+  if (!c->m->debug || !c->m->moe) return fail(HY_ERR_ARG, "needs a MoE model created with HY_FLAG_DEBUG");
+  const hy_config& cf = c->m->cfg;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (logits_dev)
+    HY_CK(cudaMemcpyAsync(logits_dev, c->dbg_rlog + (size_t)layer * (cf.n_experts + 1),
+                          sizeof(float) * (cf.n_experts + 1), cudaMemcpyDeviceToDevice, st));
+  if (ids_dev)
+    HY_CK(cudaMemcpyAsync(ids_dev, c->dbg_rids + (size_t)layer * cf.top_k, sizeof(int) * cf.top_k,
+                          cudaMemcpyDeviceToDevice, st));
+  return HY_OK;
+}
+
+// ---------------------------------------------------------------- single ops
+
+static int op_guard(unsigned** g) {
+  int dev = 0, nsm = 0;
+  int rc = current_device(&dev, &nsm);
+  if (rc != HY_OK) return rc;
+  if ((rc = ensure_init(dev)) != HY_OK) return rc;
+  std::lock_guard<std::mutex> lk(g_init_mu);
+  auto it = g_op_guard.find(dev);
+  if (it == g_op_guard.end()) {
+    unsigned* p = nullptr;
+    HY_CK(cudaMalloc(&p, sizeof(unsigned)));
+    HY_CK(cudaMemset(p, 0, sizeof(unsigned)));
+    it = g_op_guard.emplace(dev, p).first;
+  }
+  *g = it->second;
+  return HY_OK;
+}
+
+static int op_nsm() {
+  int dev = 0, nsm = 0;
+  if (current_device(&dev, &nsm) != HY_OK) return 0;
+  return nsm;
+}
+
+static int op_gemv_run(gemv::Params& p, int in, int epi, void* stream) {
+  unsigned* guard = nullptr;
+  int rc = op_guard(&guard);
+  if (rc != HY_OK) return rc;
+  p.guard = guard;
+  const gemv::Plan pl = gemv::plan(p.R, p.C, epi == gemv::kEpiSwiglu ? 2 : 1, op_nsm());
+  if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no GEMV plan for %d x %d", p.R, p.C);
+  cudaError_t e = gemv::launch(p, pl, gemv::kSrcDense, in, epi, (cudaStream_t)stream, false);
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "GEMV launch: %s", cudaGetErrorString(e));
+  return HY_OK;
+}
+
+int hy_op_gemv(const void* W_dev, int32_t rows, int32_t cols, const float* x_dev, const float* norm_g_dev, float eps,
+               float* y_dev, int32_t accumulate, void* stream) {
+  if (!aligned16(W_dev) || !aligned16(x_dev) || !y_dev || rows <= 0 || cols <= 0 || cols % 8)
+    return fail(HY_ERR_ARG, "bad GEMV arguments");
+  gemv::Params p;
+  memset(&p, 0, sizeof(p));
+  p.W[0] = (const uint8_t*)W_dev;
+  p.R = rows;
+  p.C = cols;
+  p.x = x_dev;
+  p.norm_g = norm_g_dev;
+  p.eps = eps;
+  p.y = y_dev;
+  return op_gemv_run(p, gemv::kInX, accumulate ? gemv::kEpiResid : gemv::kEpiStore, stream);
+}
+
+int hy_op_gemv_swiglu(const void* Wg_dev, const void* Wu_dev, int32_t rows, int32_t cols, const float* x_dev,
+                      const float* norm_g_dev, float eps, float* h_dev, void* stream) {
+  if (!aligned16(Wg_dev) || !aligned16(Wu_dev) || !aligned16(x_dev) || !h_dev || rows <= 0 || cols <= 0 || cols % 8)
+    return fail(HY_ERR_ARG, "bad GEMV arguments");
+  gemv::Params p;
+  memset(&p, 0, sizeof(p));
+  p.W[0] = (const uint8_t*)Wg_dev;
+  p.W[1] = (const uint8_t*)Wu_dev;
+  p.R = rows;
+  p.C = cols;
+  p.x = x_dev;
+  p.norm_g = norm_g_dev;
+  p.eps = eps;
+  p.y = h_dev;
+  return op_gemv_run(p, gemv::kInX, gemv::kEpiSwiglu, stream);
+}
+
+size_t hy_op_argmax_workspace(void) { return 256 + 1024 * 8; }
+
+int hy_op_gemv_argmax(const void* W_dev, int32_t rows, int32_t cols, const float* x_dev, const float* norm_g_dev,
+                      float eps, float* logits_dev, int32_t* id_dev, void* workspace_dev, void* stream) {
+  if (!aligned16(W_dev) || !aligned16(x_dev) || !id_dev || !aligned16(workspace_dev) || rows <= 0 || cols <= 0 ||
+      cols % 8)
+    return fail(HY_ERR_ARG, "bad GEMV arguments");
+  uint8_t* ws = (uint8_t*)workspace_dev;
+  gemv::Params p;
+  memset(&p, 0, sizeof(p));
+  p.W[0] = (const uint8_t*)W_dev;
+  p.R = rows;
+  p.C = cols;
+  p.x = x_dev;
+  p.norm_g = norm_g_dev;
+  p.eps = eps;
+  p.y = logits_dev;
+  p.counter = (unsigned*)ws;
+  p.part_val = (float*)(ws + 256);
+  p.part_idx = (int*)(ws + 256 + 1024 * 4);
+  p.ids_out = id_dev;
+  return op_gemv_run(p, gemv::kInX, gemv::kEpiArgmax, stream);
+}
+
+int hy_op_gdn_step(const float* y_dev, const void* conv_w_dev, float* conv_state_dev, float* S_dev, float* o_dev,
+                   int32_t nh, int32_t dk, int32_t dv, int32_t conv_k, const int32_t* pos_dev, void* stream) {
+  if (!y_dev || !conv_w_dev || !conv_state_dev || !aligned16(S_dev) || !o_dev || !pos_dev || nh <= 0 || dv <= 0)
+    return fail(HY_ERR_ARG, "bad GDN arguments");
+  if (dk != 64 && dk != 128 && dk != 256) return fail(HY_ERR_UNSUPPORTED, "dk must be 64, 128 or 256");
+  if (conv_k < 1 || conv_k > 8) return fail(HY_ERR_ARG, "conv_k must be in 1..8");
+  unsigned* guard = nullptr;
+  int rc = op_guard(&guard);
+  if (rc != HY_OK) return rc;
+  gdn::Params g;
+  memset(&g, 0, sizeof(g));
+  g.y = y_dev;
+  g.conv_w = (const uint16_t*)conv_w_dev;
+  g.conv_state = conv_state_dev;
+  g.S = S_dev;
+  g.o = o_dev;
+  g.nh = nh;
+  g.dk = dk;
+  g.dv = dv;
+  g.conv_k = conv_k;
+  g.pos = pos_dev;
+  g.guard = guard;
+  cudaError_t e = gdn::launch(g, (cudaStream_t)stream, false);
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "GDN launch: %s", cudaGetErrorString(e));
+  return HY_OK;
+}
+
+int hy_op_rope_table(float* table_dev, int32_t cap, int32_t hd, float theta, void* stream) {
+  if (!table_dev || cap <= 0 || hd <= 0 || hd % 2) return fail(HY_ERR_ARG, "bad RoPE table arguments");
+  cudaError_t e = attn::rope_table((float2*)table_dev, cap, hd, (double)theta, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "RoPE table: %s", cudaGetErrorString(e));
+  return HY_OK;
+}
+
+size_t hy_op_attention_workspace(int32_t nq, int32_t nkv, int32_t hd, int32_t nsplit) {
+  if (nkv <= 0 || nq <= 0) return 0;
+  if (nsplit <= 0) nsplit = attn::auto_splits(nkv, op_nsm());
+  return 256 + ((size_t)nkv * 4 + 255) / 256 * 256 + attn::part_floats(nq, nkv, hd, nsplit) * 4;
+}
+
+int hy_op_attention(const float* y_dev, void* K_dev, void* V_dev, int32_t cap, int32_t nq, int32_t nkv, int32_t hd,
+                    const int32_t* len_dev, const float* rope_table_dev, int32_t nsplit, float* o_dev,
+                    void* workspace_dev, void* stream) {
+  if (!y_dev || !aligned16(K_dev) || !aligned16(V_dev) || !len_dev || !rope_table_dev || !o_dev ||
+      !aligned16(workspace_dev) || cap <= 0 || nkv <= 0 || nq <= 0 || nq % nkv)
+    return fail(HY_ERR_ARG, "bad attention arguments");
+  if ((hd != 64 && hd != 128 && hd != 256) || nq / nkv > 8 || ((nq / nkv) & (nq / nkv - 1)))
+    return fail(HY_ERR_UNSUPPORTED, "attention: head_dim 64/128/256 and nq/nkv in {1,2,4,8}");
+  unsigned* guard = nullptr;
+  int rc = op_guard(&guard);
+  if (rc != HY_OK) return rc;
+  if (nsplit <= 0) nsplit = attn::auto_splits(nkv, op_nsm());
+  uint8_t* ws = (uint8_t*)workspace_dev;
+  attn::Params a;
+  memset(&a, 0, sizeof(a));
+  a.y = y_dev;
+  a.K = (uint16_t*)K_dev;
+  a.V = (uint16_t*)V_dev;
+  a.len = len_dev;
+  a.rope = (const float2*)rope_table_dev;
+  a.cap = cap;
+  a.nq = nq;
+  a.nkv = nkv;
+  a.hd = hd;
+  a.nsplit = nsplit;
+  a.scale = 1.0f / sqrtf((float)hd);
+  a.counter = (unsigned*)ws;
+  a.part = (float*)(ws + 256 + ((size_t)nkv * 4 + 255) / 256 * 256);
+  a.o = o_dev;
+  a.guard = guard;
+  cudaError_t e = attn::launch(a, (cudaStream_t)stream, false);
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  return HY_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,134 @@
+// Internal launch interface of the decode-step kernels (host side).  Not part
+// of the public C ABI (include/hybrid.h); used by engine.cu and capi.cu.
+#pragma once
+
+#include <cstdint>
+#include <utility>
+
+#include <cuda_runtime.h>
+
+namespace hy {
+
+// ---------------------------------------------------------------- GEMV
+namespace gemv {
+
+enum Src : int { kSrcDense = 0, kSrcExpertRows = 1, kSrcExpertSegs = 2 };
+enum In : int { kInX = 0, kInEmbed = 1, kInMoeZ = 2 };
+enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiArgmax = 3, kEpiRouter = 4 };
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 8;
+constexpr int kStageTarget = 24 * 1024;     // preferred bytes per pipeline stage
+constexpr int kStageCap = 32 * 1024;        // largest preferred minimum tile
+constexpr int kInFlight = 96 * 1024;        // bytes kept in flight per CTA
+constexpr int kMaxSmem = 220 * 1024;        // dynamic; leaves room for static shared data
+
+struct Params {
+  // ---- weights (bf16 rows of C columns)
+  const uint8_t* W[2];          // kSrcDense: matrix bases (W[1]: up matrix of a gate/up pair)
+  const uint8_t* exp_base[2];   // MoE: routed-expert tensor bases ([E][rows][cols])
+  const uint8_t* sh_base[2];    // MoE: shared-expert matrices
+  long long exp_stride;         // bytes from one routed expert to the next
+  const int* moe_ids;           // [top_k] selected experts
+  const float* moe_w;           // [top_k + 1] routing weights; last = shared-expert gate
+  int top_k, n_experts;
+  int slot_rows;                // kSrcExpertRows: rows per routed expert slot
+  int sh_rows;                  // kSrcExpertRows: rows of the shared slot
+  int seg_cols;                 // kSrcExpertSegs: columns per expert segment
+  int R, C, npair;
+  // ---- input
+  const float* x;               // kInX: [C]; kInMoeZ: expert activations [(top_k+1)*seg_cols]
+  const uint16_t* embed;        // kInEmbed: bf16 [vocab][C]
+  const int* tok;               // kInEmbed: token id
+  int vocab;
+  float* x_out;                 // kInEmbed: residual stream to initialise (CTA 0 writes it)
+  const float* norm_g;          // RMSNorm gain; null = no norm
+  float eps;
+  // ---- output
+  float* y;                     // store / residual target / SwiGLU output / logits (nullable for argmax)
+  float* part_val;              // argmax partials [ncta]
+  int* part_idx;
+  unsigned* counter;            // last-CTA ticket (zero between launches)
+  int* ids_out;                 // argmax result
+  int* len_inc;                 // incremented once after the argmax (nullable)
+  float* router_logits;         // kEpiRouter: [n_experts + 1] scratch, always written
+  int* out_ids;                 // kEpiRouter: [top_k]
+  float* out_w;                 // kEpiRouter: [top_k + 1]
+  int* dbg_ids;                 // kEpiRouter debug copies (nullable)
+  float* dbg_logits;
+  // ---- plan
+  int ncta, tile_rows, nchunk, chunk_vecs, stage_bytes, nstages, rows_cta_max, xs_floats;
+  unsigned* guard;
+};
+
+struct Plan {
+  int ncta, tile_rows, nchunk, chunk_vecs, vpl, stage_bytes, nstages, rows_cta_max, xs_floats, smem;
+  bool ok;
+};
+
+Plan plan(int R, int C, int npair, int nsm);
+cudaError_t init();
+cudaError_t launch(const Params& p, const Plan& pl, int src, int in, int epi, cudaStream_t st, bool pdl);
+
+}  // namespace gemv
+
+// ---------------------------------------------------------------- GDN
+namespace gdn {
+constexpr int kRowsPerCta = 16;
+constexpr int kThreads = 128;
+struct Params {
+  const float* y;          // projection output: q|k|v|a|b  (conv_channels + 2*nh)
+  const uint16_t* conv_w;  // bf16 [channels][conv_k]
+  float* conv_state;       // ring of conv_k slots [conv_k][channels]; slot t % conv_k holds input t
+  float* S;                // [nh][dv][dk]
+  const int* pos;          // position t of the token
+  float* o;                // [nh*dv]
+  int nh, dk, dv, conv_k;
+  unsigned* guard;
+};
+cudaError_t launch(const Params& p, cudaStream_t st, bool pdl);
+}  // namespace gdn
+
+// ---------------------------------------------------------------- attention
+namespace attn {
+constexpr int kThreads = 288;  // 8 compute warps + 1 copy warp
+constexpr int kStages = 3;
+struct Params {
+  const float* y;          // projection output: q|k|v
+  uint16_t* K;             // bf16 [nkv][cap][hd]
+  uint16_t* V;
+  const int* len;          // position of the new token (= cached rows)
+  const float2* rope;      // [>= cap][hd/2] (cos, sin) of position * theta^(-2i/hd)
+  int cap, nq, nkv, hd, nsplit;
+  float scale;
+  float* part;             // [nkv][nsplit][G][hd + 2]
+  unsigned* counter;       // [nkv], zero between launches
+  float* o;                // [nq*hd]
+  unsigned* guard;
+};
+size_t part_floats(int nq, int nkv, int hd, int nsplit);
+int auto_splits(int nkv, int nsm);
+cudaError_t init();
+cudaError_t launch(const Params& p, cudaStream_t st, bool pdl);
+cudaError_t rope_table(float2* tab, int cap, int hd, double theta, cudaStream_t st);
+}  // namespace attn
+
+// Launch with the programmatic-stream-serialization attribute when pdl is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
+
+}  // namespace hy

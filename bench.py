@@ -1,0 +1,361 @@
+#!/usr/bin/env python
+"""Decode benchmark: batch-1 greedy decode tokens/s of a hybrid Gated-DeltaNet /
+GQA / MoE model on one GB300, and achieved HBM GB/s as a fraction of the
+measured peak.
+
+Default workload: the dense 4B-shaped hybrid (32 layers, 3:1 DeltaNet:GQA,
+hidden 2560, FFN 9216, vocab 151936) with seeded synthetic bf16 weights and a
+random 4096-token prompt; the timed region is --steps greedy decode steps
+(one CUDA-graph launch each, the argmax fed back on the device).
+
+One JSON line on rank 0.  `--impl reference` times the FP64 CPU oracle on the
+same metric and config instead.  With torchrun (N > 1) every rank runs an
+independent replica (the decode step has no cross-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 decode tokens/s; achieved HBM GB/s as fraction of GB300 peak"
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="dense4b")
+    ap.add_argument("--splits", type=int, default=0, help="split-KV chunks per kv head (0 = automatic)")
+    ap.add_argument("--layers", type=int, default=0, help="truncate depth (profiling captures only)")
+    ap.add_argument("--prompt", type=int, default=-1, help="override the prompt length (profiling captures only)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kernel-timing", action="store_true")
+    return ap.parse_args(argv)
+
+
+def workload_of(args):
+    from synth import workloads
+    w = workloads.WORKLOADS[args.workload]
+    shape = w.shape
+    if args.layers:
+        shape = dataclasses.replace(shape, name=f"{shape.name}-l{args.layers}", n_layers=args.layers,
+                                    attn_layers=tuple(l for l in shape.attn_layers if l < args.layers))
+    prompt = w.prompt_len if args.prompt < 0 else args.prompt
+    return w, shape, prompt
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def load_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if any."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        for ln in f:
+            parts = ln.split()
+            if len(parts) >= 3 and not ln.startswith("#") and parts[0] == kernel and parts[1] == workload:
+                return int(parts[2])
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        for ln in out.strip().splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(REASONS, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_decode_sample(shape, context: int, budget_s: float, max_tokens: int, host_w=None):
+    """Time full-depth oracle decode tokens at position `context` from a seeded
+    synthetic cache (random K/V rows and recurrent state: the prompt itself is
+    not replayed on the CPU).  Returns (tokens/s, threads, tokens, seconds)."""
+    import numpy as np
+
+    from oracle import oracle as orc
+    from synth import gen, workloads
+    if host_w is None:
+        host_w = workloads.host_weights(shape)
+    o = orc.Oracle(shape, host_w, context + max_tokens + 2)
+    rng = np.random.default_rng(1234)
+    n_attn = sum(1 for l in range(shape.n_layers) if shape.is_attn(l))
+    for a in range(n_attn):
+        K, V = o.kv_cache(a)
+        K[:, :context] = gen.f32_to_bf16_bits(rng.standard_normal((shape.attn_kv_heads, context, shape.head_dim))
+                                              .astype(np.float32))
+        V[:, :context] = gen.f32_to_bf16_bits(rng.standard_normal((shape.attn_kv_heads, context, shape.head_dim))
+                                              .astype(np.float32) * 0.1)
+    for gi in range(shape.n_layers - n_attn):
+        S = o.gdn_state(gi)
+        S[:] = (rng.standard_normal(S.shape) * 0.01).astype(np.float32)
+    o.cache.len = context
+    tok = 17
+    t0 = time.perf_counter()
+    o.forward(tok, want_hidden=False)
+    t1 = time.perf_counter() - t0
+    n = max(1, min(max_tokens, int(math.ceil(budget_s / max(t1, 1e-3)))))
+    t0 = time.perf_counter()
+    for i in range(n):
+        tok = int(orc.argmax(o.forward(tok, want_hidden=False)["logits"]))
+    dt = time.perf_counter() - t0
+    return n / dt, orc.threads(), n, dt
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w, shape, prompt = workload_of(args)
+    from synth import workloads
+    host_w = workloads.host_weights(shape)
+    import numpy as np  # noqa: F401
+
+    from oracle import oracle as orc
+    o_warm = max(args.warmup, 0)
+    # warm-up tokens are part of the same sampler run; time K tokens
+    tps, cores, n, dt = oracle_decode_sample(shape, prompt, budget_s=1e9, max_tokens=o_warm + args.steps,
+                                             host_w=host_w)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000.0 / tps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "context": prompt, "batch": 1},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} full-depth FP64 oracle decode tokens at context {prompt} from a seeded "
+                                   f"synthetic cache (prompt not replayed on the CPU)"},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    del orc
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+
+    from bandwidth_bound_hybrid_gb300 import accounting as acc
+    from bandwidth_bound_hybrid_gb300 import build as hb
+    from bandwidth_bound_hybrid_gb300.model import HybridModel
+    from synth import workloads
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    if rank == 0:
+        hb.build()
+    if dist:
+        dist.barrier()
+
+    w, shape, prompt = workload_of(args)
+    peak, peak_kind = load_peaks()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = torch.cuda.current_stream()
+
+    weights = workloads.device_weights(shape)
+    cap = prompt + args.warmup + 2 * args.steps + 16
+    model = HybridModel(shape, weights, [cap], splits=args.splits)
+    toks = torch.from_numpy(workloads.prompt_ids(w, n=prompt)).to(dev) if prompt else None
+    ids = torch.zeros(1, dtype=torch.int32, device=dev)
+    if prompt:
+        model.prefill(0, toks)
+        ids.copy_(toks[-1:])
+    for _ in range(args.warmup):
+        model.decode_step(0, ids, ids)
+    torch.cuda.synchronize()
+    assert model.check_device() == 0, "device guard fired during warm-up"
+    ctx0 = model.seq_len(0)
+
+    # ---- timed region: K graph launches, inputs resident in HBM
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0.record(st)
+    for _ in range(args.steps):
+        model.decode_step(0, ids, ids)
+    ev1.record(st)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    t = ev0.elapsed_time(ev1) / 1e3
+    if dist:
+        tt = torch.tensor([t], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    assert model.check_device() == 0, "device guard fired in the timed region"
+    n = max(ws, 1)
+    value = n * args.steps / t
+    mid_ctx = ctx0 + args.steps // 2
+    sb = acc.step_bytes(shape, mid_ctx)
+    step_gbs = sb.total * args.steps / t / 1e9
+
+    # ---- dominant kernel: the gate/up SwiGLU GEMV, timed per launch over every layer's weights
+    roof = None
+    if not args.no_kernel_timing and shape.ffn > 0:
+        from bandwidth_bound_hybrid_gb300 import capi
+        L = capi.lib()
+        x = torch.randn(shape.hidden, device=dev)
+        g = torch.ones(shape.hidden, device=dev)
+        h = torch.empty(shape.ffn, device=dev)
+        durs = []
+        for rep in range(3):
+            for l in range(shape.n_layers):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                capi.check(L.hy_op_gemv_swiglu(weights[f"l{l}.w_gate"].data_ptr(), weights[f"l{l}.w_up"].data_ptr(),
+                                               shape.ffn, shape.hidden, x.data_ptr(), g.data_ptr(), 1e-6, h.data_ptr(),
+                                               st.cuda_stream), "gemv_swiglu")
+                b.record(st)
+                durs.append((a, b))
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in durs[shape.n_layers:]]  # first sweep is warm-up
+        bytes_launch = acc.gemv_swiglu_bytes(shape.ffn, shape.hidden)
+        achieved = bytes_launch / (statistics.mean(ms) / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "gemv gate/up + SwiGLU (k_gemv<5,0,0,2>)", "achieved": achieved,
+                "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": load_traffic("gemv_swiglu", args.workload),
+                "bytes_per_launch": bytes_launch, "launch_us_mean": statistics.mean(ms) * 1e3,
+                "peak_source": f"{peak_kind} hbm_gbs"}
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    tok_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    ids_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    tok_h[0] = int(ids.item())
+    e2e_steps = args.steps
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        model.decode_step_host(0, tok_h, ids_h)
+        tok_h[0] = ids_h[0]
+    e2e_t = time.perf_counter() - t0
+    if dist:
+        tt = torch.tensor([e2e_t], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_t = float(tt.item())
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tps, cores, ntok, dt = oracle_decode_sample(shape, mid_ctx, budget_s=12.0, max_tokens=16)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{ntok} full-depth FP64 oracle decode tokens at context {mid_ctx} from a seeded synthetic "
+                         f"cache ({dt:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "shape": shape.name, "batch": 1, "prompt": prompt,
+                       "context_timed": [ctx0, ctx0 + args.steps], "weights": "bf16", "kv": "bf16",
+                       "splits": model_splits(args, shape), "parallelism": f"replicas x{n}",
+                       "l2": "inputs larger than L2: every step streams all weights (GBs) through the 129 MB L2"},
+            "roofline": roof,
+            "step_roofline": {"bound": "hbm", "bytes_per_step": sb.total, "achieved": step_gbs, "peak": peak,
+                              "unit": "GB/s", "frac": step_gbs / peak},
+            "cpu_baseline": cpu,
+            "e2e": {"value": n * e2e_steps / e2e_t, "unit": "tokens/s", "h2d_bytes_per_step": 4,
+                    "d2h_bytes_per_step": 4},
+            "gpu_launches": acc.kernels_per_step(shape) * args.steps,
+            "graph_launches_per_token": 1,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    model.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def model_splits(args, shape):
+    if args.splits:
+        return args.splits
+    import torch
+    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return max(1, min(32, (2 * nsm) // max(shape.attn_kv_heads, 1)))
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

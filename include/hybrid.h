@@ -1,0 +1,238 @@
+/* hybrid.h -- C ABI of the GB300 (sm_103a) decode library for hybrid
+ * Gated-DeltaNet / GQA-attention / MoE transformers.
+ *
+ * The library runs the single-token decode step (batch 1) of such a model on
+ * one GPU: fused RMSNorm + bf16 GEMV chains, an in-place Gated DeltaNet state
+ * update, split-KV GQA attention with a log-sum-exp combine, a fused router
+ * top-k with expert-gathered GEMV, and a greedy argmax, all captured into one
+ * CUDA graph per decode step.
+ *
+ * Sources (pages this interface follows):
+ *   [Strata] "Beating llama.cpp from Scratch on Consumer AMD: Building Strata,
+ *            a Native Rust + HIP Local AI Engine"
+ *   [14h]    "Fourteen hours to 100 tokens per second"
+ *   [Flash]  "Flash-Next on Strix Halo"
+ *
+ * Conventions for every call:
+ *   - Pointers named *_dev are CUDA device pointers; *_host are host pointers.
+ *     Weights are borrowed (caller-owned device memory that must outlive the
+ *     model); caches and scratch are owned by the library; output buffers are
+ *     caller-owned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls are stream-ordered and do not synchronise unless stated.
+ *   - Every call returns HY_OK (0) or an HY_ERR_* code; a text description of
+ *     the last error of the calling thread is available from hy_last_error().
+ *     No call aborts the process.
+ *   - All matrices are row-major; bf16 values are IEEE bfloat16 bit patterns
+ *     (uint16).  Every weight pointer must be 16-byte aligned and every row
+ *     length (in bytes) a multiple of 16.
+ */
+#ifndef HYBRID_H
+#define HYBRID_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status */
+#define HY_OK 0
+#define HY_ERR_ARG 1          /* invalid argument (null pointer, bad shape, misalignment) */
+#define HY_ERR_CAPACITY 2     /* a sequence would grow past its cache capacity; nothing was launched */
+#define HY_ERR_CUDA 3         /* a CUDA runtime call failed */
+#define HY_ERR_DEVICE_GUARD 4 /* a device-side guard fired (see hy_check_device) */
+#define HY_ERR_UNSUPPORTED 5  /* a shape or option this build does not handle */
+#define HY_ERR_NOMEM 6        /* device allocation failed */
+
+/* Device guard bits reported by hy_check_device(). */
+#define HY_GUARD_WAIT_TIMEOUT 1u  /* a bounded in-kernel wait gave up */
+#define HY_GUARD_BAD_INDEX 2u     /* a token or expert id was out of range */
+#define HY_GUARD_BAD_POSITION 4u  /* a position was outside the cache capacity */
+
+/* Model flags. */
+#define HY_FLAG_DEBUG 1u    /* keep per-layer hidden states and router results of the last step */
+#define HY_FLAG_NO_GRAPH 2u /* launch kernels one by one instead of replaying a CUDA graph */
+#define HY_FLAG_NO_PDL 4u   /* no programmatic dependent launch between kernels */
+
+/* Model shape.  [Strata] "The Beast: Qwen 3.5 Hybrid Architecture": Gated
+ * DeltaNet layers with a fixed FP32 state plus full GQA layers with a bf16 KV
+ * cache; [14h] "Starting point": MoE FFN with 256 experts, top-8 plus one
+ * shared expert. */
+typedef struct {
+  int32_t n_layers;        /* <= 64 */
+  int32_t hidden;          /* H */
+  int32_t vocab;           /* V */
+  int32_t ffn;             /* dense SwiGLU width F; 0 selects the MoE FFN */
+  int32_t gdn_heads;       /* Gated DeltaNet heads nh */
+  int32_t gdn_dk;          /* key dim (64, 128 or 256) */
+  int32_t gdn_dv;          /* value dim */
+  int32_t conv_k;          /* causal conv width (4) */
+  int32_t attn_q_heads;    /* nq */
+  int32_t attn_kv_heads;   /* nkv (nq % nkv == 0, nq / nkv <= 8) */
+  int32_t head_dim;        /* 64, 128 or 256 */
+  uint64_t attn_layer_mask;/* bit l set: layer l is GQA attention, else Gated DeltaNet */
+  int32_t n_experts;       /* E (MoE) */
+  int32_t top_k;           /* k (MoE, <= 16) */
+  int32_t expert_ffn;      /* Fe (MoE) */
+  int32_t shared_ffn;      /* Fs (MoE shared expert) */
+  float rms_eps;           /* RMSNorm epsilon */
+  float rope_theta;        /* RoPE base */
+  int32_t weight_format;   /* 0 = bf16 (only format of this build) */
+  int32_t attn_splits;     /* split-KV chunks per kv head; 0 = chosen from the SM count */
+  uint32_t flags;          /* HY_FLAG_* */
+} hy_config;
+
+/* One linear weight: bf16 [rows][cols] in `w` (`scales` unused for bf16). */
+typedef struct {
+  const void* w;
+  const void* scales;
+} hy_tensor;
+
+/* Weights of one layer (device pointers).  Layouts:
+ *   norm1, norm2 : float [H]                    RMSNorm gains
+ *   w_in  GDN    : [2*nh*dk + nh*dv + 2*nh][H]  rows q | k | v | a | b
+ *         attn   : [(nq + 2*nkv)*hd][H]         rows q | k | v
+ *   conv_w (GDN) : bf16 [2*nh*dk + nh*dv][conv_k]  taps, the last on the current input
+ *   w_o    GDN   : [H][nh*dv];  attn: [H][nq*hd]
+ *   dense FFN    : w_gate, w_up [F][H], w_down [H][F]
+ *   MoE FFN      : router bf16 [E + 1][H] (row E gates the shared expert),
+ *                  exp_gate, exp_up [E][Fe][H], exp_down [E][H][Fe],
+ *                  sh_gate, sh_up [Fs][H], sh_down [H][Fs] */
+typedef struct {
+  const float* norm1;
+  hy_tensor w_in;
+  const void* conv_w;
+  hy_tensor w_o;
+  const float* norm2;
+  hy_tensor w_gate, w_up, w_down;
+  const void* router;
+  hy_tensor exp_gate, exp_up, exp_down;
+  hy_tensor sh_gate, sh_up, sh_down;
+} hy_layer_weights;
+
+typedef struct {
+  const void* embed;             /* bf16 [V][H] */
+  const float* final_norm;       /* float [H] */
+  hy_tensor lm_head;             /* [V][H] */
+  const hy_layer_weights* layers;/* host array [n_layers]; copied by hy_model_create */
+} hy_weights;
+
+typedef struct hy_model hy_model;
+typedef struct hy_cache hy_cache;
+
+/* Text of the calling thread's last error ("" if none). */
+const char* hy_last_error(void);
+
+/* Validate the config and weight pointers and record them (borrowed) for
+ * the current CUDA device.  No graph is captured yet.  [Strata] "Why Safe
+ * Rust with HIP?": raw device pointers confined behind one narrow interface. */
+int hy_model_create(const hy_config* cfg, const hy_weights* weights, hy_model** out);
+void hy_model_free(hy_model* m);
+
+/* Allocate, for up to max_seqs sequences, the per-sequence KV cache (bf16
+ * [nkv][capacity][hd] per attention layer), the Gated DeltaNet state (FP32
+ * [nh][dv][dk] per GDN layer), the conv state and the decode scratch, all
+ * zeroed, all owned by the library.  capacity_host[s] is the most tokens
+ * sequence s may hold ([Strata] "What Broke" section 2: a pre-allocated cache
+ * with a hard bound).  Synchronises the device. */
+int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, hy_cache** out);
+void hy_cache_free(hy_cache* c);
+
+/* Forget sequence `seq`: length 0, recurrent and conv state zeroed
+ * (stream-ordered). */
+int hy_seq_reset(hy_cache* c, int32_t seq, void* stream);
+
+/* Tokens held by sequence `seq`, or -1 for a bad handle.  A sequence is
+ * exhausted when hy_seq_len == its capacity ([Strata] "What Broke" section 2,
+ * context_exhausted()). */
+int32_t hy_seq_len(const hy_cache* c, int32_t seq);
+int32_t hy_seq_capacity(const hy_cache* c, int32_t seq);
+
+/* Run the n prompt tokens tokens_dev[0..n) of sequence `seq` through the
+ * model one position at a time, filling its caches.  logits_dev (nullable)
+ * receives the FP32 logits [V] of the last token.  HY_ERR_CAPACITY (nothing
+ * launched) if len + n > capacity. */
+int hy_prefill(hy_model* m, hy_cache* c, int32_t seq, const int32_t* tokens_dev, int32_t n, float* logits_dev,
+               void* stream);
+
+/* One greedy decode step for the sequences seqs_host[0..nseq) (this build:
+ * nseq == 1): consumes tokens_dev[i] at position len(seqs[i]), writes the
+ * FP32 logits [nseq][V] to logits_dev (nullable) and the argmax token id
+ * (lowest index on ties) to ids_dev[i], then len += 1.  The first call for a
+ * given (sequence set, logits_dev, ids_dev) captures a CUDA graph; later
+ * calls replay it: one graph launch per token ([Strata] "Act 0", pass 3).
+ * HY_ERR_CAPACITY (nothing launched) if a sequence is full. */
+int hy_decode_step(hy_model* m, hy_cache* c, const int32_t* seqs_host, int32_t nseq, const int32_t* tokens_dev,
+                   float* logits_dev, int32_t* ids_dev, void* stream);
+
+/* hy_decode_step with host buffers: copies tokens_host to the device, runs
+ * the step, copies ids (and logits when logits_host is not NULL) back, and
+ * synchronises `stream` before returning. */
+int hy_decode_step_host(hy_model* m, hy_cache* c, const int32_t* seqs_host, int32_t nseq, const int32_t* tokens_host,
+                        float* logits_host, int32_t* ids_host, void* stream);
+
+/* Synchronise `stream` and read (then clear) the device guard word of the
+ * cache; *bits_out receives HY_GUARD_* bits.  Returns HY_ERR_DEVICE_GUARD
+ * when any bit was set. */
+int hy_check_device(hy_cache* c, void* stream, uint32_t* bits_out);
+
+/* With HY_FLAG_DEBUG: copy the residual stream after layer `layer` of the
+ * last step (FP32 [H]) into dst_dev. */
+int hy_debug_hidden(hy_cache* c, int32_t layer, float* dst_dev, void* stream);
+/* With HY_FLAG_DEBUG, MoE layers: the last step's router logits (FP32
+ * [E + 1]) and selected experts (int32 [top_k], in selection order). */
+int hy_debug_router(hy_cache* c, int32_t layer, float* logits_dev, int32_t* ids_dev, void* stream);
+
+/* ------------------------------------------------------------- single ops
+ * The kernels of the decode step, callable on their own (used by tests and
+ * measurements).  All device pointers, stream-ordered. */
+
+/* y = W * xhat, xhat = x (norm_g == NULL) or RMSNorm(x) * norm_g with eps:
+ * W bf16 [rows][cols], x, y FP32.  accumulate != 0: y += W * xhat.
+ * [Strata] "Act 0", pass 3 (vectorised GEMV for M = 1 decode). */
+int hy_op_gemv(const void* W_dev, int32_t rows, int32_t cols, const float* x_dev, const float* norm_g_dev, float eps,
+               float* y_dev, int32_t accumulate, void* stream);
+
+/* h = silu(Wg * xhat) * (Wu * xhat), Wg, Wu bf16 [rows][cols].  [14h] "Eight
+ * levers that worked" (silu(gate) * x in the gated kernel). */
+int hy_op_gemv_swiglu(const void* Wg_dev, const void* Wu_dev, int32_t rows, int32_t cols, const float* x_dev,
+                      const float* norm_g_dev, float eps, float* h_dev, void* stream);
+
+/* Greedy head: logits = W * xhat (logits_dev nullable), *id_dev = argmax
+ * (lowest index on ties).  workspace_dev: hy_op_argmax_workspace() bytes,
+ * zeroed before its first use and left zeroed after each call.
+ * [Strata] "Act 0", pass 3 (on-device argmax, a 4-byte result). */
+size_t hy_op_argmax_workspace(void);
+int hy_op_gemv_argmax(const void* W_dev, int32_t rows, int32_t cols, const float* x_dev, const float* norm_g_dev,
+                      float eps, float* logits_dev, int32_t* id_dev, void* workspace_dev, void* stream);
+
+/* One Gated DeltaNet decode step of one layer at position *pos_dev:
+ * y_dev = projection output [2*nh*dk + nh*dv + 2*nh] (q|k|v|a|b), conv_w
+ * bf16 [channels][conv_k], conv_state FP32 ring [conv_k][channels] (slot
+ * t % conv_k holds the input of position t), S FP32 [nh][dv][dk] updated in
+ * place, o_dev FP32 [nh*dv].  [Strata] "The Beast". */
+int hy_op_gdn_step(const float* y_dev, const void* conv_w_dev, float* conv_state_dev, float* S_dev, float* o_dev,
+                   int32_t nh, int32_t dk, int32_t dv, int32_t conv_k, const int32_t* pos_dev, void* stream);
+
+/* (cos, sin) of position * theta^(-2i/hd) for positions [0, cap), i < hd/2:
+ * table_dev float2 [cap][hd/2] (computed in double, rounded once). */
+int hy_op_rope_table(float* table_dev, int32_t cap, int32_t hd, float theta, void* stream);
+
+/* GQA decode attention of one layer at position T = *len_dev: y_dev =
+ * projection output [(nq + 2*nkv)*hd] (q|k|v, before RoPE); rotates q and
+ * the new k with rope_table_dev, appends bf16 k, v at row T of K_dev, V_dev
+ * (bf16 [nkv][cap][hd]), attends over rows [0, T], writes o_dev FP32
+ * [nq*hd].  nsplit chunks per kv head (0 = automatic).  workspace_dev:
+ * hy_op_attention_workspace() bytes, zeroed before first use, left zeroed.
+ * [Strata] "Act 4" and "What Broke" section 1. */
+size_t hy_op_attention_workspace(int32_t nq, int32_t nkv, int32_t hd, int32_t nsplit);
+int hy_op_attention(const float* y_dev, void* K_dev, void* V_dev, int32_t cap, int32_t nq, int32_t nkv, int32_t hd,
+                    const int32_t* len_dev, const float* rope_table_dev, int32_t nsplit, float* o_dev,
+                    void* workspace_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,56 @@
+"""The C-ABI library loads and exports every function include/hybrid.h
+declares; the Python binding covers exactly those names (CPU only: no
+compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hybrid.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(hy_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def built_lib():
+    from bandwidth_bound_hybrid_gb300 import build
+    return ctypes.CDLL(build.build())
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("hy_model_create", "hy_model_free", "hy_cache_alloc", "hy_cache_free", "hy_prefill",
+              "hy_decode_step", "hy_decode_step_host", "hy_seq_len", "hy_seq_reset", "hy_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(built_lib):
+    missing = [n for n in declared_functions() if not hasattr(built_lib, n)]
+    assert not missing, missing
+
+
+def test_binding_signatures_match_header(built_lib):
+    from bandwidth_bound_hybrid_gb300 import capi
+    assert sorted(capi.SIGNATURES) == declared_functions()
+
+
+def test_last_error_is_empty_string_before_any_call(built_lib):
+    built_lib.hy_last_error.restype = ctypes.c_char_p
+    assert built_lib.hy_last_error() == b""
+
+
+def test_null_arguments_are_rejected_without_a_gpu(built_lib):
+    from bandwidth_bound_hybrid_gb300 import capi
+    L = capi.lib()
+    out = ctypes.c_void_p()
+    assert L.hy_model_create(None, None, ctypes.byref(out)) == capi.HY_ERR_ARG
+    assert b"null" in L.hy_last_error()
+    assert L.hy_seq_len(None, 0) == -1
+    assert L.hy_decode_step(None, None, None, 1, None, None, None, None) == capi.HY_ERR_ARG
