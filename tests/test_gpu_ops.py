@@ -52,8 +52,9 @@ def test_gemv_parity(L, R, C, norm):
     x = rng.standard_normal(C).astype(np.float32)
     g = rng.uniform(0.5, 1.5, C).astype(np.float32)
     y = torch.full((R,), 7.0, dtype=torch.float32, device="cuda")
-    rc = L.hy_op_gemv(bf16_tensor(W).data_ptr(), R, C, torch.from_numpy(x).cuda().data_ptr(),
-                      torch.from_numpy(g).cuda().data_ptr() if norm else None, 1e-6, y.data_ptr(), 0, stream())
+    Wd, xd, gd = bf16_tensor(W), torch.from_numpy(x).cuda(), torch.from_numpy(g).cuda()  # held until synchronised
+    rc = L.hy_op_gemv(Wd.data_ptr(), R, C, xd.data_ptr(), gd.data_ptr() if norm else None, 1e-6, y.data_ptr(), 0,
+                      stream())
     assert rc == 0
     torch.cuda.synchronize()
     xn = orc.rmsnorm(x, g, 1e-6) if norm else x.astype(np.float64)
@@ -70,8 +71,8 @@ def test_gemv_accumulate_adds_to_output(L):
     x = rng.standard_normal(C).astype(np.float32)
     y0 = rng.standard_normal(R).astype(np.float32)
     y = torch.from_numpy(y0.copy()).cuda()
-    assert L.hy_op_gemv(bf16_tensor(W).data_ptr(), R, C, torch.from_numpy(x).cuda().data_ptr(), None, 0.0,
-                        y.data_ptr(), 1, stream()) == 0
+    Wd, xd = bf16_tensor(W), torch.from_numpy(x).cuda()
+    assert L.hy_op_gemv(Wd.data_ptr(), R, C, xd.data_ptr(), None, 0.0, y.data_ptr(), 1, stream()) == 0
     torch.cuda.synchronize()
     ref = y0.astype(np.float64) + orc.gemv(W, x)
     assert_dot_close(to_np(y), ref, np.abs(widen(W)) @ np.abs(x) + np.abs(y0), C + 64, "gemv accumulate")
@@ -86,8 +87,8 @@ def test_gemv_full_lm_head_sampled_rows(L):
     rng = np.random.default_rng(11)
     x = rng.standard_normal(C).astype(np.float32)
     y = torch.empty(R, dtype=torch.float32, device="cuda")
-    assert L.hy_op_gemv(W.data_ptr(), R, C, torch.from_numpy(x).cuda().data_ptr(), None, 0.0, y.data_ptr(), 0,
-                        stream()) == 0
+    xd = torch.from_numpy(x).cuda()
+    assert L.hy_op_gemv(W.data_ptr(), R, C, xd.data_ptr(), None, 0.0, y.data_ptr(), 0, stream()) == 0
     torch.cuda.synchronize()
     rows = np.unique(np.r_[0, 1, R - 1, rng.integers(0, R, 600)])
     Wh = bf16_bits(W[torch.from_numpy(rows).cuda()])
@@ -108,8 +109,8 @@ def test_gemv_swiglu_parity(L, R, C):
     x = rng.standard_normal(C).astype(np.float32)
     g = np.ones(C, dtype=np.float32)
     h = torch.empty(R, dtype=torch.float32, device="cuda")
-    assert L.hy_op_gemv_swiglu(bf16_tensor(Wg).data_ptr(), bf16_tensor(Wu).data_ptr(), R, C,
-                               torch.from_numpy(x).cuda().data_ptr(), torch.from_numpy(g).cuda().data_ptr(), 1e-6,
+    Wgd, Wud, xd, gd = bf16_tensor(Wg), bf16_tensor(Wu), torch.from_numpy(x).cuda(), torch.from_numpy(g).cuda()
+    assert L.hy_op_gemv_swiglu(Wgd.data_ptr(), Wud.data_ptr(), R, C, xd.data_ptr(), gd.data_ptr(), 1e-6,
                                h.data_ptr(), stream()) == 0
     torch.cuda.synchronize()
     xn = orc.rmsnorm(x, g, 1e-6)
@@ -161,8 +162,9 @@ def test_argmax_ties_pick_lowest_index(L):
         W[r] = W[best]
     ws = torch.zeros(L.hy_op_argmax_workspace(), dtype=torch.uint8, device="cuda")
     out = torch.full((1,), -1, dtype=torch.int32, device="cuda")
-    assert L.hy_op_gemv_argmax(bf16_tensor(W).data_ptr(), R, C, torch.from_numpy(x).cuda().data_ptr(), None, 0.0,
-                               None, out.data_ptr(), ws.data_ptr(), stream()) == 0
+    Wd, xd = bf16_tensor(W), torch.from_numpy(x).cuda()
+    assert L.hy_op_gemv_argmax(Wd.data_ptr(), R, C, xd.data_ptr(), None, 0.0, None, out.data_ptr(), ws.data_ptr(),
+                               stream()) == 0
     torch.cuda.synchronize()
     assert int(out.item()) == min(dup + [best])
 
@@ -201,8 +203,9 @@ def test_gdn_step_sequence(L, nh, dk, dv, steps):
     for t in range(steps):
         y = rng.standard_normal(CC + 2 * nh).astype(np.float32)
         pos.fill_(t)
-        assert L.hy_op_gdn_step(torch.from_numpy(y).cuda().data_ptr(), cw.data_ptr(), ring.data_ptr(), S.data_ptr(),
-                                o.data_ptr(), nh, dk, dv, K, pos.data_ptr(), stream()) == 0
+        yd = torch.from_numpy(y).cuda()
+        assert L.hy_op_gdn_step(yd.data_ptr(), cw.data_ptr(), ring.data_ptr(), S.data_ptr(), o.data_ptr(), nh, dk,
+                                dv, K, pos.data_ptr(), stream()) == 0
         torch.cuda.synchronize()
         o_ref, hist, S_ref = oracle_gdn_step(y.astype(np.float64), conv_w, hist, S_ref, nh, dk, dv, K)
         assert rel_l2(to_np(o), o_ref) < 2e-5, f"step {t}"
@@ -241,8 +244,9 @@ def run_attention(L, rng, nq, nkv, hd, cap, T, nsplit):
     ln = torch.tensor([T], dtype=torch.int32, device="cuda")
     o = torch.empty(nq * hd, dtype=torch.float32, device="cuda")
     ws = torch.zeros(L.hy_op_attention_workspace(nq, nkv, hd, nsplit), dtype=torch.uint8, device="cuda")
-    assert L.hy_op_attention(torch.from_numpy(y).cuda().data_ptr(), Kd.data_ptr(), Vd.data_ptr(), cap, nq, nkv, hd,
-                             ln.data_ptr(), table.data_ptr(), nsplit, o.data_ptr(), ws.data_ptr(), stream()) == 0
+    yd = torch.from_numpy(y).cuda()
+    assert L.hy_op_attention(yd.data_ptr(), Kd.data_ptr(), Vd.data_ptr(), cap, nq, nkv, hd, ln.data_ptr(),
+                             table.data_ptr(), nsplit, o.data_ptr(), ws.data_ptr(), stream()) == 0
     torch.cuda.synchronize()
     # oracle: rotate, append bf16 k/v at row T, single-pass softmax over [0, T]
     yd = y.astype(np.float64)
