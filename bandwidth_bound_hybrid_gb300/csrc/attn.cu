@@ -284,22 +284,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p) {
   if (!s_last) return;
   __threadfence();
   // ------------------------------------------------------------ combine (last CTA of kv head g)
+  // Split weights first (one load per (split, head), all in flight together),
+  // then each thread merges its (head, dim) outputs with batches of
+  // independent loads, so the merge costs a few L2 round trips.
   const float* pg0 = p.part + (long long)g * p.nsplit * G * (HD + 2);
+  float* s_w = reinterpret_cast<float*>(stages);              // [nsplit][G] weights e^{m_s - M}
+  float* s_den = s_w + p.nsplit * G;                           // [G]
+  for (int e = ctid; e < p.nsplit * G; e += kCThreads) {
+    const float* ps = pg0 + (long long)e * (HD + 2);
+    s_w[e] = __ldcg(ps + HD);                                  // m_s, replaced by its weight below
+    ored[e] = __ldcg(ps + HD + 1);                             // l_s
+  }
+  named_barrier(1, kCThreads);
+  if (ctid < G) {
+    const int j = ctid;
+    float M = -INFINITY;
+    for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, s_w[s * G + j]);
+    float den = 0.f;
+    for (int s = 0; s < p.nsplit; ++s) {
+      const float l = ored[s * G + j];
+      const float w = (l > 0.f) ? __expf(s_w[s * G + j] - M) : 0.f;
+      s_w[s * G + j] = w;
+      den = fmaf(w, l, den);
+    }
+    s_den[j] = den;
+  }
+  named_barrier(1, kCThreads);
   for (int e = ctid; e < G * HD; e += kCThreads) {
     const int j = e / HD, d = e % HD;
-    float M = -INFINITY;
-    for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, __ldcg(pg0 + (s * G + j) * (HD + 2) + HD));
-    float num = 0.f, den = 0.f;
-    for (int s = 0; s < p.nsplit; ++s) {
-      const float* ps = pg0 + (s * G + j) * (HD + 2);
-      const float l = __ldcg(ps + HD + 1);
-      if (l > 0.f) {
-        const float w = __expf(__ldcg(ps + HD) - M);
-        num = fmaf(w, __ldcg(ps + d), num);
-        den = fmaf(w, l, den);
-      }
+    float num = 0.f;
+    for (int s0 = 0; s0 < p.nsplit; s0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = (s0 + u < p.nsplit) ? __ldcg(pg0 + ((long long)(s0 + u) * G + j) * (HD + 2) + d) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (s0 + u < p.nsplit) num = fmaf(s_w[(s0 + u) * G + j], v[u], num);
     }
-    p.o[(long long)(g * G + j) * HD + d] = num / den;
+    p.o[(long long)(g * G + j) * HD + d] = num / s_den[j];
   }
   if (ctid == 0) p.counter[g] = 0u;
 }

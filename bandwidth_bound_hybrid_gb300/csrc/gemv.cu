@@ -13,6 +13,8 @@
 //     FP32, and reduce with warp shuffles;
 //   * fused prologues (RMSNorm, embedding gather, MoE weighted activations) and
 //     epilogues (store, residual add, SwiGLU, argmax, router top-k).
+#include <cstdlib>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -83,52 +85,53 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
   __syncthreads();
 
   // ------------------------------------------------------------ copy warp
+  // Lanes 0..nprod-1 each own the stages s with s % nprod == lane and issue
+  // the tiles that land there (independent copy streams).
   if (warp == kConsumerWarps) {
-    if (lane == 0) {
+    if (lane < p.nprod) {
       const uint64_t pol = l2_evict_first_policy();
       if (SRC != kSrcDense) pdl_wait();  // expert ids come from the router kernel
-      int issued = 0, t = 0;
-      bool abort = false;
+      int lastt[kMaxStages];
+      for (int s = 0; s < kMaxStages; ++s) lastt[s] = -1;
+      int t = 0;
       for (int a = r0; a < r1; ++t) {
         const int rows = TileWalk::rows_of(p, SRC, a, r1);
         const int s = t % kStages, k = t / kStages;
-        if (t >= kStages && !mbar_wait(&empty[s], (k - 1) & 1)) {
-          set_guard(p.guard, kGuardWaitTimeout);
-          abort = true;
-          break;
-        }
-        uint8_t* dst = stages + s * p.stage_bytes;
-        if (SRC == kSrcExpertSegs) {
-          const uint32_t seg_bytes = (uint32_t)rows * seg_row_bytes;
-          mbar_arrive_expect_tx(&full[s], seg_bytes * nseg);
-          for (int g = 0; g < nseg; ++g) {
-            const uint8_t* base;
-            if (g < p.top_k) {
-              int e = p.moe_ids[g];
-              if (e < 0 || e >= p.n_experts) {
-                set_guard(p.guard, kGuardBadIndex);
-                e = 0;
-              }
-              base = p.exp_base[0] + (long long)e * p.exp_stride;
-            } else {
-              base = p.sh_base[0];
-            }
-            bulk_g2s(dst + g * seg_bytes, base + (long long)a * seg_row_bytes, seg_bytes, &full[s], pol);
+        if (s % p.nprod == lane) {
+          if (t >= kStages && !mbar_wait(&empty[s], (k - 1) & 1)) {
+            set_guard(p.guard, kGuardWaitTimeout);
+            break;
           }
-        } else {
-          const uint32_t bytes = (uint32_t)rows * p.C * 2;
-          mbar_arrive_expect_tx(&full[s], bytes * npair);
-          for (int j = 0; j < npair; ++j) bulk_g2s(dst + j * bytes, row_src(p, SRC, j, a), bytes, &full[s], pol);
+          uint8_t* dst = stages + s * p.stage_bytes;
+          if (SRC == kSrcExpertSegs) {
+            const uint32_t seg_bytes = (uint32_t)rows * seg_row_bytes;
+            mbar_arrive_expect_tx(&full[s], seg_bytes * nseg);
+            for (int g = 0; g < nseg; ++g) {
+              const uint8_t* base;
+              if (g < p.top_k) {
+                int e = p.moe_ids[g];
+                if (e < 0 || e >= p.n_experts) {
+                  set_guard(p.guard, kGuardBadIndex);
+                  e = 0;
+                }
+                base = p.exp_base[0] + (long long)e * p.exp_stride;
+              } else {
+                base = p.sh_base[0];
+              }
+              bulk_g2s(dst + g * seg_bytes, base + (long long)a * seg_row_bytes, seg_bytes, &full[s], pol);
+            }
+          } else {
+            const uint32_t bytes = (uint32_t)rows * p.C * 2;
+            mbar_arrive_expect_tx(&full[s], bytes * npair);
+            for (int j = 0; j < npair; ++j) bulk_g2s(dst + j * bytes, row_src(p, SRC, j, a), bytes, &full[s], pol);
+          }
+          lastt[s] = t;
         }
-        ++issued;
         a += rows;
       }
-      // Drain: the CTA must not retire while copies it issued are in flight.
-      const int first = issued > kStages ? issued - kStages : 0;
-      for (int u = first; u < issued; ++u) {
-        if (!mbar_wait(&full[u % kStages], (u / kStages) & 1)) set_guard(p.guard, kGuardWaitTimeout);
-      }
-      (void)abort;
+      // Drain: the CTA must not retire while copies this lane issued are in flight.
+      for (int s = 0; s < kStages; ++s)
+        if (lastt[s] >= 0 && !mbar_wait(&full[s], (lastt[s] / kStages) & 1)) set_guard(p.guard, kGuardWaitTimeout);
     }
     return;
   }
@@ -215,27 +218,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
     }
     const uint8_t* st = stages + s * p.stage_bytes;
     const int items = rows * npair;
-    for (int q = rg; q < items; q += nrg) {
+    const int segstride = (SRC == kSrcExpertSegs) ? rows * seg_row_bytes : 0;
+    auto item_ptr = [&](int q) -> const uint8_t* {
       const int j = q / rows, i = q - j * rows;
-      const uint8_t* rowp;
-      int segstride;
-      if (SRC == kSrcExpertSegs) {
-        rowp = st + i * seg_row_bytes;
-        segstride = rows * seg_row_bytes;
-      } else {
-        rowp = st + (j * rows + i) * p.C * 2;
-        segstride = 0;
-      }
-      float acc = 0.f;
+      return (SRC == kSrcExpertSegs) ? st + i * seg_row_bytes : st + (j * rows + i) * p.C * 2;
+    };
+    auto item_red = [&](int q) -> float* {
+      const int j = q / rows, i = q - j * rows;
+      return red + ((j * rows_cta) + (a - r0) + i) * p.nchunk + chunk;
+    };
+    // two items per pass: independent loads and FMA chains, then one paired
+    // butterfly (lanes 0..15 finish item 0, lanes 16..31 item 1)
+    for (int q = rg; q < items; q += 2 * nrg) {
+      const int q2 = q + nrg;
+      const bool has2 = q2 < items;
+      const uint8_t* p0 = item_ptr(q);
+      const uint8_t* p1 = has2 ? item_ptr(q2) : p0;
+      uint4 w0[VPL], w1[VPL];
 #pragma unroll
       for (int u = 0; u < VPL; ++u) {
         if (valid[u]) {
-          const uint4 w = *reinterpret_cast<const uint4*>(rowp + segof[u] * segstride + off[u]);
-          acc += dot8(w, xr[u]);
+          w0[u] = *reinterpret_cast<const uint4*>(p0 + segof[u] * segstride + off[u]);
+          w1[u] = *reinterpret_cast<const uint4*>(p1 + segof[u] * segstride + off[u]);
         }
       }
-      acc = warp_sum(acc);
-      if (lane == 0) red[((j * rows_cta) + (a - r0) + i) * p.nchunk + chunk] = acc;
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int u = 0; u < VPL; ++u) {
+        if (valid[u]) {
+          a0 += dot8(w0[u], xr[u]);
+          a1 += dot8(w1[u], xr[u]);
+        }
+      }
+      float keep = (lane < 16) ? a0 : a1;
+      keep += __shfl_xor_sync(0xffffffffu, (lane < 16) ? a1 : a0, 16);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+      if (lane == 0) *item_red(q) = keep;
+      if (lane == 16 && has2) *item_red(q2) = keep;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -416,7 +436,21 @@ cudaError_t init() {
   return cudaSuccess;
 }
 
+namespace {
+// Tuning overrides (environment, read when a launch is planned).
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  const int x = atoi(v);
+  return x > 0 ? x : dflt;
+}
+}  // namespace
+
 Plan plan(int R, int C, int npair, int nsm) {
+  const int stage_target = env_int("HY_GEMV_STAGE_KB", kStageTarget / 1024) * 1024;
+  const int in_flight = env_int("HY_GEMV_INFLIGHT_KB", kInFlight / 1024) * 1024;
+  const int ctas_per_sm = env_int("HY_GEMV_CTAS_PER_SM", kCtasPerSm);
+  const int nprod = env_int("HY_GEMV_PRODUCERS", kProducers);
   Plan pl = {};
   pl.ok = false;
   if (R <= 0 || C <= 0 || C % 8 != 0) return pl;
@@ -438,7 +472,7 @@ Plan plan(int R, int C, int npair, int nsm) {
     const int cv = (nvec + nc - 1) / nc;
     const int v = (cv + 31) / 32;
     if (v > 8) continue;
-    const int unit_items = kConsumerWarps / nc;
+    const int unit_items = 2 * kConsumerWarps / nc;  // two items per warp per tile
     const int tu = (unit_items + npair - 1) / npair;
     nchunk = nc;
     vpl = v;
@@ -450,14 +484,17 @@ Plan plan(int R, int C, int npair, int nsm) {
   pl.nchunk = nchunk;
   pl.vpl = vpl;
   pl.chunk_vecs = (nvec + nchunk - 1) / nchunk;
-  int tr = (kStageTarget / row_bytes / tr_unit) * tr_unit;
+  int tr = (stage_target / row_bytes / tr_unit) * tr_unit;
   if (tr < tr_unit) tr = tr_unit;
   if (tr * row_bytes > 2 * kStageCap) tr = 1;
   pl.tile_rows = tr;
   pl.stage_bytes = ((tr * row_bytes) + 127) & ~127;
-  int ns = kInFlight / pl.stage_bytes;
-  pl.nstages = ns < 2 ? 2 : (ns > kMaxStages ? kMaxStages : ns);
-  pl.ncta = R < nsm ? R : nsm;
+  int ns = in_flight / pl.stage_bytes;
+  ns = ns < 2 ? 2 : (ns > kMaxStages ? kMaxStages : ns);
+  pl.nprod = nprod > ns ? ns : nprod;
+  ns = (ns / pl.nprod) * pl.nprod;  // every producer lane owns the same number of stages
+  pl.nstages = ns;
+  pl.ncta = R < nsm * ctas_per_sm ? R : nsm * ctas_per_sm;
   pl.rows_cta_max = (R + pl.ncta - 1) / pl.ncta;
   pl.xs_floats = (C + 3) & ~3;
   const int red_floats = ((pl.rows_cta_max * npair * nchunk) + 1) & ~1;
@@ -476,6 +513,7 @@ cudaError_t launch(const Params& p0, const Plan& pl, int src, int in, int epi, c
   p.chunk_vecs = pl.chunk_vecs;
   p.stage_bytes = pl.stage_bytes;
   p.nstages = pl.nstages;
+  p.nprod = pl.nprod;
   p.rows_cta_max = pl.rows_cta_max;
   p.xs_floats = pl.xs_floats;
   p.npair = (epi == kEpiSwiglu) ? 2 : 1;

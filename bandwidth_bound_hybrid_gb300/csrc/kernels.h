@@ -19,10 +19,12 @@ enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiArgmax = 3, k
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 8;
-constexpr int kStageTarget = 24 * 1024;     // preferred bytes per pipeline stage
-constexpr int kStageCap = 32 * 1024;        // largest preferred minimum tile
-constexpr int kInFlight = 96 * 1024;        // bytes kept in flight per CTA
+constexpr int kStageTarget = 40 * 1024;     // preferred bytes per pipeline stage
+constexpr int kStageCap = 40 * 1024;        // largest preferred minimum tile
+constexpr int kInFlight = 120 * 1024;       // bytes kept in flight per CTA
 constexpr int kMaxSmem = 220 * 1024;        // dynamic; leaves room for static shared data
+constexpr int kCtasPerSm = 1;
+constexpr int kProducers = 1;
 
 struct Params {
   // ---- weights (bf16 rows of C columns)
@@ -59,11 +61,12 @@ struct Params {
   float* dbg_logits;
   // ---- plan
   int ncta, tile_rows, nchunk, chunk_vecs, stage_bytes, nstages, rows_cta_max, xs_floats;
+  int nprod;                    // copy-issuing lanes
   unsigned* guard;
 };
 
 struct Plan {
-  int ncta, tile_rows, nchunk, chunk_vecs, vpl, stage_bytes, nstages, rows_cta_max, xs_floats, smem;
+  int ncta, tile_rows, nchunk, chunk_vecs, vpl, stage_bytes, nstages, rows_cta_max, xs_floats, smem, nprod;
   bool ok;
 };
 
