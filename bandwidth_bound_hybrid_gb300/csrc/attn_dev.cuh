@@ -1,0 +1,315 @@
+// Device building blocks of split-KV GQA decode attention, shared by the
+// standalone attention kernel (attn.cu) and the persistent decode-step kernel
+// (step.cu).
+//
+// One work item (g, s) = kv head g, split s: positions [s L / S, (s+1) L / S)
+// of the L = T + 1 keys.  Its cached K/V rows arrive as shared-memory tiles
+// (copied by the TMA engine); the new row T (rotated, rounded to bf16 and
+// appended to the cache by the item that holds it) is attended from shared
+// memory.  The item leaves (m, l, o) partials for its G query heads; the last
+// item of kv head g to finish merges them with log-sum-exp weights
+// ("Beating llama.cpp from Scratch on Consumer AMD", Act 4 and "What Broke"
+// section 1: partial sums over segments of the KV cache, combined across
+// separate workgroups).
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace hy {
+namespace attn {
+
+constexpr int kCWarps = 8;
+constexpr int kCT = kCWarps * 32;
+
+template <int HD>
+struct Tile {
+  static constexpr int TP = HD >= 256 ? 32 : (HD >= 128 ? 64 : 128);  // positions per tile
+  static constexpr int kBytesKV = TP * HD * 2;                          // one of K or V
+  static constexpr int kStageBytes = 2 * kBytesKV;
+};
+
+// Shared memory a work item uses besides its tiles (floats unless noted).
+template <int HD, int G>
+struct Work {
+  static constexpr int NP = HD / 2;          // dim pairs
+  static constexpr int NG = kCT / NP;        // position groups in P V
+  static constexpr int TP = Tile<HD>::TP;
+  static constexpr size_t q = (size_t)G * HD * 4;
+  static constexpr size_t sc = (size_t)G * TP * 4;
+  static constexpr size_t ored = (size_t)NG * G * HD * 4;
+  static constexpr size_t kvnew = 2 * HD * 2;
+  static constexpr size_t small = 3 * G * 4 + 16;  // m, l, corr, last
+  static constexpr size_t total = q + sc + ored + kvnew + small;
+};
+
+template <int HD, int G>
+struct WorkPtrs {
+  float* q_s;
+  float* sc;
+  float* ored;
+  uint16_t* kn;
+  uint16_t* vn;
+  float* m;
+  float* l;
+  float* corr;
+  int* last;
+  __device__ __forceinline__ void carve(uint8_t* base) {
+    using W = Work<HD, G>;
+    q_s = reinterpret_cast<float*>(base);
+    sc = reinterpret_cast<float*>(base + W::q);
+    ored = reinterpret_cast<float*>(base + W::q + W::sc);
+    kn = reinterpret_cast<uint16_t*>(base + W::q + W::sc + W::ored);
+    vn = kn + HD;
+    m = reinterpret_cast<float*>(base + W::q + W::sc + W::ored + W::kvnew);
+    l = m + G;
+    corr = l + G;
+    last = reinterpret_cast<int*>(corr + G);
+  }
+};
+
+struct Item {
+  int p0, p1, pc1, ntiles;
+  bool has_new;
+};
+
+template <int HD>
+__device__ __forceinline__ Item item_of(const Params& p, int T, int sp) {
+  Item it;
+  const long long L = (long long)T + 1;
+  it.p0 = (int)((long long)sp * L / p.nsplit);
+  it.p1 = (int)((long long)(sp + 1) * L / p.nsplit);
+  it.pc1 = it.p1 < T ? it.p1 : T;  // cached rows [p0, pc1)
+  const int nc = it.pc1 > it.p0 ? it.pc1 - it.p0 : 0;
+  it.ntiles = (nc + Tile<HD>::TP - 1) / Tile<HD>::TP;
+  it.has_new = (T >= it.p0 && T < it.p1);
+  return it;
+}
+
+// Copy lane: K and V rows of tile t of the item into dst (K at 0, V at kBytesKV).
+template <int HD>
+__device__ __forceinline__ void issue_tile(const Params& p, int g, const Item& it, int t, uint8_t* dst, uint64_t* bar,
+                                           uint64_t pol) {
+  constexpr int TP = Tile<HD>::TP;
+  const int r0 = it.p0 + t * TP;
+  const int rows = (it.pc1 - r0) < TP ? (it.pc1 - r0) : TP;
+  const uint32_t bytes = (uint32_t)rows * HD * 2;
+  mbar_arrive_expect_tx(bar, 2 * bytes);
+  bulk_g2s(dst, p.K + ((long long)g * p.cap + r0) * HD, bytes, bar, pol);
+  bulk_g2s(dst + Tile<HD>::kBytesKV, p.V + ((long long)g * p.cap + r0) * HD, bytes, bar, pol);
+}
+
+template <int HD>
+__device__ __forceinline__ int tile_rows(const Item& it, int t) {
+  const int r0 = it.p0 + t * Tile<HD>::TP;
+  return (it.pc1 - r0) < Tile<HD>::TP ? (it.pc1 - r0) : Tile<HD>::TP;
+}
+
+// Per-thread state of a work item.
+template <int HD, int G>
+struct Acc {
+  float qr[G][8];   // query slice: 8 dims per lane
+  float acc[G][2];  // P V: two output dims per thread
+};
+
+// Compute threads: rotated, scaled queries; the new row (rotated k and v in
+// bf16, also appended to the cache) when the item holds position T.
+template <int HD, int G>
+__device__ __forceinline__ void begin_item(const Params& p, int g, int T, const Item& it, const WorkPtrs<HD, G>& w,
+                                           Acc<HD, G>& A, int ctid) {
+  const int lane = ctid & 31;
+  const float2* rope = p.rope + (long long)T * (HD / 2);
+  for (int e = ctid; e < G * (HD / 2); e += kCT) {
+    const int j = e / (HD / 2), i = e % (HD / 2);
+    const float* qh = p.y + (long long)(g * G + j) * HD;
+    const float2 cs = rope[i];
+    const float a = qh[i], b = qh[i + HD / 2];
+    w.q_s[j * HD + i] = (a * cs.x - b * cs.y) * p.scale;
+    w.q_s[j * HD + i + HD / 2] = (b * cs.x + a * cs.y) * p.scale;
+  }
+  if (it.has_new) {
+    const float* kh = p.y + (long long)(p.nq + g) * HD;
+    const float* vh = p.y + (long long)(p.nq + p.nkv + g) * HD;
+    uint16_t* Kw = p.K + ((long long)g * p.cap + T) * HD;
+    uint16_t* Vw = p.V + ((long long)g * p.cap + T) * HD;
+    for (int i = ctid; i < HD / 2; i += kCT) {
+      const float2 cs = rope[i];
+      const float a = kh[i], b = kh[i + HD / 2];
+      const uint16_t k0 = f32_to_bf16_rne(a * cs.x - b * cs.y), k1 = f32_to_bf16_rne(b * cs.x + a * cs.y);
+      w.kn[i] = k0;
+      w.kn[i + HD / 2] = k1;
+      Kw[i] = k0;
+      Kw[i + HD / 2] = k1;
+    }
+    for (int i = ctid; i < HD; i += kCT) {
+      const uint16_t v = f32_to_bf16_rne(vh[i]);
+      w.vn[i] = v;
+      Vw[i] = v;
+    }
+  }
+  if (ctid < G) {
+    w.m[ctid] = -INFINITY;
+    w.l[ctid] = 0.f;
+  }
+  named_barrier(1, kCT);
+  constexpr int LPR = HD / 8;
+  const int li = lane % LPR;
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) A.qr[j][e] = w.q_s[j * HD + li * 8 + e];
+    A.acc[j][0] = A.acc[j][1] = 0.f;
+  }
+}
+
+// One tile of rows: scores -> online softmax (one warp per head) -> P V.
+template <int HD, int G>
+__device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t* tv, int rows,
+                                             const WorkPtrs<HD, G>& w, Acc<HD, G>& A, int ctid) {
+  using W = Work<HD, G>;
+  constexpr int TP = W::TP;
+  constexpr int LPR = HD / 8, RPW = 32 / LPR;
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int sub = lane / LPR, li = lane % LPR;
+  for (int base = warp * RPW; base < rows; base += kCWarps * RPW) {
+    const int row = base + sub;
+    float d[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) d[j] = 0.f;
+    if (row < rows) {
+      const uint4 kv = *reinterpret_cast<const uint4*>(tk + row * HD + li * 8);
+#pragma unroll
+      for (int j = 0; j < G; ++j) d[j] = dot8(kv, A.qr[j]);
+    }
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1)
+#pragma unroll
+      for (int j = 0; j < G; ++j) d[j] += __shfl_xor_sync(0xffffffffu, d[j], o);
+    if (li == 0 && row < rows)
+#pragma unroll
+      for (int j = 0; j < G; ++j) w.sc[j * TP + row] = d[j];
+  }
+  named_barrier(1, kCT);
+  if (warp < G) {
+    const int j = warp;
+    float mx = -INFINITY;
+    for (int r = lane; r < rows; r += 32) mx = fmaxf(mx, w.sc[j * TP + r]);
+    mx = warp_max(mx);
+    const float m_old = w.m[j];
+    const float m_new = fmaxf(m_old, mx);
+    float sum = 0.f;
+    for (int r = lane; r < rows; r += 32) {
+      const float e = __expf(w.sc[j * TP + r] - m_new);
+      w.sc[j * TP + r] = e;
+      sum += e;
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) {
+      const float corr = (m_old == -INFINITY) ? 0.f : __expf(m_old - m_new);
+      w.corr[j] = corr;
+      w.l[j] = w.l[j] * corr + sum;
+      w.m[j] = m_new;
+    }
+  }
+  named_barrier(1, kCT);
+  const int pg = ctid / W::NP, dp = ctid % W::NP;
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const float c = w.corr[j];
+    A.acc[j][0] *= c;
+    A.acc[j][1] *= c;
+  }
+  const uint32_t* tv32 = reinterpret_cast<const uint32_t*>(tv);
+  for (int r = pg; r < rows; r += W::NG) {
+    const uint32_t v2 = tv32[r * W::NP + dp];
+    const float vx = bf16_lo(v2), vy = bf16_hi(v2);
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const float pj = w.sc[j * TP + r];
+      A.acc[j][0] = fmaf(pj, vx, A.acc[j][0]);
+      A.acc[j][1] = fmaf(pj, vy, A.acc[j][1]);
+    }
+  }
+  named_barrier(1, kCT);
+}
+
+// Partials of the item, then (last item of kv head g only) the merge.
+// scratch: >= nsplit * G + G floats of shared memory that no tile uses.
+template <int HD, int G>
+__device__ __forceinline__ void end_item(const Params& p, int g, int sp, const WorkPtrs<HD, G>& w, Acc<HD, G>& A,
+                                         float* scratch, int ctid) {
+  using W = Work<HD, G>;
+  const int pg = ctid / W::NP, dp = ctid % W::NP;
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    w.ored[(pg * G + j) * HD + 2 * dp] = A.acc[j][0];
+    w.ored[(pg * G + j) * HD + 2 * dp + 1] = A.acc[j][1];
+  }
+  named_barrier(1, kCT);
+  float* part = p.part + ((long long)g * p.nsplit + sp) * G * (HD + 2);
+  for (int e = ctid; e < G * HD; e += kCT) {
+    const int j = e / HD, d = e % HD;
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < W::NG; ++q) v += w.ored[(q * G + j) * HD + d];
+    part[j * (HD + 2) + d] = v;
+  }
+  if (ctid < G) {
+    part[ctid * (HD + 2) + HD] = w.m[ctid];
+    part[ctid * (HD + 2) + HD + 1] = w.l[ctid];
+  }
+  named_barrier(1, kCT);
+  if (ctid == 0) {
+    __threadfence();
+    const unsigned ticket = atomicAdd(p.counter + g, 1u);
+    *w.last = (ticket == (unsigned)(p.nsplit - 1));
+  }
+  named_barrier(1, kCT);
+  if (!*w.last) return;
+  __threadfence();
+  // merge: split weights first (all loads in flight together), then each
+  // thread merges its (head, dim) outputs with batches of independent loads
+  const float* pg0 = p.part + (long long)g * p.nsplit * G * (HD + 2);
+  float* s_w = scratch;                  // [nsplit][G]: m_s, then e^{m_s - M}
+  float* s_den = scratch + p.nsplit * G; // [G]
+  float* s_l = w.ored;                   // [nsplit][G]
+  for (int e = ctid; e < p.nsplit * G; e += kCT) {
+    const float* ps = pg0 + (long long)e * (HD + 2);
+    s_w[e] = __ldcg(ps + HD);
+    s_l[e] = __ldcg(ps + HD + 1);
+  }
+  named_barrier(1, kCT);
+  if (ctid < G) {
+    const int j = ctid;
+    float M = -INFINITY;
+    for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, s_w[s * G + j]);
+    float den = 0.f;
+    for (int s = 0; s < p.nsplit; ++s) {
+      const float l = s_l[s * G + j];
+      const float wt = (l > 0.f) ? __expf(s_w[s * G + j] - M) : 0.f;
+      s_w[s * G + j] = wt;
+      den = fmaf(wt, l, den);
+    }
+    s_den[j] = den;
+  }
+  named_barrier(1, kCT);
+  for (int e = ctid; e < G * HD; e += kCT) {
+    const int j = e / HD, d = e % HD;
+    float num = 0.f;
+    for (int s0 = 0; s0 < p.nsplit; s0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = (s0 + u < p.nsplit) ? __ldcg(pg0 + ((long long)(s0 + u) * G + j) * (HD + 2) + d) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (s0 + u < p.nsplit) num = fmaf(s_w[(s0 + u) * G + j], v[u], num);
+    }
+    p.o[(long long)(g * G + j) * HD + d] = num / s_den[j];
+  }
+  if (ctid == 0) p.counter[g] = 0u;
+  named_barrier(1, kCT);
+}
+
+}  // namespace attn
+}  // namespace hy
