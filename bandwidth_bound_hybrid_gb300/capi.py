@@ -28,6 +28,8 @@ HY_FLAG_DEBUG = 1
 HY_FLAG_NO_GRAPH = 2
 HY_FLAG_NO_PDL = 4
 
+HY_NOALLOC_SCRATCH_BYTES = 1 << 20
+
 i32, u32, u64, f32, vp, sz = ctypes.c_int32, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 P = ctypes.POINTER
 
@@ -79,6 +81,7 @@ SIGNATURES = {
     "hy_op_rope_table": (ctypes.c_int, [vp, i32, i32, f32, vp]),
     "hy_op_attention_workspace": (sz, [i32, i32, i32, i32]),
     "hy_op_attention": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, i32, vp, vp, vp]),
+    "hy_op_attention_noalloc": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, i32, vp, vp]),
 }
 
 _lib = None

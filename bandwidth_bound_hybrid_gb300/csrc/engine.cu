@@ -72,6 +72,8 @@ __global__ void k_copy_f32(const float* __restrict__ src, float* __restrict__ ds
 
 }  // namespace
 
+int hy::set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 // ====================================================================== model
 
 struct hy_model {

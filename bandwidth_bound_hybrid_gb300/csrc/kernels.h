@@ -117,6 +117,10 @@ cudaError_t launch(const Params& p, cudaStream_t st, bool pdl);
 cudaError_t rope_table(float2* tab, int cap, int hd, double theta, cudaStream_t st);
 }  // namespace attn
 
+// Record `msg` as the calling thread's last error (hy_last_error) and return
+// `code`; for C-ABI entry points defined outside engine.cu.
+int set_error(int code, const char* msg);
+
 // Launch with the programmatic-stream-serialization attribute when pdl is set.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,

@@ -232,6 +232,34 @@ int hy_op_attention(const float* y_dev, void* K_dev, void* V_dev, int32_t cap, i
                     const int32_t* len_dev, const float* rope_table_dev, int32_t nsplit, float* o_dev,
                     void* workspace_dev, void* stream);
 
+/* hy_op_attention without a caller-provided workspace, for callers that
+ * cannot allocate device memory: a host framework that owns the whole memory
+ * budget through its own pool, a latency path where an allocation and the
+ * synchronisation it implies are not allowed, or a plug-in whose host forbids
+ * allocations outside its allocator.  The pages have no counterpart of this
+ * call; it exists only for such callers.
+ *
+ * Same arguments, layout and results as hy_op_attention; the scratch (guard
+ * word, per-kv-head tickets, per-split partials) lives instead in one fixed
+ * device array of HY_NOALLOC_SCRATCH_BYTES that every GPU loading this
+ * library holds until the process exits.  The call makes no allocation: it
+ * clears the guard word and the tickets on `stream`, then launches.
+ *   - Returns HY_ERR_UNSUPPORTED, launching nothing, when the scratch this
+ *     shape needs (hy_op_attention_workspace(nq, nkv, hd, nsplit) bytes, with
+ *     nsplit = 0 resolved as hy_op_attention resolves it) exceeds
+ *     HY_NOALLOC_SCRATCH_BYTES.
+ *   - The first call on a device (the current one) sets up that device: it
+ *     looks up the array's device address and the kernels' shared-memory
+ *     limits.  Make that first call before any stream capture begins.
+ *   - Every call on a device uses the same array, which keeps what the last
+ *     call left: calls that can overlap on the GPU (other streams, other host
+ *     threads without ordering between them) race and corrupt each other's
+ *     results.  Order them on one stream or otherwise serialise them. */
+#define HY_NOALLOC_SCRATCH_BYTES (1u << 20)
+int hy_op_attention_noalloc(const float* y_dev, void* K_dev, void* V_dev, int32_t cap, int32_t nq, int32_t nkv,
+                            int32_t hd, const int32_t* len_dev, const float* rope_table_dev, int32_t nsplit,
+                            float* o_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
