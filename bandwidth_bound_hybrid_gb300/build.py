@@ -21,6 +21,12 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "--extended-lambda"]
 
 
+def _extra_flags() -> list[str]:
+    """Additional nvcc flags from HY_NVCC_EXTRA (e.g. tuning macros); a change
+    of them rebuilds every object."""
+    return os.environ.get("HY_NVCC_EXTRA", "").split()
+
+
 def _deps() -> list[str]:
     return [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "hybrid.h")]
 
@@ -36,7 +42,7 @@ def _compile(src: str) -> str:
     obj = os.path.join(OUT, os.path.splitext(src)[0] + ".o")
     path = os.path.join(CSRC, src)
     if _stale(obj, [path] + _deps()):
-        cmd = ["nvcc", *ARCH, *FLAGS, "-I", os.path.join(ROOT, "include"), "-c", path, "-o", obj]
+        cmd = ["nvcc", *ARCH, *FLAGS, *_extra_flags(), "-I", os.path.join(ROOT, "include"), "-c", path, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -45,6 +51,12 @@ def _compile(src: str) -> str:
 
 def build(force: bool = False) -> str:
     os.makedirs(OUT, exist_ok=True)
+    stamp = os.path.join(OUT, "flags.txt")
+    flags = " ".join(_extra_flags())
+    if not os.path.exists(stamp) or open(stamp).read() != flags:
+        force = True
+        with open(stamp, "w") as f:
+            f.write(flags)
     if force:
         for s in SOURCES:
             o = os.path.join(OUT, os.path.splitext(s)[0] + ".o")

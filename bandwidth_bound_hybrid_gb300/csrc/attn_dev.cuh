@@ -1,6 +1,4 @@
-// Device building blocks of split-KV GQA decode attention, shared by the
-// standalone attention kernel (attn.cu) and the persistent decode-step kernel
-// (step.cu).
+// Device building blocks of split-KV GQA decode attention (kernel in attn.cu).
 //
 // One work item (g, s) = kv head g, split s: positions [s L / S, (s+1) L / S)
 // of the L = T + 1 keys.  Its cached K/V rows arrive as shared-memory tiles
@@ -293,19 +291,38 @@ __device__ __forceinline__ void end_item(const Params& p, int g, int sp, const W
     s_den[j] = den;
   }
   named_barrier(1, kCT);
-  for (int e = ctid; e < G * HD; e += kCT) {
-    const int j = e / HD, d = e % HD;
-    float num = 0.f;
-    for (int s0 = 0; s0 < p.nsplit; s0 += 8) {
-      float v[8];
+  // each thread merges its NE (head, dim) outputs; every load of a batch of
+  // eight splits is in flight at once
+  constexpr int NE = (G * HD + kCT - 1) / kCT;
+  float num[NE];
+#pragma unroll
+  for (int q = 0; q < NE; ++q) num[q] = 0.f;
+  for (int s0 = 0; s0 < p.nsplit; s0 += 8) {
+    float v[NE][8];
+#pragma unroll
+    for (int q = 0; q < NE; ++q) {
+      const int e = ctid + q * kCT;
+      const int j = e / HD, d = e % HD;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        v[u] = (s0 + u < p.nsplit) ? __ldcg(pg0 + ((long long)(s0 + u) * G + j) * (HD + 2) + d) : 0.f;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (s0 + u < p.nsplit) num = fmaf(s_w[(s0 + u) * G + j], v[u], num);
+        v[q][u] = (e < G * HD && s0 + u < p.nsplit) ? __ldcg(pg0 + ((long long)(s0 + u) * G + j) * (HD + 2) + d) : 0.f;
     }
-    p.o[(long long)(g * G + j) * HD + d] = num / s_den[j];
+#pragma unroll
+    for (int q = 0; q < NE; ++q) {
+      const int e = ctid + q * kCT;
+      const int j = (e < G * HD) ? e / HD : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (s0 + u < p.nsplit) num[q] = fmaf(s_w[(s0 + u) * G + j], v[q][u], num[q]);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < NE; ++q) {
+    const int e = ctid + q * kCT;
+    if (e < G * HD) {
+      const int j = e / HD, d = e % HD;
+      p.o[(long long)(g * G + j) * HD + d] = num[q] / s_den[j];
+    }
   }
   if (ctid == 0) p.counter[g] = 0u;
   named_barrier(1, kCT);

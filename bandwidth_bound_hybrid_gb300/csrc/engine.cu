@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -133,13 +134,84 @@ uint16_t* kv_cache(hy_cache* c, int seq, int ai, int which) {
   return reinterpret_cast<uint16_t*>(c->mem[seq] + c->off_kv[seq]) + ((size_t)ai * 2 + which) * per;
 }
 
+// One kernel of the decode step, recorded before any is launched so that each
+// GEMV can be told what the kernels after it read first.
+struct StepOp {
+  enum Kind { kGemv, kGdn, kAttn, kCopy } kind;
+  gemv::Params g;
+  int src, in, epi;
+  const char* what;
+  gdn::Params d;
+  attn::Params a;
+  const float* csrc;
+  float* cdst;
+  int cn;
+};
+
+// Bytes of each of the next GEMV's CTA row ranges that the CTAs of the GEMV
+// before it prefetch into L2 once their own rows are in flight.
+int next_prefetch_bytes() {
+  const char* v = getenv("HY_GEMV_NEXT_KB");
+  return (v && *v) ? atoi(v) * 1024 : 128 * 1024;
+}
+
+// Prefetch spans of GEMV op i: the first rows of the next dense-source GEMV
+// (wrapping to the start of the step: the graph replays it per token) and the
+// recurrent state of a Gated DeltaNet kernel that directly follows.
+void plan_prefetch(std::vector<StepOp>& ops, size_t i, int nsm) {
+  gemv::Params& g = ops[i].g;
+  g.n_nx = 0;
+  const int nb = next_prefetch_bytes();
+  if (nb <= 0) return;
+  const int my_ncta = gemv::plan(g.R, g.C, ops[i].epi == gemv::kEpiSwiglu ? 2 : 1, nsm, g.norm_g != nullptr).ncta;
+  if (i + 1 < ops.size() && ops[i + 1].kind == StepOp::kGdn) {
+    const gdn::Params& d = ops[i + 1].d;
+    g.nx[g.n_nx++] = gemv::PfSpan{(const uint8_t*)d.S, d.nh * d.dv, d.dk * 4, my_ncta, 1 << 30};
+  }
+  for (size_t k = 1; k <= ops.size(); ++k) {
+    const StepOp& o = ops[(i + k) % ops.size()];
+    if (o.kind != StepOp::kGemv) continue;
+    if (o.src != gemv::kSrcDense) break;  // expert rows are known only after the router
+    const int npair = o.epi == gemv::kEpiSwiglu ? 2 : 1;
+    const gemv::Plan pl = gemv::plan(o.g.R, o.g.C, npair, nsm, o.g.norm_g != nullptr);
+    for (int j = 0; j < npair && g.n_nx < gemv::kMaxPfSpans; ++j)
+      g.nx[g.n_nx++] = gemv::PfSpan{o.g.W[j], o.g.R, o.g.C * 2, pl.ncta, nb};
+    break;
+  }
+}
+
+int launch_ops(hy_model* m, std::vector<StepOp>& ops, cudaStream_t st) {
+  const bool pdl = m->pdl;
+  for (size_t i = 0; i < ops.size(); ++i) {
+    StepOp& o = ops[i];
+    cudaError_t e = cudaSuccess;
+    if (o.kind == StepOp::kGemv) {
+      plan_prefetch(ops, i, m->nsm);
+      const int npair = (o.epi == gemv::kEpiSwiglu) ? 2 : 1;
+      const gemv::Plan pl = gemv::plan(o.g.R, o.g.C, npair, m->nsm, o.g.norm_g != nullptr);
+      if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no GEMV plan for %s (%d x %d)", o.what, o.g.R, o.g.C);
+      e = gemv::launch(o.g, pl, o.src, o.in, o.epi, st, pdl);
+    } else if (o.kind == StepOp::kGdn) {
+      e = gdn::launch(o.d, st, pdl);
+    } else if (o.kind == StepOp::kAttn) {
+      e = attn::launch(o.a, st, pdl);
+    } else {
+      e = launch_k(k_copy_f32, dim3((o.cn + 255) / 256), dim3(256), 0, st, pdl, o.csrc, o.cdst, o.cn);
+    }
+    if (e != cudaSuccess) return fail(HY_ERR_CUDA, "%s launch: %s", o.kind == StepOp::kGemv ? o.what : "kernel",
+                                      cudaGetErrorString(e));
+  }
+  return HY_OK;
+}
+
 // Issue every kernel of one decode step for sequence `seq` on `st`.
 int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) {
   hy_model* m = c->m;
   const hy_config& cf = m->cfg;
   const int H = cf.hidden;
-  const bool pdl = m->pdl;
   int* pos = c->d_len + seq;
+  std::vector<StepOp> ops;
+  ops.reserve(8 * cf.n_layers + 2);
 
   auto gemv_base = [&]() {
     gemv::Params p;
@@ -149,11 +221,15 @@ int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) 
     return p;
   };
   auto run = [&](gemv::Params& p, int src, int in, int epi, const char* what) -> int {
-    const int npair = (epi == gemv::kEpiSwiglu) ? 2 : 1;
-    const gemv::Plan pl = gemv::plan(p.R, p.C, npair, m->nsm);
-    if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no GEMV plan for %s (%d x %d)", what, p.R, p.C);
-    cudaError_t e = gemv::launch(p, pl, src, in, epi, st, pdl);
-    if (e != cudaSuccess) return fail(HY_ERR_CUDA, "GEMV %s launch: %s", what, cudaGetErrorString(e));
+    StepOp o;
+    memset(&o, 0, sizeof(o));
+    o.kind = StepOp::kGemv;
+    o.g = p;
+    o.src = src;
+    o.in = in;
+    o.epi = epi;
+    o.what = what;
+    ops.push_back(o);
     return HY_OK;
   };
 
@@ -197,8 +273,11 @@ int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) 
       a.counter = c->cnt_attn;
       a.o = c->o;
       a.guard = c->guard;
-      cudaError_t e = attn::launch(a, st, pdl);
-      if (e != cudaSuccess) return fail(HY_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+      StepOp o;
+      memset(&o, 0, sizeof(o));
+      o.kind = StepOp::kAttn;
+      o.a = a;
+      ops.push_back(o);
     } else {
       gdn::Params g;
       memset(&g, 0, sizeof(g));
@@ -213,8 +292,11 @@ int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) 
       g.conv_k = cf.conv_k;
       g.pos = pos;
       g.guard = c->guard;
-      cudaError_t e = gdn::launch(g, st, pdl);
-      if (e != cudaSuccess) return fail(HY_ERR_CUDA, "GDN launch: %s", cudaGetErrorString(e));
+      StepOp o;
+      memset(&o, 0, sizeof(o));
+      o.kind = StepOp::kGdn;
+      o.d = g;
+      ops.push_back(o);
     }
     {  // output projection + residual
       gemv::Params p = gemv_base();
@@ -294,9 +376,13 @@ int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) 
       if ((rc = run(dn, gemv::kSrcExpertSegs, gemv::kInMoeZ, gemv::kEpiResid, "expert down")) != HY_OK) return rc;
     }
     if (m->debug) {
-      cudaError_t e = launch_k(k_copy_f32, dim3((H + 255) / 256), dim3(256), 0, st, pdl, (const float*)c->x,
-                               c->dbg_hidden + (size_t)l * H, H);
-      if (e != cudaSuccess) return fail(HY_ERR_CUDA, "debug copy: %s", cudaGetErrorString(e));
+      StepOp o;
+      memset(&o, 0, sizeof(o));
+      o.kind = StepOp::kCopy;
+      o.csrc = c->x;
+      o.cdst = c->dbg_hidden + (size_t)l * H;
+      o.cn = H;
+      ops.push_back(o);
     }
   }
   {  // final RMSNorm + LM head + argmax; the last CTA advances the position
@@ -315,7 +401,7 @@ int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) 
     int rc = run(p, gemv::kSrcDense, gemv::kInX, gemv::kEpiArgmax, "lm-head");
     if (rc != HY_OK) return rc;
   }
-  return HY_OK;
+  return launch_ops(m, ops, st);
 }
 
 int get_graph(hy_cache* c, int seq, float* logits, int* ids, cudaGraphExec_t* out) {
@@ -533,7 +619,7 @@ int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, 
       (rc = dalloc(c, &c->y, m->y_len)) || (rc = dalloc(c, &c->o, std::max(m->o_len, 1))) ||
       (rc = dalloc(c, &c->h, std::max(m->h_len, 1))) || (rc = dalloc(c, &c->part, part)) ||
       (rc = dalloc(c, &c->am_val, 1024)) || (rc = dalloc(c, &c->am_idx, 1024)) ||
-      (rc = dalloc(c, &c->rlog, std::max(cf.n_experts + 1, 1))) || (rc = dalloc(c, &c->moe_w, 17)) ||
+      (rc = dalloc(c, &c->rlog, std::max(cf.n_experts + 1, 1))) || (rc = dalloc(c, &c->moe_w, gemv::kMaxTopK + 4)) ||
       (rc = dalloc(c, &c->moe_ids, 16)) || (rc = dalloc(c, &c->tok, max_seqs)) || (rc = dalloc(c, &c->ids, max_seqs)) ||
       (rc = dalloc(c, &c->cnt_attn, std::max(cf.attn_kv_heads, 1))) || (rc = dalloc(c, &c->cnt_am, 1)) ||
       (rc = dalloc(c, &c->cnt_router, 1)) || (rc = dalloc(c, &c->guard, 1)) ||
@@ -713,7 +799,7 @@ static int op_gemv_run(gemv::Params& p, int in, int epi, void* stream) {
   int rc = op_guard(&guard);
   if (rc != HY_OK) return rc;
   p.guard = guard;
-  const gemv::Plan pl = gemv::plan(p.R, p.C, epi == gemv::kEpiSwiglu ? 2 : 1, op_nsm());
+  const gemv::Plan pl = gemv::plan(p.R, p.C, epi == gemv::kEpiSwiglu ? 2 : 1, op_nsm(), p.norm_g != nullptr);
   if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no GEMV plan for %d x %d", p.R, p.C);
   cudaError_t e = gemv::launch(p, pl, gemv::kSrcDense, in, epi, (cudaStream_t)stream, false);
   if (e != cudaSuccess) return fail(HY_ERR_CUDA, "GEMV launch: %s", cudaGetErrorString(e));

@@ -2,9 +2,10 @@
 // math and its sources are in gdn_dev.cuh).
 //
 // Grid: (heads, dv / 16); a CTA is one work item: 16 value rows of one head
-// (4 warps x 4 rows).  The state rows are loaded before griddepcontrol.wait:
-// no earlier kernel of the same step writes them, so their HBM latency
-// overlaps the projection GEMV's tail.
+// (4 warps x 4 rows).  The state rows, the conv taps and the conv history are
+// loaded before griddepcontrol.wait: no earlier kernel of the same step writes
+// them, so their latency overlaps the projection GEMV's tail and only the
+// projection output is read after the wait.
 #include "common.cuh"
 #include "gdn_dev.cuh"
 #include "kernels.h"
@@ -14,23 +15,24 @@ namespace gdn {
 namespace {
 
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxK = 8;
 
 template <int EPL>  // state elements per lane: dk / 32
 __global__ void __launch_bounds__(kThreads) k_gdn(const Params p) {
   __shared__ ItemShared<EPL> sh;
   const int h = blockIdx.x, rc = blockIdx.y;
   Rows<EPL, kWarps> R;
+  ConvRegs<EPL, kWarps> V;
   load_rows<EPL, kWarps>(p, h, rc, R, threadIdx.x);  // pre-wait
+  load_conv<EPL, kWarps>(p, h, rc, V, threadIdx.x);  // pre-wait
   pdl_wait();
   pdl_launch_dependents();
-  run_item<EPL, kWarps>(p, h, rc, R, sh, threadIdx.x, [] __device__() { __syncthreads(); });
+  run_item<EPL, kWarps>(p, h, rc, R, V, sh, threadIdx.x, [] __device__() { __syncthreads(); });
 }
 
 }  // namespace
 
 cudaError_t launch(const Params& p, cudaStream_t st, bool pdl) {
-  if (p.dk % 32 != 0 || p.conv_k < 1 || p.conv_k > kMaxK) return cudaErrorInvalidValue;
+  if (p.dk % 32 != 0 || p.conv_k < 1 || p.conv_k > kMaxConvK) return cudaErrorInvalidValue;
   const dim3 grid(p.nh, (p.dv + kRowsPerCta - 1) / kRowsPerCta);
   switch (p.dk / 32) {
     case 2: return launch_k(k_gdn<2>, grid, dim3(kThreads), 0, st, pdl, p);

@@ -1,5 +1,4 @@
-// Device building block of the Gated DeltaNet decode step, shared by the
-// standalone kernel (gdn.cu) and the persistent decode-step kernel (step.cu).
+// Device building block of the Gated DeltaNet decode step (kernel in gdn.cu).
 //
 // One work item = 16 value rows of one head h (row chunk rc):
 //   causal depthwise conv (width conv_k) + SiLU over q_h, k_h and this item's
@@ -41,6 +40,55 @@ struct Rows {
   float* ptr[RPW];
 };
 
+// The part of this thread's conv outputs that does not depend on the
+// projection output: the taps applied to the conv_k - 1 previous inputs from
+// the ring, and the tap of the new input.  Computed before
+// griddepcontrol.wait (no kernel of the current step writes the ring or the
+// position before this one).
+constexpr int kMaxConvK = 8;
+template <int EPL, int NW>
+struct ConvRegs {
+  static constexpr int NCH = (2 * EPL * 32 + kRowsPerCta + NW * 32 - 1) / (NW * 32);  // channels per thread
+  float part[NCH];  // sum over the previous inputs
+  float last[NCH];  // tap of the new input
+  int ch[NCH];      // -1: no channel
+  int t;
+};
+
+template <int EPL, int NW>
+__device__ __forceinline__ void load_conv(const Params& p, int h, int rc, ConvRegs<EPL, NW>& V, int tid) {
+  constexpr int NCH = ConvRegs<EPL, NW>::NCH;
+  constexpr int NT = NW * 32;
+  constexpr int dk = EPL * 32;
+  const int nh = p.nh, dv = p.dv, K = p.conv_k;
+  const int CC = 2 * nh * dk + nh * dv;
+  const int t = *p.pos;
+  V.t = t;
+#pragma unroll
+  for (int q = 0; q < NCH; ++q) {
+    const int c = tid + q * NT;
+    int ch = -1;
+    if (c < 2 * dk) {
+      ch = (c < dk) ? h * dk + c : nh * dk + h * dk + (c - dk);
+    } else if (c < 2 * dk + kRowsPerCta) {
+      const int i = rc * kRowsPerCta + (c - 2 * dk);
+      if (i < dv) ch = 2 * nh * dk + h * dv + i;
+    }
+    V.ch[q] = ch;
+    float acc = 0.f, last = 0.f;
+    if (ch >= 0) {
+      for (int j = 0; j < K - 1; ++j) {
+        const int slot = (t - (K - 1) + j) % K;
+        acc = fmaf(bf16_to_f32(p.conv_w[(long long)ch * K + j]),
+                   p.conv_state[(long long)(slot < 0 ? slot + K : slot) * CC + ch], acc);
+      }
+      last = bf16_to_f32(p.conv_w[(long long)ch * K + K - 1]);
+    }
+    V.part[q] = acc;
+    V.last[q] = last;
+  }
+}
+
 template <int EPL, int NW>
 __device__ __forceinline__ void load_rows(const Params& p, int h, int rc, Rows<EPL, NW>& R, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
@@ -66,40 +114,34 @@ __device__ __forceinline__ void load_rows(const Params& p, int h, int rc, Rows<E
 }
 
 template <int EPL, int NW, typename Sync>
-__device__ __forceinline__ void run_item(const Params& p, int h, int rc, Rows<EPL, NW>& R, ItemShared<EPL>& sh,
-                                         int tid, Sync sync) {
+__device__ __forceinline__ void run_item(const Params& p, int h, int rc, Rows<EPL, NW>& R,
+                                         const ConvRegs<EPL, NW>& V, ItemShared<EPL>& sh, int tid, Sync sync) {
+  constexpr int kChanPerThread = ConvRegs<EPL, NW>::NCH;
   constexpr int NT = NW * 32;
   constexpr int RPW = Rows<EPL, NW>::RPW;
   constexpr int dk = EPL * 32;
   const int warp = tid >> 5, lane = tid & 31;
   const int nh = p.nh, dv = p.dv, K = p.conv_k;
   const int CC = 2 * nh * dk + nh * dv;
-  const int t = *p.pos;
-  // conv + SiLU over this item's channels: q and k of head h, its v rows
+  const int t = V.t;
+  // conv + SiLU over this item's channels (q and k of head h, its v rows):
+  // only the new input comes from the projection output
   const int nqk = 2 * dk;
-  for (int c = tid; c < nqk + kRowsPerCta; c += NT) {
-    int ch;
-    if (c < nqk) {
-      ch = (c < dk) ? h * dk + c : nh * dk + h * dk + (c - dk);
-    } else {
-      const int i = rc * kRowsPerCta + (c - nqk);
-      if (i >= dv) continue;
-      ch = 2 * nh * dk + h * dv + i;
-    }
-    const float u = p.y[ch];
-    float acc = 0.f;
-    for (int j = 0; j < K - 1; ++j) {
-      const int slot = (t - (K - 1) + j) % K;
-      const int sl = slot < 0 ? slot + K : slot;
-      acc = fmaf(bf16_to_f32(p.conv_w[(long long)ch * K + j]), p.conv_state[(long long)sl * CC + ch], acc);
-    }
-    acc = fmaf(bf16_to_f32(p.conv_w[(long long)ch * K + (K - 1)]), u, acc);
+  float u[kChanPerThread];
+#pragma unroll
+  for (int q = 0; q < kChanPerThread; ++q) u[q] = V.ch[q] >= 0 ? p.y[V.ch[q]] : 0.f;
+#pragma unroll
+  for (int q = 0; q < kChanPerThread; ++q) {
+    const int ch = V.ch[q];
+    if (ch < 0) continue;
+    const int c = tid + q * NT;
+    const float acc = fmaf(V.last[q], u[q], V.part[q]);
     const float cv = siluf_(acc);
     if (c < dk) sh.q[c] = cv;
     else if (c < nqk) sh.k[c - dk] = cv;
     else sh.v[c - nqk] = cv;
     // ring write of the new input: q/k channels by row chunk 0 only
-    if (c >= nqk || rc == 0) p.conv_state[(long long)(t % K) * CC + ch] = u;
+    if (c >= nqk || rc == 0) p.conv_state[(long long)(t % K) * CC + ch] = u[q];
   }
   sync();
   float sq = 0.f, sk = 0.f;

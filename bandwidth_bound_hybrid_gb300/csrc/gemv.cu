@@ -4,13 +4,15 @@
 // whole cost ("Beating llama.cpp from Scratch on Consumer AMD", Act 0, pass 3
 // and Act 6: weight GEMV kernels take 88.85% of the 4B decode time).  Design:
 //   * persistent grid, one CTA per SM, each owning a contiguous row range;
-//   * one copy warp streams row tiles HBM -> shared memory with bulk copies on
-//     the TMA engine (cp.async.bulk, L2 evict-first), ~96 KB deep, completion
+//   * one copy lane streams row tiles HBM -> shared memory with bulk copies on
+//     the TMA engine (cp.async.bulk, L2 evict-first), ~180 KB deep, completion
 //     on mbarriers; tiles of the next kernel's weights start streaming before
 //     griddepcontrol.wait releases the kernel (programmatic dependent launch);
-//   * eight compute warps hold their slice of the (normalised) input vector in
-//     registers, read 16-byte bf16 vectors from shared memory, accumulate in
-//     FP32, and reduce with warp shuffles;
+//     an optional L2 prefetch cursor runs ahead of the ring, then covers the
+//     first rows the next kernels read;
+//   * twelve compute warps hold their slice of the (normalised) input vector
+//     in registers, read 16-byte bf16 vectors from shared memory, accumulate
+//     in FP32, and reduce with warp shuffles;
 //   * fused prologues (RMSNorm, embedding gather, MoE weighted activations) and
 //     epilogues (store, residual add, SwiGLU, argmax, router top-k).
 #include <cstdlib>
@@ -30,11 +32,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
   const int nst = p.nstages;
   uint8_t* stages = smem;
   float* xs = reinterpret_cast<float*>(smem + nst * p.stage_bytes);
-  float* red = xs + p.xs_floats;
+  float* gs = xs + p.xs_floats;
+  float* red = gs + p.gs_floats;
   constexpr int npair = (EPI == kEpiSwiglu) ? 2 : 1;
   uint64_t* full = reinterpret_cast<uint64_t*>(red + ((p.rows_cta_max * npair * p.nchunk + 1) & ~1));
   uint64_t* empty = full + kMaxStages;
-  __shared__ EpiShared esh;
+  uint64_t* xbar = empty + kMaxStages;
+  __shared__ __align__(16) EpiShared esh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = (int)((long long)blockIdx.x * p.R / p.ncta);
@@ -45,6 +49,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
+    mbar_init(xbar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -53,9 +58,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
   if (warp == kConsumerWarps) {
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      if (SRC != kSrcDense) pdl_wait();  // expert ids come from the router kernel
-      int t = 0;
+      const uint64_t keep = l2_evict_last_policy();  // the input and gain are read by every CTA
+      mbar_arrive_expect_tx(xbar, input_bytes(p, IN) + (p.norm_g ? p.C * 4 : 0));
+      if (p.norm_g) bulk_g2s(gs, p.norm_g, p.C * 4, xbar, keep);
+      // Dense weights do not depend on earlier kernels: pre_stages tiles go out
+      // before griddepcontrol.wait; expert ids come from the router kernel.
+      const int pre = (SRC == kSrcDense) ? p.pre_stages : 0;
+      bool input_issued = false;
+      int t = 0, pf = r0;                // pf: first row the L2 prefetch cursor has not covered
+      bool next_done = false;
+      const int row_bytes = (SRC == kSrcExpertSegs) ? (p.top_k + 1) * p.seg_cols * 2 : p.C * 2 * npair;
       for (int a = r0; a < r1; ++t) {
+        if (!input_issued && t >= pre) {
+          pdl_wait();
+          issue_input(p, IN, xs, esh.mw, xbar, keep);
+          input_issued = true;
+        }
         const int rows = tile_rows_at(p, SRC, a, r1);
         const int s = t % nst, k = t / nst;
         if (t >= nst && !mbar_wait(&empty[s], (k - 1) & 1)) {
@@ -64,8 +82,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
         }
         issue_tile(p, SRC, npair, a, rows, stages + s * p.stage_bytes, &full[s], pol);
         a += rows;
+        if (p.pf_ahead > 0 && t + 1 >= nst && !next_done) {
+          // once the ring is full, keep the prefetch cursor pf_ahead bytes
+          // beyond what it has issued; past the last row, prefetch what the
+          // next kernels read first
+          if (pf < a) pf = a;
+          while (pf < r1 && (long long)(pf - a) * row_bytes < p.pf_ahead) {
+            const int pr = tile_rows_at(p, SRC, pf, r1);
+            prefetch_tile(p, SRC, npair, pf, pr);
+            pf += pr;
+          }
+          if (pf >= r1) {
+            prefetch_next(p);
+            next_done = true;
+          }
+        }
       }
+      if (!input_issued) {  // fewer tiles than pre_stages
+        pdl_wait();
+        issue_input(p, IN, xs, esh.mw, xbar, keep);
+      }
+      if (!next_done) prefetch_next(p);
       // Drain: the CTA must not retire while copies it issued are in flight.
+      if (!mbar_wait(xbar, 0)) set_guard(p.guard, kGuardWaitTimeout);
       for (int u = (t > nst ? t - nst : 0); u < t; ++u)
         if (!mbar_wait(&full[u % nst], (u / nst) & 1)) set_guard(p.guard, kGuardWaitTimeout);
     }
@@ -76,9 +115,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
   const int ctid = threadIdx.x;
   pdl_wait();
   pdl_launch_dependents();
-  load_input(p, IN, xs, esh.red, ctid);
+  if (!mbar_wait(xbar, 0) && ctid == 0) set_guard(p.guard, kGuardWaitTimeout);
+  const float sc = input_scale(p, IN, xs, esh.mw, esh.red, ctid);
   LaneSlice<VPL> L;
-  lane_setup<VPL>(p, SRC, xs, L, warp, lane);
+  lane_setup<VPL>(p, SRC, IN, xs, gs, esh.mw, sc, L, warp, lane);
   const int rows_cta = r1 - r0;
   bool abort = false;
   int t = 0;
@@ -97,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
   }
   named_barrier(1, kCT);
   if (abort) return;
-  epilogue(p, EPI, red, r0, rows_cta, esh, ctid);
+  epilogue(p, EPI, red, r0, rows_cta, esh, reinterpret_cast<float*>(stages), ctid);
 }
 
 template <int SRC, int IN, int EPI>
@@ -108,6 +148,7 @@ void* pick_vpl(int vpl) {
     case 3: return (void*)k_gemv<3, SRC, IN, EPI>;
     case 4: return (void*)k_gemv<4, SRC, IN, EPI>;
     case 5: return (void*)k_gemv<5, SRC, IN, EPI>;
+    case 6: return (void*)k_gemv<6, SRC, IN, EPI>;
     case 8: return (void*)k_gemv<8, SRC, IN, EPI>;
     default: return nullptr;
   }
@@ -136,7 +177,7 @@ const int kCombos[][3] = {
 // Opt every instantiation in to the full dynamic shared memory once, so that
 // launches (including those recorded into CUDA graphs) need no attribute call.
 cudaError_t init() {
-  const int vpls[] = {1, 2, 3, 4, 5, 8};
+  const int vpls[] = {1, 2, 3, 4, 5, 6, 8};
   for (const auto& c : kCombos)
     for (int v : vpls) {
       cudaError_t e = cudaFuncSetAttribute(pick(c[0], c[1], c[2], v), cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -156,44 +197,41 @@ int env_int(const char* name, int dflt) {
 }
 }  // namespace
 
-Plan plan(int R, int C, int npair, int nsm) {
+Plan plan(int R, int C, int npair, int nsm, bool norm) {
   const int stage_target = env_int("HY_GEMV_STAGE_KB", kStageTarget / 1024) * 1024;
   const int in_flight = env_int("HY_GEMV_INFLIGHT_KB", kInFlight / 1024) * 1024;
   const int ctas_per_sm = env_int("HY_GEMV_CTAS_PER_SM", kCtasPerSm);
-  const int nprod = env_int("HY_GEMV_PRODUCERS", kProducers);
   Plan pl = {};
   pl.ok = false;
   if (R <= 0 || C <= 0 || C % 8 != 0) return pl;
   const int nvec = C / 8;
-  int nchunk = 1, vpl = 0;
-  for (nchunk = 1; nchunk <= 8; nchunk *= 2) {
-    const int cv = (nvec + nchunk - 1) / nchunk;
-    vpl = (cv + 31) / 32;
-    if (vpl <= 8) break;
-  }
-  if (nchunk > 8) return pl;
-  if (vpl == 6 || vpl == 7) vpl = 8;
   const int row_bytes = C * 2 * npair;
-  // Smallest column split whose minimum tile (enough row items for all eight
-  // compute warps) fits the preferred stage size; a wider split keeps more of
-  // the input vector per lane in registers.
+  // Column split nc (a divisor of the compute-warp count, so every warp has a
+  // chunk and a row group): fewest lanes idle on a ragged last vector, then at
+  // least two row items per warp per tile, then the fewest chunks.
+  double best = 1e30;
   int tr_unit = 1;
-  for (int nc = 1; nc <= 8; nc *= 2) {
+  for (int nc = 1; nc <= kConsumerWarps; ++nc) {
+    if (kConsumerWarps % nc) continue;
     const int cv = (nvec + nc - 1) / nc;
-    const int v = (cv + 31) / 32;
+    int v = (cv + 31) / 32;
     if (v > 8) continue;
-    const int unit_items = 2 * kConsumerWarps / nc;  // two items per warp per tile
-    const int tu = (unit_items + npair - 1) / npair;
-    nchunk = nc;
-    vpl = v;
-    tr_unit = tu;
-    if (tu * row_bytes <= kStageCap) break;
+    if (v == 7) v = 8;
+    const int nrg = kConsumerWarps / nc;
+    int tu = (2 * nrg + npair - 1) / npair;        // rows for two items per warp
+    if (tu * row_bytes > kStageCap) tu = (nrg + npair - 1) / npair;
+    const int ipw = (tu * npair) / nrg;
+    const double waste = 1.0 - (double)cv / (32.0 * v);
+    const double score = waste + 0.5 * (ipw < 2) + 0.001 * nc + (tu * row_bytes > kStageCap ? 1.0 : 0.0);
+    if (score < best) {
+      best = score;
+      pl.nchunk = nc;
+      pl.vpl = v;
+      tr_unit = tu;
+    }
   }
-  if (vpl < 1 || vpl > 8) return pl;
-  if (vpl == 6 || vpl == 7) vpl = 8;
-  pl.nchunk = nchunk;
-  pl.vpl = vpl;
-  pl.chunk_vecs = (nvec + nchunk - 1) / nchunk;
+  if (pl.vpl < 1) return pl;
+  pl.chunk_vecs = (nvec + pl.nchunk - 1) / pl.nchunk;
   int tr = (stage_target / row_bytes / tr_unit) * tr_unit;
   if (tr < tr_unit) tr = tr_unit;
   if (tr * row_bytes > 2 * kStageCap) tr = 1;
@@ -201,14 +239,23 @@ Plan plan(int R, int C, int npair, int nsm) {
   pl.stage_bytes = ((tr * row_bytes) + 127) & ~127;
   int ns = in_flight / pl.stage_bytes;
   ns = ns < 2 ? 2 : (ns > kMaxStages ? kMaxStages : ns);
-  pl.nprod = nprod > ns ? ns : nprod;
-  ns = (ns / pl.nprod) * pl.nprod;  // every producer lane owns the same number of stages
   pl.nstages = ns;
   pl.ncta = R < nsm * ctas_per_sm ? R : nsm * ctas_per_sm;
   pl.rows_cta_max = (R + pl.ncta - 1) / pl.ncta;
   pl.xs_floats = (C + 3) & ~3;
-  const int red_floats = ((pl.rows_cta_max * npair * nchunk) + 1) & ~1;
-  pl.smem = pl.nstages * pl.stage_bytes + 4 * (pl.xs_floats + red_floats) + 2 * kMaxStages * 8;
+  pl.gs_floats = norm ? pl.xs_floats : 0;
+  pl.pre_stages = env_int("HY_GEMV_PRE_STAGES", kPreStages);
+  const char* ps0 = getenv("HY_GEMV_PRE_STAGES");
+  if (ps0 && *ps0 == '0') pl.pre_stages = 0;
+  pl.pf_ahead = env_int("HY_GEMV_PREFETCH_KB", kPrefetchAhead / 1024) * 1024;
+  const char* pf0 = getenv("HY_GEMV_PREFETCH_KB");
+  if (pf0 && *pf0 == '0') pl.pf_ahead = 0;
+  const int red_floats = ((pl.rows_cta_max * npair * pl.nchunk) + 1) & ~1;
+  pl.smem = pl.nstages * pl.stage_bytes + 4 * (pl.xs_floats + pl.gs_floats + red_floats) + (2 * kMaxStages + 1) * 8;
+  while (pl.smem > kMaxSmem && pl.nstages > 2) {
+    pl.nstages -= 1;
+    pl.smem -= pl.stage_bytes;
+  }
   pl.ok = pl.smem <= kMaxSmem;
   return pl;
 }
@@ -223,9 +270,11 @@ cudaError_t launch(const Params& p0, const Plan& pl, int src, int in, int epi, c
   p.chunk_vecs = pl.chunk_vecs;
   p.stage_bytes = pl.stage_bytes;
   p.nstages = pl.nstages;
-  p.nprod = pl.nprod;
+  p.pf_ahead = pl.pf_ahead;
   p.rows_cta_max = pl.rows_cta_max;
   p.xs_floats = pl.xs_floats;
+  p.gs_floats = pl.gs_floats;
+  p.pre_stages = pl.pre_stages;
   p.npair = (epi == kEpiSwiglu) ? 2 : 1;
   return launch_k(reinterpret_cast<void (*)(Params)>(k), dim3(pl.ncta), dim3(kThreads), (size_t)pl.smem, st, pdl, p);
 }

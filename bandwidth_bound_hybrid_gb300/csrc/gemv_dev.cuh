@@ -1,9 +1,8 @@
-// Device building blocks of the streaming GEMV, shared by the standalone GEMV
-// kernel (gemv.cu) and the persistent decode-step kernel (step.cu).
+// Device building blocks of the streaming GEMV kernel (gemv.cu).
 //
-// A GEMV phase: a CTA owns rows [r0, r1) of y = W * f(x).  A copy lane
-// streams row tiles of W into a ring of shared-memory stages with bulk copies
-// (TMA engine); eight compute warps hold their column slice of f(x) in
+// A CTA owns rows [r0, r1) of y = W * f(x).  A copy lane streams row tiles
+// of W into a ring of shared-memory stages with bulk copies (TMA engine);
+// the compute warps hold their column slice of f(x) in
 // registers and consume every tile, two (row, column-chunk) items per warp per
 // pass with independent FMA chains and one paired butterfly reduction.
 #pragma once
@@ -65,49 +64,121 @@ __device__ __forceinline__ void issue_tile(const Params& p, int src, int npair, 
   }
 }
 
-// Compute threads: the input vector f(x) into shared memory xs (RMSNorm when
-// p.norm_g is set).  s_red: >= 8 floats of shared scratch.
-__device__ __forceinline__ void load_input(const Params& p, int in, float* xs, float* s_red, int ctid) {
-  const int warp = ctid >> 5, lane = ctid & 31;
-  int tok = 0;
+// Copy lane: L2 prefetch of the tile [a, a + rows) (same addresses as issue_tile).
+__device__ __forceinline__ void prefetch_tile(const Params& p, int src, int npair, int a, int rows) {
+  if (src == kSrcExpertSegs) {
+    const uint32_t seg_bytes = (uint32_t)rows * p.seg_cols * 2;
+    for (int g = 0; g <= p.top_k; ++g) {
+      const uint8_t* base = (g < p.top_k) ? p.exp_base[0] + (long long)checked_expert(p, g) * p.exp_stride : p.sh_base[0];
+      bulk_prefetch_l2(base + (long long)a * p.seg_cols * 2, seg_bytes);
+    }
+  } else {
+    const uint32_t bytes = (uint32_t)rows * p.C * 2;
+    for (int j = 0; j < npair; ++j) bulk_prefetch_l2(row_src(p, src, j, a), bytes);
+  }
+}
+
+// Copy lane: L2 prefetch of this CTA's share of the next kernels' first reads.
+__device__ __forceinline__ void prefetch_next(const Params& p) {
+  const int b = blockIdx.x;
+  for (int i = 0; i < p.n_nx; ++i) {
+    const PfSpan& s = p.nx[i];
+    if (b >= s.ncta) continue;
+    const long long r0 = (long long)b * s.rows / s.ncta, r1 = (long long)(b + 1) * s.rows / s.ncta;
+    long long bytes = (r1 - r0) * s.row_bytes;
+    if (bytes > s.bytes) bytes = s.bytes & ~15LL;
+    const uint8_t* src = s.base + r0 * s.row_bytes;
+    for (long long o = 0; o < bytes; o += 65536) bulk_prefetch_l2(src + o, (uint32_t)(bytes - o < 65536 ? bytes - o : 65536));
+  }
+}
+
+// The input vector f(x) reaches shared memory by bulk copy from the copy
+// lane, right after griddepcontrol.wait and ahead of all but the first weight
+// tiles: a load issued by the compute warps would queue behind the whole ring
+// already requested for this SM.  xs holds x (FP32) or the embedding row
+// (bf16), gs the RMSNorm gain (requested before the wait: it is a weight), mw
+// the routing weights of the MoE down projection.
+__device__ __forceinline__ uint32_t input_bytes(const Params& p, int in) {
+  uint32_t b = (in == kInEmbed) ? p.C * 2 : p.C * 4;
+  if (in == kInMoeZ) b += ((p.top_k + 1) * 4 + 15) & ~15;
+  return b;
+}
+
+// Copy lane, after griddepcontrol.wait.
+__device__ __forceinline__ void issue_input(const Params& p, int in, float* xs, float* mw, uint64_t* xbar,
+                                            uint64_t pol) {
   if (in == kInEmbed) {
-    tok = p.tok[0];
-    if (tok < 0 || tok >= p.vocab) {
-      if (ctid == 0) set_guard(p.guard, kGuardBadIndex);
+    int tok = *p.tok;
+    if (tok < 0 || tok >= p.vocab) {  // never read outside the embedding table
+      set_guard(p.guard, kGuardBadIndex);
       tok = 0;
     }
+    bulk_g2s(xs, p.embed + (long long)tok * p.C, p.C * 2, xbar, pol);
+  } else {
+    bulk_g2s(xs, p.x, p.C * 4, xbar, pol);
+    if (in == kInMoeZ) bulk_g2s(mw, p.moe_w, ((p.top_k + 1) * 4 + 15) & ~15, xbar, pol);
   }
-  float ss = 0.f;
-  for (int c = ctid * 4; c < p.C; c += kCT * 4) {
-    float4 v;
-    if (in == kInX) {
-      v = *reinterpret_cast<const float4*>(p.x + c);
-    } else if (in == kInEmbed) {
-      const uint2 e = *reinterpret_cast<const uint2*>(p.embed + (long long)tok * p.C + c);
-      v = make_float4(bf16_lo(e.x), bf16_hi(e.x), bf16_lo(e.y), bf16_hi(e.y));
-      if (blockIdx.x == 0) *reinterpret_cast<float4*>(p.x_out + c) = v;
-    } else {  // kInMoeZ: routing-weighted expert activations
-      const float w = p.moe_w[c / p.seg_cols];
-      v = *reinterpret_cast<const float4*>(p.x + c);
-      v.x *= w;
-      v.y *= w;
-      v.z *= w;
-      v.w *= w;
+}
+
+// Elements 8v .. 8v+7 of the input before normalisation, with 16-byte shared
+// loads (a lane's 32 contiguous bytes in two accesses, not eight scalar ones
+// that would hit the same banks as seven other lanes).
+__device__ __forceinline__ void input_vec8(const Params& p, int in, const float* xs, const float* mw, int v,
+                                           float* out) {
+  if (in == kInEmbed) {
+    const uint4 u = reinterpret_cast<const uint4*>(xs)[v];
+    out[0] = bf16_lo(u.x);
+    out[1] = bf16_hi(u.x);
+    out[2] = bf16_lo(u.y);
+    out[3] = bf16_hi(u.y);
+    out[4] = bf16_lo(u.z);
+    out[5] = bf16_hi(u.z);
+    out[6] = bf16_lo(u.w);
+    out[7] = bf16_hi(u.w);
+    return;
+  }
+  const float4 a = reinterpret_cast<const float4*>(xs)[2 * v];
+  const float4 b = reinterpret_cast<const float4*>(xs)[2 * v + 1];
+  const float w = (in == kInMoeZ) ? mw[(8 * v) / p.seg_cols] : 1.f;
+  out[0] = a.x * w;
+  out[1] = a.y * w;
+  out[2] = a.z * w;
+  out[3] = a.w * w;
+  out[4] = b.x * w;
+  out[5] = b.y * w;
+  out[6] = b.z * w;
+  out[7] = b.w * w;
+}
+
+// Compute threads, once the input has landed: the RMSNorm scale (1 without a
+// gain); CTA 0 of the embedding GEMV also initialises the residual stream.
+// s_red: >= kConsumerWarps floats of shared scratch.
+__device__ __forceinline__ float input_scale(const Params& p, int in, const float* xs, const float* mw, float* s_red,
+                                             int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int nvec = p.C / 8;
+  if (in == kInEmbed && blockIdx.x == 0)
+    for (int v = ctid; v < nvec; v += kCT) {
+      float e[8];
+      input_vec8(p, in, xs, mw, v, e);
+      reinterpret_cast<float4*>(p.x_out)[2 * v] = make_float4(e[0], e[1], e[2], e[3]);
+      reinterpret_cast<float4*>(p.x_out)[2 * v + 1] = make_float4(e[4], e[5], e[6], e[7]);
     }
-    *reinterpret_cast<float4*>(xs + c) = v;
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-  }
-  if (p.norm_g) {
-    ss = warp_sum(ss);
-    if (lane == 0) s_red[warp] = ss;
-    named_barrier(1, kCT);
-    float t = 0.f;
+  if (!p.norm_g) return 1.f;
+  float ss = 0.f;
+  for (int v = ctid; v < nvec; v += kCT) {
+    float e[8];
+    input_vec8(p, in, xs, mw, v, e);
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) t += s_red[w];
-    const float sc = 1.0f / sqrtf(t / (float)p.C + p.eps);
-    for (int c = ctid; c < p.C; c += kCT) xs[c] = xs[c] * sc * p.norm_g[c];
+    for (int i = 0; i < 8; ++i) ss = fmaf(e[i], e[i], ss);
   }
+  ss = warp_sum(ss);
+  if (lane == 0) s_red[warp] = ss;
   named_barrier(1, kCT);
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) t += s_red[w];
+  return 1.0f / sqrtf(t / (float)p.C + p.eps);
 }
 
 // Per-lane state of a compute warp: its column chunk, the input slice in
@@ -122,8 +193,8 @@ struct LaneSlice {
 };
 
 template <int VPL>
-__device__ __forceinline__ void lane_setup(const Params& p, int src, const float* xs, LaneSlice<VPL>& L, int warp,
-                                           int lane) {
+__device__ __forceinline__ void lane_setup(const Params& p, int src, int in, const float* xs, const float* gs,
+                                           const float* mw, float sc, LaneSlice<VPL>& L, int warp, int lane) {
   L.chunk = warp % p.nchunk;
   L.rg = warp / p.nchunk;
   L.nrg = kConsumerWarps / p.nchunk;
@@ -138,8 +209,17 @@ __device__ __forceinline__ void lane_setup(const Params& p, int src, const float
     const int vv = L.valid[j] ? v : 0;
     L.segof[j] = vv / seg_vecs;
     L.off[j] = (vv % seg_vecs) * 16;
+    float e8[8];
+    input_vec8(p, in, xs, mw, vv, e8);
+    if (p.norm_g) {
+      const float4 g0 = reinterpret_cast<const float4*>(gs)[2 * vv];
+      const float4 g1 = reinterpret_cast<const float4*>(gs)[2 * vv + 1];
+      const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) L.xr[j][e] = L.valid[j] ? xs[vv * 8 + e] : 0.f;
+      for (int e = 0; e < 8; ++e) e8[e] = e8[e] * sc * g[e];
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) L.xr[j][e] = L.valid[j] ? e8[e] : 0.f;
   }
 }
 
@@ -187,10 +267,11 @@ __device__ __forceinline__ void consume_tile(const Params& p, int src, int npair
 
 // Shared scratch of the epilogue.
 struct EpiShared {
+  float mw[kMaxTopK + 4];  // routing weights (bulk-copy destination: 16-byte multiple)
+  int sel[kMaxTopK];
+  float selv[kMaxTopK];
   float red[kConsumerWarps];
   int redi[kConsumerWarps];
-  int sel[64];
-  float selv[64];
   int last;
 };
 
@@ -204,8 +285,10 @@ __device__ __forceinline__ void argmax_merge(float& bv, int& bi, float ov, int o
 // Epilogue over the CTA's rows (after all tiles): store, residual add,
 // SwiGLU, or argmax / router top-k finished by the last CTA to arrive (an
 // atomic ticket: no CTA waits for another).
+// scratch: >= n_experts + 1 floats of shared memory no longer in use (the
+// drained weight ring).
 __device__ __forceinline__ void epilogue(const Params& p, int epi, const float* red, int r0, int rows_cta,
-                                         EpiShared& sh, int ctid) {
+                                         EpiShared& sh, float* scratch, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   auto row_val = [&](int jj, int i) {
     float v = 0.f;
@@ -283,34 +366,26 @@ __device__ __forceinline__ void epilogue(const Params& p, int epi, const float* 
   // router: top-k over the E expert logits (FP32 compare, lowest index on
   // ties), softmax over the selected logits, sigmoid gate of the shared
   // expert's row ("Fourteen hours to 100 tokens per second", "The router with
-  // 257 rows").
+  // 257 rows").  The logits go to shared scratch in one pass; then every
+  // expert's rank (the number of logits above it, or equal with a lower
+  // index) is counted in parallel, and the experts of rank < top_k are the
+  // selection in order: the same set and order as top_k successive argmaxes.
   const int E = p.n_experts;
-  for (int kk = 0; kk < p.top_k; ++kk) {
-    float v = -INFINITY;
-    int vi = 0x7fffffff;
-    for (int e = ctid; e < E; e += kCT) {
-      bool taken = false;
-      for (int q = 0; q < kk; ++q) taken |= (sh.sel[q] == e);
-      if (!taken) argmax_merge(v, vi, __ldcg(p.router_logits + e), e);
+  for (int e = ctid; e <= E; e += kCT) scratch[e] = __ldcg(p.router_logits + e);
+  named_barrier(1, kCT);
+  for (int e = ctid; e < E; e += kCT) {
+    const float v = scratch[e];
+    int rank = 0;
+    for (int f = 0; f < E; ++f) {
+      const float w = scratch[f];
+      rank += (w > v || (w == v && f < e)) ? 1 : 0;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, vi, o);
-      argmax_merge(v, vi, ov, oi);
+    if (rank < p.top_k) {
+      sh.sel[rank] = e;
+      sh.selv[rank] = v;
     }
-    if (lane == 0) {
-      sh.red[warp] = v;
-      sh.redi[warp] = vi;
-    }
-    named_barrier(1, kCT);
-    if (ctid == 0) {
-      for (int w = 1; w < kConsumerWarps; ++w) argmax_merge(v, vi, sh.red[w], sh.redi[w]);
-      sh.sel[kk] = vi;
-      sh.selv[kk] = v;
-    }
-    named_barrier(1, kCT);
   }
+  named_barrier(1, kCT);
   if (ctid == 0) {
     const float m = sh.selv[0];
     float den = 0.f;
@@ -320,11 +395,11 @@ __device__ __forceinline__ void epilogue(const Params& p, int epi, const float* 
       p.out_w[q] = __expf(sh.selv[q] - m) / den;
       if (p.dbg_ids) p.dbg_ids[q] = sh.sel[q];
     }
-    p.out_w[p.top_k] = sigmoidf_(__ldcg(p.router_logits + E));
+    p.out_w[p.top_k] = sigmoidf_(scratch[E]);
     *p.counter = 0u;
   }
   if (p.dbg_logits)
-    for (int e = ctid; e <= E; e += kCT) p.dbg_logits[e] = __ldcg(p.router_logits + e);
+    for (int e = ctid; e <= E; e += kCT) p.dbg_logits[e] = scratch[e];
 }
 
 }  // namespace gemv

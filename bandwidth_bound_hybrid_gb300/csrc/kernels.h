@@ -16,15 +16,29 @@ enum Src : int { kSrcDense = 0, kSrcExpertRows = 1, kSrcExpertSegs = 2 };
 enum In : int { kInX = 0, kInEmbed = 1, kInMoeZ = 2 };
 enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiArgmax = 3, kEpiRouter = 4 };
 
-constexpr int kConsumerWarps = 8;
+#ifndef HY_GEMV_WARPS
+#define HY_GEMV_WARPS 12
+#endif
+constexpr int kConsumerWarps = HY_GEMV_WARPS;  // compute warps; one more warp issues the copies
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 8;
-constexpr int kStageTarget = 40 * 1024;     // preferred bytes per pipeline stage
-constexpr int kStageCap = 40 * 1024;        // largest preferred minimum tile
-constexpr int kInFlight = 120 * 1024;       // bytes kept in flight per CTA
+constexpr int kStageTarget = 60 * 1024;     // preferred bytes per pipeline stage
+constexpr int kStageCap = 60 * 1024;        // largest preferred minimum tile
+constexpr int kInFlight = 180 * 1024;       // bytes kept in flight per CTA in shared memory
+constexpr int kPrefetchAhead = 0;           // bytes the L2 prefetch cursor runs ahead of the ring
 constexpr int kMaxSmem = 220 * 1024;        // dynamic; leaves room for static shared data
 constexpr int kCtasPerSm = 1;
-constexpr int kProducers = 1;
+constexpr int kPreStages = 0;               // tiles issued before the input vector is requested
+constexpr int kMaxTopK = 16;
+
+// Rows of a matrix that CTA b of an ncta-CTA GEMV owns, prefetched into L2 by
+// CTA b of the kernel before it: [b*rows/ncta, (b+1)*rows/ncta), at most
+// `bytes` from the start of that range.
+struct PfSpan {
+  const uint8_t* base;
+  int rows, row_bytes, ncta, bytes;
+};
+constexpr int kMaxPfSpans = 3;
 
 struct Params {
   // ---- weights (bf16 rows of C columns)
@@ -59,18 +73,25 @@ struct Params {
   float* out_w;                 // kEpiRouter: [top_k + 1]
   int* dbg_ids;                 // kEpiRouter debug copies (nullable)
   float* dbg_logits;
+  // ---- prefetch
+  PfSpan nx[kMaxPfSpans];       // what the next kernels read first (weights known when the step is recorded)
+  int n_nx;
   // ---- plan
-  int ncta, tile_rows, nchunk, chunk_vecs, stage_bytes, nstages, rows_cta_max, xs_floats;
-  int nprod;                    // copy-issuing lanes
+  int ncta, tile_rows, nchunk, chunk_vecs, stage_bytes, nstages, rows_cta_max, xs_floats, gs_floats;
+  int pre_stages;               // tiles issued before griddepcontrol.wait (ahead of the input vector)
+  int pf_ahead;                 // L2 prefetch cursor distance in bytes (0 = off)
   unsigned* guard;
 };
 
 struct Plan {
-  int ncta, tile_rows, nchunk, chunk_vecs, vpl, stage_bytes, nstages, rows_cta_max, xs_floats, smem, nprod;
+  int ncta, tile_rows, nchunk, chunk_vecs, vpl, stage_bytes, nstages, rows_cta_max, xs_floats, gs_floats, smem;
+  int pre_stages, pf_ahead;
   bool ok;
 };
 
-Plan plan(int R, int C, int npair, int nsm);
+// Launch plan of an R x C GEMV (npair matrices sharing the input; `norm`: the
+// input is RMS-normalised with a gain vector) on nsm SMs.
+Plan plan(int R, int C, int npair, int nsm, bool norm);
 cudaError_t init();
 cudaError_t launch(const Params& p, const Plan& pl, int src, int in, int epi, cudaStream_t st, bool pdl);
 
