@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p) {
 
   // ------------------------------------------------------------ copy lane
   if (warp == kCWarps) {
+    pdl_launch_dependents();  // the CTA's trigger needs every thread (or its exit)
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       int t = 0;

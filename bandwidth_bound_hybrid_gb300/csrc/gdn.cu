@@ -24,8 +24,8 @@ __global__ void __launch_bounds__(kThreads) k_gdn(const Params p) {
   ConvRegs<EPL, kWarps> V;
   load_rows<EPL, kWarps>(p, h, rc, R, threadIdx.x);  // pre-wait
   load_conv<EPL, kWarps>(p, h, rc, V, threadIdx.x);  // pre-wait
+  pdl_launch_dependents();  // the next GEMV may stage its weights meanwhile
   pdl_wait();
-  pdl_launch_dependents();
   run_item<EPL, kWarps>(p, h, rc, R, V, sh, threadIdx.x, [] __device__() { __syncthreads(); });
 }
 

@@ -27,7 +27,7 @@ namespace gemv {
 namespace {
 
 template <int VPL, int SRC, int IN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
+__global__ void __maxnreg__(kMaxRegs) k_gemv(const Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int nst = p.nstages;
   uint8_t* stages = smem;
@@ -56,6 +56,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
 
   // ------------------------------------------------------------ copy lane
   if (warp == kConsumerWarps) {
+    // A CTA releases its dependents once every thread has triggered or
+    // exited: trigger here too, or the next kernel would launch only when the
+    // copy lane retires at the end.
+    pdl_launch_dependents();
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       const uint64_t keep = l2_evict_last_policy();  // the input and gain are read by every CTA
@@ -130,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
       abort = true;
       break;
     }
-    consume_tile<VPL>(p, SRC, npair, L, stages + s * p.stage_bytes, rows, a, r0, rows_cta, red, lane);
+    consume_tile<VPL, SRC, npair>(p, L, stages + s * p.stage_bytes, rows, a - r0, rows_cta, red, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     a += rows;
@@ -222,7 +226,8 @@ Plan plan(int R, int C, int npair, int nsm, bool norm) {
     if (tu * row_bytes > kStageCap) tu = (nrg + npair - 1) / npair;
     const int ipw = (tu * npair) / nrg;
     const double waste = 1.0 - (double)cv / (32.0 * v);
-    const double score = waste + 0.5 * (ipw < 2) + 0.001 * nc + (tu * row_bytes > kStageCap ? 1.0 : 0.0);
+    // VPL above 5 does not fit the register cap without spills
+    const double score = waste + 0.5 * (ipw < 2) + 0.001 * nc + (tu * row_bytes > kStageCap ? 1.0 : 0.0) + (v > 5 ? 0.2 : 0.0);
     if (score < best) {
       best = score;
       pl.nchunk = nc;

@@ -223,45 +223,74 @@ __device__ __forceinline__ void lane_setup(const Params& p, int src, int in, con
   }
 }
 
-// Consume one tile (rows [a, a + rows) of the CTA range starting at r0):
-// partial dot products of this warp's column chunk go to red.
-template <int VPL>
-__device__ __forceinline__ void consume_tile(const Params& p, int src, int npair, const LaneSlice<VPL>& L,
-                                             const uint8_t* st, int rows, int a, int r0, int rows_cta, float* red,
-                                             int lane) {
-  const int items = rows * npair;
-  const int segstride = (src == kSrcExpertSegs) ? rows * L.seg_row_bytes : 0;
-  for (int q = L.rg; q < items; q += 2 * L.nrg) {
-    const int q2 = q + L.nrg;
-    const bool has2 = q2 < items;
-    const int j0 = q / rows, i0 = q - j0 * rows;
-    const int qq = has2 ? q2 : q;
-    const int j1 = qq / rows, i1 = qq - j1 * rows;
-    const uint8_t* p0 = (src == kSrcExpertSegs) ? st + i0 * L.seg_row_bytes : st + (j0 * rows + i0) * p.C * 2;
-    const uint8_t* p1 = (src == kSrcExpertSegs) ? st + i1 * L.seg_row_bytes : st + (j1 * rows + i1) * p.C * 2;
-    uint4 w0[VPL], w1[VPL];
+// dot of 8 bf16 (one 16-byte vector) with 8 FP32 values, accumulated into acc
+__device__ __forceinline__ float dot8_acc(const uint4 w, const float* x, float acc) {
+  acc = fmaf(bf16_lo(w.x), x[0], acc);
+  acc = fmaf(bf16_hi(w.x), x[1], acc);
+  acc = fmaf(bf16_lo(w.y), x[2], acc);
+  acc = fmaf(bf16_hi(w.y), x[3], acc);
+  acc = fmaf(bf16_lo(w.z), x[4], acc);
+  acc = fmaf(bf16_hi(w.z), x[5], acc);
+  acc = fmaf(bf16_lo(w.w), x[6], acc);
+  acc = fmaf(bf16_hi(w.w), x[7], acc);
+  return acc;
+}
+
+// Consume one tile (rows [a, a + rows) of the CTA range starting at r0): the
+// partial dot products of this warp's column chunk go to red.  A warp owns
+// the rows i = rg (mod nrg) of every tile and finishes two items per pass
+// (rows i and i + nrg, or the gate and up rows of row i) with one paired
+// butterfly; addresses advance by a fixed row stride, without divisions.
+template <int VPL, int SRC, int NPAIR>
+__device__ __forceinline__ void consume_tile(const Params& p, const LaneSlice<VPL>& L, const uint8_t* st, int rows,
+                                             int row0, int rows_cta, float* red, int lane) {
+  // byte offset of this lane's vector u within a row, and the row stride
+  int uoff[VPL];
+  int stride;
+  if (SRC == kSrcExpertSegs) {
+    stride = L.seg_row_bytes;
 #pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-      if (L.valid[u]) {
-        w0[u] = *reinterpret_cast<const uint4*>(p0 + L.segof[u] * segstride + L.off[u]);
-        w1[u] = *reinterpret_cast<const uint4*>(p1 + L.segof[u] * segstride + L.off[u]);
-      }
+    for (int u = 0; u < VPL; ++u) uoff[u] = L.segof[u] * rows * L.seg_row_bytes + L.off[u];
+  } else {
+    stride = p.C * 2;
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) uoff[u] = L.off[u];
+  }
+  const int member_bytes = rows * stride;  // gate rows, then up rows (pairs)
+  const int step = (NPAIR == 2) ? L.nrg : 2 * L.nrg;
+  for (int i = L.rg; i < rows; i += step) {
+    int i1, j1;
+    const uint8_t* p0 = st + i * stride;
+    const uint8_t* p1;
+    bool has2;
+    if (NPAIR == 2) {
+      i1 = i;
+      j1 = 1;
+      has2 = true;
+      p1 = p0 + member_bytes;
+    } else {
+      i1 = i + L.nrg;
+      j1 = 0;
+      has2 = i1 < rows;
+      p1 = has2 ? st + i1 * stride : p0;
     }
     float a0 = 0.f, a1 = 0.f;
 #pragma unroll
     for (int u = 0; u < VPL; ++u) {
       if (L.valid[u]) {
-        a0 += dot8(w0[u], L.xr[u]);
-        a1 += dot8(w1[u], L.xr[u]);
+        const uint4 w0 = *reinterpret_cast<const uint4*>(p0 + uoff[u]);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(p1 + uoff[u]);
+        a0 = dot8_acc(w0, L.xr[u], a0);
+        a1 = dot8_acc(w1, L.xr[u], a1);
       }
     }
-    // paired butterfly: lanes 0..15 finish item q, lanes 16..31 item q2
+    // paired butterfly: lanes 0..15 finish the first item, lanes 16..31 the second
     float keep = (lane < 16) ? a0 : a1;
     keep += __shfl_xor_sync(0xffffffffu, (lane < 16) ? a1 : a0, 16);
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
-    if (lane == 0) red[((j0 * rows_cta) + (a - r0) + i0) * p.nchunk + L.chunk] = keep;
-    if (lane == 16 && has2) red[((j1 * rows_cta) + (a - r0) + i1) * p.nchunk + L.chunk] = keep;
+    if (lane == 0) red[(row0 + i) * p.nchunk + L.chunk] = keep;
+    if (lane == 16 && has2) red[(j1 * rows_cta + row0 + i1) * p.nchunk + L.chunk] = keep;
   }
 }
 

@@ -21,6 +21,13 @@ enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiArgmax = 3, k
 #endif
 constexpr int kConsumerWarps = HY_GEMV_WARPS;  // compute warps; one more warp issues the copies
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
+#ifndef HY_GEMV_MAXREG
+#define HY_GEMV_MAXREG 112
+#endif
+// Register cap: 13 warps of 112 leave each SM sub-partition room for a warp of
+// a small kernel (the DeltaNet step) launched early by programmatic dependent
+// launch, so that it runs beside the GEMV instead of after it.
+constexpr int kMaxRegs = HY_GEMV_MAXREG;
 constexpr int kMaxStages = 8;
 constexpr int kStageTarget = 60 * 1024;     // preferred bytes per pipeline stage
 constexpr int kStageCap = 60 * 1024;        // largest preferred minimum tile
