@@ -64,6 +64,24 @@ __device__ __forceinline__ float dot8(const uint4 w, const float* x) {
   return a;
 }
 
+// Two FP32 FMAs in one packed instruction (sm_100 family): (a0, a1) +=
+// (w0 * x0, w1 * x1), each rounded once as fmaf would.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float w0, float w1, float x0, float x1) {
+  asm("{\n .reg .b64 a, w, x;\n mov.b64 a, {%0, %1};\n mov.b64 w, {%2, %3};\n mov.b64 x, {%4, %5};\n"
+      " fma.rn.f32x2 a, w, x, a;\n mov.b64 {%0, %1}, a;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
+}
+
+// 8 bf16 (one 16-byte vector) times 8 FP32 values, accumulated into the pair
+// (even elements, odd elements) with packed FMAs.
+__device__ __forceinline__ void dot8_acc2(const uint4 w, const float* x, float& ae, float& ao) {
+  fma2(ae, ao, bf16_lo(w.x), bf16_hi(w.x), x[0], x[1]);
+  fma2(ae, ao, bf16_lo(w.y), bf16_hi(w.y), x[2], x[3]);
+  fma2(ae, ao, bf16_lo(w.z), bf16_hi(w.z), x[4], x[5]);
+  fma2(ae, ao, bf16_lo(w.w), bf16_hi(w.w), x[6], x[7]);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -104,13 +122,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase of the given parity; false after kWaitLimitNs.
+// The clock is read once every 1024 polls, not on every poll.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  uint64_t t0 = 0;
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023u) == 0) {
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > kWaitLimitNs) return false;
+    }
   }
-  return true;
 }
 
 // L2 policy for streamed-once weights: evict first, so KV, state and

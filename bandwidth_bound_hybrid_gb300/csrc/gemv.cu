@@ -26,7 +26,7 @@ namespace gemv {
 
 namespace {
 
-template <int VPL, int SRC, int IN, int EPI>
+template <int VPL, int SRC, int IN, int EPI, bool FULL>
 __global__ void __maxnreg__(kMaxRegs) k_gemv(const Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int nst = p.nstages;
@@ -134,7 +134,7 @@ __global__ void __maxnreg__(kMaxRegs) k_gemv(const Params p) {
       abort = true;
       break;
     }
-    consume_tile<VPL, SRC, npair>(p, L, stages + s * p.stage_bytes, rows, a - r0, rows_cta, red, lane);
+    consume_tile<VPL, SRC, npair, FULL>(p, L, stages + s * p.stage_bytes, rows, a - r0, rows_cta, red, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     a += rows;
@@ -144,29 +144,34 @@ __global__ void __maxnreg__(kMaxRegs) k_gemv(const Params p) {
   epilogue(p, EPI, red, r0, rows_cta, esh, reinterpret_cast<float*>(stages), ctid);
 }
 
-template <int SRC, int IN, int EPI>
+template <int SRC, int IN, int EPI, bool FULL>
 void* pick_vpl(int vpl) {
   switch (vpl) {
-    case 1: return (void*)k_gemv<1, SRC, IN, EPI>;
-    case 2: return (void*)k_gemv<2, SRC, IN, EPI>;
-    case 3: return (void*)k_gemv<3, SRC, IN, EPI>;
-    case 4: return (void*)k_gemv<4, SRC, IN, EPI>;
-    case 5: return (void*)k_gemv<5, SRC, IN, EPI>;
-    case 6: return (void*)k_gemv<6, SRC, IN, EPI>;
-    case 8: return (void*)k_gemv<8, SRC, IN, EPI>;
+    case 1: return (void*)k_gemv<1, SRC, IN, EPI, FULL>;
+    case 2: return (void*)k_gemv<2, SRC, IN, EPI, FULL>;
+    case 3: return (void*)k_gemv<3, SRC, IN, EPI, FULL>;
+    case 4: return (void*)k_gemv<4, SRC, IN, EPI, FULL>;
+    case 5: return (void*)k_gemv<5, SRC, IN, EPI, FULL>;
+    case 6: return (void*)k_gemv<6, SRC, IN, EPI, FULL>;
+    case 8: return (void*)k_gemv<8, SRC, IN, EPI, FULL>;
     default: return nullptr;
   }
 }
 
-void* pick(int src, int in, int epi, int vpl) {
-  if (src == kSrcDense && in == kInX && epi == kEpiStore) return pick_vpl<kSrcDense, kInX, kEpiStore>(vpl);
-  if (src == kSrcDense && in == kInEmbed && epi == kEpiStore) return pick_vpl<kSrcDense, kInEmbed, kEpiStore>(vpl);
-  if (src == kSrcDense && in == kInX && epi == kEpiResid) return pick_vpl<kSrcDense, kInX, kEpiResid>(vpl);
-  if (src == kSrcDense && in == kInX && epi == kEpiSwiglu) return pick_vpl<kSrcDense, kInX, kEpiSwiglu>(vpl);
-  if (src == kSrcDense && in == kInX && epi == kEpiArgmax) return pick_vpl<kSrcDense, kInX, kEpiArgmax>(vpl);
-  if (src == kSrcDense && in == kInX && epi == kEpiRouter) return pick_vpl<kSrcDense, kInX, kEpiRouter>(vpl);
-  if (src == kSrcExpertRows && in == kInX && epi == kEpiSwiglu) return pick_vpl<kSrcExpertRows, kInX, kEpiSwiglu>(vpl);
-  if (src == kSrcExpertSegs && in == kInMoeZ && epi == kEpiResid) return pick_vpl<kSrcExpertSegs, kInMoeZ, kEpiResid>(vpl);
+template <int SRC, int IN, int EPI>
+void* pick_vpl(int vpl, bool full) {
+  return full ? pick_vpl<SRC, IN, EPI, true>(vpl) : pick_vpl<SRC, IN, EPI, false>(vpl);
+}
+
+void* pick(int src, int in, int epi, int vpl, bool full) {
+  if (src == kSrcDense && in == kInX && epi == kEpiStore) return pick_vpl<kSrcDense, kInX, kEpiStore>(vpl, full);
+  if (src == kSrcDense && in == kInEmbed && epi == kEpiStore) return pick_vpl<kSrcDense, kInEmbed, kEpiStore>(vpl, full);
+  if (src == kSrcDense && in == kInX && epi == kEpiResid) return pick_vpl<kSrcDense, kInX, kEpiResid>(vpl, full);
+  if (src == kSrcDense && in == kInX && epi == kEpiSwiglu) return pick_vpl<kSrcDense, kInX, kEpiSwiglu>(vpl, full);
+  if (src == kSrcDense && in == kInX && epi == kEpiArgmax) return pick_vpl<kSrcDense, kInX, kEpiArgmax>(vpl, full);
+  if (src == kSrcDense && in == kInX && epi == kEpiRouter) return pick_vpl<kSrcDense, kInX, kEpiRouter>(vpl, full);
+  if (src == kSrcExpertRows && in == kInX && epi == kEpiSwiglu) return pick_vpl<kSrcExpertRows, kInX, kEpiSwiglu>(vpl, full);
+  if (src == kSrcExpertSegs && in == kInMoeZ && epi == kEpiResid) return pick_vpl<kSrcExpertSegs, kInMoeZ, kEpiResid>(vpl, full);
   return nullptr;
 }
 
@@ -183,11 +188,12 @@ const int kCombos[][3] = {
 cudaError_t init() {
   const int vpls[] = {1, 2, 3, 4, 5, 6, 8};
   for (const auto& c : kCombos)
-    for (int v : vpls) {
-      cudaError_t e = cudaFuncSetAttribute(pick(c[0], c[1], c[2], v), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kMaxSmem);
-      if (e != cudaSuccess) return e;
-    }
+    for (int v : vpls)
+      for (int f = 0; f < 2; ++f) {
+        cudaError_t e = cudaFuncSetAttribute(pick(c[0], c[1], c[2], v, f != 0),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+        if (e != cudaSuccess) return e;
+      }
   return cudaSuccess;
 }
 
@@ -237,6 +243,7 @@ Plan plan(int R, int C, int npair, int nsm, bool norm) {
   }
   if (pl.vpl < 1) return pl;
   pl.chunk_vecs = (nvec + pl.nchunk - 1) / pl.nchunk;
+  pl.full = (pl.chunk_vecs == 32 * pl.vpl) && (pl.nchunk * pl.chunk_vecs == nvec);
   int tr = (stage_target / row_bytes / tr_unit) * tr_unit;
   if (tr < tr_unit) tr = tr_unit;
   if (tr * row_bytes > 2 * kStageCap) tr = 1;
@@ -266,7 +273,7 @@ Plan plan(int R, int C, int npair, int nsm, bool norm) {
 }
 
 cudaError_t launch(const Params& p0, const Plan& pl, int src, int in, int epi, cudaStream_t st, bool pdl) {
-  void* k = pick(src, in, epi, pl.vpl);
+  void* k = pick(src, in, epi, pl.vpl, pl.full);
   if (!k || !pl.ok) return cudaErrorInvalidValue;
   Params p = p0;
   p.ncta = pl.ncta;

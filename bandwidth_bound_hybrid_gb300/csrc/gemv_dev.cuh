@@ -241,7 +241,9 @@ __device__ __forceinline__ float dot8_acc(const uint4 w, const float* x, float a
 // the rows i = rg (mod nrg) of every tile and finishes two items per pass
 // (rows i and i + nrg, or the gate and up rows of row i) with one paired
 // butterfly; addresses advance by a fixed row stride, without divisions.
-template <int VPL, int SRC, int NPAIR>
+// FULL: every lane's VPL vectors lie inside its chunk (chunk_vecs == 32 VPL),
+// so no vector is predicated off and a dense row's vectors sit 512 bytes apart.
+template <int VPL, int SRC, int NPAIR, bool FULL>
 __device__ __forceinline__ void consume_tile(const Params& p, const LaneSlice<VPL>& L, const uint8_t* st, int rows,
                                              int row0, int rows_cta, float* red, int lane) {
   // byte offset of this lane's vector u within a row, and the row stride
@@ -254,7 +256,7 @@ __device__ __forceinline__ void consume_tile(const Params& p, const LaneSlice<VP
   } else {
     stride = p.C * 2;
 #pragma unroll
-    for (int u = 0; u < VPL; ++u) uoff[u] = L.off[u];
+    for (int u = 0; u < VPL; ++u) uoff[u] = FULL ? L.off[0] + 512 * u : L.off[u];
   }
   const int member_bytes = rows * stride;  // gate rows, then up rows (pairs)
   const int step = (NPAIR == 2) ? L.nrg : 2 * L.nrg;
@@ -274,16 +276,19 @@ __device__ __forceinline__ void consume_tile(const Params& p, const LaneSlice<VP
       has2 = i1 < rows;
       p1 = has2 ? st + i1 * stride : p0;
     }
-    float a0 = 0.f, a1 = 0.f;
+    // four independent packed accumulator pairs: item x (vector parity)
+    float e0[2] = {0.f, 0.f}, o0[2] = {0.f, 0.f}, e1[2] = {0.f, 0.f}, o1[2] = {0.f, 0.f};
 #pragma unroll
     for (int u = 0; u < VPL; ++u) {
-      if (L.valid[u]) {
+      if (FULL || L.valid[u]) {
         const uint4 w0 = *reinterpret_cast<const uint4*>(p0 + uoff[u]);
         const uint4 w1 = *reinterpret_cast<const uint4*>(p1 + uoff[u]);
-        a0 = dot8_acc(w0, L.xr[u], a0);
-        a1 = dot8_acc(w1, L.xr[u], a1);
+        dot8_acc2(w0, L.xr[u], e0[u & 1], o0[u & 1]);
+        dot8_acc2(w1, L.xr[u], e1[u & 1], o1[u & 1]);
       }
     }
+    const float a0 = (e0[0] + o0[0]) + (e0[1] + o0[1]);
+    const float a1 = (e1[0] + o1[0]) + (e1[1] + o1[1]);
     // paired butterfly: lanes 0..15 finish the first item, lanes 16..31 the second
     float keep = (lane < 16) ? a0 : a1;
     keep += __shfl_xor_sync(0xffffffffu, (lane < 16) ? a1 : a0, 16);

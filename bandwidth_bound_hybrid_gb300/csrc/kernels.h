@@ -29,9 +29,15 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 // launch, so that it runs beside the GEMV instead of after it.
 constexpr int kMaxRegs = HY_GEMV_MAXREG;
 constexpr int kMaxStages = 8;
-constexpr int kStageTarget = 60 * 1024;     // preferred bytes per pipeline stage
-constexpr int kStageCap = 60 * 1024;        // largest preferred minimum tile
-constexpr int kInFlight = 180 * 1024;       // bytes kept in flight per CTA in shared memory
+#ifndef HY_GEMV_STAGE_KB
+#define HY_GEMV_STAGE_KB 60
+#endif
+#ifndef HY_GEMV_INFLIGHT_KB
+#define HY_GEMV_INFLIGHT_KB 180
+#endif
+constexpr int kStageTarget = HY_GEMV_STAGE_KB * 1024;  // preferred bytes per pipeline stage
+constexpr int kStageCap = HY_GEMV_STAGE_KB * 1024;     // largest preferred minimum tile
+constexpr int kInFlight = HY_GEMV_INFLIGHT_KB * 1024;  // bytes kept in flight per CTA in shared memory
 constexpr int kPrefetchAhead = 0;           // bytes the L2 prefetch cursor runs ahead of the ring
 constexpr int kMaxSmem = 220 * 1024;        // dynamic; leaves room for static shared data
 constexpr int kCtasPerSm = 1;
@@ -93,6 +99,7 @@ struct Params {
 struct Plan {
   int ncta, tile_rows, nchunk, chunk_vecs, vpl, stage_bytes, nstages, rows_cta_max, xs_floats, gs_floats, smem;
   int pre_stages, pf_ahead;
+  bool full;  // every lane's vectors lie inside its column chunk
   bool ok;
 };
 
