@@ -27,6 +27,7 @@ HY_GUARD_BAD_POSITION = 4
 HY_FLAG_DEBUG = 1
 HY_FLAG_NO_GRAPH = 2
 HY_FLAG_NO_PDL = 4
+HY_FLAG_PERSISTENT = 8
 
 HY_NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -67,6 +68,7 @@ SIGNATURES = {
     "hy_seq_reset": (ctypes.c_int, [vp, i32, vp]),
     "hy_seq_len": (i32, [vp, i32]),
     "hy_seq_capacity": (i32, [vp, i32]),
+    "hy_step_kernels": (i32, [vp]),
     "hy_prefill": (ctypes.c_int, [vp, vp, i32, vp, i32, vp, vp]),
     "hy_decode_step": (ctypes.c_int, [vp, vp, P(i32), i32, vp, vp, vp, vp]),
     "hy_decode_step_host": (ctypes.c_int, [vp, vp, P(i32), i32, vp, vp, vp, vp]),

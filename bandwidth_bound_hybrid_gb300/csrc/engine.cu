@@ -55,6 +55,7 @@ int ensure_init(int dev) {
   if (g_inited[dev]) return HY_OK;
   HY_CK(gemv::init());
   HY_CK(attn::init());
+  HY_CK(step::init());
   g_inited[dev] = true;
   return HY_OK;
 }
@@ -89,6 +90,7 @@ struct hy_model {
   int y_len = 0, o_len = 0, h_len = 0;
   int splits = 1;
   bool moe = false, pdl = true, graphs = true, debug = false;
+  bool persistent = false;  // the step as one cooperative kernel (when the shape allows it)
 };
 
 struct hy_cache {
@@ -109,6 +111,16 @@ struct hy_cache {
   int* dbg_rids = nullptr;
   std::vector<void*> allocs;
   cudaStream_t cap_stream = nullptr;
+  unsigned* step_bar = nullptr;  // grid barrier of the persistent step kernel
+  int last_kernels = 0;          // kernels of the last recorded step
+  struct Prog {
+    int seq;
+    float* logits;
+    int* ids;
+    step::Phase* dev;
+    step::Program pr;
+  };
+  std::vector<Prog> progs;
   struct Graph {
     int seq;
     float* logits;
@@ -204,13 +216,13 @@ int launch_ops(hy_model* m, std::vector<StepOp>& ops, cudaStream_t st) {
   return HY_OK;
 }
 
-// Issue every kernel of one decode step for sequence `seq` on `st`.
-int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) {
+// The operations of one decode step for sequence `seq`, in order.
+int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepOp>& ops) {
   hy_model* m = c->m;
   const hy_config& cf = m->cfg;
   const int H = cf.hidden;
   int* pos = c->d_len + seq;
-  std::vector<StepOp> ops;
+  ops.clear();
   ops.reserve(8 * cf.n_layers + 2);
 
   auto gemv_base = [&]() {
@@ -401,6 +413,146 @@ int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) 
     int rc = run(p, gemv::kSrcDense, gemv::kInX, gemv::kEpiArgmax, "lm-head");
     if (rc != HY_OK) return rc;
   }
+  return HY_OK;
+}
+
+int env_kb(const char* name, int dflt_kb) {
+  const char* v = getenv(name);
+  return ((v && *v) ? atoi(v) : dflt_kb) * 1024;
+}
+
+// The step's operations as phases of the persistent kernel; false when some
+// operation has no persistent form (the step then runs one kernel per
+// operation).
+bool build_program(hy_cache* c, const std::vector<StepOp>& ops, std::vector<step::Phase>& phases,
+                   step::Program& pr) {
+  hy_model* m = c->m;
+  const hy_config& cf = m->cfg;
+  memset(&pr, 0, sizeof(pr));
+  pr.hd = m->n_attn ? cf.head_dim : 64;
+  pr.G = m->n_attn ? cf.attn_q_heads / cf.attn_kv_heads : 2;
+  pr.epl = m->n_gdn ? cf.gdn_dk / 32 : (pr.hd == 64 ? 2 : 4);
+  if (!step::supported(pr.hd, pr.G, pr.epl)) return false;
+  const int pf = env_kb("HY_STEP_PREFETCH_KB", 128);
+  size_t region = 0, scratch = 1;
+  int stage = 0;
+  phases.assign(ops.size(), step::Phase());
+  for (size_t i = 0; i < ops.size(); ++i) {
+    const StepOp& o = ops[i];
+    step::Phase& ph = phases[i];
+    memset(&ph, 0, sizeof(ph));
+    if (o.kind == StepOp::kGemv) {
+      const int npair = o.epi == gemv::kEpiSwiglu ? 2 : 1;
+      const gemv::Plan pl = gemv::plan(o.g.R, o.g.C, npair, m->nsm, o.g.norm_g != nullptr);
+      if (!pl.ok || pl.vpl > 5 || !pl.full) return false;
+      ph.kind = step::kGemv;
+      ph.src = o.src;
+      ph.in = o.in;
+      ph.epi = o.epi;
+      ph.vpl = pl.vpl;
+      ph.full = 1;
+      ph.pf_bytes = o.src == gemv::kSrcDense ? pf : 0;
+      ph.g = o.g;
+      ph.g.n_nx = 0;
+      ph.g.ncta = pl.ncta;
+      ph.g.tile_rows = pl.tile_rows;
+      ph.g.nchunk = pl.nchunk;
+      ph.g.chunk_vecs = pl.chunk_vecs;
+      ph.g.stage_bytes = pl.stage_bytes;
+      ph.g.nstages = 0;
+      ph.g.rows_cta_max = pl.rows_cta_max;
+      ph.g.xs_floats = pl.xs_floats;
+      ph.g.gs_floats = pl.gs_floats;
+      ph.g.pre_stages = 0;
+      ph.g.pf_ahead = 0;
+      ph.g.npair = npair;
+      stage = std::max(stage, pl.stage_bytes);
+      region = std::max(region, (size_t)4 * (pl.xs_floats + pl.gs_floats +
+                                              ((pl.rows_cta_max * npair * pl.nchunk + 1) & ~1)));
+      if (o.epi == gemv::kEpiRouter) scratch = std::max(scratch, (size_t)o.g.n_experts + 1);
+    } else if (o.kind == StepOp::kGdn) {
+      if (o.d.dk != 32 * pr.epl) return false;
+      ph.kind = step::kGdn;
+      ph.d = o.d;
+      ph.pf_bytes = 1;
+      region = std::max(region, step::gdn_work_bytes(pr.epl));
+    } else if (o.kind == StepOp::kAttn) {
+      if (o.a.hd != pr.hd || o.a.nq / o.a.nkv != pr.G) return false;
+      ph.kind = step::kAttn;
+      ph.a = o.a;
+      region = std::max(region, step::attn_work_bytes(pr.hd, pr.G));
+      stage = std::max(stage, step::attn_stage_bytes(pr.hd));
+      scratch = std::max(scratch, (size_t)o.a.nsplit * pr.G + pr.G);
+    } else {
+      ph.kind = step::kCopy;
+      ph.csrc = o.csrc;
+      ph.cdst = o.cdst;
+      ph.cn = o.cn;
+    }
+  }
+  pr.nphases = (int)phases.size();
+  pr.bar = c->step_bar;
+  pr.guard = c->guard;
+  pr.stage_bytes = stage;
+  pr.region_bytes = (int)((region + 15) & ~(size_t)15);
+  pr.scratch_floats = (int)scratch;
+  int ns = env_kb("HY_STEP_INFLIGHT_KB", 180) / std::max(stage, 1);
+  ns = std::max(2, std::min(ns, step::kMaxStagesStep));
+  for (pr.nstages = ns; pr.nstages >= 2 && !step::smem_bytes(pr); --pr.nstages) {
+  }
+  if (pr.nstages < 2 || !step::smem_bytes(pr)) return false;
+  return step::blocks_per_sm(pr) >= 1;
+}
+
+// The persistent program of (seq, logits, ids): built and copied to the
+// device on first use.  Allocates, so never call it while capturing.
+int get_program(hy_cache* c, int seq, float* logits, int* ids, const step::Program** out) {
+  *out = nullptr;
+  for (auto& p : c->progs)
+    if (p.seq == seq && p.logits == logits && p.ids == ids) {
+      *out = &p.pr;
+      return HY_OK;
+    }
+  std::vector<StepOp> ops;
+  int rc = collect_ops(c, seq, logits, ids, ops);
+  if (rc != HY_OK) return rc;
+  std::vector<step::Phase> phases;
+  step::Program pr;
+  if (!build_program(c, ops, phases, pr)) {
+    c->m->persistent = false;  // this shape runs one kernel per operation
+    return HY_OK;
+  }
+  void* dev = nullptr;
+  HY_CK(cudaMalloc(&dev, phases.size() * sizeof(step::Phase)));
+  cudaError_t e = cudaMemcpy(dev, phases.data(), phases.size() * sizeof(step::Phase), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(dev);
+    return fail(HY_ERR_CUDA, "program upload: %s", cudaGetErrorString(e));
+  }
+  pr.phases = reinterpret_cast<step::Phase*>(dev);
+  c->progs.push_back({seq, logits, ids, reinterpret_cast<step::Phase*>(dev), pr});
+  *out = &c->progs.back().pr;
+  return HY_OK;
+}
+
+// Issue one decode step for sequence `seq` on `st`: the persistent kernel
+// (its program must exist), or one kernel per operation.
+int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) {
+  hy_model* m = c->m;
+  if (m->persistent) {
+    for (auto& p : c->progs)
+      if (p.seq == seq && p.logits == logits && p.ids == ids) {
+        cudaError_t e = step::launch(p.pr, m->nsm, st);
+        if (e != cudaSuccess) return fail(HY_ERR_CUDA, "step launch: %s", cudaGetErrorString(e));
+        c->last_kernels = 1;
+        return HY_OK;
+      }
+    return fail(HY_ERR_ARG, "no step program for sequence %d", seq);
+  }
+  std::vector<StepOp> ops;
+  int rc = collect_ops(c, seq, logits, ids, ops);
+  if (rc != HY_OK) return rc;
+  c->last_kernels = (int)ops.size();
   return launch_ops(m, ops, st);
 }
 
@@ -413,6 +565,11 @@ int get_graph(hy_cache* c, int seq, float* logits, int* ids, cudaGraphExec_t* ou
   if (c->graphs.size() >= 16) {
     cudaGraphExecDestroy(c->graphs.front().exec);
     c->graphs.erase(c->graphs.begin());
+  }
+  if (c->m->persistent) {
+    const step::Program* pr = nullptr;
+    int rc0 = get_program(c, seq, logits, ids, &pr);
+    if (rc0 != HY_OK) return rc0;
   }
   HY_CK(cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
   int rc = record_step(c, seq, logits, ids, c->cap_stream);
@@ -434,7 +591,14 @@ int get_graph(hy_cache* c, int seq, float* logits, int* ids, cudaGraphExec_t* ou
 
 // one step of sequence `seq` whose token id is already in c->tok
 int run_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) {
-  if (!c->m->graphs) return record_step(c, seq, logits, ids, st);
+  if (!c->m->graphs) {
+    if (c->m->persistent) {
+      const step::Program* pr = nullptr;
+      int rc0 = get_program(c, seq, logits, ids, &pr);
+      if (rc0 != HY_OK) return rc0;
+    }
+    return record_step(c, seq, logits, ids, st);
+  }
   cudaGraphExec_t exec;
   int rc = get_graph(c, seq, logits, ids, &exec);
   if (rc != HY_OK) return rc;
@@ -476,6 +640,8 @@ int check_model_cfg(const hy_config* c) {
 void free_cache_mem(hy_cache* c) {
   for (auto& g : c->graphs) cudaGraphExecDestroy(g.exec);
   c->graphs.clear();
+  for (auto& p : c->progs) cudaFree(p.dev);
+  c->progs.clear();
   for (void* p : c->allocs) cudaFree(p);
   c->allocs.clear();
   for (uint8_t* p : c->mem) cudaFree(p);
@@ -569,6 +735,7 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
   m->pdl = !(c.flags & HY_FLAG_NO_PDL);
   m->graphs = !(c.flags & HY_FLAG_NO_GRAPH);
   m->debug = (c.flags & HY_FLAG_DEBUG) != 0;
+  m->persistent = (c.flags & HY_FLAG_PERSISTENT) != 0;
   *out = m;
   g_err.clear();
   return HY_OK;
@@ -622,7 +789,7 @@ int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, 
       (rc = dalloc(c, &c->rlog, std::max(cf.n_experts + 1, 1))) || (rc = dalloc(c, &c->moe_w, gemv::kMaxTopK + 4)) ||
       (rc = dalloc(c, &c->moe_ids, 16)) || (rc = dalloc(c, &c->tok, max_seqs)) || (rc = dalloc(c, &c->ids, max_seqs)) ||
       (rc = dalloc(c, &c->cnt_attn, std::max(cf.attn_kv_heads, 1))) || (rc = dalloc(c, &c->cnt_am, 1)) ||
-      (rc = dalloc(c, &c->cnt_router, 1)) || (rc = dalloc(c, &c->guard, 1)) ||
+      (rc = dalloc(c, &c->cnt_router, 1)) || (rc = dalloc(c, &c->guard, 1)) || (rc = dalloc(c, &c->step_bar, 1)) ||
       (rc = dalloc(c, &c->logits_buf, (size_t)cf.vocab))) {
     free_cache_mem(c);
     delete c;
@@ -680,6 +847,7 @@ int hy_seq_reset(hy_cache* c, int32_t seq, void* stream) {
 
 int32_t hy_seq_len(const hy_cache* c, int32_t seq) { return valid_seq(c, seq) ? c->len[seq] : -1; }
 int32_t hy_seq_capacity(const hy_cache* c, int32_t seq) { return valid_seq(c, seq) ? c->cap[seq] : -1; }
+int32_t hy_step_kernels(const hy_cache* c) { return c ? c->last_kernels : 0; }
 
 int hy_prefill(hy_model* m, hy_cache* c, int32_t seq, const int32_t* tokens_dev, int32_t n, float* logits_dev,
                void* stream) {

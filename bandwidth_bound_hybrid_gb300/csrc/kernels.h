@@ -152,6 +152,53 @@ cudaError_t launch(const Params& p, cudaStream_t st, bool pdl);
 cudaError_t rope_table(float2* tab, int cap, int hd, double theta, cudaStream_t st);
 }  // namespace attn
 
+// ---------------------------------------------------------------- persistent step
+// The whole decode step as one cooperative kernel: one CTA per SM runs the
+// step's kernels as phases separated by grid barriers, and its copy lane keeps
+// streaming across phase boundaries.
+namespace step {
+enum Kind : int { kGemv = 0, kGdn = 1, kAttn = 2, kCopy = 3 };
+struct alignas(16) Phase {
+  int kind;
+  int src, in, epi, vpl, full;  // GEMV launch variant (full: every lane's vectors inside its chunk)
+  int pf_bytes;                 // L2 prefetch of this phase's first bytes per CTA, issued during the previous phase
+  int pad_;
+  gemv::Params g;  // plan fields filled for ncta = the grid (CTAs past g.ncta idle in this phase)
+  gdn::Params d;
+  attn::Params a;
+  const float* csrc;  // kCopy: csrc[0, cn) -> cdst
+  float* cdst;
+  int cn, pad2_;
+};
+struct Program {
+  const Phase* phases;  // device array
+  int nphases;
+  unsigned* bar;        // grid-barrier arrivals; zero at launch, reset by the last arrival of the step
+  unsigned* guard;
+  int stage_bytes, nstages;
+  int region_bytes;     // per-phase working area (input vector, gain, partial sums / attention / DeltaNet)
+  int scratch_floats;   // router logits or split-merge weights
+  int hd, G, epl;       // attention and DeltaNet shapes the kernel is instantiated for
+};
+constexpr int kNW = gemv::kConsumerWarps;   // compute warps
+constexpr int kThreads = (kNW + 1) * 32;
+constexpr int kMaxSmem = 226 * 1024;  // dynamic; the rest is static shared data
+constexpr int kMaxStagesStep = 8;
+// Shared memory of a program, or 0 when it does not fit.
+size_t smem_bytes(const Program& pr);
+// Whether a kernel is instantiated for (hd, G, epl).
+bool supported(int hd, int G, int epl);
+// Working-area bytes of an attention item and of a DeltaNet item, and the
+// ring stage an attention tile needs.
+size_t attn_work_bytes(int hd, int G);
+size_t gdn_work_bytes(int epl);
+int attn_stage_bytes(int hd);
+// CTAs of the program's kernel that fit on one SM (0: none).
+int blocks_per_sm(const Program& pr);
+cudaError_t init();
+cudaError_t launch(const Program& pr, int nctas, cudaStream_t st);
+}  // namespace step
+
 // Record `msg` as the calling thread's last error (hy_last_error) and return
 // `code`; for C-ABI entry points defined outside engine.cu.
 int set_error(int code, const char* msg);

@@ -104,6 +104,10 @@ class HybridModel:
     def seq_capacity(self, seq: int) -> int:
         return int(capi.lib().hy_seq_capacity(self.c, seq))
 
+    def step_kernels(self) -> int:
+        """Kernels the last recorded decode step launches (1: the persistent step)."""
+        return int(capi.lib().hy_step_kernels(self.c))
+
     def reset(self, seq: int, stream=None) -> None:
         check(capi.lib().hy_seq_reset(self.c, seq, _stream(stream)), "hy_seq_reset")
 

@@ -48,6 +48,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernel-timing", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="no programmatic dependent launch between kernels")
+    ap.add_argument("--persistent", action="store_true", help="run the step as one persistent cooperative kernel")
     return ap.parse_args(argv)
 
 
@@ -227,7 +228,8 @@ def run_ours(args):
     weights = workloads.device_weights(shape)
     cap = prompt + args.warmup + 2 * args.steps + 16
     from bandwidth_bound_hybrid_gb300 import capi as _capi
-    model = HybridModel(shape, weights, [cap], splits=args.splits, flags=_capi.HY_FLAG_NO_PDL if args.no_pdl else 0)
+    flags = (_capi.HY_FLAG_NO_PDL if args.no_pdl else 0) | (_capi.HY_FLAG_PERSISTENT if args.persistent else 0)
+    model = HybridModel(shape, weights, [cap], splits=args.splits, flags=flags)
     toks = torch.from_numpy(workloads.prompt_ids(w, n=prompt)).to(dev) if prompt else None
     ids = torch.zeros(1, dtype=torch.int32, device=dev)
     if prompt:
@@ -347,7 +349,8 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": n * e2e_steps / e2e_t, "unit": "tokens/s", "h2d_bytes_per_step": 4,
                     "d2h_bytes_per_step": 4},
-            "gpu_launches": acc.kernels_per_step(shape) * args.steps,
+            "gpu_launches": model.step_kernels() * args.steps,
+            "kernels_per_step": model.step_kernels(),
             "graph_launches_per_token": 1,
             "clocks": clk,
         }

@@ -55,6 +55,7 @@ extern "C" {
 #define HY_FLAG_DEBUG 1u    /* keep per-layer hidden states and router results of the last step */
 #define HY_FLAG_NO_GRAPH 2u /* launch kernels one by one instead of replaying a CUDA graph */
 #define HY_FLAG_NO_PDL 4u   /* no programmatic dependent launch between kernels */
+#define HY_FLAG_PERSISTENT 8u /* run the step as one persistent cooperative kernel (phases and grid barriers) */
 
 /* Model shape.  [Strata] "The Beast: Qwen 3.5 Hybrid Architecture": Gated
  * DeltaNet layers with a fixed FP32 state plus full GQA layers with a bf16 KV
@@ -149,6 +150,11 @@ int hy_seq_reset(hy_cache* c, int32_t seq, void* stream);
  * context_exhausted()). */
 int32_t hy_seq_len(const hy_cache* c, int32_t seq);
 int32_t hy_seq_capacity(const hy_cache* c, int32_t seq);
+
+/* Kernels the last recorded decode step launches: 1 when the whole step runs
+ * as one persistent kernel (HY_FLAG_PERSISTENT), else one per operation.  0
+ * before any step. */
+int32_t hy_step_kernels(const hy_cache* c);
 
 /* Run the n prompt tokens tokens_dev[0..n) of sequence `seq` through the
  * model one position at a time, filling its caches.  logits_dev (nullable)
