@@ -77,6 +77,8 @@ SIGNATURES = {
     "hy_debug_router": (ctypes.c_int, [vp, i32, vp, vp, vp]),
     "hy_op_gemv": (ctypes.c_int, [vp, i32, i32, vp, vp, f32, vp, i32, vp]),
     "hy_op_gemv_swiglu": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, f32, vp, vp]),
+    "hy_op_gemv_batch": (ctypes.c_int, [P(hy_tensor), P(hy_tensor), i32, i32, i32, i32, vp, i32, vp, f32, vp, i32, i32,
+                                        vp]),
     "hy_op_argmax_workspace": (sz, []),
     "hy_op_gemv_argmax": (ctypes.c_int, [vp, i32, i32, vp, vp, f32, vp, vp, vp, vp]),
     "hy_op_gdn_step": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp]),

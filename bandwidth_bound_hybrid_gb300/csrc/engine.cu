@@ -56,6 +56,7 @@ int ensure_init(int dev) {
   HY_CK(gemv::init());
   HY_CK(attn::init());
   HY_CK(step::init());
+  HY_CK(bgemv::init());
   g_inited[dev] = true;
   return HY_OK;
 }
@@ -1005,6 +1006,46 @@ int hy_op_gemv_swiglu(const void* Wg_dev, const void* Wu_dev, int32_t rows, int3
   p.eps = eps;
   p.y = h_dev;
   return op_gemv_run(p, gemv::kInX, gemv::kEpiSwiglu, stream);
+}
+
+int hy_op_gemv_batch(const hy_tensor* w, const hy_tensor* w_up, int32_t weight_format, int32_t rows, int32_t cols,
+                     int32_t batch, const float* x_dev, int32_t ldx, const float* norm_g_dev, float eps, float* y_dev,
+                     int32_t ldy, int32_t accumulate, void* stream) {
+  if (!w || !aligned16(w->w) || !x_dev || !y_dev || rows <= 0 || cols <= 0 || batch < 1 ||
+      batch > bgemv::kMaxB || ldx < cols || ldy < rows || (weight_format != 0 && weight_format != 1))
+    return fail(HY_ERR_ARG, "bad batched GEMV arguments");
+  if (weight_format == 1 && !aligned16(w->scales)) return fail(HY_ERR_ARG, "4-bit weights need scales");
+  if (w_up && (!aligned16(w_up->w) || (weight_format == 1 && !aligned16(w_up->scales))))
+    return fail(HY_ERR_ARG, "bad up matrix");
+  unsigned* guard = nullptr;
+  int rc = op_guard(&guard);
+  if (rc != HY_OK) return rc;
+  bgemv::Params p;
+  memset(&p, 0, sizeof(p));
+  p.fmt = weight_format;
+  p.in = bgemv::kInX;
+  p.epi = w_up ? bgemv::kEpiSwiglu : (accumulate ? bgemv::kEpiResid : bgemv::kEpiStore);
+  p.W[0] = (const uint8_t*)w->w;
+  p.S[0] = (const uint16_t*)w->scales;
+  if (w_up) {
+    p.W[1] = (const uint8_t*)w_up->w;
+    p.S[1] = (const uint16_t*)w_up->scales;
+  }
+  p.R = rows;
+  p.C = cols;
+  p.B = batch;
+  p.x = x_dev;
+  p.ldx = ldx;
+  p.norm_g = norm_g_dev;
+  p.eps = eps;
+  p.y = y_dev;
+  p.ldy = ldy;
+  p.guard = guard;
+  const bgemv::Plan pl = bgemv::plan(rows, cols, weight_format, p.epi, op_nsm());
+  if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no batched GEMV plan for %d x %d (format %d)", rows, cols, weight_format);
+  cudaError_t e = bgemv::launch(p, pl, (cudaStream_t)stream, false);
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "batched GEMV launch: %s", cudaGetErrorString(e));
+  return HY_OK;
 }
 
 size_t hy_op_argmax_workspace(void) { return 256 + 1024 * 8; }

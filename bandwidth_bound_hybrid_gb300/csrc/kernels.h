@@ -152,6 +152,53 @@ cudaError_t launch(const Params& p, cudaStream_t st, bool pdl);
 cudaError_t rope_table(float2* tab, int cap, int hd, double theta, cudaStream_t st);
 }  // namespace attn
 
+// ---------------------------------------------------------------- batched GEMV
+// Up to kMaxB token vectors through one weight stream (tensor-core MMA), bf16
+// or 4-bit block weights.
+namespace bgemv {
+constexpr int kWarps = 8;
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kMaxB = 8;
+constexpr int kTileRows = 16;
+constexpr int kMaxStages = 8;
+constexpr int kInFlight = 160 * 1024;
+constexpr int kMaxSmem = 220 * 1024;
+enum Fmt : int { kFmtBf16 = 0, kFmtQ4 = 1 };
+enum In : int { kInX = 0, kInEmbed = 1 };
+enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiArgmax = 3 };
+struct Params {
+  int fmt, in, epi;
+  const uint8_t* W[2];      // bf16 [R][C] or packed nibbles [R][C/2] (W[1]: up matrix of a gate/up pair)
+  const uint16_t* S[2];     // 4-bit: fp16 scales [R][C/32]
+  int R, C, B;
+  const float* x;           // kInX: [B][ldx]
+  int ldx;
+  const uint16_t* embed;    // kInEmbed: bf16 [vocab][C]
+  const int* tok;           // kInEmbed: [B]
+  int vocab;
+  float* x_out;             // kInEmbed: residual streams to initialise [B][ldx_out] (CTA 0)
+  int ldx_out;
+  const float* norm_g;      // per-token RMSNorm gain (null: none)
+  float eps;
+  float* y;                 // [B][ldy]: store / residual / SwiGLU / logits (nullable for argmax)
+  int ldy;
+  float* part_val;          // argmax partials [ncta][kMaxB]
+  int* part_idx;
+  unsigned* counter;        // argmax ticket (zero between launches)
+  int* ids_out;             // [B]
+  int* len_inc[kMaxB];      // per token, incremented after the argmax (nullable)
+  int ncta, nstages, rows_cta_max;
+  unsigned* guard;
+};
+struct Plan {
+  int ncta, nstages, rows_cta_max, smem;
+  bool ok;
+};
+Plan plan(int R, int C, int fmt, int epi, int nsm);
+cudaError_t init();
+cudaError_t launch(const Params& p, const Plan& pl, cudaStream_t st, bool pdl);
+}  // namespace bgemv
+
 // ---------------------------------------------------------------- persistent step
 // The whole decode step as one cooperative kernel: one CTA per SM runs the
 // step's kernels as phases separated by grid barriers, and its copy lane keeps

@@ -206,6 +206,21 @@ int hy_op_gemv(const void* W_dev, int32_t rows, int32_t cols, const float* x_dev
 int hy_op_gemv_swiglu(const void* Wg_dev, const void* Wu_dev, int32_t rows, int32_t cols, const float* x_dev,
                       const float* norm_g_dev, float eps, float* h_dev, void* stream);
 
+/* Batched GEMV over `batch` (1..8) token vectors through one weight stream:
+ * y[b] = W * xhat[b] (accumulate != 0: y[b] += ...), or with w_up non-null
+ * y[b] = silu(W * xhat[b]) * (W_up * xhat[b]).  xhat[b] = x[b], or its
+ * RMSNorm times norm_g.  x_dev [batch][ldx], y_dev [batch][ldy] FP32.
+ * weight_format 0: bf16 W.w [rows][cols]; 1: 4-bit blocks of 32 along cols,
+ * W.w packed nibbles [rows][cols/2] (byte i of a block holds elements i and
+ * i+16 as value+8), W.scales fp16 [rows][cols/32]; cols % 256 == 0.  The
+ * products run on the tensor cores with xhat rounded to the MMA operand type
+ * (bf16 for bf16 weights, FP16 for 4-bit weights); 4-bit weights are
+ * dequantised exactly.  [Strata] "Act 5" (batched decode rows),
+ * [Flash] "Correctness fixes" (the 4-bit block layout). */
+int hy_op_gemv_batch(const hy_tensor* w, const hy_tensor* w_up, int32_t weight_format, int32_t rows, int32_t cols,
+                     int32_t batch, const float* x_dev, int32_t ldx, const float* norm_g_dev, float eps, float* y_dev,
+                     int32_t ldy, int32_t accumulate, void* stream);
+
 /* Greedy head: logits = W * xhat (logits_dev nullable), *id_dev = argmax
  * (lowest index on ties).  workspace_dev: hy_op_argmax_workspace() bytes,
  * zeroed before its first use and left zeroed after each call.
