@@ -37,7 +37,19 @@ struct Smem {
 };
 
 template <int HD, int G>
-__global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p) {
+__global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p0) {
+  Params p = p0;
+  if (p0.nb > 0) {  // token blockIdx.z of a batch: its sequence's cache and scratch
+    const int z = blockIdx.z;
+    p.y = p0.y + (long long)z * p0.ld_y;
+    p.o = p0.o + (long long)z * p0.ld_o;
+    p.part = p0.part + (long long)z * p0.ld_part;
+    p.counter = p0.counter + z * p0.nkv;
+    p.K = p0.K_b[z];
+    p.V = p0.V_b[z];
+    p.len = p0.len_b[z];
+    p.cap = p0.cap_b[z];
+  }
   using S_ = Smem<HD, G>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
@@ -166,7 +178,9 @@ cudaError_t launch(const Params& p, cudaStream_t st, bool pdl) {
   size_t smem = 0;
   void* k = pick(p.hd, p.nq / p.nkv, &smem);
   if (!k) return cudaErrorInvalidValue;
-  return launch_k(reinterpret_cast<void (*)(Params)>(k), dim3(p.nkv, p.nsplit), dim3(kThreads), smem, st, pdl, p);
+  if (p.nb < 0 || p.nb > 8) return cudaErrorInvalidValue;
+  return launch_k(reinterpret_cast<void (*)(Params)>(k), dim3(p.nkv, p.nsplit, p.nb > 0 ? p.nb : 1), dim3(kThreads),
+                  smem, st, pdl, p);
 }
 
 cudaError_t rope_table(float2* tab, int cap, int hd, double theta, cudaStream_t st) {

@@ -16,8 +16,10 @@
 //     and one packed subtract), the block scale is applied to the FP32 result
 //     of the block's two MMAs, so the weights are dequantised exactly;
 //   * the token vectors are RMS-normalised per token and stored once per CTA
-//     in shared memory as FP16 (4-bit weights) or bf16 (bf16 weights, the MMA
-//     needs one operand type), in the K order the weight fragments use;
+//     in shared memory as FP16 (4-bit weights), or for bf16 weights (the MMA
+//     needs one operand type) as two bf16 parts hi + lo, each multiplied by
+//     the weights, so the products keep about 16 bits of the FP32 vector; in
+//     the K order the weight fragments use;
 //   * per tile the eight warps' partial sums are reduced in a fixed order, and
 //     the CTA's rows are finished at the end: store, residual add, SwiGLU or a
 //     per-token argmax.
@@ -71,6 +73,7 @@ struct Layout {
   int scale_bytes;   // bytes of one row's scales (unpadded: one copy per tile); 0 for bf16
   int member_bytes;  // one pair member's 16 rows, then their scales
   int x_stride;      // bytes of one staged token vector (padded)
+  int x_parts;       // bf16 weights: the vector as hi + lo bf16 parts (two MMAs); FP16: one part
 };
 
 __device__ __forceinline__ Layout layout_of(const Params& p) {
@@ -84,32 +87,104 @@ __device__ __forceinline__ Layout layout_of(const Params& p) {
   }
   L.member_bytes = kTileRows * (L.row_bytes + L.scale_bytes);
   L.x_stride = p.C * 2 + 16;
+  L.x_parts = p.fmt == kFmtBf16 ? 2 : 1;
   return L;
 }
 
-// Copy lane: rows [a, a + rows) of pair member j into the stage.
-__device__ __forceinline__ void issue_tile(const Params& p, const Layout& L, int a, int rows, uint8_t* dst,
+// Tile t of the launch: its union entry u (0 for dense), first output row a
+// (virtual row for kSrcUnionRows), row count, and the first weight row and
+// scale row of each pair member.
+struct TileSrc {
+  int u, a, rows;
+  const uint8_t* w[2];
+  const uint16_t* sc[2];
+};
+
+__device__ __forceinline__ int checked_union_expert(const Params& p, int u) {
+  int e = p.union_ids[u];
+  if (e < 0) {  // never read outside the expert tensor (the router's ids are < n_experts)
+    set_guard(p.guard, kGuardBadIndex);
+    e = 0;
+  }
+  return e;
+}
+
+__device__ __forceinline__ int tiles_of(const Params& p, int U) {
+  if (p.src == kSrcUnionRows) return (U + 1) * (p.slot_rows / kTileRows);
+  if (p.src == kSrcUnionDown) return (U + 1) * (p.R / kTileRows);
+  return (p.R + kTileRows - 1) / kTileRows;
+}
+
+__device__ __forceinline__ TileSrc tile_src(const Params& p, int t, int U) {
+  TileSrc ts;
+  const long long wb = p.fmt == kFmtBf16 ? (long long)p.C * 2 : p.C / 2;  // bytes of a weight row
+  const long long sb = p.C / 32;                                           // scales of a row (fp16)
+  int wrow;
+  if (p.src == kSrcDense) {
+    ts.u = 0;
+    ts.a = t * kTileRows;
+    ts.rows = min(kTileRows, p.R - ts.a);
+    wrow = ts.a;
+  } else if (p.src == kSrcUnionRows) {
+    ts.a = t * kTileRows;
+    ts.u = ts.a / p.slot_rows;
+    ts.rows = kTileRows;
+    wrow = ts.a - ts.u * p.slot_rows;
+  } else {
+    const int nrb = p.R / kTileRows;
+    ts.u = t / nrb;
+    ts.a = (t - ts.u * nrb) * kTileRows;
+    ts.rows = kTileRows;
+    wrow = ts.a;
+  }
+  for (int j = 0; j < 2; ++j) {
+    const uint8_t* w = p.W[j];
+    const uint16_t* sc = p.S[j];
+    if (p.src != kSrcDense) {
+      if (ts.u < U) {
+        const long long e = checked_union_expert(p, ts.u);
+        w = p.exp_base[j] ? p.exp_base[j] + e * p.exp_stride : nullptr;
+        sc = p.exp_scale[j] ? reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.exp_scale[j]) +
+                                                                 e * p.exp_sstride)
+                            : nullptr;
+      } else {
+        w = p.sh_base[j];
+        sc = p.sh_scale[j];
+      }
+    }
+    ts.w[j] = w ? w + wrow * wb : nullptr;
+    ts.sc[j] = sc ? sc + wrow * sb : nullptr;
+  }
+  return ts;
+}
+
+// Copy lane: the tile's rows of each pair member into the stage.
+__device__ __forceinline__ void issue_tile(const Params& p, const Layout& L, const TileSrc& ts, uint8_t* dst,
                                            uint64_t* bar, uint64_t pol) {
   const int npair = p.epi == kEpiSwiglu ? 2 : 1;
   const uint32_t wb = p.fmt == kFmtBf16 ? p.C * 2 : p.C / 2;
   const uint32_t sb = p.fmt == kFmtBf16 ? 0 : p.C / 16;
-  mbar_arrive_expect_tx(bar, (uint32_t)rows * (wb + sb) * npair);
+  mbar_arrive_expect_tx(bar, (uint32_t)ts.rows * (wb + sb) * npair);
   for (int j = 0; j < npair; ++j) {
     uint8_t* m = dst + j * L.member_bytes;
-    for (int r = 0; r < rows; ++r) bulk_g2s(m + r * L.row_bytes, p.W[j] + (long long)(a + r) * wb, wb, bar, pol);
-    if (sb) bulk_g2s(m + kTileRows * L.row_bytes, p.S[j] + (long long)a * (sb / 2), rows * sb, bar, pol);
+    for (int r = 0; r < ts.rows; ++r) bulk_g2s(m + r * L.row_bytes, ts.w[j] + (long long)r * wb, wb, bar, pol);
+    if (sb) bulk_g2s(m + kTileRows * L.row_bytes, ts.sc[j], ts.rows * sb, bar, pol);
   }
 }
 
 // Compute threads: the token vectors, normalised per token, into xs (FP16 or
 // bf16, permuted for 4-bit weights), zero for padding tokens.  s_red: >= B
 // floats of scratch.
-__device__ __forceinline__ void stage_inputs(const Params& p, const Layout& L, uint8_t* xs, float* s_red, int ctid) {
+__device__ __forceinline__ void stage_inputs(const Params& p, const Layout& L, uint8_t* xs, float* s_red, int ctid,
+                                             long long x_off) {
   const int warp = ctid >> 5, lane = ctid & 31;
   for (int b = 0; b < kMaxB; ++b) {
     uint8_t* row = xs + b * L.x_stride;
     if (b >= p.B) {
-      for (int k = ctid; k < p.C / 2; k += kCT) reinterpret_cast<uint32_t*>(row)[k] = 0u;
+      for (int k = ctid; k < p.C / 2; k += kCT) {
+        reinterpret_cast<uint32_t*>(row)[k] = 0u;
+        if (L.x_parts == 2) reinterpret_cast<uint32_t*>(row + kMaxB * L.x_stride)[k] = 0u;
+      }
       continue;
     }
     const float* src = nullptr;
@@ -122,7 +197,7 @@ __device__ __forceinline__ void stage_inputs(const Params& p, const Layout& L, u
       }
       emb = p.embed + (long long)tok * p.C;
     } else {
-      src = p.x + (long long)b * p.ldx;
+      src = p.x + (long long)b * p.ldx + x_off;
     }
     auto val = [&](int k) { return emb ? bf16_to_f32(emb[k]) : src[k]; };
     float sc = 1.f;
@@ -146,8 +221,13 @@ __device__ __forceinline__ void stage_inputs(const Params& p, const Layout& L, u
       if (p.in == kInEmbed && blockIdx.x == 0) p.x_out[(long long)b * p.ldx_out + k] = v;
       if (p.norm_g) v = v * sc * p.norm_g[k];
       const int pos = xperm(p.fmt, k);
-      if (p.fmt == kFmtBf16) reinterpret_cast<uint16_t*>(row)[pos] = f32_to_bf16_rne(v);
-      else reinterpret_cast<__half*>(row)[pos] = __float2half_rn(v);
+      if (p.fmt == kFmtBf16) {  // v = hi + lo to ~16 bits: the products stay near FP32 accuracy
+        const uint16_t hi = f32_to_bf16_rne(v);
+        reinterpret_cast<uint16_t*>(row)[pos] = hi;
+        reinterpret_cast<uint16_t*>(row + kMaxB * L.x_stride)[pos] = f32_to_bf16_rne(v - bf16_to_f32(hi));
+      } else {
+        reinterpret_cast<__half*>(row)[pos] = __float2half_rn(v);
+      }
     }
   }
   named_barrier(1, kCT);
@@ -159,6 +239,7 @@ __device__ __forceinline__ void tile_mma(const Params& p, const Layout& L, const
                                          int k1, float* d, int lane) {
   const int g = lane >> 2, t = lane & 3;
   const uint8_t* xg = xs + g * L.x_stride;  // token g (the MMA's column n = g)
+  const uint8_t* xl = xg + kMaxB * L.x_stride;  // its lo part (bf16 weights)
   if (p.fmt == kFmtBf16) {
     const uint8_t* r0 = m + g * L.row_bytes;
     const uint8_t* r8 = m + (g + 8) * L.row_bytes;
@@ -170,6 +251,9 @@ __device__ __forceinline__ void tile_mma(const Params& p, const Layout& L, const
       a[3] = *reinterpret_cast<const uint32_t*>(r8 + (k + 8 + 2 * t) * 2);
       b[0] = *reinterpret_cast<const uint32_t*>(xg + (k + 2 * t) * 2);
       b[1] = *reinterpret_cast<const uint32_t*>(xg + (k + 8 + 2 * t) * 2);
+      mma_bf16(d, a, b);
+      b[0] = *reinterpret_cast<const uint32_t*>(xl + (k + 2 * t) * 2);
+      b[1] = *reinterpret_cast<const uint32_t*>(xl + (k + 8 + 2 * t) * 2);
       mma_bf16(d, a, b);
     }
     return;
@@ -224,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const Params p) {
   const int stage_bytes = npair * L.member_bytes;
   uint8_t* stages = smem;
   uint8_t* xs = smem + nst * stage_bytes;                               // [8][C] staged tokens
-  float* part = reinterpret_cast<float*>(xs + kMaxB * L.x_stride);     // [2][npair][kWarps][16][8]
+  float* part = reinterpret_cast<float*>(xs + L.x_parts * kMaxB * L.x_stride);  // [2][npair][kWarps][16][8]
   float* red = part + 2 * npair * kWarps * kTileRows * kMaxB;           // [npair][rows_cta][8]
   uint64_t* full = reinterpret_cast<uint64_t*>(red + npair * p.rows_cta_max * kMaxB);
   uint64_t* empty = full + kMaxStages;
@@ -234,9 +318,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const Params p) {
   __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt = (p.R + kTileRows - 1) / kTileRows;
-  const int t0 = (int)((long long)blockIdx.x * nt / p.ncta), t1 = (int)((long long)(blockIdx.x + 1) * nt / p.ncta);
-  const int r0 = t0 * kTileRows, r1 = min(t1 * kTileRows, p.R);
+  // the tile range of this CTA; for MoE sources it depends on the union the
+  // routing kernel wrote, so it is read after griddepcontrol.wait
+  auto tile_range = [&](int& U, int& t0, int& t1) {
+    U = 0;
+    if (p.src != kSrcDense) {
+      U = *p.n_union;
+      if (U < 0 || U > kMaxUnion) {
+        set_guard(p.guard, kGuardBadIndex);
+        U = 0;
+      }
+    }
+    const int nt = tiles_of(p, U);
+    t0 = (int)((long long)blockIdx.x * nt / p.ncta);
+    t1 = (int)((long long)(blockIdx.x + 1) * nt / p.ncta);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < nst; ++s) {
@@ -252,17 +348,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const Params p) {
     pdl_launch_dependents();
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      int t = 0;
-      for (int a = r0; a < r1; a += kTileRows, ++t) {
-        const int rows = min(kTileRows, r1 - a);
-        const int s = t % nst, k = t / nst;
-        if (t >= nst && !mbar_wait(&empty[s], (k - 1) & 1)) {
+      if (p.src != kSrcDense) pdl_wait();  // union and expert ids come from the routing kernel
+      int U, t0, t1;
+      tile_range(U, t0, t1);
+      int n = 0;
+      for (int t = t0; t < t1; ++t, ++n) {
+        const int s = n % nst, k = n / nst;
+        if (n >= nst && !mbar_wait(&empty[s], (k - 1) & 1)) {
           set_guard(p.guard, kGuardWaitTimeout);
           break;
         }
-        issue_tile(p, L, a, rows, stages + s * stage_bytes, &full[s], pol);
+        issue_tile(p, L, tile_src(p, t, U), stages + s * stage_bytes, &full[s], pol);
       }
-      for (int u = (t > nst ? t - nst : 0); u < t; ++u)
+      for (int u = (n > nst ? n - nst : 0); u < n; ++u)
         if (!mbar_wait(&full[u % nst], (u / nst) & 1)) set_guard(p.guard, kGuardWaitTimeout);
     }
     return;
@@ -272,20 +370,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const Params p) {
   const int ctid = threadIdx.x;
   pdl_wait();
   pdl_launch_dependents();
-  stage_inputs(p, L, xs, s_red, ctid);
+  int U, t0, t1;
+  tile_range(U, t0, t1);
+  const int r0 = (p.src == kSrcDense || p.src == kSrcUnionRows) ? t0 * kTileRows : 0;
+  const int r1 = (p.src == kSrcDense) ? min(t1 * kTileRows, p.R) : (p.src == kSrcUnionRows ? t1 * kTileRows : 0);
+  int staged_u = -1;
+  if (p.src != kSrcUnionDown) {
+    stage_inputs(p, L, xs, s_red, ctid, 0);
+    staged_u = 0;
+  }
   // K chunk of this warp (a multiple of 32 columns)
   const int nblk = p.C / 32;
   const int k0 = (int)((long long)warp * nblk / kWarps) * 32, k1 = (int)((long long)(warp + 1) * nblk / kWarps) * 32;
   const int g = lane >> 2, tq = lane & 3;
   bool ok = true;
-  int t = 0;
-  for (int a = r0; a < r1; a += kTileRows, ++t) {
-    const int s = t % nst, k = t / nst;
+  int n = 0;
+  for (int t = t0; t < t1; ++t, ++n) {
+    const TileSrc ts = tile_src(p, t, U);
+    if (p.src == kSrcUnionDown && ts.u != staged_u) {  // the tile's expert input, for every token
+      named_barrier(1, kCT);
+      stage_inputs(p, L, xs, s_red, ctid, (long long)ts.u * p.C);
+      staged_u = ts.u;
+    }
+    const int s = n % nst, k = n / nst;
     if (ok && !mbar_wait(&full[s], k & 1)) {
       if (lane == 0) set_guard(p.guard, kGuardWaitTimeout);
       ok = false;
     }
-    float* pt = part + (t & 1) * npair * kWarps * kTileRows * kMaxB;
+    float* pt = part + (n & 1) * npair * kWarps * kTileRows * kMaxB;
     for (int j = 0; j < npair; ++j) {
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       if (ok) tile_mma(p, L, stages + s * stage_bytes + j * L.member_bytes, xs, k0, k1, d, lane);
@@ -304,11 +416,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const Params p) {
       float v = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) v += pt[(j * kWarps + w) * kTileRows * kMaxB + rr];
-      const int row = a - r0 + rr / kMaxB;
-      if (row < r1 - r0) red[(j * p.rows_cta_max + row) * kMaxB + rr % kMaxB] = v;
+      const int b = rr % kMaxB, ri = rr / kMaxB;
+      if (p.src == kSrcUnionDown) {
+        // partial output of expert u for the tokens that selected it
+        const int slot = (ts.u < U) ? p.slot_of[ts.u * kMaxB + b] : p.top_k;
+        if (b < p.B && slot >= 0 && ri < ts.rows)
+          p.part_out[((long long)b * (p.top_k + 1) + slot) * p.R + ts.a + ri] = v;
+      } else {
+        const int row = ts.a - r0 + ri;
+        if (row < r1 - r0) red[(j * p.rows_cta_max + row) * kMaxB + b] = v;
+      }
     }
   }
   if (named_barrier_or(1, kCT, !ok)) return;  // one decision for all compute threads
+  if (p.src == kSrcUnionDown) return;
 
   // ------------------------------------------------------------ epilogue
   const int rows_cta = r1 - r0;
@@ -381,7 +502,93 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const Params p) {
   if (ctid == 0) *p.counter = 0u;
 }
 
+// One CTA: routing of every token, then the union of the selected experts.
+__global__ void __launch_bounds__(256) k_route(const Route r) {
+  __shared__ float lg[kMaxB][512];  // logits of up to 511 experts + the shared gate per token
+  __shared__ int sel[kMaxB][16];
+  __shared__ float selv[kMaxB][16];
+  __shared__ int flag[512];
+  __shared__ int pos[512];
+  __shared__ int s_n;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tid = threadIdx.x;
+  const int E = r.E, K = r.top_k;
+  for (int b = 0; b < r.B; ++b)
+    for (int e = tid; e <= E; e += blockDim.x) lg[b][e] = r.logits[(long long)b * r.ld + e];
+  for (int e = tid; e < E; e += blockDim.x) flag[e] = 0;
+  __syncthreads();
+  // rank of every (token, expert): logits above it, or equal with a lower index
+  for (int i = tid; i < r.B * E; i += blockDim.x) {
+    const int b = i / E, e = i % E;
+    const float v = lg[b][e];
+    int rank = 0;
+    for (int f = 0; f < E; ++f) {
+      const float w = lg[b][f];
+      rank += (w > v || (w == v && f < e)) ? 1 : 0;
+    }
+    if (rank < K) {
+      sel[b][rank] = e;
+      selv[b][rank] = v;
+      flag[e] = 1;
+    }
+  }
+  __syncthreads();
+  if (tid < r.B) {  // softmax over the selected logits, sigmoid gate of the shared expert
+    const int b = tid;
+    const float m = selv[b][0];
+    float den = 0.f;
+    for (int k = 0; k < K; ++k) den += __expf(selv[b][k] - m);
+    for (int k = 0; k < K; ++k) {
+      r.w[b * (K + 1) + k] = __expf(selv[b][k] - m) / den;
+      if (r.ids) r.ids[b * K + k] = sel[b][k];
+    }
+    r.w[b * (K + 1) + K] = sigmoidf_(lg[b][E]);
+  }
+  if (tid == 0) {  // ascending union (serial scan over at most 511 flags)
+    int n = 0;
+    for (int e = 0; e < E; ++e) {
+      pos[e] = n;
+      if (flag[e]) r.union_ids[n++] = e;
+    }
+    *r.n_union = n;
+    s_n = n;
+  }
+  __syncthreads();
+  const int U = s_n;
+  for (int i = tid; i < (kMaxUnion + 1) * kMaxB; i += blockDim.x) r.slot_of[i] = -1;
+  __syncthreads();
+  for (int i = tid; i < r.B * K; i += blockDim.x) {
+    const int b = i / K, k = i % K;
+    r.slot_of[pos[sel[b][k]] * kMaxB + b] = k;
+  }
+  for (int b = tid; b < kMaxB; b += blockDim.x) r.slot_of[U * kMaxB + b] = K;
+}
+
+__global__ void k_moe_reduce(float* y, int ldy, const float* part, const float* w, int R, int B, int K) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < R * B; i += gridDim.x * blockDim.x) {
+    const int b = i / R, row = i % R;
+    float acc = 0.f;
+    for (int k = 0; k <= K; ++k) acc = fmaf(w[b * (K + 1) + k], part[((long long)b * (K + 1) + k) * R + row], acc);
+    y[(long long)b * ldy + row] += acc;
+  }
+}
+
 }  // namespace
+
+cudaError_t route(const Route& r, cudaStream_t st, bool pdl) {
+  if (r.B < 1 || r.B > kMaxB || r.E < 1 || r.E > 511 || r.top_k < 1 || r.top_k > 16 || r.B * r.top_k > kMaxUnion)
+    return cudaErrorInvalidValue;
+  return launch_k(k_route, dim3(1), dim3(256), 0, st, pdl, r);
+}
+
+cudaError_t moe_reduce(float* y, int ldy, const float* part, const float* w, int R, int B, int top_k, cudaStream_t st,
+                       bool pdl) {
+  const int n = R * B;
+  return launch_k(k_moe_reduce, dim3((n + 255) / 256), dim3(256), 0, st, pdl, y, ldy, part, w, R, B, top_k);
+}
 
 Plan plan(int R, int C, int fmt, int epi, int nsm) {
   Plan pl = {};
@@ -396,7 +603,7 @@ Plan plan(int R, int C, int fmt, int epi, int nsm) {
   pl.ncta = ntiles < nsm ? ntiles : nsm;
   const int tiles_cta = (ntiles + pl.ncta - 1) / pl.ncta;
   pl.rows_cta_max = tiles_cta * kTileRows;
-  const int fixed = kMaxB * (C * 2 + 16) + 4 * (2 * npair * kWarps * kTileRows * kMaxB) +
+  const int fixed = (fmt == kFmtBf16 ? 2 : 1) * kMaxB * (C * 2 + 16) + 4 * (2 * npair * kWarps * kTileRows * kMaxB) +
                     4 * npair * pl.rows_cta_max * kMaxB + 2 * kMaxStages * 8;
   int ns = kInFlight / stage_bytes;
   ns = ns < 2 ? 2 : (ns > kMaxStages ? kMaxStages : ns);

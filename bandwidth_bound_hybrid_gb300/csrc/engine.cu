@@ -92,6 +92,7 @@ struct hy_model {
   int splits = 1;
   bool moe = false, pdl = true, graphs = true, debug = false;
   bool persistent = false;  // the step as one cooperative kernel (when the shape allows it)
+  bool q4 = false;          // 4-bit linear weights: every step runs the batched path
 };
 
 struct hy_cache {
@@ -113,6 +114,21 @@ struct hy_cache {
   std::vector<void*> allocs;
   cudaStream_t cap_stream = nullptr;
   unsigned* step_bar = nullptr;  // grid barrier of the persistent step kernel
+  // batched steps (several sequences, or 4-bit weights): per-token scratch
+  float *bx = nullptr, *by = nullptr, *bo = nullptr, *bh = nullptr, *brlog = nullptr, *bw = nullptr;
+  float *bpart = nullptr, *bapart = nullptr, *bam_val = nullptr;
+  int *btok = nullptr, *bids = nullptr, *bunion = nullptr, *bnu = nullptr, *bslot = nullptr, *bam_idx = nullptr;
+  int* brids = nullptr;
+  unsigned *bcnt_attn = nullptr, *bcnt_am = nullptr;
+  int bh_len = 0;
+  size_t bapart_len = 0;
+  struct BGraph {
+    std::vector<int> seqs;
+    float* logits;
+    int* ids;
+    cudaGraphExec_t exec;
+  };
+  std::vector<BGraph> bgraphs;
   int last_kernels = 0;          // kernels of the last recorded step
   struct Prog {
     int seq;
@@ -557,6 +573,329 @@ int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) 
   return launch_ops(m, ops, st);
 }
 
+// ---------------------------------------------------------------- batched step
+// Issue one decode step for the sequences `seqs` (their token ids already in
+// c->btok): every weight is read once for all of them.
+int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* ids, cudaStream_t st) {
+  hy_model* m = c->m;
+  const hy_config& cf = m->cfg;
+  const int H = cf.hidden, B = (int)seqs.size(), fmt = m->q4 ? 1 : 0;
+  const bool pdl = m->pdl;
+  int kernels = 0;
+  auto ck = [&](cudaError_t e, const char* what) -> int {
+    if (e != cudaSuccess) return fail(HY_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+    ++kernels;
+    return HY_OK;
+  };
+  auto bparams = [&](int wfmt, int src, int in, int epi) {
+    bgemv::Params p;
+    memset(&p, 0, sizeof(p));
+    p.fmt = wfmt;
+    p.src = src;
+    p.in = in;
+    p.epi = epi;
+    p.B = B;
+    p.eps = cf.rms_eps;
+    p.guard = c->guard;
+    return p;
+  };
+  auto set_w = [](bgemv::Params& p, int j, const hy_tensor& t) {
+    p.W[j] = (const uint8_t*)t.w;
+    p.S[j] = (const uint16_t*)t.scales;
+  };
+  // A dense batched GEMV; bf16 matrices too wide for its tiles run per token
+  // through the single-token kernel instead (same epilogue).
+  auto dense = [&](bgemv::Params p, const char* what) -> int {
+    const bgemv::Plan pl = bgemv::plan(p.R, p.C, p.fmt, p.epi, m->nsm);
+    if (pl.ok) return ck(bgemv::launch(p, pl, st, pdl), what);
+    if (p.fmt != bgemv::kFmtBf16) return fail(HY_ERR_UNSUPPORTED, "no batched plan for %s (%d x %d)", what, p.R, p.C);
+    for (int b = 0; b < B; ++b) {
+      gemv::Params g;
+      memset(&g, 0, sizeof(g));
+      g.guard = c->guard;
+      g.eps = cf.rms_eps;
+      g.W[0] = p.W[0];
+      g.W[1] = p.W[1];
+      g.R = p.R;
+      g.C = p.C;
+      g.norm_g = p.norm_g;
+      int in = gemv::kInX, epi = gemv::kEpiStore;
+      if (p.in == bgemv::kInEmbed) {
+        in = gemv::kInEmbed;
+        g.embed = p.embed;
+        g.tok = p.tok + b;
+        g.vocab = p.vocab;
+        g.x_out = p.x_out + (size_t)b * p.ldx_out;
+      } else {
+        g.x = p.x + (size_t)b * p.ldx;
+      }
+      if (p.epi == bgemv::kEpiResid) epi = gemv::kEpiResid;
+      if (p.epi == bgemv::kEpiSwiglu) epi = gemv::kEpiSwiglu;
+      if (p.epi == bgemv::kEpiArgmax) {
+        epi = gemv::kEpiArgmax;
+        g.y = p.y ? p.y + (size_t)b * p.ldy : nullptr;
+        g.part_val = c->am_val;
+        g.part_idx = c->am_idx;
+        g.counter = c->cnt_am;
+        g.ids_out = p.ids_out + b;
+        g.len_inc = p.len_inc[b];
+      } else {
+        g.y = p.y + (size_t)b * p.ldy;
+      }
+      const gemv::Plan gp = gemv::plan(g.R, g.C, epi == gemv::kEpiSwiglu ? 2 : 1, m->nsm, g.norm_g != nullptr);
+      if (!gp.ok) return fail(HY_ERR_UNSUPPORTED, "no GEMV plan for %s (%d x %d)", what, g.R, g.C);
+      int rc = ck(gemv::launch(g, gp, gemv::kSrcDense, in, epi, st, pdl), what);
+      if (rc != HY_OK) return rc;
+    }
+    return HY_OK;
+  };
+
+  for (int l = 0; l < cf.n_layers; ++l) {
+    const hy_layer_weights& L = m->layers[l];
+    const bool attn_l = m->is_attn[l];
+    int rc;
+    {  // RMSNorm + input projection (layer 0 gathers the embedding rows)
+      bgemv::Params p = bparams(fmt, bgemv::kSrcDense, l == 0 ? bgemv::kInEmbed : bgemv::kInX, bgemv::kEpiStore);
+      set_w(p, 0, L.w_in);
+      p.R = attn_l ? m->attn_rows : m->gdn_rows;
+      p.C = H;
+      p.x = c->bx;
+      p.ldx = H;
+      p.embed = (const uint16_t*)m->w.embed;
+      p.tok = c->btok;
+      p.vocab = cf.vocab;
+      p.x_out = c->bx;
+      p.ldx_out = H;
+      p.norm_g = L.norm1;
+      p.y = c->by;
+      p.ldy = m->y_len;
+      if ((rc = dense(p, "in-proj")) != HY_OK) return rc;
+    }
+    if (attn_l) {
+      attn::Params a;
+      memset(&a, 0, sizeof(a));
+      a.y = c->by;
+      a.rope = c->rope;
+      a.nq = cf.attn_q_heads;
+      a.nkv = cf.attn_kv_heads;
+      a.hd = cf.head_dim;
+      a.nsplit = m->splits;
+      a.scale = 1.0f / sqrtf((float)cf.head_dim);
+      a.part = c->bapart;
+      a.counter = c->bcnt_attn;
+      a.o = c->bo;
+      a.guard = c->guard;
+      a.nb = B;
+      a.ld_y = m->y_len;
+      a.ld_o = m->o_len;
+      a.ld_part = (long long)c->bapart_len;
+      for (int b = 0; b < B; ++b) {
+        a.K_b[b] = kv_cache(c, seqs[b], m->sub[l], 0);
+        a.V_b[b] = kv_cache(c, seqs[b], m->sub[l], 1);
+        a.len_b[b] = c->d_len + seqs[b];
+        a.cap_b[b] = c->cap[seqs[b]];
+      }
+      a.K = a.K_b[0];
+      a.V = a.V_b[0];
+      a.len = a.len_b[0];
+      a.cap = a.cap_b[0];
+      if ((rc = ck(attn::launch(a, st, pdl), "attention")) != HY_OK) return rc;
+    } else {
+      gdn::Params g;
+      memset(&g, 0, sizeof(g));
+      g.y = c->by;
+      g.conv_w = (const uint16_t*)L.conv_w;
+      g.o = c->bo;
+      g.nh = cf.gdn_heads;
+      g.dk = cf.gdn_dk;
+      g.dv = cf.gdn_dv;
+      g.conv_k = cf.conv_k;
+      g.guard = c->guard;
+      g.nb = B;
+      g.ld_y = m->y_len;
+      g.ld_o = m->o_len;
+      for (int b = 0; b < B; ++b) {
+        g.S_b[b] = gdn_state(c, seqs[b], m->sub[l]);
+        g.conv_b[b] = conv_state(c, seqs[b], m->sub[l]);
+        g.pos_b[b] = c->d_len + seqs[b];
+      }
+      g.S = g.S_b[0];
+      g.conv_state = g.conv_b[0];
+      g.pos = g.pos_b[0];
+      if ((rc = ck(gdn::launch(g, st, pdl), "DeltaNet")) != HY_OK) return rc;
+    }
+    {  // output projection + residual
+      bgemv::Params p = bparams(fmt, bgemv::kSrcDense, bgemv::kInX, bgemv::kEpiResid);
+      set_w(p, 0, L.w_o);
+      p.R = H;
+      p.C = attn_l ? cf.attn_q_heads * cf.head_dim : cf.gdn_heads * cf.gdn_dv;
+      p.x = c->bo;
+      p.ldx = m->o_len;
+      p.y = c->bx;
+      p.ldy = H;
+      if ((rc = dense(p, "out-proj")) != HY_OK) return rc;
+    }
+    if (!m->moe) {
+      bgemv::Params p = bparams(fmt, bgemv::kSrcDense, bgemv::kInX, bgemv::kEpiSwiglu);
+      set_w(p, 0, L.w_gate);
+      set_w(p, 1, L.w_up);
+      p.R = cf.ffn;
+      p.C = H;
+      p.x = c->bx;
+      p.ldx = H;
+      p.norm_g = L.norm2;
+      p.y = c->bh;
+      p.ldy = c->bh_len;
+      if ((rc = dense(p, "gate/up")) != HY_OK) return rc;
+      bgemv::Params d = bparams(fmt, bgemv::kSrcDense, bgemv::kInX, bgemv::kEpiResid);
+      set_w(d, 0, L.w_down);
+      d.R = H;
+      d.C = cf.ffn;
+      d.x = c->bh;
+      d.ldx = c->bh_len;
+      d.y = c->bx;
+      d.ldy = H;
+      if ((rc = dense(d, "down")) != HY_OK) return rc;
+    } else {
+      const int E = cf.n_experts, K = cf.top_k, Fe = cf.expert_ffn;
+      {  // router logits of every token (the router stays bf16)
+        bgemv::Params r = bparams(bgemv::kFmtBf16, bgemv::kSrcDense, bgemv::kInX, bgemv::kEpiStore);
+        r.W[0] = (const uint8_t*)L.router;
+        r.R = E + 1;
+        r.C = H;
+        r.x = c->bx;
+        r.ldx = H;
+        r.norm_g = L.norm2;
+        r.y = c->brlog;
+        r.ldy = E + 1;
+        if ((rc = dense(r, "router")) != HY_OK) return rc;
+      }
+      bgemv::Route ro;
+      memset(&ro, 0, sizeof(ro));
+      ro.logits = c->brlog;
+      ro.ld = E + 1;
+      ro.B = B;
+      ro.E = E;
+      ro.top_k = K;
+      ro.ids = c->brids;
+      ro.w = c->bw;
+      ro.union_ids = c->bunion;
+      ro.n_union = c->bnu;
+      ro.slot_of = c->bslot;
+      ro.guard = c->guard;
+      if ((rc = ck(bgemv::route(ro, st, pdl), "route")) != HY_OK) return rc;
+      const long long ew = fmt ? (long long)Fe * H / 2 : (long long)Fe * H * 2;  // bytes of one expert matrix
+      const long long es = fmt ? (long long)Fe * H / 16 : 0;                     // bytes of its scales
+      {  // gate/up + SwiGLU over the union of selected experts and the shared expert
+        bgemv::Params p = bparams(fmt, bgemv::kSrcUnionRows, bgemv::kInX, bgemv::kEpiSwiglu);
+        p.exp_base[0] = (const uint8_t*)L.exp_gate.w;
+        p.exp_base[1] = (const uint8_t*)L.exp_up.w;
+        p.exp_scale[0] = (const uint16_t*)L.exp_gate.scales;
+        p.exp_scale[1] = (const uint16_t*)L.exp_up.scales;
+        p.exp_stride = ew;
+        p.exp_sstride = es;
+        p.sh_base[0] = (const uint8_t*)L.sh_gate.w;
+        p.sh_base[1] = (const uint8_t*)L.sh_up.w;
+        p.sh_scale[0] = (const uint16_t*)L.sh_gate.scales;
+        p.sh_scale[1] = (const uint16_t*)L.sh_up.scales;
+        p.union_ids = c->bunion;
+        p.n_union = c->bnu;
+        p.slot_of = c->bslot;
+        p.slot_rows = Fe;
+        p.top_k = K;
+        p.R = (bgemv::kMaxUnion + 1) * Fe;
+        p.C = H;
+        p.x = c->bx;
+        p.ldx = H;
+        p.norm_g = L.norm2;
+        p.y = c->bh;
+        p.ldy = c->bh_len;
+        const bgemv::Plan pl = bgemv::plan(p.R, p.C, p.fmt, p.epi, m->nsm);
+        if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no batched plan for the expert gate/up (%d x %d)", Fe, H);
+        if ((rc = ck(bgemv::launch(p, pl, st, pdl), "expert gate/up")) != HY_OK) return rc;
+      }
+      {  // down projections of the union, per (expert, token) slot
+        bgemv::Params p = bparams(fmt, bgemv::kSrcUnionDown, bgemv::kInX, bgemv::kEpiStore);
+        p.exp_base[0] = (const uint8_t*)L.exp_down.w;
+        p.exp_scale[0] = (const uint16_t*)L.exp_down.scales;
+        p.exp_stride = ew;
+        p.exp_sstride = es;
+        p.sh_base[0] = (const uint8_t*)L.sh_down.w;
+        p.sh_scale[0] = (const uint16_t*)L.sh_down.scales;
+        p.union_ids = c->bunion;
+        p.n_union = c->bnu;
+        p.slot_of = c->bslot;
+        p.slot_rows = Fe;
+        p.top_k = K;
+        p.R = H;
+        p.C = Fe;
+        p.x = c->bh;
+        p.ldx = c->bh_len;
+        p.part_out = c->bpart;
+        const bgemv::Plan pl = bgemv::plan(p.R, p.C, p.fmt, p.epi, m->nsm);
+        if (!pl.ok || H % bgemv::kTileRows) return fail(HY_ERR_UNSUPPORTED, "no batched plan for the expert down");
+        if ((rc = ck(bgemv::launch(p, pl, st, pdl), "expert down")) != HY_OK) return rc;
+      }
+      if ((rc = ck(bgemv::moe_reduce(c->bx, H, c->bpart, c->bw, H, B, K, st, pdl), "expert sum")) != HY_OK) return rc;
+      if (m->debug) {  // the first token's router results
+        HY_CK(cudaMemcpyAsync(c->dbg_rlog + (size_t)l * (E + 1), c->brlog, sizeof(float) * (E + 1),
+                              cudaMemcpyDeviceToDevice, st));
+        HY_CK(cudaMemcpyAsync(c->dbg_rids + (size_t)l * K, c->brids, sizeof(int) * K, cudaMemcpyDeviceToDevice, st));
+      }
+    }
+    if (m->debug)  // the residual stream of every token after this layer
+      HY_CK(cudaMemcpyAsync(c->dbg_hidden + (size_t)l * H, c->bx, sizeof(float) * H, cudaMemcpyDeviceToDevice, st));
+  }
+  {  // final RMSNorm + LM head + argmax per token; each sequence's position advances
+    bgemv::Params p = bparams(fmt, bgemv::kSrcDense, bgemv::kInX, bgemv::kEpiArgmax);
+    set_w(p, 0, m->w.lm_head);
+    p.R = cf.vocab;
+    p.C = H;
+    p.x = c->bx;
+    p.ldx = H;
+    p.norm_g = m->w.final_norm;
+    p.y = logits;
+    p.ldy = cf.vocab;
+    p.part_val = c->bam_val;
+    p.part_idx = c->bam_idx;
+    p.counter = c->bcnt_am;
+    p.ids_out = ids;
+    for (int b = 0; b < B; ++b) p.len_inc[b] = c->d_len + seqs[b];
+    int rc = dense(p, "lm-head");
+    if (rc != HY_OK) return rc;
+  }
+  c->last_kernels = kernels;
+  return HY_OK;
+}
+
+int run_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* ids, cudaStream_t st) {
+  if (!c->m->graphs) return record_batch(c, seqs, logits, ids, st);
+  cudaGraphExec_t exec = nullptr;
+  for (auto& g : c->bgraphs)
+    if (g.seqs == seqs && g.logits == logits && g.ids == ids) exec = g.exec;
+  if (!exec) {
+    if (c->bgraphs.size() >= 16) {
+      cudaGraphExecDestroy(c->bgraphs.front().exec);
+      c->bgraphs.erase(c->bgraphs.begin());
+    }
+    HY_CK(cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
+    int rc = record_batch(c, seqs, logits, ids, c->cap_stream);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(c->cap_stream, &graph);
+    if (rc != HY_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return rc;
+    }
+    if (e != cudaSuccess) return fail(HY_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e));
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return fail(HY_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    c->bgraphs.push_back({seqs, logits, ids, exec});
+  }
+  HY_CK(cudaGraphLaunch(exec, st));
+  return HY_OK;
+}
+
 int get_graph(hy_cache* c, int seq, float* logits, int* ids, cudaGraphExec_t* out) {
   for (auto& g : c->graphs)
     if (g.seq == seq && g.logits == logits && g.ids == ids) {
@@ -610,7 +949,13 @@ int run_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) {
 int check_model_cfg(const hy_config* c) {
   if (c->n_layers < 1 || c->n_layers > 64) return fail(HY_ERR_ARG, "n_layers must be in 1..64");
   if (c->hidden <= 0 || c->hidden % 8 || c->vocab <= 0) return fail(HY_ERR_ARG, "hidden must be a positive multiple of 8");
-  if (c->weight_format != 0) return fail(HY_ERR_UNSUPPORTED, "only bf16 weights (weight_format 0) in this build");
+  if (c->weight_format != 0 && c->weight_format != 1) return fail(HY_ERR_ARG, "weight_format must be 0 or 1");
+  if (c->weight_format == 1) {
+    // 4-bit rows: 32-element blocks whose scale rows stay 16-byte aligned
+    const int odim = std::max(c->gdn_heads * c->gdn_dv, c->attn_q_heads * c->head_dim);
+    if (c->hidden % 256 || odim % 256 || (c->ffn > 0 && c->ffn % 256) || (c->ffn == 0 && c->expert_ffn % 256))
+      return fail(HY_ERR_UNSUPPORTED, "4-bit weights need hidden, head outputs and FFN widths divisible by 256");
+  }
   const uint64_t mask = c->n_layers == 64 ? c->attn_layer_mask : (c->attn_layer_mask & ((1ull << c->n_layers) - 1));
   const bool any_attn = mask != 0, any_gdn = (uint64_t)__builtin_popcountll(mask) < (uint64_t)c->n_layers;
   if (any_gdn) {
@@ -641,6 +986,8 @@ int check_model_cfg(const hy_config* c) {
 void free_cache_mem(hy_cache* c) {
   for (auto& g : c->graphs) cudaGraphExecDestroy(g.exec);
   c->graphs.clear();
+  for (auto& g : c->bgraphs) cudaGraphExecDestroy(g.exec);
+  c->bgraphs.clear();
   for (auto& p : c->progs) cudaFree(p.dev);
   c->progs.clear();
   for (void* p : c->allocs) cudaFree(p);
@@ -688,6 +1035,14 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
   if ((rc = need(w->embed, "embed", -1)) || (rc = need(w->final_norm, "final_norm", -1)) ||
       (rc = need(w->lm_head.w, "lm_head", -1)))
     return rc;
+  const bool q4 = c.weight_format == 1;
+  auto need_t = [&](const hy_tensor& t, const char* name, int l) -> int {
+    int r = need(t.w, name, l);
+    if (r == HY_OK && q4 && !aligned16(t.scales))
+      r = fail(HY_ERR_ARG, "4-bit weight %s of layer %d has no 16-byte aligned scales", name, l);
+    return r;
+  };
+  if ((rc = need_t(w->lm_head, "lm_head", -1))) return rc;
   auto* m = new hy_model();
   m->cfg = c;
   m->w = *w;
@@ -699,18 +1054,19 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
     m->is_attn[l] = (c.attn_layer_mask >> l) & 1ull;
     m->sub[l] = m->is_attn[l] ? m->n_attn++ : m->n_gdn++;
     const hy_layer_weights& L = m->layers[l];
-    if ((rc = need(L.norm1, "norm1", l)) || (rc = need(L.w_in.w, "w_in", l)) || (rc = need(L.w_o.w, "w_o", l)) ||
+    if ((rc = need(L.norm1, "norm1", l)) || (rc = need_t(L.w_in, "w_in", l)) || (rc = need_t(L.w_o, "w_o", l)) ||
         (rc = need(L.norm2, "norm2", l)))
       break;
     if (!m->is_attn[l] && !L.conv_w) { rc = fail(HY_ERR_ARG, "conv_w of layer %d is null", l); break; }
     if (c.ffn > 0) {
-      if ((rc = need(L.w_gate.w, "w_gate", l)) || (rc = need(L.w_up.w, "w_up", l)) || (rc = need(L.w_down.w, "w_down", l)))
+      if ((rc = need_t(L.w_gate, "w_gate", l)) || (rc = need_t(L.w_up, "w_up", l)) ||
+          (rc = need_t(L.w_down, "w_down", l)))
         break;
     } else {
-      if ((rc = need(L.router, "router", l)) || (rc = need(L.exp_gate.w, "exp_gate", l)) ||
-          (rc = need(L.exp_up.w, "exp_up", l)) || (rc = need(L.exp_down.w, "exp_down", l)) ||
-          (rc = need(L.sh_gate.w, "sh_gate", l)) || (rc = need(L.sh_up.w, "sh_up", l)) ||
-          (rc = need(L.sh_down.w, "sh_down", l)))
+      if ((rc = need(L.router, "router", l)) || (rc = need_t(L.exp_gate, "exp_gate", l)) ||
+          (rc = need_t(L.exp_up, "exp_up", l)) || (rc = need_t(L.exp_down, "exp_down", l)) ||
+          (rc = need_t(L.sh_gate, "sh_gate", l)) || (rc = need_t(L.sh_up, "sh_up", l)) ||
+          (rc = need_t(L.sh_down, "sh_down", l)))
         break;
     }
   }
@@ -737,6 +1093,7 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
   m->graphs = !(c.flags & HY_FLAG_NO_GRAPH);
   m->debug = (c.flags & HY_FLAG_DEBUG) != 0;
   m->persistent = (c.flags & HY_FLAG_PERSISTENT) != 0;
+  m->q4 = c.weight_format == 1;
   *out = m;
   g_err.clear();
   return HY_OK;
@@ -791,10 +1148,29 @@ int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, 
       (rc = dalloc(c, &c->moe_ids, 16)) || (rc = dalloc(c, &c->tok, max_seqs)) || (rc = dalloc(c, &c->ids, max_seqs)) ||
       (rc = dalloc(c, &c->cnt_attn, std::max(cf.attn_kv_heads, 1))) || (rc = dalloc(c, &c->cnt_am, 1)) ||
       (rc = dalloc(c, &c->cnt_router, 1)) || (rc = dalloc(c, &c->guard, 1)) || (rc = dalloc(c, &c->step_bar, 1)) ||
-      (rc = dalloc(c, &c->logits_buf, (size_t)cf.vocab))) {
+      (rc = dalloc(c, &c->logits_buf, (size_t)cf.vocab * bgemv::kMaxB))) {
     free_cache_mem(c);
     delete c;
     return rc;
+  }
+  {  // batched-step scratch
+    const int B = bgemv::kMaxB, K = std::max(cf.top_k, 1), E1 = std::max(cf.n_experts + 1, 1);
+    c->bh_len = m->moe ? (bgemv::kMaxUnion + 1) * cf.expert_ffn : std::max(cf.ffn, 1);
+    c->bapart_len = part;
+    if ((rc = dalloc(c, &c->bx, (size_t)B * cf.hidden)) || (rc = dalloc(c, &c->by, (size_t)B * m->y_len)) ||
+        (rc = dalloc(c, &c->bo, (size_t)B * std::max(m->o_len, 1))) || (rc = dalloc(c, &c->bh, (size_t)B * c->bh_len)) ||
+        (rc = dalloc(c, &c->brlog, (size_t)B * E1)) || (rc = dalloc(c, &c->bw, (size_t)B * (K + 1))) ||
+        (rc = dalloc(c, &c->bpart, m->moe ? (size_t)B * (K + 1) * cf.hidden : 1)) ||
+        (rc = dalloc(c, &c->bapart, (size_t)B * part)) || (rc = dalloc(c, &c->bam_val, (size_t)1024 * B)) ||
+        (rc = dalloc(c, &c->bam_idx, (size_t)1024 * B)) || (rc = dalloc(c, &c->btok, B)) ||
+        (rc = dalloc(c, &c->bids, B)) || (rc = dalloc(c, &c->bunion, bgemv::kMaxUnion)) ||
+        (rc = dalloc(c, &c->bnu, 1)) || (rc = dalloc(c, &c->bslot, (size_t)(bgemv::kMaxUnion + 1) * B)) ||
+        (rc = dalloc(c, &c->brids, (size_t)B * K)) ||
+        (rc = dalloc(c, &c->bcnt_attn, (size_t)B * std::max(cf.attn_kv_heads, 1))) || (rc = dalloc(c, &c->bcnt_am, 1))) {
+      free_cache_mem(c);
+      delete c;
+      return rc;
+    }
   }
   if (m->n_attn) {
     if ((rc = dalloc(c, &c->rope, (size_t)max_cap * (cf.head_dim / 2)))) {
@@ -857,46 +1233,82 @@ int hy_prefill(hy_model* m, hy_cache* c, int32_t seq, const int32_t* tokens_dev,
   if ((long long)c->len[seq] + n > c->cap[seq])
     return fail(HY_ERR_CAPACITY, "sequence %d: %d + %d tokens exceed capacity %d", seq, c->len[seq], n, c->cap[seq]);
   cudaStream_t st = (cudaStream_t)stream;
+  const std::vector<int> one{seq};
   for (int i = 0; i < n; ++i) {
-    HY_CK(cudaMemcpyAsync(c->tok, tokens_dev + i, sizeof(int), cudaMemcpyDeviceToDevice, st));
-    int rc = run_step(c, seq, (i == n - 1) ? logits_dev : nullptr, c->ids, st);
+    float* lg = (i == n - 1) ? logits_dev : nullptr;
+    int rc;
+    if (m->q4) {  // 4-bit weights: the batched path, with one sequence
+      HY_CK(cudaMemcpyAsync(c->btok, tokens_dev + i, sizeof(int), cudaMemcpyDeviceToDevice, st));
+      rc = run_batch(c, one, lg, c->bids, st);
+    } else {
+      HY_CK(cudaMemcpyAsync(c->tok, tokens_dev + i, sizeof(int), cudaMemcpyDeviceToDevice, st));
+      rc = run_step(c, seq, lg, c->ids, st);
+    }
     if (rc != HY_OK) return rc;
     c->len[seq] += 1;
   }
   return HY_OK;
 }
 
+namespace {
+// Checks of a decode step's sequence list (distinct, valid, not full).
+int check_seqs(hy_cache* c, const int32_t* seqs_host, int32_t nseq, std::vector<int>& seqs) {
+  if (nseq < 1 || nseq > bgemv::kMaxB) return fail(HY_ERR_ARG, "nseq must be in 1..%d", bgemv::kMaxB);
+  seqs.assign(seqs_host, seqs_host + nseq);
+  for (int i = 0; i < nseq; ++i) {
+    if (!valid_seq(c, seqs[i])) return fail(HY_ERR_ARG, "bad sequence handle %d", seqs[i]);
+    for (int j = 0; j < i; ++j)
+      if (seqs[j] == seqs[i]) return fail(HY_ERR_ARG, "sequence %d appears twice in one step", seqs[i]);
+    if (c->len[seqs[i]] >= c->cap[seqs[i]])
+      return fail(HY_ERR_CAPACITY, "sequence %d is at its capacity %d", seqs[i], c->cap[seqs[i]]);
+  }
+  return HY_OK;
+}
+}  // namespace
+
 int hy_decode_step(hy_model* m, hy_cache* c, const int32_t* seqs_host, int32_t nseq, const int32_t* tokens_dev,
                    float* logits_dev, int32_t* ids_dev, void* stream) {
   if (!m || !c || c->m != m || !seqs_host || !tokens_dev || !ids_dev) return fail(HY_ERR_ARG, "null argument");
-  if (nseq != 1) return fail(HY_ERR_UNSUPPORTED, "this build decodes one sequence per step (nseq == 1)");
-  const int seq = seqs_host[0];
-  if (!valid_seq(c, seq)) return fail(HY_ERR_ARG, "bad sequence handle %d", seq);
-  if (c->len[seq] >= c->cap[seq]) return fail(HY_ERR_CAPACITY, "sequence %d is at its capacity %d", seq, c->cap[seq]);
-  cudaStream_t st = (cudaStream_t)stream;
-  HY_CK(cudaMemcpyAsync(c->tok, tokens_dev, sizeof(int), cudaMemcpyDeviceToDevice, st));
-  int rc = run_step(c, seq, logits_dev, ids_dev, st);
+  std::vector<int> seqs;
+  int rc = check_seqs(c, seqs_host, nseq, seqs);
   if (rc != HY_OK) return rc;
-  c->len[seq] += 1;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (nseq == 1 && !m->q4) {
+    HY_CK(cudaMemcpyAsync(c->tok, tokens_dev, sizeof(int), cudaMemcpyDeviceToDevice, st));
+    rc = run_step(c, seqs[0], logits_dev, ids_dev, st);
+  } else {
+    HY_CK(cudaMemcpyAsync(c->btok, tokens_dev, sizeof(int) * nseq, cudaMemcpyDeviceToDevice, st));
+    rc = run_batch(c, seqs, logits_dev, ids_dev, st);
+  }
+  if (rc != HY_OK) return rc;
+  for (int s : seqs) c->len[s] += 1;
   return HY_OK;
 }
 
 int hy_decode_step_host(hy_model* m, hy_cache* c, const int32_t* seqs_host, int32_t nseq, const int32_t* tokens_host,
                         float* logits_host, int32_t* ids_host, void* stream) {
   if (!m || !c || c->m != m || !seqs_host || !tokens_host || !ids_host) return fail(HY_ERR_ARG, "null argument");
-  if (nseq != 1) return fail(HY_ERR_UNSUPPORTED, "this build decodes one sequence per step (nseq == 1)");
-  const int seq = seqs_host[0];
-  if (!valid_seq(c, seq)) return fail(HY_ERR_ARG, "bad sequence handle %d", seq);
-  if (c->len[seq] >= c->cap[seq]) return fail(HY_ERR_CAPACITY, "sequence %d is at its capacity %d", seq, c->cap[seq]);
-  cudaStream_t st = (cudaStream_t)stream;
-  HY_CK(cudaMemcpyAsync(c->tok, tokens_host, sizeof(int), cudaMemcpyHostToDevice, st));
-  float* lg = logits_host ? c->logits_buf : nullptr;
-  int rc = run_step(c, seq, lg, c->ids, st);
+  std::vector<int> seqs;
+  int rc = check_seqs(c, seqs_host, nseq, seqs);
   if (rc != HY_OK) return rc;
-  c->len[seq] += 1;
-  HY_CK(cudaMemcpyAsync(ids_host, c->ids, sizeof(int), cudaMemcpyDeviceToHost, st));
+  cudaStream_t st = (cudaStream_t)stream;
+  float* lg = logits_host ? c->logits_buf : nullptr;
+  int* ids = nullptr;
+  if (nseq == 1 && !m->q4) {
+    HY_CK(cudaMemcpyAsync(c->tok, tokens_host, sizeof(int), cudaMemcpyHostToDevice, st));
+    ids = c->ids;
+    rc = run_step(c, seqs[0], lg, ids, st);
+  } else {
+    HY_CK(cudaMemcpyAsync(c->btok, tokens_host, sizeof(int) * nseq, cudaMemcpyHostToDevice, st));
+    ids = c->bids;
+    rc = run_batch(c, seqs, lg, ids, st);
+  }
+  if (rc != HY_OK) return rc;
+  for (int s : seqs) c->len[s] += 1;
+  HY_CK(cudaMemcpyAsync(ids_host, ids, sizeof(int) * nseq, cudaMemcpyDeviceToHost, st));
   if (logits_host)
-    HY_CK(cudaMemcpyAsync(logits_host, c->logits_buf, sizeof(float) * (size_t)m->cfg.vocab, cudaMemcpyDeviceToHost, st));
+    HY_CK(cudaMemcpyAsync(logits_host, c->logits_buf, sizeof(float) * (size_t)m->cfg.vocab * nseq,
+                          cudaMemcpyDeviceToHost, st));
   HY_CK(cudaStreamSynchronize(st));
   return HY_OK;
 }

@@ -115,6 +115,7 @@ cudaError_t launch(const Params& p, const Plan& pl, int src, int in, int epi, cu
 namespace gdn {
 constexpr int kRowsPerCta = 16;
 constexpr int kThreads = 128;
+constexpr int kMaxB = 8;
 struct Params {
   const float* y;          // projection output: q|k|v|a|b  (conv_channels + 2*nh)
   const uint16_t* conv_w;  // bf16 [channels][conv_k]
@@ -124,6 +125,12 @@ struct Params {
   float* o;                // [nh*dv]
   int nh, dk, dv, conv_k;
   unsigned* guard;
+  // batch (nb > 0): token z = blockIdx.z uses y + z*ld_y, o + z*ld_o and its
+  // own sequence's state, conv ring and position
+  int nb, ld_y, ld_o;
+  float* S_b[kMaxB];
+  float* conv_b[kMaxB];
+  const int* pos_b[kMaxB];
 };
 cudaError_t launch(const Params& p, cudaStream_t st, bool pdl);
 }  // namespace gdn
@@ -144,6 +151,14 @@ struct Params {
   unsigned* counter;       // [nkv], zero between launches
   float* o;                // [nq*hd]
   unsigned* guard;
+  // batch (nb > 0): token z = blockIdx.z uses y + z*ld_y, o + z*ld_o,
+  // part + z*ld_part, counter + z*nkv and its own sequence's cache
+  int nb, ld_y, ld_o;
+  long long ld_part;
+  uint16_t* K_b[8];
+  uint16_t* V_b[8];
+  const int* len_b[8];
+  int cap_b[8];
 };
 size_t part_floats(int nq, int nkv, int hd, int nsplit);
 int auto_splits(int nkv, int nsm);
@@ -164,10 +179,28 @@ constexpr int kMaxStages = 8;
 constexpr int kInFlight = 160 * 1024;
 constexpr int kMaxSmem = 220 * 1024;
 enum Fmt : int { kFmtBf16 = 0, kFmtQ4 = 1 };
+enum Src : int { kSrcDense = 0, kSrcUnionRows = 1, kSrcUnionDown = 2 };
 enum In : int { kInX = 0, kInEmbed = 1 };
 enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiArgmax = 3 };
+constexpr int kMaxUnion = 64;  // distinct routed experts of one step (top_k * batch at most)
 struct Params {
-  int fmt, in, epi;
+  int fmt, src, in, epi;
+  // ---- MoE over the union of the experts the batch selected (src != kSrcDense)
+  //   kSrcUnionRows: virtual rows u * slot_rows + r, u < n_union: routed expert
+  //     union_ids[u]; u == n_union: the shared expert (R = (n_union + 1) * slot_rows)
+  //   kSrcUnionDown: tiles (u, 16 output rows of R); the input of tile u is
+  //     x + b * ldx + u * C; outputs go to part_out[(b * (top_k + 1) + slot) * R + row]
+  //     for the tokens b whose slot slot_of[u * kMaxB + b] >= 0
+  const uint8_t* exp_base[2];
+  const uint16_t* exp_scale[2];
+  long long exp_stride, exp_sstride;  // bytes from one routed expert to the next (weights, scales)
+  const uint8_t* sh_base[2];
+  const uint16_t* sh_scale[2];
+  const int* union_ids;
+  const int* n_union;
+  const int* slot_of;
+  int slot_rows, top_k;
+  float* part_out;
   const uint8_t* W[2];      // bf16 [R][C] or packed nibbles [R][C/2] (W[1]: up matrix of a gate/up pair)
   const uint16_t* S[2];     // 4-bit: fp16 scales [R][C/32]
   int R, C, B;
@@ -194,9 +227,30 @@ struct Plan {
   int ncta, nstages, rows_cta_max, smem;
   bool ok;
 };
+// R: rows (for kSrcUnionRows the most rows a step can have).
 Plan plan(int R, int C, int fmt, int epi, int nsm);
 cudaError_t init();
 cudaError_t launch(const Params& p, const Plan& pl, cudaStream_t st, bool pdl);
+
+// MoE routing of a batch: per token the top_k experts of logits [B][ld]
+// (FP32 compare, lowest index on ties), their softmax weights and the shared
+// gate sigmoid(logit E) into w [B][top_k + 1]; the union of the selected
+// experts (ascending) and, per union entry and token, the slot that selected
+// it (shared expert: entry n_union, slot top_k for every token).
+struct Route {
+  const float* logits;
+  int ld, B, E, top_k;
+  int* ids;        // [B][top_k] (nullable)
+  float* w;        // [B][top_k + 1]
+  int* union_ids;  // [kMaxUnion]
+  int* n_union;
+  int* slot_of;    // [(kMaxUnion + 1)][kMaxB]
+  unsigned* guard;
+};
+cudaError_t route(const Route& r, cudaStream_t st, bool pdl);
+// y[b][row] += sum_{k <= top_k} w[b][k] * part[(b * (top_k + 1) + k) * R + row]
+cudaError_t moe_reduce(float* y, int ldy, const float* part, const float* w, int R, int B, int top_k, cudaStream_t st,
+                       bool pdl);
 }  // namespace bgemv
 
 // ---------------------------------------------------------------- persistent step

@@ -12,6 +12,15 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+def _tensor(t) -> hy_tensor:
+    """hy_tensor of a bf16 matrix, or of a 4-bit (packed nibbles, fp16 scales) pair."""
+    if t is None:
+        return hy_tensor(None, None)
+    if isinstance(t, tuple):
+        return hy_tensor(t[0].data_ptr(), t[1].data_ptr())
+    return hy_tensor(t.data_ptr(), None)
+
+
 def _stream(stream=None) -> int | None:
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
@@ -56,17 +65,17 @@ class HybridModel:
             w = layers[l]
             g = lambda n: weights.get(f"l{l}.{n}")  # noqa: E731
             w.norm1, w.norm2 = _ptr(g("norm1")), _ptr(g("norm2"))
-            w.w_in = hy_tensor(_ptr(g("w_in")), None)
-            w.w_o = hy_tensor(_ptr(g("w_o")), None)
+            w.w_in = _tensor(g("w_in"))
+            w.w_o = _tensor(g("w_o"))
             w.conv_w = _ptr(g("conv_w"))
             for n in ("w_gate", "w_up", "w_down", "exp_gate", "exp_up", "exp_down", "sh_gate", "sh_up", "sh_down"):
-                setattr(w, n, hy_tensor(_ptr(g(n)), None))
+                setattr(w, n, _tensor(g(n)))
             w.router = _ptr(g("router"))
         self._layers = layers
         hw = hy_weights()
         hw.embed = _ptr(weights["embed"])
         hw.final_norm = _ptr(weights["final_norm"])
-        hw.lm_head = hy_tensor(_ptr(weights["lm_head"]), None)
+        hw.lm_head = _tensor(weights["lm_head"])
         hw.layers = layers
         self._hw = hw
         m = ctypes.c_void_p()
@@ -89,6 +98,13 @@ class HybridModel:
     def decode_step(self, seq: int, token, ids, logits=None, stream=None) -> None:
         seqs = (ctypes.c_int32 * 1)(seq)
         check(capi.lib().hy_decode_step(self.m, self.c, seqs, 1, _ptr(token), _ptr(logits), _ptr(ids),
+                                        _stream(stream)), "hy_decode_step")
+
+    def decode_batch(self, seqs, tokens, ids, logits=None, stream=None) -> None:
+        """One step for the distinct sequences `seqs` (tokens, ids: int32 CUDA
+        tensors [len(seqs)]; logits: FP32 [len(seqs)][V] or None)."""
+        arr = (ctypes.c_int32 * len(seqs))(*[int(s) for s in seqs])
+        check(capi.lib().hy_decode_step(self.m, self.c, arr, len(seqs), _ptr(tokens), _ptr(logits), _ptr(ids),
                                         _stream(stream)), "hy_decode_step")
 
     def decode_step_host(self, seq: int, token_host, ids_host, logits_host=None, stream=None) -> None:

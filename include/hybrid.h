@@ -80,12 +80,18 @@ typedef struct {
   int32_t shared_ffn;      /* Fs (MoE shared expert) */
   float rms_eps;           /* RMSNorm epsilon */
   float rope_theta;        /* RoPE base */
-  int32_t weight_format;   /* 0 = bf16 (only format of this build) */
+  int32_t weight_format;   /* 0 = bf16; 1 = 4-bit blocks of 32 for the linear weights (see hy_tensor) */
   int32_t attn_splits;     /* split-KV chunks per kv head; 0 = chosen from the SM count */
   uint32_t flags;          /* HY_FLAG_* */
 } hy_config;
 
-/* One linear weight: bf16 [rows][cols] in `w` (`scales` unused for bf16). */
+/* One linear weight [rows][cols]: bf16 in `w` (`scales` unused), or with
+ * weight_format 1 packed 4-bit blocks of 32 along cols in `w` ([rows][cols/2]
+ * bytes; byte i of a block holds element i in its low nibble and element
+ * i + 16 in its high nibble, each stored as value + 8) and one fp16 scale per
+ * block in `scales` ([rows][cols/32]): w = scale * (nibble - 8) ([Flash]
+ * "Correctness fixes").  The router, the conv taps and the embedding stay
+ * bf16 in 4-bit models. */
 typedef struct {
   const void* w;
   const void* scales;
@@ -163,13 +169,17 @@ int32_t hy_step_kernels(const hy_cache* c);
 int hy_prefill(hy_model* m, hy_cache* c, int32_t seq, const int32_t* tokens_dev, int32_t n, float* logits_dev,
                void* stream);
 
-/* One greedy decode step for the sequences seqs_host[0..nseq) (this build:
- * nseq == 1): consumes tokens_dev[i] at position len(seqs[i]), writes the
- * FP32 logits [nseq][V] to logits_dev (nullable) and the argmax token id
- * (lowest index on ties) to ids_dev[i], then len += 1.  The first call for a
- * given (sequence set, logits_dev, ids_dev) captures a CUDA graph; later
- * calls replay it: one graph launch per token ([Strata] "Act 0", pass 3).
- * HY_ERR_CAPACITY (nothing launched) if a sequence is full. */
+/* One greedy decode step for the distinct sequences seqs_host[0..nseq)
+ * (1 <= nseq <= 8): consumes tokens_dev[i] at position len(seqs[i]), writes
+ * the FP32 logits [nseq][V] to logits_dev (nullable) and the argmax token id
+ * (lowest index on ties) to ids_dev[i], then len += 1 for each.  With
+ * nseq > 1 (and always for 4-bit models) every weight is read once for all
+ * the sequences: the projections run as batched tensor-core GEMVs, the MoE
+ * FFN over the union of the experts the tokens selected ([Strata] "Act 5":
+ * batched decode rows).  The first call for a given (sequence list,
+ * logits_dev, ids_dev) captures a CUDA graph; later calls replay it: one
+ * graph launch per step ([Strata] "Act 0", pass 3).  HY_ERR_CAPACITY
+ * (nothing launched) if a sequence is full. */
 int hy_decode_step(hy_model* m, hy_cache* c, const int32_t* seqs_host, int32_t nseq, const int32_t* tokens_dev,
                    float* logits_dev, int32_t* ids_dev, void* stream);
 
