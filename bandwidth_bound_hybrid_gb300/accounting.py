@@ -79,6 +79,38 @@ def step_bytes(shape, context: int, experts_touched: int | None = None) -> StepB
     return StepBytes(weights=w, state=state, kv_read=kv_read, kv_write=kv_write, activations=0)
 
 
+def expected_union(n_experts: int, top_k: int, batch: int) -> float:
+    """Expected number of distinct experts `batch` tokens select when each
+    picks top_k of n_experts uniformly without replacement, independently."""
+    return n_experts * (1.0 - (1.0 - top_k / n_experts) ** batch)
+
+
+def batch_step_bytes(shape, contexts, experts_touched: float | None = None) -> StepBytes:
+    """Bytes one step over a batch of sequences at positions `contexts` must
+    move: the weights once (MoE: the union of the experts the batch selects,
+    by default its expectation under uniform routing), and per sequence its
+    recurrent state and KV cache."""
+    B = len(contexts)
+    if shape.ffn == 0 and experts_touched is None:
+        experts_touched = expected_union(shape.n_experts, shape.top_k, B)
+    one = step_bytes(shape, 0, None if shape.ffn > 0 else int(round(experts_touched)))
+    w = one.weights + (B - 1) * (shape.hidden * BF16)  # an embedding row per token
+    if shape.ffn == 0:  # fractional expected union
+        fmt = getattr(shape, "weight_format", 0)
+        per_exp = 2 * linear_bytes(shape.expert_ffn, shape.hidden, fmt) + linear_bytes(shape.hidden, shape.expert_ffn, fmt)
+        w += int(round(shape.n_layers * per_exp * (experts_touched - round(experts_touched))))
+    n_attn = sum(1 for l in range(shape.n_layers) if shape.is_attn(l))
+    kv1 = kv_bytes_per_token(n_attn, shape.attn_kv_heads, shape.head_dim)
+    return StepBytes(weights=w, state=B * one.state, kv_read=kv1 * int(sum(contexts)), kv_write=B * kv1,
+                     activations=0)
+
+
+def gemv_batch_bytes(rows: int, cols: int, batch: int, weight_format: int) -> int:
+    """One batched GEMV launch: the matrix once, `batch` FP32 input vectors and
+    `batch` FP32 output vectors."""
+    return linear_bytes(rows, cols, weight_format) + batch * (cols + rows) * F32
+
+
 def gemv_swiglu_bytes(rows: int, cols: int) -> int:
     """One gate/up SwiGLU GEMV launch: two bf16 [rows][cols] matrices, the FP32
     input vector and the FP32 output."""

@@ -8,21 +8,29 @@
 // With 8 token columns the product is a small dense contraction, so it runs
 // on the tensor cores with mma.sync m16n8k16 (A = 16 weight rows x 16 k,
 // B = 16 k x 8 tokens, FP32 accumulators):
-//   * one copy lane streams 16-row tiles HBM -> shared memory with bulk copies
-//     (TMA engine), one copy per row into a row stride padded by 16 bytes, so
-//     that the fragment loads of 8 rows fall into 8 different bank groups;
-//   * eight compute warps split the tile's K range; 4-bit weights are turned
-//     into exact FP16 integers (nibble - 8) in registers (a magic-exponent OR
-//     and one packed subtract), the block scale is applied to the FP32 result
-//     of the block's two MMAs, so the weights are dequantised exactly;
-//   * the token vectors are RMS-normalised per token and stored once per CTA
-//     in shared memory as FP16 (4-bit weights), or for bf16 weights (the MMA
-//     needs one operand type) as two bf16 parts hi + lo, each multiplied by
-//     the weights, so the products keep about 16 bits of the FP32 vector; in
-//     the K order the weight fragments use;
-//   * per tile the eight warps' partial sums are reduced in a fixed order, and
-//     the CTA's rows are finished at the end: store, residual add, SwiGLU or a
-//     per-token argmax.
+//   * the matrix is seen as 3D, {128-byte strip of a row, row, strip index},
+//     and one copy lane streams stages of 16*GW rows x KS strips (16 KB, plus
+//     2 KB of 4-bit scales) with one tensor copy each (TMA, 128-byte swizzle:
+//     the fragment reads of 8 rows fall into 8 different bank groups without
+//     padding); rows past the end of the matrix arrive as zeros;
+//   * the 8 compute warps are GW row groups x KS strip lanes (GW * KS = 8);
+//     warp (gw, ks) accumulates its 16 rows over strips ks, ks + KS, ... of
+//     a row block in registers, so warps meet only at the end of a row block
+//     (KS > 1: a fixed-order sum of the KS partials), not once per stage;
+//   * 4-bit weights are turned into exact FP16 integers (nibble - 8) in
+//     registers (a magic-exponent OR and one packed subtract) and the block
+//     scale is applied to the FP32 result of the block's two MMAs, so the
+//     weights are dequantised exactly;
+//   * the token vectors are RMS-normalised per token (one warp per token) and
+//     stored once per CTA in shared memory as FP16 (4-bit weights), or for
+//     bf16 weights (the MMA needs one operand type) as two bf16 parts hi + lo,
+//     each multiplied by the weights, so the products keep about 16 bits of
+//     the FP32 vector; in the K order the weight fragments use;
+//   * each row block is finished as soon as its last strip is in: store,
+//     residual add, SwiGLU, per-(expert, token) partial, or a per-token
+//     argmax candidate (merged across CTAs by the last one to finish).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -30,9 +38,20 @@
 
 namespace hy {
 namespace bgemv {
+
+// Tensor maps of one launch, passed by value.
+struct Maps {
+  CUtensorMap w[2], s[2];    // the dense matrix, or the shared expert of a union source
+  CUtensorMap ew[2], es[2];  // the routed experts of a union source, their rows stacked
+};
+
 namespace {
 
 constexpr int kCT = kWarps * 32;
+constexpr int kStrip = 128;      // bytes of a row in one strip
+constexpr int kStageW = 16384;   // weight bytes of a stage member: 16 * GW rows x KS strips x 128 B
+constexpr int kStageS = 2048;    // 4-bit scales of a stage member: 16 * GW rows x KS strips x 16 B
+constexpr int kPartFloats = kWarps * kTileRows * kMaxB;  // one member's per-warp partials
 
 __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, const uint32_t* b) {
   asm volatile(
@@ -49,6 +68,17 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, const uint
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// Tensor copy of box {0, c1, c2} of a 3D map into shared memory, completing
+// on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c1, int c2, uint64_t* bar,
+                                            uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(c1), "r"(c2), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
 // Two nibbles (bits 0..3 and 16..19 of v) -> FP16 pair (n - 8), exactly:
 // 0x6400 | n is 1024 + n, minus 1032.
 __device__ __forceinline__ uint32_t nib2_to_f16x2(uint32_t v) {
@@ -59,196 +89,236 @@ __device__ __forceinline__ uint32_t nib2_to_f16x2(uint32_t v) {
 
 __device__ __forceinline__ float f16_bits_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 
-// Position of element k of a row in the staged token vector: bf16 weights
-// keep k; 4-bit weights use, inside each 16-element half block, the order in
-// which a lane's 32-bit nibble word feeds the A fragment (evens, then odds).
-__device__ __forceinline__ int xperm(int fmt, int k) {
-  if (fmt == kFmtBf16) return k;
-  const int base = k & ~15, j = k & 15;
-  return base + ((j & 1) ? 8 + (j >> 1) : (j >> 1));
-}
-
-struct Layout {
-  int row_bytes;     // bytes of one weight row in the tile (padded)
-  int scale_bytes;   // bytes of one row's scales (unpadded: one copy per tile); 0 for bf16
-  int member_bytes;  // one pair member's 16 rows, then their scales
-  int x_stride;      // bytes of one staged token vector (padded)
-  int x_parts;       // bf16 weights: the vector as hi + lo bf16 parts (two MMAs); FP16: one part
+// The staged token vectors: 8 rows of x_stride bytes (padded by 16 so that
+// the fragment reads of 8 tokens fall into 8 bank groups), two parts for bf16
+// weights.
+struct XLayout {
+  int x_stride, x_parts;
 };
 
-__device__ __forceinline__ Layout layout_of(const Params& p) {
-  Layout L;
-  if (p.fmt == kFmtBf16) {
-    L.row_bytes = p.C * 2 + 16;
-    L.scale_bytes = 0;
-  } else {
-    L.row_bytes = p.C / 2 + 16;
-    L.scale_bytes = p.C / 16;
+// Four consecutive elements k..k+3 of a token vector (FP32 rows, 16-byte
+// aligned or not, or a bf16 embedding row).
+__device__ __forceinline__ float4 load4(const float* src, const uint16_t* emb, bool vec, int k) {
+  if (emb) {
+    const uint2 u = *reinterpret_cast<const uint2*>(emb + k);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xFFFF0000u));
   }
-  L.member_bytes = kTileRows * (L.row_bytes + L.scale_bytes);
-  L.x_stride = p.C * 2 + 16;
-  L.x_parts = p.fmt == kFmtBf16 ? 2 : 1;
-  return L;
+  if (vec) return *reinterpret_cast<const float4*>(src + k);
+  return make_float4(src[k], src[k + 1], src[k + 2], src[k + 3]);
 }
 
-// Tile t of the launch: its union entry u (0 for dense), first output row a
-// (virtual row for kSrcUnionRows), row count, and the first weight row and
-// scale row of each pair member.
-struct TileSrc {
-  int u, a, rows;
-  const uint8_t* w[2];
-  const uint16_t* sc[2];
-};
-
-__device__ __forceinline__ int checked_union_expert(const Params& p, int u) {
-  int e = p.union_ids[u];
-  if (e < 0) {  // never read outside the expert tensor (the router's ids are < n_experts)
-    set_guard(p.guard, kGuardBadIndex);
-    e = 0;
-  }
-  return e;
-}
-
-__device__ __forceinline__ int tiles_of(const Params& p, int U) {
-  if (p.src == kSrcUnionRows) return (U + 1) * (p.slot_rows / kTileRows);
-  if (p.src == kSrcUnionDown) return (U + 1) * (p.R / kTileRows);
-  return (p.R + kTileRows - 1) / kTileRows;
-}
-
-__device__ __forceinline__ TileSrc tile_src(const Params& p, int t, int U) {
-  TileSrc ts;
-  const long long wb = p.fmt == kFmtBf16 ? (long long)p.C * 2 : p.C / 2;  // bytes of a weight row
-  const long long sb = p.C / 32;                                           // scales of a row (fp16)
-  int wrow;
-  if (p.src == kSrcDense) {
-    ts.u = 0;
-    ts.a = t * kTileRows;
-    ts.rows = min(kTileRows, p.R - ts.a);
-    wrow = ts.a;
-  } else if (p.src == kSrcUnionRows) {
-    ts.a = t * kTileRows;
-    ts.u = ts.a / p.slot_rows;
-    ts.rows = kTileRows;
-    wrow = ts.a - ts.u * p.slot_rows;
-  } else {
-    const int nrb = p.R / kTileRows;
-    ts.u = t / nrb;
-    ts.a = (t - ts.u * nrb) * kTileRows;
-    ts.rows = kTileRows;
-    wrow = ts.a;
-  }
-  for (int j = 0; j < 2; ++j) {
-    const uint8_t* w = p.W[j];
-    const uint16_t* sc = p.S[j];
-    if (p.src != kSrcDense) {
-      if (ts.u < U) {
-        const long long e = checked_union_expert(p, ts.u);
-        w = p.exp_base[j] ? p.exp_base[j] + e * p.exp_stride : nullptr;
-        sc = p.exp_scale[j] ? reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.exp_scale[j]) +
-                                                                 e * p.exp_sstride)
-                            : nullptr;
-      } else {
-        w = p.sh_base[j];
-        sc = p.sh_scale[j];
-      }
-    }
-    ts.w[j] = w ? w + wrow * wb : nullptr;
-    ts.sc[j] = sc ? sc + wrow * sb : nullptr;
-  }
-  return ts;
-}
-
-// Copy lane: the tile's rows of each pair member into the stage.
-__device__ __forceinline__ void issue_tile(const Params& p, const Layout& L, const TileSrc& ts, uint8_t* dst,
-                                           uint64_t* bar, uint64_t pol) {
-  const int npair = p.epi == kEpiSwiglu ? 2 : 1;
-  const uint32_t wb = p.fmt == kFmtBf16 ? p.C * 2 : p.C / 2;
-  const uint32_t sb = p.fmt == kFmtBf16 ? 0 : p.C / 16;
-  mbar_arrive_expect_tx(bar, (uint32_t)ts.rows * (wb + sb) * npair);
-  for (int j = 0; j < npair; ++j) {
-    uint8_t* m = dst + j * L.member_bytes;
-    for (int r = 0; r < ts.rows; ++r) bulk_g2s(m + r * L.row_bytes, ts.w[j] + (long long)r * wb, wb, bar, pol);
-    if (sb) bulk_g2s(m + kTileRows * L.row_bytes, ts.sc[j], ts.rows * sb, bar, pol);
-  }
-}
-
-// Compute threads: the token vectors, normalised per token, into xs (FP16 or
-// bf16, permuted for 4-bit weights), zero for padding tokens.  s_red: >= B
-// floats of scratch.
-__device__ __forceinline__ void stage_inputs(const Params& p, const Layout& L, uint8_t* xs, float* s_red, int ctid,
-                                             long long x_off) {
-  const int warp = ctid >> 5, lane = ctid & 31;
-  for (int b = 0; b < kMaxB; ++b) {
-    uint8_t* row = xs + b * L.x_stride;
-    if (b >= p.B) {
-      for (int k = ctid; k < p.C / 2; k += kCT) {
-        reinterpret_cast<uint32_t*>(row)[k] = 0u;
-        if (L.x_parts == 2) reinterpret_cast<uint32_t*>(row + kMaxB * L.x_stride)[k] = 0u;
-      }
-      continue;
-    }
-    const float* src = nullptr;
-    const uint16_t* emb = nullptr;
-    if (p.in == kInEmbed) {
-      int tok = p.tok[b];
-      if (tok < 0 || tok >= p.vocab) {
-        if (ctid == 0) set_guard(p.guard, kGuardBadIndex);
-        tok = 0;
-      }
-      emb = p.embed + (long long)tok * p.C;
-    } else {
-      src = p.x + (long long)b * p.ldx + x_off;
-    }
-    auto val = [&](int k) { return emb ? bf16_to_f32(emb[k]) : src[k]; };
-    float sc = 1.f;
-    if (p.norm_g) {
-      float ss = 0.f;
-      for (int k = ctid; k < p.C; k += kCT) {
-        const float v = val(k);
-        ss = fmaf(v, v, ss);
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) s_red[warp] = ss;
-      named_barrier(1, kCT);
-      float t = 0.f;
+// Elements k..k+3 (k a multiple of 4) into the staged row: bf16 hi + lo parts,
+// or FP16 at the permuted positions (k -> k/2 and k+2 -> k/2+1 among the evens
+// of the half block, k+1 and k+3 likewise among its odds).
+__device__ __forceinline__ void store4(int fmt, uint8_t* row, uint8_t* row_lo, int k, float4 v) {
+  if (fmt == kFmtBf16) {
+    const float f[4] = {v.x, v.y, v.z, v.w};
+    uint16_t h[4], l[4];
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) t += s_red[w];
-      sc = 1.0f / sqrtf(t / (float)p.C + p.eps);
-      named_barrier(1, kCT);  // s_red is reused by the next token
+    for (int i = 0; i < 4; ++i) {
+      h[i] = f32_to_bf16_rne(f[i]);
+      l[i] = f32_to_bf16_rne(f[i] - bf16_to_f32(h[i]));
     }
-    for (int k = ctid; k < p.C; k += kCT) {
-      float v = val(k);
-      if (p.in == kInEmbed && blockIdx.x == 0) p.x_out[(long long)b * p.ldx_out + k] = v;
-      if (p.norm_g) v = v * sc * p.norm_g[k];
-      const int pos = xperm(p.fmt, k);
-      if (p.fmt == kFmtBf16) {  // v = hi + lo to ~16 bits: the products stay near FP32 accuracy
-        const uint16_t hi = f32_to_bf16_rne(v);
-        reinterpret_cast<uint16_t*>(row)[pos] = hi;
-        reinterpret_cast<uint16_t*>(row + kMaxB * L.x_stride)[pos] = f32_to_bf16_rne(v - bf16_to_f32(hi));
-      } else {
-        reinterpret_cast<__half*>(row)[pos] = __float2half_rn(v);
+    *reinterpret_cast<uint2*>(row + 2 * k) = make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+    *reinterpret_cast<uint2*>(row_lo + 2 * k) =
+        make_uint2(l[0] | ((uint32_t)l[1] << 16), l[2] | ((uint32_t)l[3] << 16));
+    return;
+  }
+  const int base = k & ~15, j = k & 15;
+  *reinterpret_cast<__half2*>(row + 2 * (base + (j >> 1))) = __floats2half2_rn(v.x, v.z);
+  *reinterpret_cast<__half2*>(row + 2 * (base + 8 + (j >> 1))) = __floats2half2_rn(v.y, v.w);
+}
+
+// Compute warps: token b = warp into xs, RMS-normalised when norm_g is set
+// (FP16, permuted for 4-bit weights; bf16 hi + lo for bf16 weights), zero for
+// padding tokens.  Each warp loads its whole vector at once (up to 2048
+// elements held in registers; longer vectors in two passes), so staging costs
+// about one L2 round trip.  Ends with a barrier of the compute warps.
+constexpr int kHold = 16;  // float4 per lane held in registers
+static_assert(kWarps == kMaxB, "one compute warp per token");
+__device__ __forceinline__ void stage_inputs(const Params& p, const XLayout& L, uint8_t* xs, int ctid,
+                                             long long x_off) {
+  const int b = ctid >> 5, lane = ctid & 31;
+  uint8_t* row = xs + b * L.x_stride;
+  uint8_t* row_lo = row + kMaxB * L.x_stride;
+  const int ng = p.C / 4;  // groups of four elements
+  if (b >= p.B) {
+    for (int i = lane; i < ng; i += 32) {
+      *reinterpret_cast<uint2*>(row + 8 * i) = make_uint2(0u, 0u);
+      if (L.x_parts == 2) *reinterpret_cast<uint2*>(row_lo + 8 * i) = make_uint2(0u, 0u);
+    }
+    named_barrier(1, kCT);
+    return;
+  }
+  const float* src = nullptr;
+  const uint16_t* emb = nullptr;
+  if (p.in == kInEmbed) {
+    int tok = p.tok[b];
+    if (tok < 0 || tok >= p.vocab) {
+      if (lane == 0) set_guard(p.guard, kGuardBadIndex);
+      tok = 0;
+    }
+    emb = p.embed + (long long)tok * p.C;
+  } else {
+    src = p.x + (long long)b * p.ldx + x_off;
+  }
+  const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+  float* xo = (p.in == kInEmbed && blockIdx.x == 0) ? p.x_out + (long long)b * p.ldx_out : nullptr;
+  const float* gn = p.norm_g;
+  auto finish = [&](int k, float4 v, float sc) {
+    if (xo) {
+      xo[k] = v.x;
+      xo[k + 1] = v.y;
+      xo[k + 2] = v.z;
+      xo[k + 3] = v.w;
+    }
+    if (gn) {
+      v.x *= sc * gn[k];
+      v.y *= sc * gn[k + 1];
+      v.z *= sc * gn[k + 2];
+      v.w *= sc * gn[k + 3];
+    }
+    store4(p.fmt, row, row_lo, k, v);
+  };
+  if (ng <= 32 * kHold) {
+    float4 v[kHold];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < kHold; ++j) {
+      const int i = lane + 32 * j;
+      v[j] = i < ng ? load4(src, emb, vec, 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < kHold; ++j)
+      ss = fmaf(v[j].x, v[j].x, fmaf(v[j].y, v[j].y, fmaf(v[j].z, v[j].z, fmaf(v[j].w, v[j].w, ss))));
+    const float sc = gn ? 1.0f / sqrtf(warp_sum(ss) / (float)p.C + p.eps) : 1.f;
+#pragma unroll
+    for (int j = 0; j < kHold; ++j) {
+      const int i = lane + 32 * j;
+      if (i < ng) finish(4 * i, v[j], sc);
+    }
+  } else {
+    float ss = 0.f;
+    if (gn) {
+      for (int i = lane; i < ng; i += 32) {
+        const float4 v = load4(src, emb, vec, 4 * i);
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
       }
     }
+    const float sc = gn ? 1.0f / sqrtf(warp_sum(ss) / (float)p.C + p.eps) : 1.f;
+    for (int i = lane; i < ng; i += 32) finish(4 * i, load4(src, emb, vec, 4 * i), sc);
   }
   named_barrier(1, kCT);
 }
 
-// One warp's share of one pair member of a tile: 16 rows x 8 tokens, over the
-// warp's K chunk [k0, k1) (multiples of 32).  d: the MMA accumulator.
-__device__ __forceinline__ void tile_mma(const Params& p, const Layout& L, const uint8_t* m, const uint8_t* xs, int k0,
-                                         int k1, float* d, int lane) {
-  const int g = lane >> 2, t = lane & 3;
+
+// Where a unit (one row block) comes from: union entry u (0 for dense), first
+// output row a (virtual row for kSrcUnionRows), valid rows, the row
+// coordinate in the maps and which maps.
+struct UnitSrc {
+  int u, a, rows, crow;
+  bool routed;  // the routed-expert maps (else the dense / shared ones)
+};
+
+__device__ __forceinline__ int units_of(const Params& p, int U) {
+  const int tr = kTileRows * p.gw;
+  if (p.src == kSrcUnionRows) return (U + 1) * (p.slot_rows / tr);
+  if (p.src == kSrcUnionDown) return (U + 1) * (p.R / tr);
+  return (p.R + tr - 1) / tr;
+}
+
+__device__ __forceinline__ UnitSrc unit_src(const Params& p, int t, int U) {
+  const int tr = kTileRows * p.gw;
+  UnitSrc us;
+  us.routed = false;
+  if (p.src == kSrcDense) {
+    us.u = 0;
+    us.a = t * tr;
+    us.rows = min(tr, p.R - us.a);
+    us.crow = us.a;
+    return us;
+  }
+  int r, per;
+  if (p.src == kSrcUnionRows) {
+    us.a = t * tr;
+    us.u = us.a / p.slot_rows;
+    r = us.a - us.u * p.slot_rows;
+    per = p.slot_rows;
+  } else {
+    const int nrb = p.R / tr;
+    us.u = t / nrb;
+    us.a = (t - us.u * nrb) * tr;
+    r = us.a;
+    per = p.R;
+  }
+  us.rows = tr;
+  us.crow = r;
+  if (us.u < U) {
+    int e = p.union_ids[us.u];
+    if (e < 0 || e >= p.n_exp) {  // never address past the expert tensor
+      set_guard(p.guard, kGuardBadIndex);
+      e = 0;
+    }
+    us.crow = e * per + r;
+    us.routed = true;
+  }
+  return us;
+}
+
+// One warp's MMAs over one strip of one stage member: its 16 rows (lines
+// line0 and line0 + 8 of the member; line0 & 7 == g, the swizzle phase) x 8
+// tokens, strip elements kb.. of the row.
+template <int FMT>
+__device__ __forceinline__ void strip_mma(const uint8_t* mem, const uint8_t* xs, const XLayout& L, int line0, int kb,
+                                          float* d, int g, int t) {
+  const uint8_t* l0 = mem + line0 * kStrip;
+  const uint8_t* l8 = l0 + 8 * kStrip;
   const uint8_t* xg = xs + g * L.x_stride;  // token g (the MMA's column n = g)
-  const uint8_t* xl = xg + kMaxB * L.x_stride;  // its lo part (bf16 weights)
-  if (p.fmt == kFmtBf16) {
-    const uint8_t* r0 = m + g * L.row_bytes;
-    const uint8_t* r8 = m + (g + 8) * L.row_bytes;
-    for (int k = k0; k < k1; k += 16) {
+  if (FMT == kFmtQ4) {
+    const uint16_t* s0 = reinterpret_cast<const uint16_t*>(mem + kStageW + line0 * 16);
+    const uint16_t* s8 = reinterpret_cast<const uint16_t*>(mem + kStageW + (line0 + 8) * 16);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // 32-element blocks of the strip
+      const int off = ((j ^ g) << 4) + 4 * t;
+      const uint32_t u0 = *reinterpret_cast<const uint32_t*>(l0 + off);
+      const uint32_t u8 = *reinterpret_cast<const uint32_t*>(l8 + off);
+      const int k = kb + 32 * j;
       uint32_t a[4], b[2];
-      a[0] = *reinterpret_cast<const uint32_t*>(r0 + (k + 2 * t) * 2);
-      a[1] = *reinterpret_cast<const uint32_t*>(r8 + (k + 2 * t) * 2);
-      a[2] = *reinterpret_cast<const uint32_t*>(r0 + (k + 8 + 2 * t) * 2);
-      a[3] = *reinterpret_cast<const uint32_t*>(r8 + (k + 8 + 2 * t) * 2);
+      float e[4] = {0.f, 0.f, 0.f, 0.f};
+      // low nibbles: elements k + 0..15
+      a[0] = nib2_to_f16x2(u0);
+      a[1] = nib2_to_f16x2(u8);
+      a[2] = nib2_to_f16x2(u0 >> 8);
+      a[3] = nib2_to_f16x2(u8 >> 8);
+      b[0] = *reinterpret_cast<const uint32_t*>(xg + (k + 2 * t) * 2);
+      b[1] = *reinterpret_cast<const uint32_t*>(xg + (k + 8 + 2 * t) * 2);
+      mma_f16(e, a, b);
+      // high nibbles: elements k + 16..31
+      a[0] = nib2_to_f16x2(u0 >> 4);
+      a[1] = nib2_to_f16x2(u8 >> 4);
+      a[2] = nib2_to_f16x2(u0 >> 12);
+      a[3] = nib2_to_f16x2(u8 >> 12);
+      b[0] = *reinterpret_cast<const uint32_t*>(xg + (k + 16 + 2 * t) * 2);
+      b[1] = *reinterpret_cast<const uint32_t*>(xg + (k + 24 + 2 * t) * 2);
+      mma_f16(e, a, b);
+      const float sg = f16_bits_to_f32(s0[j]), sg8 = f16_bits_to_f32(s8[j]);
+      d[0] = fmaf(sg, e[0], d[0]);
+      d[1] = fmaf(sg, e[1], d[1]);
+      d[2] = fmaf(sg8, e[2], d[2]);
+      d[3] = fmaf(sg8, e[3], d[3]);
+    }
+  } else {
+    const uint8_t* xl = xg + kMaxB * L.x_stride;  // the token's lo part
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // 16-element steps of the 64-element strip
+      const int o0 = (((2 * q) ^ g) << 4) + 4 * t, o1 = (((2 * q + 1) ^ g) << 4) + 4 * t;
+      uint32_t a[4], b[2];
+      a[0] = *reinterpret_cast<const uint32_t*>(l0 + o0);
+      a[1] = *reinterpret_cast<const uint32_t*>(l8 + o0);
+      a[2] = *reinterpret_cast<const uint32_t*>(l0 + o1);
+      a[3] = *reinterpret_cast<const uint32_t*>(l8 + o1);
+      const int k = kb + 16 * q;
       b[0] = *reinterpret_cast<const uint32_t*>(xg + (k + 2 * t) * 2);
       b[1] = *reinterpret_cast<const uint32_t*>(xg + (k + 8 + 2 * t) * 2);
       mma_bf16(d, a, b);
@@ -256,39 +326,6 @@ __device__ __forceinline__ void tile_mma(const Params& p, const Layout& L, const
       b[1] = *reinterpret_cast<const uint32_t*>(xl + (k + 8 + 2 * t) * 2);
       mma_bf16(d, a, b);
     }
-    return;
-  }
-  const uint8_t* r0 = m + g * L.row_bytes;
-  const uint8_t* r8 = m + (g + 8) * L.row_bytes;
-  const uint16_t* s0 = reinterpret_cast<const uint16_t*>(m + kTileRows * L.row_bytes + g * L.scale_bytes);
-  const uint16_t* s8 = reinterpret_cast<const uint16_t*>(m + kTileRows * L.row_bytes + (g + 8) * L.scale_bytes);
-  for (int k = k0; k < k1; k += 32) {
-    const int blk = k >> 5;
-    const uint32_t u0 = *reinterpret_cast<const uint32_t*>(r0 + blk * 16 + 4 * t);
-    const uint32_t u8 = *reinterpret_cast<const uint32_t*>(r8 + blk * 16 + 4 * t);
-    uint32_t a[4], b[2];
-    float e[4] = {0.f, 0.f, 0.f, 0.f};
-    // low nibbles: elements 32 blk + 0..15
-    a[0] = nib2_to_f16x2(u0);
-    a[1] = nib2_to_f16x2(u8);
-    a[2] = nib2_to_f16x2(u0 >> 8);
-    a[3] = nib2_to_f16x2(u8 >> 8);
-    b[0] = *reinterpret_cast<const uint32_t*>(xg + (k + 2 * t) * 2);
-    b[1] = *reinterpret_cast<const uint32_t*>(xg + (k + 8 + 2 * t) * 2);
-    mma_f16(e, a, b);
-    // high nibbles: elements 32 blk + 16..31
-    a[0] = nib2_to_f16x2(u0 >> 4);
-    a[1] = nib2_to_f16x2(u8 >> 4);
-    a[2] = nib2_to_f16x2(u0 >> 12);
-    a[3] = nib2_to_f16x2(u8 >> 12);
-    b[0] = *reinterpret_cast<const uint32_t*>(xg + (k + 16 + 2 * t) * 2);
-    b[1] = *reinterpret_cast<const uint32_t*>(xg + (k + 24 + 2 * t) * 2);
-    mma_f16(e, a, b);
-    const float sg = f16_bits_to_f32(s0[blk]), sg8 = f16_bits_to_f32(s8[blk]);
-    d[0] = fmaf(sg, e[0], d[0]);
-    d[1] = fmaf(sg, e[1], d[1]);
-    d[2] = fmaf(sg8, e[2], d[2]);
-    d[3] = fmaf(sg8, e[3], d[3]);
   }
 }
 
@@ -299,28 +336,49 @@ __device__ __forceinline__ void argmax_merge(float& bv, int& bi, float ov, int o
   }
 }
 
+// (value, index) as one integer that orders like the argmax: larger value
+// first, then lower index; 0 = no candidate.
+__device__ __forceinline__ unsigned long long am_key(float v, int i) {
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)i);
+}
+__device__ __forceinline__ void am_unkey(unsigned long long k, float& v, int& i) {
+  if (k == 0ull) {
+    v = -INFINITY;
+    i = 0x7fffffff;
+    return;
+  }
+  const uint32_t h = (uint32_t)(k >> 32);
+  v = __uint_as_float((h & 0x80000000u) ? (h & 0x7fffffffu) : ~h);
+  i = (int)(0xFFFFFFFFu - (uint32_t)k);
+}
+
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1) k_bgemv(const Params p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const Layout L = layout_of(p);
+__global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ Params p, const __grid_constant__ Maps mp) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int npair = p.epi == kEpiSwiglu ? 2 : 1;
-  const int nst = p.nstages;
-  const int stage_bytes = npair * L.member_bytes;
-  uint8_t* stages = smem;
-  uint8_t* xs = smem + nst * stage_bytes;                               // [8][C] staged tokens
-  float* part = reinterpret_cast<float*>(xs + L.x_parts * kMaxB * L.x_stride);  // [2][npair][kWarps][16][8]
-  float* red = part + 2 * npair * kWarps * kTileRows * kMaxB;           // [npair][rows_cta][8]
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + npair * p.rows_cta_max * kMaxB);
+  const int nst = p.nstages, GW = p.gw, KS = p.ks, TR = kTileRows * p.gw;
+  const int member = kStageW + (FMT == kFmtQ4 ? kStageS : 0);
+  const int stage_bytes = npair * member;
+  const int strip_elems = FMT == kFmtQ4 ? 256 : 64;
+  const int spu = p.C / strip_elems / KS;  // stages per unit
+  XLayout L;
+  L.x_stride = p.C * 2 + 16;
+  L.x_parts = FMT == kFmtBf16 ? 2 : 1;
+  uint8_t* stages = smem;                                                     // 1024-aligned members
+  uint8_t* xs = smem + nst * stage_bytes;                                     // [parts][8][x_stride]
+  float* part = reinterpret_cast<float*>(xs + L.x_parts * kMaxB * L.x_stride);  // [npair][8 warps][16][8]
+  uint64_t* full = reinterpret_cast<uint64_t*>(part + npair * kPartFloats);
   uint64_t* empty = full + kMaxStages;
-  __shared__ float s_red[kWarps];
-  __shared__ float s_bv[kWarps][kMaxB];
-  __shared__ int s_bi[kWarps][kMaxB];
+  __shared__ unsigned long long s_key[kMaxB];
   __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // the tile range of this CTA; for MoE sources it depends on the union the
+  // the unit range of this CTA; for MoE sources it depends on the union the
   // routing kernel wrote, so it is read after griddepcontrol.wait
-  auto tile_range = [&](int& U, int& t0, int& t1) {
+  auto unit_range = [&](int& U, int& t0, int& t1) {
     U = 0;
     if (p.src != kSrcDense) {
       U = *p.n_union;
@@ -329,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const Params p) {
         U = 0;
       }
     }
-    const int nt = tiles_of(p, U);
+    const int nt = units_of(p, U);
     t0 = (int)((long long)blockIdx.x * nt / p.ncta);
     t1 = (int)((long long)(blockIdx.x + 1) * nt / p.ncta);
   };
@@ -341,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const Params p) {
     }
     fence_mbar_init();
   }
+  if (threadIdx.x < kMaxB) s_key[threadIdx.x] = 0ull;
   __syncthreads();
 
   // ------------------------------------------------------------ copy lane
@@ -350,16 +409,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const Params p) {
       const uint64_t pol = l2_evict_first_policy();
       if (p.src != kSrcDense) pdl_wait();  // union and expert ids come from the routing kernel
       int U, t0, t1;
-      tile_range(U, t0, t1);
+      unit_range(U, t0, t1);
+      const uint32_t tx = (uint32_t)(npair * member);
       int n = 0;
-      for (int t = t0; t < t1; ++t, ++n) {
-        const int s = n % nst, k = n / nst;
-        if (n >= nst && !mbar_wait(&empty[s], (k - 1) & 1)) {
-          set_guard(p.guard, kGuardWaitTimeout);
-          break;
+      bool alive = true;
+      for (int t = t0; t < t1 && alive; ++t) {
+        const UnitSrc us = unit_src(p, t, U);
+        for (int st = 0; st < spu; ++st, ++n) {
+          const int s = n % nst, k = n / nst;
+          if (n >= nst && !mbar_wait(&empty[s], (k - 1) & 1)) {
+            set_guard(p.guard, kGuardWaitTimeout);
+            alive = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], tx);
+          for (int j = 0; j < npair; ++j) {
+            uint8_t* dst = stages + s * stage_bytes + j * member;
+            tma_load_3d(dst, us.routed ? &mp.ew[j] : &mp.w[j], us.crow, st * KS, &full[s], pol);
+            if (FMT == kFmtQ4)
+              tma_load_3d(dst + kStageW, us.routed ? &mp.es[j] : &mp.s[j], us.crow, st * KS, &full[s], pol);
+          }
         }
-        issue_tile(p, L, tile_src(p, t, U), stages + s * stage_bytes, &full[s], pol);
       }
+      // the CTA leaves only once its copies have landed
       for (int u = (n > nst ? n - nst : 0); u < n; ++u)
         if (!mbar_wait(&full[u % nst], (u / nst) & 1)) set_guard(p.guard, kGuardWaitTimeout);
     }
@@ -371,106 +443,104 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const Params p) {
   pdl_wait();
   pdl_launch_dependents();
   int U, t0, t1;
-  tile_range(U, t0, t1);
-  const int r0 = (p.src == kSrcDense || p.src == kSrcUnionRows) ? t0 * kTileRows : 0;
-  const int r1 = (p.src == kSrcDense) ? min(t1 * kTileRows, p.R) : (p.src == kSrcUnionRows ? t1 * kTileRows : 0);
+  unit_range(U, t0, t1);
   int staged_u = -1;
   if (p.src != kSrcUnionDown) {
-    stage_inputs(p, L, xs, s_red, ctid, 0);
+    stage_inputs(p, L, xs, ctid, 0);
     staged_u = 0;
   }
-  // K chunk of this warp (a multiple of 32 columns)
-  const int nblk = p.C / 32;
-  const int k0 = (int)((long long)warp * nblk / kWarps) * 32, k1 = (int)((long long)(warp + 1) * nblk / kWarps) * 32;
+  const int gw = warp / KS, ks = warp % KS;
   const int g = lane >> 2, tq = lane & 3;
+  const int line0 = ks * TR + gw * kTileRows + g;  // TR is a multiple of 8: line0 & 7 == g
+  float bv[2] = {-INFINITY, -INFINITY};  // argmax candidates of this thread's tokens
+  int bi[2] = {0x7fffffff, 0x7fffffff};
   bool ok = true;
   int n = 0;
-  for (int t = t0; t < t1; ++t, ++n) {
-    const TileSrc ts = tile_src(p, t, U);
-    if (p.src == kSrcUnionDown && ts.u != staged_u) {  // the tile's expert input, for every token
+  for (int t = t0; t < t1; ++t) {
+    const UnitSrc us = unit_src(p, t, U);
+    if (p.src == kSrcUnionDown && us.u != staged_u) {  // the unit's expert input, for every token
       named_barrier(1, kCT);
-      stage_inputs(p, L, xs, s_red, ctid, (long long)ts.u * p.C);
-      staged_u = ts.u;
+      stage_inputs(p, L, xs, ctid, (long long)us.u * p.C);
+      staged_u = us.u;
     }
-    const int s = n % nst, k = n / nst;
-    if (ok && !mbar_wait(&full[s], k & 1)) {
-      if (lane == 0) set_guard(p.guard, kGuardWaitTimeout);
-      ok = false;
-    }
-    float* pt = part + (n & 1) * npair * kWarps * kTileRows * kMaxB;
-    for (int j = 0; j < npair; ++j) {
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      if (ok) tile_mma(p, L, stages + s * stage_bytes + j * L.member_bytes, xs, k0, k1, d, lane);
-      float* pw = pt + (j * kWarps + warp) * kTileRows * kMaxB;
-      pw[g * kMaxB + 2 * tq] = d[0];
-      pw[g * kMaxB + 2 * tq + 1] = d[1];
-      pw[(g + 8) * kMaxB + 2 * tq] = d[2];
-      pw[(g + 8) * kMaxB + 2 * tq + 1] = d[3];
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    named_barrier(1, kCT);
-    // fixed-order sum over the warps' K chunks
-    for (int e = ctid; e < npair * kTileRows * kMaxB; e += kCT) {
-      const int j = e / (kTileRows * kMaxB), rr = e % (kTileRows * kMaxB);
-      float v = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) v += pt[(j * kWarps + w) * kTileRows * kMaxB + rr];
-      const int b = rr % kMaxB, ri = rr / kMaxB;
-      if (p.src == kSrcUnionDown) {
-        // partial output of expert u for the tokens that selected it
-        const int slot = (ts.u < U) ? p.slot_of[ts.u * kMaxB + b] : p.top_k;
-        if (b < p.B && slot >= 0 && ri < ts.rows)
-          p.part_out[((long long)b * (p.top_k + 1) + slot) * p.R + ts.a + ri] = v;
-      } else {
-        const int row = ts.a - r0 + ri;
-        if (row < r1 - r0) red[(j * p.rows_cta_max + row) * kMaxB + b] = v;
+    float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int st = 0; st < spu; ++st, ++n) {
+      const int s = n % nst, k = n / nst;
+      if (ok && !mbar_wait(&full[s], k & 1)) {
+        if (lane == 0) set_guard(p.guard, kGuardWaitTimeout);
+        ok = false;
       }
+      if (ok) {
+        const int kb = (st * KS + ks) * strip_elems;
+        strip_mma<FMT>(stages + s * stage_bytes, xs, L, line0, kb, d[0], g, tq);
+        if (npair == 2) strip_mma<FMT>(stages + s * stage_bytes + member, xs, L, line0, kb, d[1], g, tq);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // finish one output (local row ri, token b) of the unit
+    auto out = [&](int ri, int b, float v, float vu, int slot_b) {
+      if (b >= p.B || ri >= us.rows) return;
+      if (p.src == kSrcUnionDown) {
+        const int slot = (us.u < U) ? p.slot_of[us.u * kMaxB + b] : p.top_k;
+        if (slot >= 0) p.part_out[((long long)b * (p.top_k + 1) + slot) * p.R + us.a + ri] = v;
+        return;
+      }
+      float* y = p.y ? p.y + (long long)b * p.ldy + us.a + ri : nullptr;
+      if (p.epi == kEpiStore) *y = v;
+      else if (p.epi == kEpiResid) *y += v;
+      else if (p.epi == kEpiSwiglu) *y = siluf_(v) * vu;
+      else {
+        if (y) *y = v;
+        argmax_merge(bv[slot_b], bi[slot_b], v, us.a + ri);
+      }
+    };
+    if (KS == 1) {  // this warp holds whole rows: finish them from registers
+      const int r0 = gw * kTileRows + g;
+      out(r0, 2 * tq, d[0][0], d[1][0], 0);
+      out(r0, 2 * tq + 1, d[0][1], d[1][1], 1);
+      out(r0 + 8, 2 * tq, d[0][2], d[1][2], 0);
+      out(r0 + 8, 2 * tq + 1, d[0][3], d[1][3], 1);
+    } else {  // fixed-order sum of the KS strip lanes of each row group
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (j == 1 && npair == 1) break;
+        float* pw = part + j * kPartFloats + warp * kTileRows * kMaxB;
+        pw[g * kMaxB + 2 * tq] = d[j][0];
+        pw[g * kMaxB + 2 * tq + 1] = d[j][1];
+        pw[(g + 8) * kMaxB + 2 * tq] = d[j][2];
+        pw[(g + 8) * kMaxB + 2 * tq + 1] = d[j][3];
+      }
+      named_barrier(1, kCT);
+      for (int e = ctid; e < TR * kMaxB; e += kCT) {  // b = ctid % 8 for every e of this thread
+        const int b = e % kMaxB, ri = e / kMaxB;
+        const int base = (ri / kTileRows) * KS * kTileRows * kMaxB + (ri % kTileRows) * kMaxB + b;
+        float v = 0.f, vu = 0.f;
+        for (int c = 0; c < KS; ++c) v += part[base + c * kTileRows * kMaxB];
+        if (npair == 2)
+          for (int c = 0; c < KS; ++c) vu += part[kPartFloats + base + c * kTileRows * kMaxB];
+        out(ri, b, v, vu, 0);
+      }
+      named_barrier(1, kCT);
     }
   }
   if (named_barrier_or(1, kCT, !ok)) return;  // one decision for all compute threads
-  if (p.src == kSrcUnionDown) return;
+  if (p.epi != kEpiArgmax) return;
 
-  // ------------------------------------------------------------ epilogue
-  const int rows_cta = r1 - r0;
-  if (p.epi != kEpiArgmax) {
-    for (int e = ctid; e < rows_cta * p.B; e += kCT) {
-      const int row = e / p.B, b = e % p.B;
-      const float v = red[row * kMaxB + b];
-      float* y = p.y + (long long)b * p.ldy + r0 + row;
-      if (p.epi == kEpiStore) *y = v;
-      else if (p.epi == kEpiResid) *y += v;
-      else *y = siluf_(v) * red[(p.rows_cta_max + row) * kMaxB + b];
-    }
-    return;
-  }
-  // per-token argmax: this CTA's candidates, then the last CTA merges
-  for (int b = 0; b < p.B; ++b) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int row = ctid; row < rows_cta; row += kCT) {
-      const float v = red[row * kMaxB + b];
-      if (p.y) p.y[(long long)b * p.ldy + r0 + row] = v;
-      argmax_merge(bv, bi, v, r0 + row);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      argmax_merge(bv, bi, ov, oi);
-    }
-    if (lane == 0) {
-      s_bv[warp][b] = bv;
-      s_bi[warp][b] = bi;
-    }
+  // ------------------------------------------------------------ per-token argmax
+  if (KS == 1) {
+    if (bi[0] != 0x7fffffff) atomicMax(&s_key[2 * tq], am_key(bv[0], bi[0]));
+    if (bi[1] != 0x7fffffff) atomicMax(&s_key[2 * tq + 1], am_key(bv[1], bi[1]));
+  } else if (bi[0] != 0x7fffffff) {
+    atomicMax(&s_key[ctid % kMaxB], am_key(bv[0], bi[0]));
   }
   named_barrier(1, kCT);
   if (ctid < p.B) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int w = 0; w < kWarps; ++w) argmax_merge(bv, bi, s_bv[w][ctid], s_bi[w][ctid]);
-    p.part_val[blockIdx.x * kMaxB + ctid] = bv;
-    p.part_idx[blockIdx.x * kMaxB + ctid] = bi;
+    float v;
+    int i;
+    am_unkey(s_key[ctid], v, i);
+    p.part_val[blockIdx.x * kMaxB + ctid] = v;
+    p.part_idx[blockIdx.x * kMaxB + ctid] = i;
   }
   named_barrier(1, kCT);
   if (ctid == 0) {
@@ -503,59 +573,92 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const Params p) {
 }
 
 // One CTA: routing of every token, then the union of the selected experts.
-__global__ void __launch_bounds__(256) k_route(const Route r) {
-  __shared__ float lg[kMaxB][512];  // logits of up to 511 experts + the shared gate per token
+// Warp b selects token b's top_k by repeated warp-wide argmax (largest logit,
+// lowest index on ties: the same set and order as ranking all experts); the
+// union is an ascending ballot scan over the experts' flags.
+constexpr int kRouteWarps = 8;
+constexpr int kRouteMaxE = 512;  // experts + the shared gate per token
+__global__ void __launch_bounds__(kRouteWarps * 32) k_route(const Route r) {
   __shared__ int sel[kMaxB][16];
   __shared__ float selv[kMaxB][16];
-  __shared__ int flag[512];
-  __shared__ int pos[512];
-  __shared__ int s_n;
+  __shared__ int flag[kRouteMaxE];
+  __shared__ int cnt[kRouteMaxE / 32 + 1];
+  __shared__ int pos[kRouteMaxE];
   pdl_wait();
   pdl_launch_dependents();
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = r.E, K = r.top_k;
-  for (int b = 0; b < r.B; ++b)
-    for (int e = tid; e <= E; e += blockDim.x) lg[b][e] = r.logits[(long long)b * r.ld + e];
-  for (int e = tid; e < E; e += blockDim.x) flag[e] = 0;
+  for (int e = tid; e < kRouteMaxE; e += blockDim.x) flag[e] = 0;
   __syncthreads();
-  // rank of every (token, expert): logits above it, or equal with a lower index
-  for (int i = tid; i < r.B * E; i += blockDim.x) {
-    const int b = i / E, e = i % E;
-    const float v = lg[b][e];
-    int rank = 0;
-    for (int f = 0; f < E; ++f) {
-      const float w = lg[b][f];
-      rank += (w > v || (w == v && f < e)) ? 1 : 0;
+  if (warp < r.B) {
+    const int b = warp;
+    constexpr int kPer = kRouteMaxE / 32;
+    float v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      const float x = e < E ? r.logits[(long long)b * r.ld + e] : -INFINITY;
+      v[i] = x == x ? x : -INFINITY;  // a NaN logit ranks last
     }
-    if (rank < K) {
-      sel[b][rank] = e;
-      selv[b][rank] = v;
-      flag[e] = 1;
-    }
-  }
-  __syncthreads();
-  if (tid < r.B) {  // softmax over the selected logits, sigmoid gate of the shared expert
-    const int b = tid;
-    const float m = selv[b][0];
-    float den = 0.f;
-    for (int k = 0; k < K; ++k) den += __expf(selv[b][k] - m);
+    uint32_t taken = 0u;
     for (int k = 0; k < K; ++k) {
-      r.w[b * (K + 1) + k] = __expf(selv[b][k] - m) / den;
-      if (r.ids) r.ids[b * K + k] = sel[b][k];
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !(taken >> i & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == 0) {
+        sel[b][k] = bi;
+        selv[b][k] = bv;
+      }
     }
-    r.w[b * (K + 1) + K] = sigmoidf_(lg[b][E]);
-  }
-  if (tid == 0) {  // ascending union (serial scan over at most 511 flags)
-    int n = 0;
-    for (int e = 0; e < E; ++e) {
-      pos[e] = n;
-      if (flag[e]) r.union_ids[n++] = e;
+    __syncwarp();
+    if (lane < K) flag[sel[b][lane]] = 1;
+    if (lane == 0) {  // softmax over the selected logits, sigmoid gate of the shared expert
+      const float m = selv[b][0];
+      float den = 0.f;
+      for (int k = 0; k < K; ++k) den += __expf(selv[b][k] - m);
+      for (int k = 0; k < K; ++k) {
+        r.w[b * (K + 1) + k] = __expf(selv[b][k] - m) / den;
+        if (r.ids) r.ids[b * K + k] = sel[b][k];
+      }
+      r.w[b * (K + 1) + K] = sigmoidf_(r.logits[(long long)b * r.ld + E]);
     }
-    *r.n_union = n;
-    s_n = n;
   }
   __syncthreads();
-  const int U = s_n;
+  const int nch = (E + 31) / 32;
+  for (int c = warp; c < nch; c += kRouteWarps) {
+    const unsigned m = __ballot_sync(0xffffffffu, flag[32 * c + lane] != 0);
+    if (lane == 0) cnt[c] = __popc(m);
+  }
+  __syncthreads();
+  for (int c = warp; c < nch; c += kRouteWarps) {
+    int base = 0;
+    for (int q = 0; q < c; ++q) base += cnt[q];
+    const int e = 32 * c + lane;
+    const unsigned m = __ballot_sync(0xffffffffu, flag[e] != 0);
+    const int at = base + __popc(m & ((1u << lane) - 1u));
+    pos[e] = at;
+    if (flag[e]) r.union_ids[at] = e;
+  }
+  int U = 0;
+  for (int q = 0; q < nch; ++q) U += cnt[q];
+  if (tid == 0) *r.n_union = U;
   for (int i = tid; i < (kMaxUnion + 1) * kMaxB; i += blockDim.x) r.slot_of[i] = -1;
   __syncthreads();
   for (int i = tid; i < r.B * K; i += blockDim.x) {
@@ -579,9 +682,9 @@ __global__ void k_moe_reduce(float* y, int ldy, const float* part, const float* 
 }  // namespace
 
 cudaError_t route(const Route& r, cudaStream_t st, bool pdl) {
-  if (r.B < 1 || r.B > kMaxB || r.E < 1 || r.E > 511 || r.top_k < 1 || r.top_k > 16 || r.B * r.top_k > kMaxUnion)
+  if (r.B < 1 || r.B > kMaxB || r.E < 1 || r.E > 511 || r.top_k < 1 || r.top_k > 16 || r.top_k > r.E || r.B * r.top_k > kMaxUnion)
     return cudaErrorInvalidValue;
-  return launch_k(k_route, dim3(1), dim3(256), 0, st, pdl, r);
+  return launch_k(k_route, dim3(1), dim3(kRouteWarps * 32), 0, st, pdl, r);
 }
 
 cudaError_t moe_reduce(float* y, int ldy, const float* part, const float* w, int R, int B, int top_k, cudaStream_t st,
@@ -590,21 +693,38 @@ cudaError_t moe_reduce(float* y, int ldy, const float* part, const float* w, int
   return launch_k(k_moe_reduce, dim3((n + 255) / 256), dim3(256), 0, st, pdl, y, ldy, part, w, R, B, top_k);
 }
 
-Plan plan(int R, int C, int fmt, int epi, int nsm) {
+Plan plan(int R, int C, int fmt, int epi, int nsm, int row_mult) {
   Plan pl = {};
   pl.ok = false;
-  if (R <= 0 || C <= 0 || C % 32 != 0) return pl;
-  if (fmt == kFmtQ4 && C % 256 != 0) return pl;  // scale rows stay 16-byte aligned
+  const int strip_elems = fmt == kFmtQ4 ? 256 : 64;
+  if (R <= 0 || C <= 0 || C % strip_elems != 0 || nsm <= 0) return pl;
+  const int nstrips = C / strip_elems;
   const int npair = epi == kEpiSwiglu ? 2 : 1;
-  const int row_bytes = fmt == kFmtBf16 ? C * 2 + 16 : C / 2 + 16;  // as the kernel's Layout
-  const int scale_bytes = fmt == kFmtBf16 ? 0 : C / 16;
-  const int stage_bytes = npair * kTileRows * (row_bytes + scale_bytes);
-  const int ntiles = (R + kTileRows - 1) / kTileRows;
-  pl.ncta = ntiles < nsm ? ntiles : nsm;
-  const int tiles_cta = (ntiles + pl.ncta - 1) / pl.ncta;
-  pl.rows_cta_max = tiles_cta * kTileRows;
-  const int fixed = (fmt == kFmtBf16 ? 2 : 1) * kMaxB * (C * 2 + 16) + 4 * (2 * npair * kWarps * kTileRows * kMaxB) +
-                    4 * npair * pl.rows_cta_max * kMaxB + 2 * kMaxStages * 8;
+  const int stage_bytes = npair * (kStageW + (fmt == kFmtQ4 ? kStageS : 0));
+  // row block of 16 * GW rows: the largest one whose units spread over the
+  // SMs almost as evenly as the best choice (fewer row blocks need fewer
+  // cross-warp sums)
+  double score[4] = {0, 0, 0, 0};
+  double best = 0;
+  for (int i = 0; i < 4; ++i) {
+    const int GW = 8 >> i, KS = kWarps / GW, TR = kTileRows * GW;
+    if (nstrips % KS != 0 || (row_mult && row_mult % TR != 0)) continue;
+    const long long units = (R + TR - 1) / TR;
+    const long long per = (units + nsm - 1) / nsm;
+    score[i] = (double)units / (double)(nsm * per) * (double)R / (double)(units * TR);
+    if (score[i] > best) best = score[i];
+  }
+  int pick = -1;
+  for (int i = 0; i < 4 && pick < 0; ++i)
+    if (score[i] > 0 && score[i] >= best - 0.08) pick = i;
+  if (pick < 0) return pl;
+  pl.gw = 8 >> pick;
+  pl.ks = kWarps / pl.gw;
+  const int TR = kTileRows * pl.gw;
+  const long long units = (R + TR - 1) / TR;
+  pl.ncta = (int)(units < nsm ? units : nsm);
+  const int fixed = (fmt == kFmtBf16 ? 2 : 1) * kMaxB * (C * 2 + 16) + 4 * npair * kPartFloats + 2 * kMaxStages * 8 +
+                    1024;  // + alignment of the stages
   int ns = kInFlight / stage_bytes;
   ns = ns < 2 ? 2 : (ns > kMaxStages ? kMaxStages : ns);
   while (ns > 2 && fixed + ns * stage_bytes > kMaxSmem) --ns;
@@ -614,21 +734,80 @@ Plan plan(int R, int C, int fmt, int epi, int nsm) {
   return pl;
 }
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// {128-byte strip, row, strip index} over `rows` rows of a matrix with
+// `row_bytes` bytes per row; box = 16 * GW rows x KS strips.
+bool encode_w(CUtensorMap* m, const void* base, long long rows, int row_bytes, int TR, int KS) {
+  if (!base || rows <= 0 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kStrip, (cuuint64_t)rows, (cuuint64_t)(row_bytes / kStrip)};
+  cuuint64_t str[2] = {(cuuint64_t)row_bytes, (cuuint64_t)kStrip};
+  cuuint32_t box[3] = {(cuuint32_t)kStrip, (cuuint32_t)TR, (cuuint32_t)KS};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, str, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// The fp16 scales of the same rows: {16 bytes (8 blocks) of a strip, row, strip index}.
+bool encode_s(CUtensorMap* m, const void* base, long long rows, int C, int TR, int KS) {
+  if (!base || rows <= 0 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+  cuuint64_t dims[3] = {16, (cuuint64_t)rows, (cuuint64_t)(C / 256)};
+  cuuint64_t str[2] = {(cuuint64_t)(C / 16), 16};
+  cuuint32_t box[3] = {16, (cuuint32_t)TR, (cuuint32_t)KS};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, str, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
 cudaError_t init() {
   cudaError_t e = cudaFuncSetAttribute(k_bgemv<kFmtBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_bgemv<kFmtQ4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+  if (e == cudaSuccess && !g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e == cudaSuccess && (q != cudaDriverEntryPointSuccess || !fn)) e = cudaErrorNotSupported;
+    if (e == cudaSuccess) g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
   return e;
 }
 
 cudaError_t launch(const Params& p0, const Plan& pl, cudaStream_t st, bool pdl) {
-  if (!pl.ok || p0.B < 1 || p0.B > kMaxB) return cudaErrorInvalidValue;
+  if (!pl.ok || !g_encode || p0.B < 1 || p0.B > kMaxB) return cudaErrorInvalidValue;
   Params p = p0;
   p.ncta = pl.ncta;
   p.nstages = pl.nstages;
-  p.rows_cta_max = pl.rows_cta_max;
+  p.gw = pl.gw;
+  p.ks = pl.ks;
+  const int TR = kTileRows * pl.gw;
+  const int npair = p.epi == kEpiSwiglu ? 2 : 1;
+  const int row_bytes = p.fmt == kFmtQ4 ? p.C / 2 : p.C * 2;
+  alignas(64) Maps mp;
+  memset(&mp, 0, sizeof(mp));
+  for (int j = 0; j < npair; ++j) {
+    if (p.src == kSrcDense) {
+      if (!encode_w(&mp.w[j], p.W[j], p.R, row_bytes, TR, pl.ks)) return cudaErrorInvalidValue;
+      if (p.fmt == kFmtQ4 && !encode_s(&mp.s[j], p.S[j], p.R, p.C, TR, pl.ks)) return cudaErrorInvalidValue;
+      continue;
+    }
+    // union sources: the experts' matrices stacked, and the shared expert's
+    const long long per = p.src == kSrcUnionRows ? p.slot_rows : p.R;
+    if (p.n_exp < 1 || per % TR != 0 || p.exp_stride != per * row_bytes ||
+        (p.fmt == kFmtQ4 && p.exp_sstride != per * (p.C / 16)))
+      return cudaErrorInvalidValue;
+    if (!encode_w(&mp.ew[j], p.exp_base[j], per * p.n_exp, row_bytes, TR, pl.ks) ||
+        !encode_w(&mp.w[j], p.sh_base[j], per, row_bytes, TR, pl.ks))
+      return cudaErrorInvalidValue;
+    if (p.fmt == kFmtQ4 && (!encode_s(&mp.es[j], p.exp_scale[j], per * p.n_exp, p.C, TR, pl.ks) ||
+                            !encode_s(&mp.s[j], p.sh_scale[j], per, p.C, TR, pl.ks)))
+      return cudaErrorInvalidValue;
+  }
   auto k = p.fmt == kFmtBf16 ? k_bgemv<kFmtBf16> : k_bgemv<kFmtQ4>;
-  return launch_k(k, dim3(pl.ncta), dim3(kThreads), (size_t)pl.smem, st, pdl, p);
+  return launch_k(k, dim3(pl.ncta), dim3(kThreads), (size_t)pl.smem, st, pdl, p, mp);
 }
 
 }  // namespace bgemv

@@ -9,6 +9,7 @@
 // iteration captured once and replayed; argmax on the device, a 4-byte id
 // back).
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -65,6 +66,29 @@ int current_device(int* dev, int* nsm) {
   HY_CK(cudaGetDevice(dev));
   HY_CK(cudaDeviceGetAttribute(nsm, cudaDevAttrMultiProcessorCount, *dev));
   return HY_OK;
+}
+
+// Seeded values for synthetic caches: a 64-bit mix of (seed, index) mapped
+// to [-scale, scale).
+__device__ __forceinline__ float synth_value(uint64_t seed, uint64_t i, float scale) {
+  uint64_t z = seed + (i + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return ((float)(uint32_t)(z >> 40) * (1.0f / 8388608.0f) - 1.0f) * scale;
+}
+
+__global__ void k_fill_bf16(uint16_t* dst, long long rows, int row_len, long long stride, uint64_t seed) {
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < rows * row_len;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long r = e / row_len, k = e % row_len;
+    dst[r * stride + k] = f32_to_bf16_rne(synth_value(seed, (uint64_t)e, 1.0f));
+  }
+}
+
+__global__ void k_fill_f32(float* dst, long long n, uint64_t seed, float scale) {
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x)
+    dst[e] = synth_value(seed, (uint64_t)e, scale);
 }
 
 __global__ void k_copy_f32(const float* __restrict__ src, float* __restrict__ dst, int n) {
@@ -784,6 +808,10 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
       ro.slot_of = c->bslot;
       ro.guard = c->guard;
       if ((rc = ck(bgemv::route(ro, st, pdl), "route")) != HY_OK) return rc;
+      // rows the union kernels spread over the SMs: the expected union of B
+      // tokens' top-K picks under uniform routing, plus the shared expert
+      const double pk = 1.0 - std::pow(1.0 - (double)K / E, (double)B);
+      const int u_exp = std::min(std::min(E, B * K), (int)std::ceil(E * pk)) + 1;
       const long long ew = fmt ? (long long)Fe * H / 2 : (long long)Fe * H * 2;  // bytes of one expert matrix
       const long long es = fmt ? (long long)Fe * H / 16 : 0;                     // bytes of its scales
       {  // gate/up + SwiGLU over the union of selected experts and the shared expert
@@ -810,7 +838,8 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
         p.norm_g = L.norm2;
         p.y = c->bh;
         p.ldy = c->bh_len;
-        const bgemv::Plan pl = bgemv::plan(p.R, p.C, p.fmt, p.epi, m->nsm);
+        p.n_exp = E;
+        const bgemv::Plan pl = bgemv::plan(u_exp * Fe, p.C, p.fmt, p.epi, m->nsm, Fe);
         if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no batched plan for the expert gate/up (%d x %d)", Fe, H);
         if ((rc = ck(bgemv::launch(p, pl, st, pdl), "expert gate/up")) != HY_OK) return rc;
       }
@@ -832,8 +861,9 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
         p.x = c->bh;
         p.ldx = c->bh_len;
         p.part_out = c->bpart;
-        const bgemv::Plan pl = bgemv::plan(p.R, p.C, p.fmt, p.epi, m->nsm);
-        if (!pl.ok || H % bgemv::kTileRows) return fail(HY_ERR_UNSUPPORTED, "no batched plan for the expert down");
+        p.n_exp = E;
+        const bgemv::Plan pl = bgemv::plan(u_exp * H, p.C, p.fmt, p.epi, m->nsm, H);
+        if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no batched plan for the expert down");
         if ((rc = ck(bgemv::launch(p, pl, st, pdl), "expert down")) != HY_OK) return rc;
       }
       if ((rc = ck(bgemv::moe_reduce(c->bx, H, c->bpart, c->bw, H, B, K, st, pdl), "expert sum")) != HY_OK) return rc;
@@ -1225,6 +1255,31 @@ int hy_seq_reset(hy_cache* c, int32_t seq, void* stream) {
 int32_t hy_seq_len(const hy_cache* c, int32_t seq) { return valid_seq(c, seq) ? c->len[seq] : -1; }
 int32_t hy_seq_capacity(const hy_cache* c, int32_t seq) { return valid_seq(c, seq) ? c->cap[seq] : -1; }
 int32_t hy_step_kernels(const hy_cache* c) { return c ? c->last_kernels : 0; }
+
+int hy_seq_fill_synthetic(hy_cache* c, int32_t seq, int32_t len, uint64_t seed, void* stream) {
+  if (!valid_seq(c, seq) || len < 0) return fail(HY_ERR_ARG, "bad argument");
+  if (len > c->cap[seq]) return fail(HY_ERR_CAPACITY, "sequence %d: length %d exceeds capacity %d", seq, len, c->cap[seq]);
+  const hy_model* m = c->m;
+  const hy_config& cf = m->cfg;
+  cudaStream_t st = (cudaStream_t)stream;
+  for (int a = 0; a < m->n_attn; ++a)
+    for (int w = 0; w < 2; ++w)
+      for (int g = 0; g < cf.attn_kv_heads && len > 0; ++g) {
+        uint16_t* base = kv_cache(c, seq, a, w) + (size_t)g * c->cap[seq] * cf.head_dim;
+        k_fill_bf16<<<1024, 256, 0, st>>>(base, len, cf.head_dim, cf.head_dim,
+                                          seed * 1000003ull + (uint64_t)((a * 2 + w) * 64 + g));
+      }
+  if (m->n_gdn) {
+    const long long n = (long long)m->n_gdn * cf.gdn_heads * cf.gdn_dv * cf.gdn_dk;
+    k_fill_f32<<<1024, 256, 0, st>>>(gdn_state(c, seq, 0), n, seed * 1000003ull + 977ull, 0.01f);
+    HY_CK(cudaMemsetAsync(conv_state(c, seq, 0), 0, sizeof(float) * (size_t)m->n_gdn * cf.conv_k * m->CC, st));
+  }
+  HY_CK(cudaGetLastError());
+  HY_CK(cudaMemcpyAsync(c->d_len + seq, &len, sizeof(int), cudaMemcpyHostToDevice, st));
+  HY_CK(cudaStreamSynchronize(st));  // &len is a host stack value
+  c->len[seq] = len;
+  return HY_OK;
+}
 
 int hy_prefill(hy_model* m, hy_cache* c, int32_t seq, const int32_t* tokens_dev, int32_t n, float* logits_dev,
                void* stream) {

@@ -220,15 +220,20 @@ struct Params {
   unsigned* counter;        // argmax ticket (zero between launches)
   int* ids_out;             // [B]
   int* len_inc[kMaxB];      // per token, incremented after the argmax (nullable)
-  int ncta, nstages, rows_cta_max;
+  int n_exp;                // union sources: routed experts in the expert tensors
+  int ncta, nstages;        // from the plan
+  int gw, ks;               // row groups of 16 x strip lanes of the 8 compute warps (gw * ks = 8)
   unsigned* guard;
 };
 struct Plan {
-  int ncta, nstages, rows_cta_max, smem;
+  int ncta, nstages, smem, gw, ks;
   bool ok;
 };
-// R: rows (for kSrcUnionRows the most rows a step can have).
-Plan plan(int R, int C, int fmt, int epi, int nsm);
+// R: rows to spread over the SMs (for a union source, the rows of the
+// expected union); row_mult: a multiple of the row block that blocks must
+// divide (the rows of one expert of a union source), 0 for a dense matrix.
+// C must be a multiple of 256 (4-bit) or 64 (bf16).
+Plan plan(int R, int C, int fmt, int epi, int nsm, int row_mult = 0);
 cudaError_t init();
 cudaError_t launch(const Params& p, const Plan& pl, cudaStream_t st, bool pdl);
 

@@ -114,6 +114,19 @@ class HybridModel:
                                              None if logits_host is None else logits_host.data_ptr(),
                                              ids_host.data_ptr(), _stream(stream)), "hy_decode_step_host")
 
+    def decode_batch_host(self, seqs, tokens_host, ids_host, logits_host=None, stream=None) -> None:
+        """decode_batch with CPU tensors (int32 [len(seqs)]; logits FP32 [len(seqs)][V])."""
+        arr = (ctypes.c_int32 * len(seqs))(*[int(s) for s in seqs])
+        check(capi.lib().hy_decode_step_host(self.m, self.c, arr, len(seqs), tokens_host.data_ptr(),
+                                             None if logits_host is None else logits_host.data_ptr(),
+                                             ids_host.data_ptr(), _stream(stream)), "hy_decode_step_host")
+
+    def fill_synthetic(self, seq: int, length: int, seed: int = 0, stream=None) -> None:
+        """Give sequence `seq` `length` positions of seeded synthetic cache
+        contents (KV rows and recurrent state) without running a prompt."""
+        check(capi.lib().hy_seq_fill_synthetic(self.c, seq, int(length), int(seed), _stream(stream)),
+              "hy_seq_fill_synthetic")
+
     def seq_len(self, seq: int) -> int:
         return int(capi.lib().hy_seq_len(self.c, seq))
 

@@ -15,6 +15,7 @@ independent replica (the decode step has no cross-GPU exchange).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import dataclasses
 import json
 import math
@@ -32,6 +33,8 @@ METRIC = "batch-1 decode tokens/s; achieved HBM GB/s as fraction of GB300 peak"
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REFERENCE_BUDGET_S = 120.0
+SYNTHETIC_FILL_ABOVE = 8192  # longer prompts: seeded synthetic cache fill instead of a token-by-token prefill
 REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
 
@@ -179,17 +182,21 @@ def run_reference(args):
 
     from oracle import oracle as orc
     o_warm = max(args.warmup, 0)
-    # warm-up tokens are part of the same sampler run; time K tokens
-    tps, cores, n, dt = oracle_decode_sample(shape, prompt, budget_s=1e9, max_tokens=o_warm + args.steps,
-                                             host_w=host_w)
+    # warm-up tokens are part of the same sampler run; up to W + K tokens,
+    # bounded to about two minutes of CPU work
+    if w.batch > 1:  # the oracle runs one sequence at a time: sample one at the batch's mean context
+        ctx = [int(c) for c in workloads.ragged_contexts(w)]
+        prompt = int(round(sum(ctx) / len(ctx)))
+    tps, cores, n, dt = oracle_decode_sample(shape, prompt, budget_s=REFERENCE_BUDGET_S,
+                                             max_tokens=o_warm + args.steps, host_w=host_w)
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1000.0 / tps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "context": prompt, "batch": 1},
+        "config": {"workload": w.name, "context": prompt, "batch": w.batch},
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{n} full-depth FP64 oracle decode tokens at context {prompt} from a seeded "
-                                   f"synthetic cache (prompt not replayed on the CPU)"},
+                         "sample": f"{n} full-depth FP64 oracle decode tokens ({dt:.1f} s) at context {prompt} from a "
+                                   f"seeded synthetic cache (prompt not replayed on the CPU)"},
         "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     del orc
@@ -221,6 +228,8 @@ def run_ours(args):
         dist.barrier()
 
     w, shape, prompt = workload_of(args)
+    if w.batch > 1:
+        return run_ours_batch(args, w, shape, dist, ws, rank, local)
     peak, peak_kind = load_peaks()
     dev = torch.device("cuda", torch.cuda.current_device())
     st = torch.cuda.current_stream()
@@ -232,7 +241,11 @@ def run_ours(args):
     model = HybridModel(shape, weights, [cap], splits=args.splits, flags=flags)
     toks = torch.from_numpy(workloads.prompt_ids(w, n=prompt)).to(dev) if prompt else None
     ids = torch.zeros(1, dtype=torch.int32, device=dev)
-    if prompt:
+    synthetic_fill = prompt > SYNTHETIC_FILL_ABOVE
+    if synthetic_fill:  # a step's cost depends on the context length, not on what the cache holds
+        model.fill_synthetic(0, prompt, seed=1)
+        ids.copy_(toks[-1:])
+    elif prompt:
         model.prefill(0, toks)
         ids.copy_(toks[-1:])
     for _ in range(args.warmup):
@@ -311,6 +324,19 @@ def run_ours(args):
                 "launches_timed": reps * shape.n_layers, "peak_source": f"{peak_kind} hbm_gbs"}
         del graph
 
+    # ---- split-KV sweep (workloads that name split counts): same timed region per count
+    sweep = None
+    if w.splits and not args.splits and args.layers == 0:
+        sweep = {}
+        for sp in w.splits:
+            m2 = HybridModel(shape, weights, [cap], splits=sp, flags=flags)
+            m2.fill_synthetic(0, ctx0, seed=1)
+            ids2 = ids.clone()
+            t2, _ = timed_region(args, dist, local, st, lambda: m2.decode_step(0, ids2, ids2))
+            assert m2.check_device() == 0
+            sweep[str(sp)] = max(ws, 1) * args.steps / t2
+            m2.close()
+
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
     tok_h = torch.zeros(1, dtype=torch.int32).pin_memory()
     ids_h = torch.zeros(1, dtype=torch.int32).pin_memory()
@@ -341,17 +367,188 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "shape": shape.name, "batch": 1, "prompt": prompt,
                        "context_timed": [ctx0, ctx0 + args.steps], "weights": "bf16", "kv": "bf16",
+                       "context_fill": "seeded synthetic KV rows and recurrent state (no prompt replay)"
+                       if synthetic_fill else "prefill of the prompt",
                        "splits": model_splits(args, shape), "parallelism": f"replicas x{n}",
                        "l2": "inputs larger than L2: every step streams all weights (GBs) through the 129 MB L2"},
             "roofline": roof,
             "step_roofline": {"bound": "hbm", "bytes_per_step": sb.total, "achieved": step_gbs, "peak": peak,
                               "unit": "GB/s", "frac": step_gbs / peak},
+            "split_sweep_tokens_per_s": sweep,
             "cpu_baseline": cpu,
             "e2e": {"value": n * e2e_steps / e2e_t, "unit": "tokens/s", "h2d_bytes_per_step": 4,
                     "d2h_bytes_per_step": 4},
             "gpu_launches": model.step_kernels() * args.steps,
             "kernels_per_step": model.step_kernels(),
             "graph_launches_per_token": 1,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    model.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def timed_region(args, dist, local, st, step):
+    """W warm-up steps, then K timed steps between barriers and device
+    synchronisations, with the clocks sampled meanwhile; returns (seconds,
+    max over ranks; clock record)."""
+    import torch
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0.record(st)
+    for _ in range(args.steps):
+        step()
+    ev1.record(st)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    t = ev0.elapsed_time(ev1) / 1e3
+    if dist:
+        tt = torch.tensor([t], dtype=torch.float64, device=torch.device("cuda", local))
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    return t, clk
+
+
+def gemv_batch_roofline(shape, weights, B, peak, peak_kind, workload):
+    """The batched tensor-core GEMV (k_bgemv) timed alone: one graph launches
+    it once per layer over that layer's input projection (every launch
+    streams a fresh matrix from HBM), B token vectors each, RMSNorm fused;
+    average launch duration = graph time / launches."""
+    import torch
+
+    from bandwidth_bound_hybrid_gb300 import accounting as acc
+    from bandwidth_bound_hybrid_gb300 import capi
+    from bandwidth_bound_hybrid_gb300.model import _tensor
+    L = capi.lib()
+    fmt = getattr(shape, "weight_format", 0)
+    H = shape.hidden
+    x = torch.randn((B, H), device="cuda")
+    g = torch.ones(H, device="cuda")
+    rows = [shape.attn_in_rows if shape.is_attn(l) else shape.gdn_in_rows for l in range(shape.n_layers)]
+    y = torch.empty((B, max(rows)), device="cuda")
+    tens = [_tensor(weights[f"l{l}.w_in"]) for l in range(shape.n_layers)]
+    side = torch.cuda.Stream()
+
+    def sweep(stream):
+        for l in range(shape.n_layers):
+            capi.check(L.hy_op_gemv_batch(ctypes.byref(tens[l]), None, fmt, rows[l], H, B, x.data_ptr(), H,
+                                          g.data_ptr(), 1e-6, y.data_ptr(), max(rows), 0, stream.cuda_stream),
+                       "gemv_batch")
+
+    with torch.cuda.stream(side):
+        sweep(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        sweep(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = 5
+    st = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(reps):
+        graph.replay()
+    b.record(st)
+    torch.cuda.synchronize()
+    launch_s = a.elapsed_time(b) / 1e3 / (reps * shape.n_layers)
+    bytes_launch = sum(acc.gemv_batch_bytes(r, H, B, fmt) for r in rows) / len(rows)
+    achieved = bytes_launch / launch_s / 1e9
+    del graph
+    return {"bound": "hbm", "kernel": f"batched tensor-core GEMV (k_bgemv<{fmt}>), input projections, batch {B}",
+            "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": load_traffic("gemv_batch", workload), "bytes_per_launch": bytes_launch,
+            "launch_us_mean": launch_s * 1e6, "launches_timed": reps * shape.n_layers,
+            "peak_source": f"{peak_kind} hbm_gbs"}
+
+
+def run_ours_batch(args, w, shape, dist, ws, rank, local):
+    """Batch decode: len(contexts) sequences with ragged cached contexts (a
+    seeded synthetic cache fill: a step's cost depends on the lengths, not on
+    the contents), one step = one token for every sequence."""
+    import torch
+
+    from bandwidth_bound_hybrid_gb300 import accounting as acc
+    from bandwidth_bound_hybrid_gb300 import capi
+    from bandwidth_bound_hybrid_gb300.model import HybridModel
+    from synth import workloads
+    peak, peak_kind = load_peaks()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = torch.cuda.current_stream()
+    ctx = [int(c) for c in workloads.ragged_contexts(w)]
+    B = len(ctx)
+    weights = workloads.device_weights(shape)
+    caps = [c + args.warmup + 2 * args.steps + 16 for c in ctx]
+    flags = capi.HY_FLAG_NO_PDL if args.no_pdl else 0
+    model = HybridModel(shape, weights, caps, splits=args.splits, flags=flags)
+    for s, c in enumerate(ctx):
+        model.fill_synthetic(s, c, seed=s + 1)
+    seqs = list(range(B))
+    ids = torch.from_numpy(workloads.host.uniform_ids(w.prompt_seed, workloads.PROMPT_TID, B, shape.vocab)).to(dev)
+    t, clk = timed_region(args, dist, local, st, lambda: model.decode_batch(seqs, ids, ids))
+    assert model.check_device() == 0, "device guard fired"
+    n = max(ws, 1)
+    value = n * B * args.steps / t
+    mid = [c + args.warmup + args.steps // 2 for c in ctx]
+    sb = acc.batch_step_bytes(shape, mid)
+    step_gbs = sb.total * args.steps / t / 1e9
+
+    roof = None if args.no_kernel_timing else gemv_batch_roofline(shape, weights, B, peak, peak_kind, args.workload)
+
+    tok_h = torch.zeros(B, dtype=torch.int32).pin_memory()
+    ids_h = torch.zeros(B, dtype=torch.int32).pin_memory()
+    tok_h.copy_(ids.cpu())
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        model.decode_batch_host(seqs, tok_h, ids_h)
+        tok_h.copy_(ids_h)
+    e2e_t = time.perf_counter() - t0
+    if dist:
+        tt = torch.tensor([e2e_t], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_t = float(tt.item())
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        c0 = int(round(sum(mid) / B))
+        tps, cores, ntok, dt = oracle_decode_sample(shape, c0, budget_s=12.0, max_tokens=16)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{ntok} full-depth FP64 oracle decode tokens of one sequence at the batch's mean context "
+                         f"{c0} from a seeded synthetic cache ({dt:.1f} s; the oracle runs sequences one at a time)"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "shape": shape.name, "batch": B, "contexts": ctx,
+                       "context_fill": "seeded synthetic KV rows and recurrent state (no prompt replay)",
+                       "weights": "4-bit blocks of 32 + fp16 scale" if getattr(shape, "weight_format", 0) else "bf16",
+                       "kv": "bf16", "parallelism": f"replicas x{n}",
+                       "l2": "inputs larger than L2: every step streams GBs of weights and KV through the 129 MB L2"},
+            "roofline": roof,
+            "step_roofline": {"bound": "hbm", "bytes_per_step": sb.total, "achieved": step_gbs, "peak": peak,
+                              "unit": "GB/s", "frac": step_gbs / peak,
+                              "experts_per_layer": acc.expected_union(shape.n_experts, shape.top_k, B)
+                              if shape.ffn == 0 else None},
+            "cpu_baseline": cpu,
+            "e2e": {"value": n * B * args.steps / e2e_t, "unit": "tokens/s", "h2d_bytes_per_step": 4 * B,
+                    "d2h_bytes_per_step": 4 * B},
+            "gpu_launches": model.step_kernels() * args.steps,
+            "kernels_per_step": model.step_kernels(),
+            "graph_launches_per_token": 1.0 / B,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)

@@ -157,6 +157,16 @@ int hy_seq_reset(hy_cache* c, int32_t seq, void* stream);
 int32_t hy_seq_len(const hy_cache* c, int32_t seq);
 int32_t hy_seq_capacity(const hy_cache* c, int32_t seq);
 
+/* Give sequence `seq` `len` positions of synthetic cache contents (KV rows
+ * [0, len) of every attention layer filled with seeded bf16 values in
+ * [-1, 1), the DeltaNet states with seeded values in [-0.01, 0.01), the conv
+ * rings zeroed), as if a prompt of that length had been run.  A decode step's
+ * cost depends on the lengths only, so benchmarks of long or ragged contexts
+ * use this instead of a token-by-token prefill; outputs after it are not
+ * those of any prompt.  HY_ERR_CAPACITY if len exceeds the capacity.
+ * Stream-ordered. */
+int hy_seq_fill_synthetic(hy_cache* c, int32_t seq, int32_t len, uint64_t seed, void* stream);
+
 /* Kernels the last recorded decode step launches: 1 when the whole step runs
  * as one persistent kernel (HY_FLAG_PERSISTENT), else one per operation.  0
  * before any step. */

@@ -127,3 +127,33 @@ def test_batch_rejects_repeated_and_full_sequences(built):
     model.decode_batch([0], toks[:1], ids)
     assert model.seq_len(0) == 1 and model.check_device() == 0
     model.close()
+
+
+def test_synthetic_fill(built):
+    """hy_seq_fill_synthetic: the same seed gives the same cache (identical
+    outputs for two sequences), another seed another cache; the length is set
+    and bounded by the capacity."""
+    import torch
+
+    from bandwidth_bound_hybrid_gb300.model import HybridModel
+    shape = TINY_MOE_Q4
+    model = HybridModel(shape, workloads.device_weights(shape), [40, 40, 40], flags=0)
+    model.fill_synthetic(0, 30, seed=5)
+    model.fill_synthetic(1, 30, seed=5)
+    model.fill_synthetic(2, 30, seed=6)
+    assert [model.seq_len(s) for s in range(3)] == [30, 30, 30]
+    toks = torch.tensor([7, 7, 7], dtype=torch.int32, device="cuda")
+    ids = torch.empty(3, dtype=torch.int32, device="cuda")
+    lg = torch.empty((3, shape.vocab), dtype=torch.float32, device="cuda")
+    model.decode_batch([0, 1, 2], toks, ids, lg)
+    torch.cuda.synchronize()
+    got = to_np(lg)
+    assert np.all(np.isfinite(got))
+    np.testing.assert_array_equal(got[0], got[1])
+    assert np.abs(got[0] - got[2]).max() > 0
+    with pytest.raises(capi.HybridError) as ei:
+        model.fill_synthetic(0, 41)
+    assert ei.value.code == capi.HY_ERR_CAPACITY and model.seq_len(0) == 31
+    model.fill_synthetic(0, 0)
+    assert model.seq_len(0) == 0 and model.check_device() == 0
+    model.close()
