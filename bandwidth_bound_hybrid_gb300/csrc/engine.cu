@@ -477,6 +477,7 @@ bool build_program(hy_cache* c, const std::vector<StepOp>& ops, std::vector<step
   const int pf = env_kb("HY_STEP_PREFETCH_KB", 128);
   size_t region = 0, scratch = 1;
   int stage = 0;
+  int routed_after = 0;  // phases up to the last router: the routed experts' rows depend on them
   phases.assign(ops.size(), step::Phase());
   for (size_t i = 0; i < ops.size(); ++i) {
     const StepOp& o = ops[i];
@@ -492,7 +493,8 @@ bool build_program(hy_cache* c, const std::vector<StepOp>& ops, std::vector<step
       ph.epi = o.epi;
       ph.vpl = pl.vpl;
       ph.full = 1;
-      ph.pf_bytes = o.src == gemv::kSrcDense ? pf : 0;
+      if (o.epi == gemv::kEpiRouter) routed_after = (int)i + 1;
+      if (o.src != gemv::kSrcDense) ph.after = routed_after;
       ph.g = o.g;
       ph.g.n_nx = 0;
       ph.g.ncta = pl.ncta;
@@ -515,7 +517,7 @@ bool build_program(hy_cache* c, const std::vector<StepOp>& ops, std::vector<step
       if (o.d.dk != 32 * pr.epl) return false;
       ph.kind = step::kGdn;
       ph.d = o.d;
-      ph.pf_bytes = 1;
+      ph.pf_bytes = pf;
       region = std::max(region, step::gdn_work_bytes(pr.epl));
     } else if (o.kind == StepOp::kAttn) {
       if (o.a.hd != pr.hd || o.a.nq / o.a.nkv != pr.G) return false;
@@ -1006,6 +1008,7 @@ int check_model_cfg(const hy_config* c) {
     if (c->n_experts <= 0 || c->top_k <= 0 || c->top_k > 16 || c->top_k > c->n_experts || c->expert_ffn <= 0 ||
         c->expert_ffn % 8)
       return fail(HY_ERR_ARG, "MoE shape");
+    if (c->n_experts > 511) return fail(HY_ERR_UNSUPPORTED, "MoE: at most 511 routed experts");
     if (c->shared_ffn != c->expert_ffn) return fail(HY_ERR_UNSUPPORTED, "MoE: shared_ffn must equal expert_ffn");
   } else if (c->ffn % 8) {
     return fail(HY_ERR_ARG, "ffn must be a multiple of 8");

@@ -352,6 +352,7 @@ __device__ __forceinline__ void epilogue(const Params& p, int epi, const float* 
       p.router_logits[r0 + i] = v;
     }
   }
+  if (epi == kEpiRouter) named_barrier(1, kCT);  // every thread's logits stored before the ticket's fence
   if (epi == kEpiArgmax) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -400,37 +401,59 @@ __device__ __forceinline__ void epilogue(const Params& p, int epi, const float* 
   // router: top-k over the E expert logits (FP32 compare, lowest index on
   // ties), softmax over the selected logits, sigmoid gate of the shared
   // expert's row ("Fourteen hours to 100 tokens per second", "The router with
-  // 257 rows").  The logits go to shared scratch in one pass; then every
-  // expert's rank (the number of logits above it, or equal with a lower
-  // index) is counted in parallel, and the experts of rank < top_k are the
-  // selection in order: the same set and order as top_k successive argmaxes.
+  // 257 rows").  This is the step's critical path (every other CTA waits for
+  // it), so one warp does it: each lane holds E/32 logits and top_k rounds of
+  // a warp-wide argmax (largest logit, lowest index on ties) pick the
+  // selection in order.
   const int E = p.n_experts;
   for (int e = ctid; e <= E; e += kCT) scratch[e] = __ldcg(p.router_logits + e);
   named_barrier(1, kCT);
-  for (int e = ctid; e < E; e += kCT) {
-    const float v = scratch[e];
-    int rank = 0;
-    for (int f = 0; f < E; ++f) {
-      const float w = scratch[f];
-      rank += (w > v || (w == v && f < e)) ? 1 : 0;
+  if (warp == 0) {
+    constexpr int kPer = kMaxExperts / 32;
+    float v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      const float x = e < E ? scratch[e] : -INFINITY;
+      v[i] = x == x ? x : -INFINITY;  // a NaN logit ranks last
     }
-    if (rank < p.top_k) {
-      sh.sel[rank] = e;
-      sh.selv[rank] = v;
-    }
-  }
-  named_barrier(1, kCT);
-  if (ctid == 0) {
-    const float m = sh.selv[0];
-    float den = 0.f;
-    for (int q = 0; q < p.top_k; ++q) den += __expf(sh.selv[q] - m);
+    uint32_t taken = 0u;
     for (int q = 0; q < p.top_k; ++q) {
-      p.out_ids[q] = sh.sel[q];
-      p.out_w[q] = __expf(sh.selv[q] - m) / den;
-      if (p.dbg_ids) p.dbg_ids[q] = sh.sel[q];
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !(taken >> i & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        argmax_merge(bv, bi, ov, oi);
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == 0) {
+        sh.sel[q] = bi;
+        sh.selv[q] = bv;
+      }
     }
-    p.out_w[p.top_k] = sigmoidf_(scratch[E]);
-    *p.counter = 0u;
+    __syncwarp();
+    if (lane == 0) {
+      const float m = sh.selv[0];
+      float den = 0.f;
+      for (int q = 0; q < p.top_k; ++q) den += __expf(sh.selv[q] - m);
+      for (int q = 0; q < p.top_k; ++q) {
+        p.out_ids[q] = sh.sel[q];
+        p.out_w[q] = __expf(sh.selv[q] - m) / den;
+        if (p.dbg_ids) p.dbg_ids[q] = sh.sel[q];
+      }
+      p.out_w[p.top_k] = sigmoidf_(scratch[E]);
+      *p.counter = 0u;
+    }
   }
   if (p.dbg_logits)
     for (int e = ctid; e <= E; e += kCT) p.dbg_logits[e] = scratch[e];

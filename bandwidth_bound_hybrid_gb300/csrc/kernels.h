@@ -43,6 +43,7 @@ constexpr int kMaxSmem = 220 * 1024;        // dynamic; leaves room for static s
 constexpr int kCtasPerSm = 1;
 constexpr int kPreStages = 0;               // tiles issued before the input vector is requested
 constexpr int kMaxTopK = 16;
+constexpr int kMaxExperts = 512;  // routed experts a router can select from
 
 // Rows of a matrix that CTA b of an ncta-CTA GEMV owns, prefetched into L2 by
 // CTA b of the kernel before it: [b*rows/ncta, (b+1)*rows/ncta), at most
@@ -267,8 +268,9 @@ enum Kind : int { kGemv = 0, kGdn = 1, kAttn = 2, kCopy = 3 };
 struct alignas(16) Phase {
   int kind;
   int src, in, epi, vpl, full;  // GEMV launch variant (full: every lane's vectors inside its chunk)
-  int pf_bytes;                 // L2 prefetch of this phase's first bytes per CTA, issued during the previous phase
-  int pad_;
+  int pf_bytes;                 // DeltaNet: L2 prefetch of the state rows, issued while earlier phases run
+  int after;                    // the copy lane issues this phase's tiles once this many phases are
+                                // complete grid-wide (0: as soon as ring slots free up)
   gemv::Params g;  // plan fields filled for ncta = the grid (CTAs past g.ncta idle in this phase)
   gdn::Params d;
   attn::Params a;

@@ -3,14 +3,15 @@
 // One CTA per SM runs the step's kernels (GEMVs, Gated DeltaNet step, split-KV
 // attention; the same device code as their standalone kernels) as phases of a
 // program held in device memory.  Phases are separated by a grid barrier: a
-// CTA's compute warps arrive once they have finished a phase, and the copy
-// lane waits until every CTA has arrived before it requests the next phase's
-// input vector and weight tiles.  What a phase reads first is prefetched into
-// L2 while the previous phase is still running, so HBM stays busy across the
-// barrier and no kernel launch, CTA start or grid drain separates the phases
-// ("Beating llama.cpp from Scratch on Consumer AMD", Act 1: the decode step
-// is a chain of small dependent kernels whose launch and drain costs add up;
-// here the chain is one launch).
+// CTA's compute warps arrive once they have finished a phase and wait until
+// every CTA has arrived before they load the next phase's input.  The copy
+// lane does not wait: weight and KV-cache tiles do not depend on the
+// activations, so it keeps streaming the next phases' tiles into the ring as
+// slots free up, and only the routed experts' tiles wait for the phase that
+// picked them.  HBM stays busy across the barriers and no kernel launch, CTA
+// start or grid drain separates the phases ("Beating llama.cpp from Scratch
+// on Consumer AMD", Act 1: the decode step is a chain of small dependent
+// kernels whose launch and drain costs add up; here the chain is one launch).
 #include "attn_dev.cuh"
 #include "common.cuh"
 #include "gdn_dev.cuh"
@@ -48,8 +49,6 @@ __device__ __forceinline__ bool bar_wait(const unsigned* bar, unsigned target) {
     }
   }
 }
-// Writes made visible by the barrier are then read by the TMA engine.
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 struct Ring {
   uint8_t* base;
@@ -67,22 +66,11 @@ __device__ __forceinline__ void gemv_rows(const gemv::Params& p, int b, int& r0,
   r1 = (int)((long long)(b + 1) * p.R / p.ncta);
 }
 
-// L2 prefetch of what CTA b reads first in phase `ph`.
+// L2 prefetch of the DeltaNet state rows CTA b updates in phase `ph` (the
+// compute warps load them with plain loads).
 __device__ __forceinline__ void prefetch_phase(const Phase& ph, int b) {
   if (ph.pf_bytes <= 0) return;
-  if (ph.kind == kGemv && ph.src == gemv::kSrcDense) {
-    const gemv::Params& p = ph.g;
-    if (b >= p.ncta) return;
-    int r0, r1;
-    gemv_rows(p, b, r0, r1);
-    const long long rb = (long long)p.C * 2;
-    long long bytes = (long long)(r1 - r0) * rb;
-    if (bytes > ph.pf_bytes) bytes = ph.pf_bytes & ~15LL;
-    const int np = ph.epi == gemv::kEpiSwiglu ? 2 : 1;
-    for (int j = 0; j < np; ++j)
-      for (long long o = 0; o < bytes; o += 65536)
-        bulk_prefetch_l2(p.W[j] + r0 * rb + o, (uint32_t)(bytes - o < 65536 ? bytes - o : 65536));
-  } else if (ph.kind == kGdn) {
+  if (ph.kind == kGdn) {
     const gdn::Params& d = ph.d;
     const int nrc = (d.dv + gdn::kRowsPerCta - 1) / gdn::kRowsPerCta;
     if (b >= d.nh * nrc) return;
@@ -93,6 +81,38 @@ __device__ __forceinline__ void prefetch_phase(const Phase& ph, int b) {
 }
 
 // ------------------------------------------------------------ compute work
+
+// A phase descriptor into shared memory (all compute threads).
+__device__ __forceinline__ void load_phase(const Program& pr, int i, Phase* dst, int ctid) {
+  const uint4* src = reinterpret_cast<const uint4*>(pr.phases + i);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  for (int k = ctid; k < (int)(sizeof(Phase) / 16); k += kCT) d[k] = __ldg(src + k);
+}
+
+// A GEMV phase's input vector (FP32, or the bf16 embedding row), the MoE
+// routing weights and the RMSNorm gain into shared memory, with plain loads
+// (not bulk copies, which would queue behind the tiles the copy lane already
+// requested); what earlier phases wrote is read past L1.
+__device__ __forceinline__ void load_input(const gemv::Params& p, int in, float* xs, float* gs, float* mw, int ctid) {
+  if (in == gemv::kInEmbed) {
+    int tok = __ldcg(p.tok);
+    if (tok < 0 || tok >= p.vocab) {  // never read outside the embedding table
+      if (ctid == 0) set_guard(p.guard, kGuardBadIndex);
+      tok = 0;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(p.embed + (long long)tok * p.C);
+    for (int v = ctid; v < p.C / 8; v += kCT) reinterpret_cast<uint4*>(xs)[v] = __ldg(src + v);
+  } else {
+    const float4* src = reinterpret_cast<const float4*>(p.x);
+    for (int v = ctid; v < p.C / 4; v += kCT) reinterpret_cast<float4*>(xs)[v] = __ldcg(src + v);
+    if (in == gemv::kInMoeZ)
+      for (int k = ctid; k <= p.top_k; k += kCT) mw[k] = __ldcg(p.moe_w + k);
+  }
+  if (p.norm_g)
+    for (int v = ctid; v < p.C / 4; v += kCT)
+      reinterpret_cast<float4*>(gs)[v] = __ldg(reinterpret_cast<const float4*>(p.norm_g) + v);
+  named_barrier(1, kCT);
+}
 
 // A wait that gives up sets *abort (shared); the CTA then skips the rest of
 // the step but still passes every block barrier and grid arrival, so nothing
@@ -129,6 +149,7 @@ __device__ __forceinline__ void gemv_phase(const Phase& ph, const Ring& rg, uint
   float* xs = reinterpret_cast<float*>(region);
   float* gs = xs + p.xs_floats;
   float* red = gs + p.gs_floats;
+  load_input(p, ph.in, xs, gs, esh.mw, ctid);
   const float sc = gemv::input_scale(p, ph.in, xs, esh.mw, esh.red, ctid);
   gemv::LaneSlice<VPL> L;
   gemv::lane_setup<VPL>(p, ph.src, ph.in, xs, gs, esh.mw, sc, L, warp, lane);
@@ -144,17 +165,21 @@ __device__ __forceinline__ void gemv_phase(const Phase& ph, const Ring& rg, uint
   if (!named_barrier_or(1, kCT, *abort != 0)) gemv::epilogue(p, ph.epi, red, r0, r1 - r0, esh, scratch, ctid);
 }
 
+// A DeltaNet phase: items blockIdx.x, + gridDim.x, ...  The first item's
+// state rows and conv taps (R, V) were loaded before the grid barrier: no
+// earlier phase of the step writes them.
 template <int EPL>
-__device__ __forceinline__ void gdn_phase(const Phase& ph, uint8_t* region, int ctid) {
+__device__ __forceinline__ void gdn_phase(const Phase& ph, uint8_t* region, int ctid, gdn::Rows<EPL, kGdnWarps>& R,
+                                          gdn::ConvRegs<EPL, kGdnWarps>& V) {
   const gdn::Params& d = ph.d;
   const int nrc = (d.dv + gdn::kRowsPerCta - 1) / gdn::kRowsPerCta;
   auto& sh = *reinterpret_cast<gdn::ItemShared<EPL>*>(region);
   for (int b = blockIdx.x; b < d.nh * nrc; b += gridDim.x) {
     const int h = b % d.nh, rc = b / d.nh;
-    gdn::Rows<EPL, kGdnWarps> R;
-    gdn::ConvRegs<EPL, kGdnWarps> V;
-    gdn::load_rows<EPL, kGdnWarps>(d, h, rc, R, ctid);
-    gdn::load_conv<EPL, kGdnWarps>(d, h, rc, V, ctid);
+    if (b != (int)blockIdx.x) {
+      gdn::load_rows<EPL, kGdnWarps>(d, h, rc, R, ctid);
+      gdn::load_conv<EPL, kGdnWarps>(d, h, rc, V, ctid);
+    }
     gdn::run_item<EPL, kGdnWarps>(d, h, rc, R, V, sh, ctid, [] __device__() { named_barrier(1, kGdnWarps * 32); });
   }
 }
@@ -217,8 +242,6 @@ __global__ void __maxnreg__(128) k_step(const Program pr) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(pbuf + 2);
   rg.full = bars;
   rg.empty = bars + kMaxStagesStep;
-  uint64_t* xbar = bars + 2 * kMaxStagesStep;  // phase start: input landed / work released
-  uint64_t* pbar = xbar + 1;                   // phase descriptor landed
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned nctas = gridDim.x;
 
@@ -227,8 +250,6 @@ __global__ void __maxnreg__(128) k_step(const Program pr) {
       mbar_init(&rg.full[s], 1);
       mbar_init(&rg.empty[s], kNW);
     }
-    mbar_init(xbar, 1);
-    mbar_init(pbar, 1);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -238,41 +259,23 @@ __global__ void __maxnreg__(128) k_step(const Program pr) {
   if (warp == kNW) {
     if (lane != 0) return;
     const uint64_t pol = l2_evict_first_policy();
-    const uint64_t keep = l2_evict_last_policy();
-    mbar_arrive_expect_tx(pbar, sizeof(Phase));
-    bulk_g2s(&pbuf[0], &pr.phases[0], sizeof(Phase), pbar, keep);
     uint32_t t = 0;
     bool ok = true;
-    for (int ph_i = 0; ph_i < pr.nphases; ++ph_i) {
-      if (ph_i > 0 && ok && !s_abort) {
-        if (!bar_wait(pr.bar, (unsigned)ph_i * nctas)) {
+    for (int ph_i = 0; ph_i < pr.nphases && ok; ++ph_i) {
+      // read from global memory: this lane runs ahead of the compute warps'
+      // descriptor copies
+      const Phase& ph = pr.phases[ph_i];
+      if (ph.after > 0) {  // tiles whose addresses an earlier phase decides
+        if (!bar_wait(pr.bar, (unsigned)ph.after * nctas)) {
           set_guard(pr.guard, kGuardWaitTimeout);
           ok = false;
+          s_abort = 1;
+          break;
         }
-        fence_proxy_async();
       }
-      if (ok && !mbar_wait(pbar, ph_i & 1)) {
-        set_guard(pr.guard, kGuardWaitTimeout);
-        ok = false;
-      }
-      if (s_abort) ok = false;
-      if (!ok) s_abort = 1;
-      const Phase& ph = pbuf[ph_i & 1];
-      if (ok && ph_i + 1 < pr.nphases) {
-        mbar_arrive_expect_tx(pbar, sizeof(Phase));
-        bulk_g2s(&pbuf[(ph_i + 1) & 1], &pr.phases[ph_i + 1], sizeof(Phase), pbar, keep);
-      }
-      if (!ok) {
-        mbar_arrive(xbar);  // compute warps see s_abort and skip the phase
-        continue;
-      }
+      if (s_abort) break;
       if (ph.kind == kGemv && (int)blockIdx.x < ph.g.ncta) {
         const gemv::Params& p = ph.g;
-        float* xs = reinterpret_cast<float*>(region);
-        float* gs = xs + p.xs_floats;
-        mbar_arrive_expect_tx(xbar, gemv::input_bytes(p, ph.in) + (p.norm_g ? p.C * 4 : 0));
-        if (p.norm_g) bulk_g2s(gs, p.norm_g, p.C * 4, xbar, keep);
-        gemv::issue_input(p, ph.in, xs, esh.mw, xbar, keep);
         const int npair = ph.epi == gemv::kEpiSwiglu ? 2 : 1;
         int r0, r1;
         gemv_rows(p, blockIdx.x, r0, r1);
@@ -290,7 +293,6 @@ __global__ void __maxnreg__(128) k_step(const Program pr) {
           ++t;
         }
       } else if (ph.kind == kAttn) {
-        mbar_arrive(xbar);
         const attn::Params& p = ph.a;
         const int T = *p.len;
         for (int b = blockIdx.x; b < p.nkv * p.nsplit && ok; b += gridDim.x) {
@@ -308,14 +310,8 @@ __global__ void __maxnreg__(128) k_step(const Program pr) {
             ++t;
           }
         }
-      } else {
-        mbar_arrive(xbar);  // DeltaNet phase, or a GEMV phase this CTA has no rows of
-      }
-      // what the next phase reads first goes to L2 during this one
-      if (ok && ph_i + 1 < pr.nphases && mbar_wait(pbar, (ph_i + 1) & 1)) {
-        prefetch_phase(pbuf[(ph_i + 1) & 1], blockIdx.x);
-        // leave the descriptor's phase to the top of the next iteration: re-arm
-        // nothing (mbar_wait on a completed phase returns at once)
+      } else if (ph.kind == kGdn) {
+        prefetch_phase(ph, blockIdx.x);
       }
     }
     // Drain: the CTA must not retire while copies it issued are in flight.
@@ -327,11 +323,31 @@ __global__ void __maxnreg__(128) k_step(const Program pr) {
   // ------------------------------------------------------------ compute warps
   const int ctid = threadIdx.x;
   uint32_t t = 0;
+  load_phase(pr, 0, &pbuf[0], ctid);
   for (int ph_i = 0; ph_i < pr.nphases; ++ph_i) {
-    const bool landed = mbar_wait(xbar, ph_i & 1);
-    if (!landed && ctid == 0) set_guard(pr.guard, kGuardWaitTimeout);
+    named_barrier(2, kCT);  // descriptor ph_i is in shared memory
+    gdn::Rows<EPL, kGdnWarps> R;
+    gdn::ConvRegs<EPL, kGdnWarps> V;
+    {
+      // work that no earlier phase feeds, done while the others finish
+      const Phase& ph = pbuf[ph_i & 1];
+      if (ph.kind == kGdn && warp < kGdnWarps) {
+        const gdn::Params& d = ph.d;
+        const int b = blockIdx.x, nrc = (d.dv + gdn::kRowsPerCta - 1) / gdn::kRowsPerCta;
+        if (b < d.nh * nrc && !s_abort) {
+          gdn::load_rows<EPL, kGdnWarps>(d, b % d.nh, b / d.nh, R, ctid);
+          gdn::load_conv<EPL, kGdnWarps>(d, b % d.nh, b / d.nh, V, ctid);
+        }
+      }
+    }
+    // the previous phase must be complete on every CTA
+    bool failed = false;
+    if (ph_i > 0 && ctid == 0 && !s_abort && !bar_wait(pr.bar, (unsigned)ph_i * nctas)) {
+      set_guard(pr.guard, kGuardWaitTimeout);
+      failed = true;
+    }
     // every compute thread takes the same skip decision
-    bool ok = !named_barrier_or(2, kCT, !landed || s_abort != 0);
+    bool ok = !named_barrier_or(2, kCT, failed || s_abort != 0);
     const Phase& ph = pbuf[ph_i & 1];
     if (ok) {
       if (ph.kind == kGemv) {
@@ -345,7 +361,7 @@ __global__ void __maxnreg__(128) k_step(const Program pr) {
           }
         }
       } else if (ph.kind == kGdn) {
-        if (warp < kGdnWarps) gdn_phase<EPL>(ph, region, ctid);
+        if (warp < kGdnWarps) gdn_phase<EPL>(ph, region, ctid, R, V);
       } else if (ph.kind == kCopy) {
         for (int i = blockIdx.x * kCT + ctid; i < ph.cn; i += gridDim.x * kCT) ph.cdst[i] = ph.csrc[i];
       } else {
@@ -364,6 +380,8 @@ __global__ void __maxnreg__(128) k_step(const Program pr) {
         if (old == (unsigned)pr.nphases * nctas - 1) atomicExch(pr.bar, 0u);
       }
     }
+    // the next descriptor goes where the previous phase's was
+    if (ph_i + 1 < pr.nphases) load_phase(pr, ph_i + 1, &pbuf[(ph_i + 1) & 1], ctid);
   }
 }
 
@@ -405,7 +423,7 @@ int attn_stage_bytes(int hd) {
 
 size_t smem_bytes(const Program& pr) {
   const size_t b = (size_t)pr.nstages * pr.stage_bytes + (((size_t)pr.region_bytes + 15) & ~(size_t)15) +
-                   (size_t)((pr.scratch_floats + 3) & ~3) * 4 + 2 * sizeof(Phase) + (2 * kMaxStagesStep + 2) * 8;
+                   (size_t)((pr.scratch_floats + 3) & ~3) * 4 + 2 * sizeof(Phase) + 2 * kMaxStagesStep * 8;
   return b <= (size_t)kMaxSmem ? b : 0;
 }
 

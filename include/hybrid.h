@@ -74,7 +74,7 @@ typedef struct {
   int32_t attn_kv_heads;   /* nkv (nq % nkv == 0, nq / nkv <= 8) */
   int32_t head_dim;        /* 64, 128 or 256 */
   uint64_t attn_layer_mask;/* bit l set: layer l is GQA attention, else Gated DeltaNet */
-  int32_t n_experts;       /* E (MoE) */
+  int32_t n_experts;       /* E (MoE), 1..511 (HY_ERR_UNSUPPORTED above) */
   int32_t top_k;           /* k (MoE, <= 16) */
   int32_t expert_ffn;      /* Fe (MoE) */
   int32_t shared_ffn;      /* Fs (MoE shared expert) */
