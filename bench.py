@@ -317,7 +317,7 @@ def run_ours(args):
         launch_s = a.elapsed_time(b) / 1e3 / (reps * shape.n_layers)
         bytes_launch = acc.gemv_swiglu_bytes(shape.ffn, shape.hidden)
         achieved = bytes_launch / launch_s / 1e9
-        roof = {"bound": "hbm", "kernel": "gemv gate/up + SwiGLU (k_gemv<5,0,0,2>)", "achieved": achieved,
+        roof = {"bound": "hbm", "kernel": "gemv gate/up + SwiGLU (k_gemv, dense rows, SwiGLU epilogue)", "achieved": achieved,
                 "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": load_traffic("gemv_swiglu", args.workload),
                 "bytes_per_launch": bytes_launch, "launch_us_mean": launch_s * 1e6,
@@ -336,6 +336,9 @@ def run_ours(args):
             assert m2.check_device() == 0
             sweep[str(sp)] = max(ws, 1) * args.steps / t2
             m2.close()
+
+    if not args.no_kernel_timing and shape.ffn == 0:
+        roof = gemv_in_roofline(shape, weights, peak, peak_kind, args.workload)
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
     tok_h = torch.zeros(1, dtype=torch.int32).pin_memory()
@@ -421,31 +424,28 @@ def timed_region(args, dist, local, st, step):
     return t, clk
 
 
-def gemv_batch_roofline(shape, weights, B, peak, peak_kind, workload):
-    """The batched tensor-core GEMV (k_bgemv) timed alone: one graph launches
-    it once per layer over that layer's input projection (every launch
-    streams a fresh matrix from HBM), B token vectors each, RMSNorm fused;
-    average launch duration = graph time / launches."""
+def gemv_in_roofline(shape, weights, peak, peak_kind, workload):
+    """The batch-1 GEMV (k_gemv) timed alone with RMSNorm fused: one graph
+    launches it once per layer over that layer's input projection (every
+    launch streams a fresh bf16 matrix from HBM); average launch duration =
+    graph time / launches."""
     import torch
 
     from bandwidth_bound_hybrid_gb300 import accounting as acc
     from bandwidth_bound_hybrid_gb300 import capi
-    from bandwidth_bound_hybrid_gb300.model import _tensor
     L = capi.lib()
-    fmt = getattr(shape, "weight_format", 0)
     H = shape.hidden
-    x = torch.randn((B, H), device="cuda")
+    x = torch.randn(H, device="cuda")
     g = torch.ones(H, device="cuda")
-    rows = [shape.attn_in_rows if shape.is_attn(l) else shape.gdn_in_rows for l in range(shape.n_layers)]
-    y = torch.empty((B, max(rows)), device="cuda")
-    tens = [_tensor(weights[f"l{l}.w_in"]) for l in range(shape.n_layers)]
+    layers = [l for l in range(shape.n_layers) if not shape.is_attn(l)]  # one launch shape: the DeltaNet layers'
+    R = shape.gdn_in_rows
+    y = torch.empty(R, device="cuda")
     side = torch.cuda.Stream()
 
     def sweep(stream):
-        for l in range(shape.n_layers):
-            capi.check(L.hy_op_gemv_batch(ctypes.byref(tens[l]), None, fmt, rows[l], H, B, x.data_ptr(), H,
-                                          g.data_ptr(), 1e-6, y.data_ptr(), max(rows), 0, stream.cuda_stream),
-                       "gemv_batch")
+        for l in layers:
+            capi.check(L.hy_op_gemv(weights[f"l{l}.w_in"].data_ptr(), R, H, x.data_ptr(), g.data_ptr(), 1e-6,
+                                    y.data_ptr(), 0, stream.cuda_stream), "gemv")
 
     with torch.cuda.stream(side):
         sweep(side)
@@ -463,14 +463,68 @@ def gemv_batch_roofline(shape, weights, B, peak, peak_kind, workload):
         graph.replay()
     b.record(st)
     torch.cuda.synchronize()
-    launch_s = a.elapsed_time(b) / 1e3 / (reps * shape.n_layers)
-    bytes_launch = sum(acc.gemv_batch_bytes(r, H, B, fmt) for r in rows) / len(rows)
+    launch_s = a.elapsed_time(b) / 1e3 / (reps * len(layers))
+    bytes_launch = acc.linear_bytes(R, H, 0) + (H + R) * acc.F32
     achieved = bytes_launch / launch_s / 1e9
     del graph
-    return {"bound": "hbm", "kernel": f"batched tensor-core GEMV (k_bgemv<{fmt}>), input projections, batch {B}",
+    return {"bound": "hbm", "kernel": f"gemv with fused RMSNorm (k_gemv), DeltaNet input projections [{R}, {H}]",
+            "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": load_traffic("gemv_in", workload), "bytes_per_launch": bytes_launch,
+            "launch_us_mean": launch_s * 1e6, "launches_timed": reps * len(layers),
+            "peak_source": f"{peak_kind} hbm_gbs"}
+
+
+def gemv_batch_roofline(shape, weights, B, peak, peak_kind, workload):
+    """The batched tensor-core GEMV (k_bgemv) timed alone: one graph launches
+    it once per layer over that layer's input projection (every launch
+    streams a fresh matrix from HBM), B token vectors each, RMSNorm fused;
+    average launch duration = graph time / launches."""
+    import torch
+
+    from bandwidth_bound_hybrid_gb300 import accounting as acc
+    from bandwidth_bound_hybrid_gb300 import capi
+    from bandwidth_bound_hybrid_gb300.model import _tensor
+    L = capi.lib()
+    fmt = getattr(shape, "weight_format", 0)
+    H = shape.hidden
+    x = torch.randn((B, H), device="cuda")
+    g = torch.ones(H, device="cuda")
+    layers = [l for l in range(shape.n_layers) if not shape.is_attn(l)]  # one launch shape: the DeltaNet layers'
+    R = shape.gdn_in_rows
+    y = torch.empty((B, R), device="cuda")
+    tens = [_tensor(weights[f"l{l}.w_in"]) for l in layers]
+    side = torch.cuda.Stream()
+
+    def sweep(stream):
+        for t in tens:
+            capi.check(L.hy_op_gemv_batch(ctypes.byref(t), None, fmt, R, H, B, x.data_ptr(), H, g.data_ptr(), 1e-6,
+                                          y.data_ptr(), R, 0, stream.cuda_stream), "gemv_batch")
+
+    with torch.cuda.stream(side):
+        sweep(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        sweep(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = 5
+    st = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(reps):
+        graph.replay()
+    b.record(st)
+    torch.cuda.synchronize()
+    launch_s = a.elapsed_time(b) / 1e3 / (reps * len(layers))
+    bytes_launch = acc.gemv_batch_bytes(R, H, B, fmt)
+    achieved = bytes_launch / launch_s / 1e9
+    del graph
+    return {"bound": "hbm",
+            "kernel": f"batched tensor-core GEMV (k_bgemv<{fmt}>), DeltaNet input projections [{R}, {H}], batch {B}",
             "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": load_traffic("gemv_batch", workload), "bytes_per_launch": bytes_launch,
-            "launch_us_mean": launch_s * 1e6, "launches_timed": reps * shape.n_layers,
+            "launch_us_mean": launch_s * 1e6, "launches_timed": reps * len(layers),
             "peak_source": f"{peak_kind} hbm_gbs"}
 
 
