@@ -702,7 +702,7 @@ Plan plan(int R, int C, int fmt, int epi, int nsm, int row_mult) {
   const int npair = epi == kEpiSwiglu ? 2 : 1;
   const int stage_bytes = npair * (kStageW + (fmt == kFmtQ4 ? kStageS : 0));
   // row block of 16 * GW rows: the largest one whose units spread over the
-  // SMs almost as evenly as the best choice (fewer row blocks need fewer
+  // SMs within 10% as evenly as the best choice (fewer row blocks need fewer
   // cross-warp sums)
   double score[4] = {0, 0, 0, 0};
   double best = 0;
@@ -716,7 +716,7 @@ Plan plan(int R, int C, int fmt, int epi, int nsm, int row_mult) {
   }
   int pick = -1;
   for (int i = 0; i < 4 && pick < 0; ++i)
-    if (score[i] > 0 && score[i] >= best - 0.08) pick = i;
+    if (score[i] > 0 && score[i] >= 0.9 * best) pick = i;
   if (pick < 0) return pl;
   pl.gw = 8 >> pick;
   pl.ks = kWarps / pl.gw;

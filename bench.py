@@ -134,6 +134,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(seconds: float, dist, device) -> float:
+    """The slowest rank's time (every rank gets it); `dist` None: this rank's."""
+    if dist is None:
+        return seconds
+    import torch
+    tt = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_throughput(n_ranks: int, units_per_rank: int, seconds: float) -> float:
+    """Whole-job units per second: every rank processed units_per_rank in at most
+    `seconds` (weak scaling: independent replicas, no exchange)."""
+    return max(n_ranks, 1) * units_per_rank / seconds
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 def oracle_decode_sample(shape, context: int, budget_s: float, max_tokens: int, host_w=None):
@@ -270,13 +286,10 @@ def run_ours(args):
     if dist:
         dist.barrier()
     t = ev0.elapsed_time(ev1) / 1e3
-    if dist:
-        tt = torch.tensor([t], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
+    t = max_over_ranks(t, dist, dev)
     assert model.check_device() == 0, "device guard fired in the timed region"
     n = max(ws, 1)
-    value = n * args.steps / t
+    value = job_throughput(n, args.steps, t)
     mid_ctx = ctx0 + args.steps // 2
     sb = acc.step_bytes(shape, mid_ctx)
     step_gbs = sb.total * args.steps / t / 1e9
@@ -351,10 +364,7 @@ def run_ours(args):
         model.decode_step_host(0, tok_h, ids_h)
         tok_h[0] = ids_h[0]
     e2e_t = time.perf_counter() - t0
-    if dist:
-        tt = torch.tensor([e2e_t], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_t = float(tt.item())
+    e2e_t = max_over_ranks(e2e_t, dist, dev)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -417,10 +427,7 @@ def timed_region(args, dist, local, st, step):
     if dist:
         dist.barrier()
     t = ev0.elapsed_time(ev1) / 1e3
-    if dist:
-        tt = torch.tensor([t], dtype=torch.float64, device=torch.device("cuda", local))
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
+    t = max_over_ranks(t, dist, torch.device("cuda", local))
     return t, clk
 
 
@@ -554,7 +561,7 @@ def run_ours_batch(args, w, shape, dist, ws, rank, local):
     t, clk = timed_region(args, dist, local, st, lambda: model.decode_batch(seqs, ids, ids))
     assert model.check_device() == 0, "device guard fired"
     n = max(ws, 1)
-    value = n * B * args.steps / t
+    value = job_throughput(n, B * args.steps, t)
     mid = [c + args.warmup + args.steps // 2 for c in ctx]
     sb = acc.batch_step_bytes(shape, mid)
     step_gbs = sb.total * args.steps / t / 1e9
@@ -570,10 +577,7 @@ def run_ours_batch(args, w, shape, dist, ws, rank, local):
         model.decode_batch_host(seqs, tok_h, ids_h)
         tok_h.copy_(ids_h)
     e2e_t = time.perf_counter() - t0
-    if dist:
-        tt = torch.tensor([e2e_t], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_t = float(tt.item())
+    e2e_t = max_over_ranks(e2e_t, dist, dev)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
