@@ -18,9 +18,10 @@
 //     a row block in registers, so warps meet only at the end of a row block
 //     (KS > 1: a fixed-order sum of the KS partials), not once per stage;
 //   * 4-bit weights are turned into exact FP16 integers (nibble - 8) in
-//     registers (a magic-exponent OR and one packed subtract) and the block
-//     scale is applied to the FP32 result of the block's two MMAs, so the
-//     weights are dequantised exactly;
+//     registers (a magic-exponent OR, then one packed subtract for the low
+//     nibbles or one packed FMA by 1/16 for the high ones, in place) and the
+//     block scale is applied to the FP32 result of the block's two MMAs, so
+//     the weights are dequantised exactly;
 //   * the token vectors are RMS-normalised per token (one warp per token) and
 //     stored once per CTA in shared memory as FP16 (4-bit weights), or for
 //     bf16 weights (the MMA needs one operand type) as two bf16 parts hi + lo,
@@ -79,19 +80,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// Two nibbles (bits 0..3 and 16..19 of v) -> FP16 pair (n - 8), exactly:
-// 0x6400 | n is 1024 + n, minus 1032.
-__device__ __forceinline__ uint32_t nib2_to_f16x2(uint32_t v) {
-  const uint32_t h = (v & 0x000F000Fu) | 0x64006400u;
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
 __device__ __forceinline__ float f16_bits_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 
-// The staged token vectors: 8 rows of x_stride bytes (padded by 16 so that
-// the fragment reads of 8 tokens fall into 8 bank groups), two parts for bf16
-// weights.
+// The staged token vectors: 8 rows of x_stride bytes, two parts for bf16
+// weights.  Rows are padded so that the fragment reads of 8 tokens do not
+// share banks: by 16 bytes for bf16 (32-bit reads), by 64 for 4-bit weights
+// (128-bit reads, two token rows per quarter warp).
 struct XLayout {
   int x_stride, x_parts;
 };
@@ -125,9 +119,15 @@ __device__ __forceinline__ void store4(int fmt, uint8_t* row, uint8_t* row_lo, i
         make_uint2(l[0] | ((uint32_t)l[1] << 16), l[2] | ((uint32_t)l[3] << 16));
     return;
   }
-  const int base = k & ~15, j = k & 15;
-  *reinterpret_cast<__half2*>(row + 2 * (base + (j >> 1))) = __floats2half2_rn(v.x, v.z);
-  *reinterpret_cast<__half2*>(row + 2 * (base + 8 + (j >> 1))) = __floats2half2_rn(v.y, v.w);
+  // 4-bit weights: the 32-element block k >> 5 occupies 64 bytes; lane t's
+  // B fragments of the block's two MMAs (elements 4t, 4t+2 | 4t+1, 4t+3 |
+  // 4t+16, 4t+18 | 4t+17, 4t+19, the order in which its nibble word feeds
+  // the A fragments) are the 16 bytes at 16 t: elements k..k+3 (k a multiple
+  // of 4) land as (k, k+2, k+1, k+3) at 16 t + 8 (k >= 16 in the block)
+  const int e0 = k & 31;
+  const __half2 p0 = __floats2half2_rn(v.x, v.z), p1 = __floats2half2_rn(v.y, v.w);
+  *reinterpret_cast<uint2*>(row + (k >> 5) * 64 + 16 * ((e0 & 15) >> 2) + 8 * (e0 >> 4)) =
+      make_uint2(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1));
 }
 
 // Compute warps: token b = warp into xs, RMS-normalised when norm_g is set
@@ -276,33 +276,55 @@ __device__ __forceinline__ void strip_mma(const uint8_t* mem, const uint8_t* xs,
   const uint8_t* l8 = l0 + 8 * kStrip;
   const uint8_t* xg = xs + g * L.x_stride;  // token g (the MMA's column n = g)
   if (FMT == kFmtQ4) {
-    const uint16_t* s0 = reinterpret_cast<const uint16_t*>(mem + kStageW + line0 * 16);
-    const uint16_t* s8 = reinterpret_cast<const uint16_t*>(mem + kStageW + (line0 + 8) * 16);
+    // the strip's 8 block scales of rows g and g + 8 (16 bytes each)
+    const uint4 sv0 = *reinterpret_cast<const uint4*>(mem + kStageW + line0 * 16);
+    const uint4 sv8 = *reinterpret_cast<const uint4*>(mem + kStageW + (line0 + 8) * 16);
+    const uint32_t sw0[4] = {sv0.x, sv0.y, sv0.z, sv0.w}, sw8[4] = {sv8.x, sv8.y, sv8.z, sv8.w};
+    const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+    const __half2 k16th = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));   // 1/16
+    const __half2 km72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));    // -72
+    // two nibbles in bits 0..3 and 16..19 (lo) or 4..7 and 20..23 (hi) of v
+    // -> FP16 pair (n - 8), exactly: 0x6400 | n is 1024 + n, minus 1032;
+    // 0x6400 | 16 n is 1024 + 16 n, times 1/16 minus 72
+    auto lo2 = [&](uint32_t v) {
+      const uint32_t h = (v & 0x000F000Fu) | 0x64006400u;
+      const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), k1032);
+      return *reinterpret_cast<const uint32_t*>(&r);
+    };
+    auto hi2 = [&](uint32_t v) {
+      const uint32_t h = (v & 0x00F000F0u) | 0x64006400u;
+      const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&h), k16th, km72);
+      return *reinterpret_cast<const uint32_t*>(&r);
+    };
+    const uint8_t* xb = xg + (kb >> 5) * 64 + 16 * t;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {  // 32-element blocks of the strip
       const int off = ((j ^ g) << 4) + 4 * t;
       const uint32_t u0 = *reinterpret_cast<const uint32_t*>(l0 + off);
       const uint32_t u8 = *reinterpret_cast<const uint32_t*>(l8 + off);
-      const int k = kb + 32 * j;
+      const uint4 bx = *reinterpret_cast<const uint4*>(xb + 64 * j);
+      const uint32_t v0 = u0 >> 8, v8 = u8 >> 8;
       uint32_t a[4], b[2];
       float e[4] = {0.f, 0.f, 0.f, 0.f};
-      // low nibbles: elements k + 0..15
-      a[0] = nib2_to_f16x2(u0);
-      a[1] = nib2_to_f16x2(u8);
-      a[2] = nib2_to_f16x2(u0 >> 8);
-      a[3] = nib2_to_f16x2(u8 >> 8);
-      b[0] = *reinterpret_cast<const uint32_t*>(xg + (k + 2 * t) * 2);
-      b[1] = *reinterpret_cast<const uint32_t*>(xg + (k + 8 + 2 * t) * 2);
+      // low nibbles: elements 0..15 of the block
+      a[0] = lo2(u0);
+      a[1] = lo2(u8);
+      a[2] = lo2(v0);
+      a[3] = lo2(v8);
+      b[0] = bx.x;
+      b[1] = bx.y;
       mma_f16(e, a, b);
-      // high nibbles: elements k + 16..31
-      a[0] = nib2_to_f16x2(u0 >> 4);
-      a[1] = nib2_to_f16x2(u8 >> 4);
-      a[2] = nib2_to_f16x2(u0 >> 12);
-      a[3] = nib2_to_f16x2(u8 >> 12);
-      b[0] = *reinterpret_cast<const uint32_t*>(xg + (k + 16 + 2 * t) * 2);
-      b[1] = *reinterpret_cast<const uint32_t*>(xg + (k + 24 + 2 * t) * 2);
+      // high nibbles: elements 16..31
+      a[0] = hi2(u0);
+      a[1] = hi2(u8);
+      a[2] = hi2(v0);
+      a[3] = hi2(v8);
+      b[0] = bx.z;
+      b[1] = bx.w;
       mma_f16(e, a, b);
-      const float sg = f16_bits_to_f32(s0[j]), sg8 = f16_bits_to_f32(s8[j]);
+      const uint32_t w0 = sw0[j >> 1], w8 = sw8[j >> 1];
+      const float sg = f16_bits_to_f32((uint16_t)((j & 1) ? (w0 >> 16) : (w0 & 0xFFFFu)));
+      const float sg8 = f16_bits_to_f32((uint16_t)((j & 1) ? (w8 >> 16) : (w8 & 0xFFFFu)));
       d[0] = fmaf(sg, e[0], d[0]);
       d[1] = fmaf(sg, e[1], d[1]);
       d[2] = fmaf(sg8, e[2], d[2]);
@@ -365,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
   const int strip_elems = FMT == kFmtQ4 ? 256 : 64;
   const int spu = p.C / strip_elems / KS;  // stages per unit
   XLayout L;
-  L.x_stride = p.C * 2 + 16;
+  L.x_stride = p.C * 2 + (FMT == kFmtQ4 ? 64 : 16);
   L.x_parts = FMT == kFmtBf16 ? 2 : 1;
   uint8_t* stages = smem;                                                     // 1024-aligned members
   uint8_t* xs = smem + nst * stage_bytes;                                     // [parts][8][x_stride]
@@ -723,7 +745,8 @@ Plan plan(int R, int C, int fmt, int epi, int nsm, int row_mult) {
   const int TR = kTileRows * pl.gw;
   const long long units = (R + TR - 1) / TR;
   pl.ncta = (int)(units < nsm ? units : nsm);
-  const int fixed = (fmt == kFmtBf16 ? 2 : 1) * kMaxB * (C * 2 + 16) + 4 * npair * kPartFloats + 2 * kMaxStages * 8 +
+  const int fixed = (fmt == kFmtBf16 ? 2 * kMaxB * (C * 2 + 16) : kMaxB * (C * 2 + 64)) + 4 * npair * kPartFloats +
+                    2 * kMaxStages * 8 +
                     1024;  // + alignment of the stages
   int ns = kInFlight / stage_bytes;
   ns = ns < 2 ? 2 : (ns > kMaxStages ? kMaxStages : ns);
