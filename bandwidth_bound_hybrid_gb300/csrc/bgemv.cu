@@ -376,6 +376,107 @@ __device__ __forceinline__ void am_unkey(unsigned long long k, float& v, int& i)
   i = (int)(0xFFFFFFFFu - (uint32_t)k);
 }
 
+// Routing of every token of a batch from its router logits (logits [B][ld],
+// row E of a token the shared gate), by the nt = 8 warps' threads tid: warp b
+// picks token b's top_k by repeated warp-wide argmax (largest logit, lowest
+// index on ties: the same set and order as ranking all experts); the union
+// of the picks is an ascending ballot scan over the experts' flags.  `sync`
+// synchronises exactly those threads.
+constexpr int kRouteMaxE = 512;  // experts + the shared gate per token
+struct RouteShared {
+  int sel[kMaxB][16];
+  float selv[kMaxB][16];
+  int flag[kRouteMaxE];
+  int cnt[kRouteMaxE / 32 + 1];
+  int pos[kRouteMaxE];
+};
+__device__ __noinline__ void route_tokens(const Params& p, RouteShared& rs, int tid) {
+  auto sync = [] { named_barrier(1, kCT); };
+  const int warp = tid >> 5, lane = tid & 31;
+  const int E = p.r_E, K = p.top_k, ld = p.ldy;
+  const float* logits = p.y;
+  int* union_ids = const_cast<int*>(p.union_ids);
+  int* slot_of = const_cast<int*>(p.slot_of);
+  for (int e = tid; e < kRouteMaxE; e += kCT) rs.flag[e] = 0;
+  sync();
+  if (warp < p.B) {
+    const int b = warp;
+    constexpr int kPer = kRouteMaxE / 32;
+    float v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      const float x = e < E ? __ldcg(logits + (long long)b * ld + e) : -INFINITY;
+      v[i] = x == x ? x : -INFINITY;  // a NaN logit ranks last
+    }
+    uint32_t taken = 0u;
+    for (int k = 0; k < K; ++k) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !(taken >> i & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == 0) {
+        rs.sel[b][k] = bi;
+        rs.selv[b][k] = bv;
+      }
+    }
+    __syncwarp();
+    if (lane < K) rs.flag[rs.sel[b][lane]] = 1;
+    if (lane == 0) {  // softmax over the selected logits, sigmoid gate of the shared expert
+      const float m = rs.selv[b][0];
+      float den = 0.f;
+      for (int k = 0; k < K; ++k) den += __expf(rs.selv[b][k] - m);
+      for (int k = 0; k < K; ++k) {
+        p.r_w[b * (K + 1) + k] = __expf(rs.selv[b][k] - m) / den;
+        if (p.r_ids) p.r_ids[b * K + k] = rs.sel[b][k];
+      }
+      p.r_w[b * (K + 1) + K] = sigmoidf_(__ldcg(logits + (long long)b * ld + E));
+    }
+  }
+  sync();
+  const int nch = (E + 31) / 32;
+  for (int c = warp; c < nch; c += kWarps) {
+    const unsigned m = __ballot_sync(0xffffffffu, rs.flag[32 * c + lane] != 0);
+    if (lane == 0) rs.cnt[c] = __popc(m);
+  }
+  sync();
+  for (int c = warp; c < nch; c += kWarps) {
+    int base = 0;
+    for (int q = 0; q < c; ++q) base += rs.cnt[q];
+    const int e = 32 * c + lane;
+    const unsigned m = __ballot_sync(0xffffffffu, rs.flag[e] != 0);
+    const int at = base + __popc(m & ((1u << lane) - 1u));
+    rs.pos[e] = at;
+    if (rs.flag[e]) union_ids[at] = e;
+  }
+  int U = 0;
+  for (int q = 0; q < nch; ++q) U += rs.cnt[q];
+  if (tid == 0) *const_cast<int*>(p.n_union) = U;
+  for (int i = tid; i < (kMaxUnion + 1) * kMaxB; i += kCT) slot_of[i] = -1;
+  sync();
+  for (int i = tid; i < p.B * K; i += kCT) {
+    const int b = i / K, k = i % K;
+    slot_of[rs.pos[rs.sel[b][k]] * kMaxB + b] = k;
+  }
+  for (int b = tid; b < kMaxB; b += kCT) slot_of[U * kMaxB + b] = K;
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ Params p, const __grid_constant__ Maps mp) {
   extern __shared__ uint8_t smem_raw[];
@@ -509,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
         return;
       }
       float* y = p.y ? p.y + (long long)b * p.ldy + us.a + ri : nullptr;
-      if (p.epi == kEpiStore) *y = v;
+      if (p.epi == kEpiStore || p.epi == kEpiRoute) *y = v;
       else if (p.epi == kEpiResid) *y += v;
       else if (p.epi == kEpiSwiglu) *y = siluf_(v) * vu;
       else {
@@ -547,6 +648,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
     }
   }
   if (named_barrier_or(1, kCT, !ok)) return;  // one decision for all compute threads
+  if (p.epi == kEpiRoute) {
+    // every thread's logits are stored (the barrier above): the last CTA to
+    // arrive routes the batch, in the drained weight ring's shared memory
+    if (ctid == 0) {
+      __threadfence();
+      s_last = (atomicAdd(p.counter, 1u) == (unsigned)(p.ncta - 1));
+    }
+    named_barrier(1, kCT);
+    if (!s_last) return;
+    __threadfence();
+    route_tokens(p, *reinterpret_cast<RouteShared*>(stages), ctid);
+    if (ctid == 0) *p.counter = 0u;
+    return;
+  }
   if (p.epi != kEpiArgmax) return;
 
   // ------------------------------------------------------------ per-token argmax
@@ -594,102 +709,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
   if (ctid == 0) *p.counter = 0u;
 }
 
-// One CTA: routing of every token, then the union of the selected experts.
-// Warp b selects token b's top_k by repeated warp-wide argmax (largest logit,
-// lowest index on ties: the same set and order as ranking all experts); the
-// union is an ascending ballot scan over the experts' flags.
-constexpr int kRouteWarps = 8;
-constexpr int kRouteMaxE = 512;  // experts + the shared gate per token
-__global__ void __launch_bounds__(kRouteWarps * 32) k_route(const Route r) {
-  __shared__ int sel[kMaxB][16];
-  __shared__ float selv[kMaxB][16];
-  __shared__ int flag[kRouteMaxE];
-  __shared__ int cnt[kRouteMaxE / 32 + 1];
-  __shared__ int pos[kRouteMaxE];
-  pdl_wait();
-  pdl_launch_dependents();
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int E = r.E, K = r.top_k;
-  for (int e = tid; e < kRouteMaxE; e += blockDim.x) flag[e] = 0;
-  __syncthreads();
-  if (warp < r.B) {
-    const int b = warp;
-    constexpr int kPer = kRouteMaxE / 32;
-    float v[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane + 32 * i;
-      const float x = e < E ? r.logits[(long long)b * r.ld + e] : -INFINITY;
-      v[i] = x == x ? x : -INFINITY;  // a NaN logit ranks last
-    }
-    uint32_t taken = 0u;
-    for (int k = 0; k < K; ++k) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !(taken >> i & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-          bv = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == 0) {
-        sel[b][k] = bi;
-        selv[b][k] = bv;
-      }
-    }
-    __syncwarp();
-    if (lane < K) flag[sel[b][lane]] = 1;
-    if (lane == 0) {  // softmax over the selected logits, sigmoid gate of the shared expert
-      const float m = selv[b][0];
-      float den = 0.f;
-      for (int k = 0; k < K; ++k) den += __expf(selv[b][k] - m);
-      for (int k = 0; k < K; ++k) {
-        r.w[b * (K + 1) + k] = __expf(selv[b][k] - m) / den;
-        if (r.ids) r.ids[b * K + k] = sel[b][k];
-      }
-      r.w[b * (K + 1) + K] = sigmoidf_(r.logits[(long long)b * r.ld + E]);
-    }
-  }
-  __syncthreads();
-  const int nch = (E + 31) / 32;
-  for (int c = warp; c < nch; c += kRouteWarps) {
-    const unsigned m = __ballot_sync(0xffffffffu, flag[32 * c + lane] != 0);
-    if (lane == 0) cnt[c] = __popc(m);
-  }
-  __syncthreads();
-  for (int c = warp; c < nch; c += kRouteWarps) {
-    int base = 0;
-    for (int q = 0; q < c; ++q) base += cnt[q];
-    const int e = 32 * c + lane;
-    const unsigned m = __ballot_sync(0xffffffffu, flag[e] != 0);
-    const int at = base + __popc(m & ((1u << lane) - 1u));
-    pos[e] = at;
-    if (flag[e]) r.union_ids[at] = e;
-  }
-  int U = 0;
-  for (int q = 0; q < nch; ++q) U += cnt[q];
-  if (tid == 0) *r.n_union = U;
-  for (int i = tid; i < (kMaxUnion + 1) * kMaxB; i += blockDim.x) r.slot_of[i] = -1;
-  __syncthreads();
-  for (int i = tid; i < r.B * K; i += blockDim.x) {
-    const int b = i / K, k = i % K;
-    r.slot_of[pos[sel[b][k]] * kMaxB + b] = k;
-  }
-  for (int b = tid; b < kMaxB; b += blockDim.x) r.slot_of[U * kMaxB + b] = K;
-}
-
 __global__ void k_moe_reduce(float* y, int ldy, const float* part, const float* w, int R, int B, int K) {
   pdl_wait();
   pdl_launch_dependents();
@@ -702,12 +721,6 @@ __global__ void k_moe_reduce(float* y, int ldy, const float* part, const float* 
 }
 
 }  // namespace
-
-cudaError_t route(const Route& r, cudaStream_t st, bool pdl) {
-  if (r.B < 1 || r.B > kMaxB || r.E < 1 || r.E > 511 || r.top_k < 1 || r.top_k > 16 || r.top_k > r.E || r.B * r.top_k > kMaxUnion)
-    return cudaErrorInvalidValue;
-  return launch_k(k_route, dim3(1), dim3(kRouteWarps * 32), 0, st, pdl, r);
-}
 
 cudaError_t moe_reduce(float* y, int ldy, const float* part, const float* w, int R, int B, int top_k, cudaStream_t st,
                        bool pdl) {

@@ -143,7 +143,7 @@ struct hy_cache {
   float *bpart = nullptr, *bapart = nullptr, *bam_val = nullptr;
   int *btok = nullptr, *bids = nullptr, *bunion = nullptr, *bnu = nullptr, *bslot = nullptr, *bam_idx = nullptr;
   int* brids = nullptr;
-  unsigned *bcnt_attn = nullptr, *bcnt_am = nullptr;
+  unsigned *bcnt_attn = nullptr, *bcnt_am = nullptr, *bcnt_route = nullptr;
   int bh_len = 0;
   size_t bapart_len = 0;
   struct BGraph {
@@ -784,8 +784,8 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
       if ((rc = dense(d, "down")) != HY_OK) return rc;
     } else {
       const int E = cf.n_experts, K = cf.top_k, Fe = cf.expert_ffn;
-      {  // router logits of every token (the router stays bf16)
-        bgemv::Params r = bparams(bgemv::kFmtBf16, bgemv::kSrcDense, bgemv::kInX, bgemv::kEpiStore);
+      {  // router logits of every token (the router stays bf16); the last CTA routes the batch
+        bgemv::Params r = bparams(bgemv::kFmtBf16, bgemv::kSrcDense, bgemv::kInX, bgemv::kEpiRoute);
         r.W[0] = (const uint8_t*)L.router;
         r.R = E + 1;
         r.C = H;
@@ -794,22 +794,19 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
         r.norm_g = L.norm2;
         r.y = c->brlog;
         r.ldy = E + 1;
-        if ((rc = dense(r, "router")) != HY_OK) return rc;
+        r.counter = c->bcnt_route;
+        r.r_ids = c->brids;
+        r.r_w = c->bw;
+        r.r_E = E;
+        r.top_k = K;
+        r.union_ids = c->bunion;
+        r.n_union = c->bnu;
+        r.slot_of = c->bslot;
+        const bgemv::Plan pl = bgemv::plan(r.R, r.C, r.fmt, r.epi, m->nsm);
+        if (!pl.ok || E > 511 || B * K > bgemv::kMaxUnion)
+          return fail(HY_ERR_UNSUPPORTED, "no batched router for %d experts at hidden %d", E, H);
+        if ((rc = ck(bgemv::launch(r, pl, st, pdl), "router")) != HY_OK) return rc;
       }
-      bgemv::Route ro;
-      memset(&ro, 0, sizeof(ro));
-      ro.logits = c->brlog;
-      ro.ld = E + 1;
-      ro.B = B;
-      ro.E = E;
-      ro.top_k = K;
-      ro.ids = c->brids;
-      ro.w = c->bw;
-      ro.union_ids = c->bunion;
-      ro.n_union = c->bnu;
-      ro.slot_of = c->bslot;
-      ro.guard = c->guard;
-      if ((rc = ck(bgemv::route(ro, st, pdl), "route")) != HY_OK) return rc;
       // rows the union kernels spread over the SMs: the expected union of B
       // tokens' top-K picks under uniform routing, plus the shared expert
       const double pk = 1.0 - std::pow(1.0 - (double)K / E, (double)B);
@@ -867,8 +864,8 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
         const bgemv::Plan pl = bgemv::plan(u_exp * H, p.C, p.fmt, p.epi, m->nsm, H);
         if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no batched plan for the expert down");
         if ((rc = ck(bgemv::launch(p, pl, st, pdl), "expert down")) != HY_OK) return rc;
+        if ((rc = ck(bgemv::moe_reduce(c->bx, H, c->bpart, c->bw, H, B, K, st, pdl), "expert sum")) != HY_OK) return rc;
       }
-      if ((rc = ck(bgemv::moe_reduce(c->bx, H, c->bpart, c->bw, H, B, K, st, pdl), "expert sum")) != HY_OK) return rc;
       if (m->debug) {  // the first token's router results
         HY_CK(cudaMemcpyAsync(c->dbg_rlog + (size_t)l * (E + 1), c->brlog, sizeof(float) * (E + 1),
                               cudaMemcpyDeviceToDevice, st));
@@ -1199,7 +1196,8 @@ int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, 
         (rc = dalloc(c, &c->bids, B)) || (rc = dalloc(c, &c->bunion, bgemv::kMaxUnion)) ||
         (rc = dalloc(c, &c->bnu, 1)) || (rc = dalloc(c, &c->bslot, (size_t)(bgemv::kMaxUnion + 1) * B)) ||
         (rc = dalloc(c, &c->brids, (size_t)B * K)) ||
-        (rc = dalloc(c, &c->bcnt_attn, (size_t)B * std::max(cf.attn_kv_heads, 1))) || (rc = dalloc(c, &c->bcnt_am, 1))) {
+        (rc = dalloc(c, &c->bcnt_attn, (size_t)B * std::max(cf.attn_kv_heads, 1))) || (rc = dalloc(c, &c->bcnt_am, 1)) ||
+        (rc = dalloc(c, &c->bcnt_route, 1))) {
       free_cache_mem(c);
       delete c;
       return rc;

@@ -182,7 +182,7 @@ constexpr int kMaxSmem = 220 * 1024;
 enum Fmt : int { kFmtBf16 = 0, kFmtQ4 = 1 };
 enum Src : int { kSrcDense = 0, kSrcUnionRows = 1, kSrcUnionDown = 2 };
 enum In : int { kInX = 0, kInEmbed = 1 };
-enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiArgmax = 3 };
+enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiArgmax = 3, kEpiRoute = 4 };
 constexpr int kMaxUnion = 64;  // distinct routed experts of one step (top_k * batch at most)
 struct Params {
   int fmt, src, in, epi;
@@ -222,6 +222,14 @@ struct Params {
   int* ids_out;             // [B]
   int* len_inc[kMaxB];      // per token, incremented after the argmax (nullable)
   int n_exp;                // union sources: routed experts in the expert tensors
+  // ---- kEpiRoute (the router: y = logits [B][E + 1]): the last CTA to finish
+  // routes every token (top_k of the E logits, FP32 compare, lowest index on
+  // ties; softmax over the picks; shared gate sigmoid(logit E)) into r_ids
+  // [B][top_k] (nullable), r_w [B][top_k + 1], and the union of the picks
+  // (ascending) with its slot map into union_ids / n_union / slot_of
+  int* r_ids;
+  float* r_w;
+  int r_E;
   int ncta, nstages;        // from the plan
   int gw, ks;               // row groups of 16 x strip lanes of the 8 compute warps (gw * ks = 8)
   unsigned* guard;
@@ -238,22 +246,6 @@ Plan plan(int R, int C, int fmt, int epi, int nsm, int row_mult = 0);
 cudaError_t init();
 cudaError_t launch(const Params& p, const Plan& pl, cudaStream_t st, bool pdl);
 
-// MoE routing of a batch: per token the top_k experts of logits [B][ld]
-// (FP32 compare, lowest index on ties), their softmax weights and the shared
-// gate sigmoid(logit E) into w [B][top_k + 1]; the union of the selected
-// experts (ascending) and, per union entry and token, the slot that selected
-// it (shared expert: entry n_union, slot top_k for every token).
-struct Route {
-  const float* logits;
-  int ld, B, E, top_k;
-  int* ids;        // [B][top_k] (nullable)
-  float* w;        // [B][top_k + 1]
-  int* union_ids;  // [kMaxUnion]
-  int* n_union;
-  int* slot_of;    // [(kMaxUnion + 1)][kMaxB]
-  unsigned* guard;
-};
-cudaError_t route(const Route& r, cudaStream_t st, bool pdl);
 // y[b][row] += sum_{k <= top_k} w[b][k] * part[(b * (top_k + 1) + k) * R + row]
 cudaError_t moe_reduce(float* y, int ldy, const float* part, const float* w, int R, int B, int top_k, cudaStream_t st,
                        bool pdl);
