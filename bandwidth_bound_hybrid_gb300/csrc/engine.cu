@@ -258,7 +258,10 @@ int launch_ops(hy_model* m, std::vector<StepOp>& ops, cudaStream_t st) {
 }
 
 // The operations of one decode step for sequence `seq`, in order.
-int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepOp>& ops) {
+// route_in_experts: the router GEMV only stores its logits and the expert
+// gate/up kernel's CTAs pick the experts themselves (kernel-per-operation
+// steps); otherwise the router's last CTA picks them (persistent step).
+int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepOp>& ops, bool route_in_experts) {
   hy_model* m = c->m;
   const hy_config& cf = m->cfg;
   const int H = cf.hidden;
@@ -395,7 +398,14 @@ int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepO
         r.dbg_ids = c->dbg_rids + (size_t)l * K;
         r.dbg_logits = c->dbg_rlog + (size_t)l * (E + 1);
       }
-      if ((rc = run(r, gemv::kSrcDense, gemv::kInX, gemv::kEpiRouter, "router")) != HY_OK) return rc;
+      if (route_in_experts) {
+        r.y = c->rlog;
+        r.dbg_ids = nullptr;
+        r.dbg_logits = nullptr;
+        if ((rc = run(r, gemv::kSrcDense, gemv::kInX, gemv::kEpiStore, "router")) != HY_OK) return rc;
+      } else if ((rc = run(r, gemv::kSrcDense, gemv::kInX, gemv::kEpiRouter, "router")) != HY_OK) {
+        return rc;
+      }
       gemv::Params gu = gemv_base();
       gu.exp_base[0] = (const uint8_t*)L.exp_gate.w;
       gu.exp_base[1] = (const uint8_t*)L.exp_up.w;
@@ -412,6 +422,16 @@ int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepO
       gu.x = c->x;
       gu.norm_g = L.norm2;
       gu.y = c->h;
+      if (route_in_experts) {
+        gu.route_here = 1;
+        gu.router_logits = c->rlog;
+        gu.out_ids = c->moe_ids;
+        gu.out_w = c->moe_w;
+        if (m->debug) {
+          gu.dbg_ids = c->dbg_rids + (size_t)l * K;
+          gu.dbg_logits = c->dbg_rlog + (size_t)l * (E + 1);
+        }
+      }
       if ((rc = run(gu, gemv::kSrcExpertRows, gemv::kInX, gemv::kEpiSwiglu, "expert gate/up")) != HY_OK) return rc;
       gemv::Params dn = gemv_base();
       dn.exp_base[0] = (const uint8_t*)L.exp_down.w;
@@ -557,7 +577,7 @@ int get_program(hy_cache* c, int seq, float* logits, int* ids, const step::Progr
       return HY_OK;
     }
   std::vector<StepOp> ops;
-  int rc = collect_ops(c, seq, logits, ids, ops);
+  int rc = collect_ops(c, seq, logits, ids, ops, false);
   if (rc != HY_OK) return rc;
   std::vector<step::Phase> phases;
   step::Program pr;
@@ -593,7 +613,7 @@ int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) 
     return fail(HY_ERR_ARG, "no step program for sequence %d", seq);
   }
   std::vector<StepOp> ops;
-  int rc = collect_ops(c, seq, logits, ids, ops);
+  int rc = collect_ops(c, seq, logits, ids, ops, true);
   if (rc != HY_OK) return rc;
   c->last_kernels = (int)ops.size();
   return launch_ops(m, ops, st);

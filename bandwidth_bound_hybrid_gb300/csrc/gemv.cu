@@ -38,6 +38,7 @@ __global__ void __maxnreg__(kMaxRegs) k_gemv(const Params p) {
   uint64_t* full = reinterpret_cast<uint64_t*>(red + ((p.rows_cta_max * npair * p.nchunk + 1) & ~1));
   uint64_t* empty = full + kMaxStages;
   uint64_t* xbar = empty + kMaxStages;
+  uint64_t* rbar = xbar + 1;  // expert ids picked (routing in this kernel)
   __shared__ __align__(16) EpiShared esh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -50,6 +51,7 @@ __global__ void __maxnreg__(kMaxRegs) k_gemv(const Params p) {
       mbar_init(&empty[s], kConsumerWarps);
     }
     mbar_init(xbar, 1);
+    mbar_init(rbar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -68,6 +70,8 @@ __global__ void __maxnreg__(kMaxRegs) k_gemv(const Params p) {
       // Dense weights do not depend on earlier kernels: pre_stages tiles go out
       // before griddepcontrol.wait; expert ids come from the router kernel.
       const int pre = (SRC == kSrcDense) ? p.pre_stages : 0;
+      // q: p, with the expert ids this CTA picked (routing in this kernel)
+      Params q = p;
       bool input_issued = false;
       int t = 0, pf = r0;                // pf: first row the L2 prefetch cursor has not covered
       bool next_done = false;
@@ -77,14 +81,21 @@ __global__ void __maxnreg__(kMaxRegs) k_gemv(const Params p) {
           pdl_wait();
           issue_input(p, IN, xs, esh.mw, xbar, keep);
           input_issued = true;
+          if (SRC == kSrcExpertRows && p.route_here) {
+            if (!mbar_wait(rbar, 0)) {
+              set_guard(p.guard, kGuardWaitTimeout);
+              break;
+            }
+            q.moe_ids = esh.sel;
+          }
         }
-        const int rows = tile_rows_at(p, SRC, a, r1);
+        const int rows = tile_rows_at(q, SRC, a, r1);
         const int s = t % nst, k = t / nst;
         if (t >= nst && !mbar_wait(&empty[s], (k - 1) & 1)) {
           set_guard(p.guard, kGuardWaitTimeout);
           break;
         }
-        issue_tile(p, SRC, npair, a, rows, stages + s * p.stage_bytes, &full[s], pol);
+        issue_tile(q, SRC, npair, a, rows, stages + s * p.stage_bytes, &full[s], pol);
         a += rows;
         if (p.pf_ahead > 0 && t + 1 >= nst && !next_done) {
           // once the ring is full, keep the prefetch cursor pf_ahead bytes
@@ -92,8 +103,8 @@ __global__ void __maxnreg__(kMaxRegs) k_gemv(const Params p) {
           // next kernels read first
           if (pf < a) pf = a;
           while (pf < r1 && (long long)(pf - a) * row_bytes < p.pf_ahead) {
-            const int pr = tile_rows_at(p, SRC, pf, r1);
-            prefetch_tile(p, SRC, npair, pf, pr);
+            const int pr = tile_rows_at(q, SRC, pf, r1);
+            prefetch_tile(q, SRC, npair, pf, pr);
             pf += pr;
           }
           if (pf >= r1) {
@@ -119,6 +130,18 @@ __global__ void __maxnreg__(kMaxRegs) k_gemv(const Params p) {
   const int ctid = threadIdx.x;
   pdl_wait();
   pdl_launch_dependents();
+  if (SRC == kSrcExpertRows && p.route_here && warp == 0) {
+    // every CTA picks the experts from the stored router logits (the same
+    // result everywhere) and hands the ids to its copy lane; CTA 0 publishes
+    // them and the routing weights for the down projection
+    warp_topk([&](int e) { return __ldcg(p.router_logits + e); }, p.n_experts, p.top_k, esh.sel, esh.selv, lane);
+    if (blockIdx.x == 0 && p.dbg_logits)
+      for (int e = lane; e <= p.n_experts; e += 32) p.dbg_logits[e] = __ldcg(p.router_logits + e);
+    if (lane == 0) {
+      if (blockIdx.x == 0) route_weights(p, esh.sel, esh.selv, __ldcg(p.router_logits + p.n_experts));
+      mbar_arrive(rbar);
+    }
+  }
   if (!mbar_wait(xbar, 0) && ctid == 0) set_guard(p.guard, kGuardWaitTimeout);
   const float sc = input_scale(p, IN, xs, esh.mw, esh.red, ctid);
   LaneSlice<VPL> L;
@@ -263,7 +286,7 @@ Plan plan(int R, int C, int npair, int nsm, bool norm) {
   const char* pf0 = getenv("HY_GEMV_PREFETCH_KB");
   if (pf0 && *pf0 == '0') pl.pf_ahead = 0;
   const int red_floats = ((pl.rows_cta_max * npair * pl.nchunk) + 1) & ~1;
-  pl.smem = pl.nstages * pl.stage_bytes + 4 * (pl.xs_floats + pl.gs_floats + red_floats) + (2 * kMaxStages + 1) * 8;
+  pl.smem = pl.nstages * pl.stage_bytes + 4 * (pl.xs_floats + pl.gs_floats + red_floats) + (2 * kMaxStages + 2) * 8;
   while (pl.smem > kMaxSmem && pl.nstages > 2) {
     pl.nstages -= 1;
     pl.smem -= pl.stage_bytes;

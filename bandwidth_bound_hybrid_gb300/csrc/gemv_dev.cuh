@@ -316,6 +316,62 @@ __device__ __forceinline__ void argmax_merge(float& bv, int& bi, float ov, int o
   }
 }
 
+// top_k of E logits (FP32 compare, lowest index on ties) by one warp: each
+// lane holds E/32 logits (load(e) reads logit e) and top_k rounds of a
+// warp-wide argmax pick the selection in order (the same set and order as
+// ranking all experts).  sel / selv (shared) receive ids and logits.
+template <typename Load>
+__device__ __forceinline__ void warp_topk(Load load, int E, int K, int* sel, float* selv, int lane) {
+  constexpr int kPer = kMaxExperts / 32;
+  float v[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    const float x = e < E ? load(e) : -INFINITY;
+    v[i] = x == x ? x : -INFINITY;  // a NaN logit ranks last
+  }
+  uint32_t taken = 0u;
+  for (int q = 0; q < K; ++q) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !(taken >> i & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      argmax_merge(bv, bi, ov, oi);
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == 0) {
+      sel[q] = bi;
+      selv[q] = bv;
+    }
+  }
+  __syncwarp();
+}
+
+// One thread: softmax over the selected logits and the shared expert's gate
+// sigmoid(gate_logit) into out_w [top_k + 1], the ids into out_ids (and the
+// debug copy).
+__device__ __forceinline__ void route_weights(const Params& p, const int* sel, const float* selv, float gate_logit) {
+  const float m = selv[0];
+  float den = 0.f;
+  for (int q = 0; q < p.top_k; ++q) den += __expf(selv[q] - m);
+  for (int q = 0; q < p.top_k; ++q) {
+    p.out_ids[q] = sel[q];
+    p.out_w[q] = __expf(selv[q] - m) / den;
+    if (p.dbg_ids) p.dbg_ids[q] = sel[q];
+  }
+  p.out_w[p.top_k] = sigmoidf_(gate_logit);
+}
+
 // Epilogue over the CTA's rows (after all tiles): store, residual add,
 // SwiGLU, or argmax / router top-k finished by the last CTA to arrive (an
 // atomic ticket: no CTA waits for another).
@@ -409,49 +465,9 @@ __device__ __forceinline__ void epilogue(const Params& p, int epi, const float* 
   for (int e = ctid; e <= E; e += kCT) scratch[e] = __ldcg(p.router_logits + e);
   named_barrier(1, kCT);
   if (warp == 0) {
-    constexpr int kPer = kMaxExperts / 32;
-    float v[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane + 32 * i;
-      const float x = e < E ? scratch[e] : -INFINITY;
-      v[i] = x == x ? x : -INFINITY;  // a NaN logit ranks last
-    }
-    uint32_t taken = 0u;
-    for (int q = 0; q < p.top_k; ++q) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !(taken >> i & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-          bv = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        argmax_merge(bv, bi, ov, oi);
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == 0) {
-        sh.sel[q] = bi;
-        sh.selv[q] = bv;
-      }
-    }
-    __syncwarp();
+    warp_topk([&](int e) { return scratch[e]; }, E, p.top_k, sh.sel, sh.selv, lane);
     if (lane == 0) {
-      const float m = sh.selv[0];
-      float den = 0.f;
-      for (int q = 0; q < p.top_k; ++q) den += __expf(sh.selv[q] - m);
-      for (int q = 0; q < p.top_k; ++q) {
-        p.out_ids[q] = sh.sel[q];
-        p.out_w[q] = __expf(sh.selv[q] - m) / den;
-        if (p.dbg_ids) p.dbg_ids[q] = sh.sel[q];
-      }
-      p.out_w[p.top_k] = sigmoidf_(scratch[E]);
+      route_weights(p, sh.sel, sh.selv, scratch[E]);
       *p.counter = 0u;
     }
   }

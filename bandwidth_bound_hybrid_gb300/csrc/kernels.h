@@ -87,6 +87,8 @@ struct Params {
   float* out_w;                 // kEpiRouter: [top_k + 1]
   int* dbg_ids;                 // kEpiRouter debug copies (nullable)
   float* dbg_logits;
+  int route_here;               // kSrcExpertRows: every CTA picks the experts itself from router_logits (the
+                                //   router kernel only stored them); CTA 0 writes out_ids / out_w (and dbg_ids)
   // ---- prefetch
   PfSpan nx[kMaxPfSpans];       // what the next kernels read first (weights known when the step is recorded)
   int n_nx;
@@ -189,7 +191,7 @@ struct Params {
   // ---- MoE over the union of the experts the batch selected (src != kSrcDense)
   //   kSrcUnionRows: virtual rows u * slot_rows + r, u < n_union: routed expert
   //     union_ids[u]; u == n_union: the shared expert (R = (n_union + 1) * slot_rows)
-  //   kSrcUnionDown: tiles (u, 16 output rows of R); the input of tile u is
+  //   kSrcUnionDown: units (u, a row block of R); the input of unit u is
   //     x + b * ldx + u * C; outputs go to part_out[(b * (top_k + 1) + slot) * R + row]
   //     for the tokens b whose slot slot_of[u * kMaxB + b] >= 0
   const uint8_t* exp_base[2];
