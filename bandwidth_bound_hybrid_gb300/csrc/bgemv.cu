@@ -228,7 +228,7 @@ __device__ __forceinline__ int units_of(const Params& p, int U) {
   return (p.R + tr - 1) / tr;
 }
 
-__device__ __forceinline__ UnitSrc unit_src(const Params& p, int t, int U) {
+__device__ __forceinline__ UnitSrc unit_src(const Params& p, const int* uids, int t, int U) {
   const int tr = kTileRows * p.gw;
   UnitSrc us;
   us.routed = false;
@@ -255,7 +255,7 @@ __device__ __forceinline__ UnitSrc unit_src(const Params& p, int t, int U) {
   us.rows = tr;
   us.crow = r;
   if (us.u < U) {
-    int e = p.union_ids[us.u];
+    int e = uids[us.u];
     if (e < 0 || e >= p.n_exp) {  // never address past the expert tensor
       set_guard(p.guard, kGuardBadIndex);
       e = 0;
@@ -389,12 +389,18 @@ struct RouteShared {
   int flag[kRouteMaxE];
   int cnt[kRouteMaxE / 32 + 1];
   int pos[kRouteMaxE];
+  int uid[kMaxUnion];  // the union, ascending
+  int U;
 };
-__device__ __noinline__ void route_tokens(const Params& p, RouteShared& rs, int tid) {
+// logits [B][ld]; the union also lands in rs.uid / rs.U.  publish: write the
+// routing weights, ids, union and slot map to global memory (p.r_w, p.r_ids,
+// p.union_ids, p.n_union, p.slot_of).  Ends with a barrier of the compute
+// threads.
+__device__ __noinline__ void route_tokens(const Params& p, const float* logits, int ld, RouteShared& rs, int tid,
+                                          bool publish) {
   auto sync = [] { named_barrier(1, kCT); };
   const int warp = tid >> 5, lane = tid & 31;
-  const int E = p.r_E, K = p.top_k, ld = p.ldy;
-  const float* logits = p.y;
+  const int E = p.r_E, K = p.top_k;
   int* union_ids = const_cast<int*>(p.union_ids);
   int* slot_of = const_cast<int*>(p.slot_of);
   for (int e = tid; e < kRouteMaxE; e += kCT) rs.flag[e] = 0;
@@ -438,7 +444,7 @@ __device__ __noinline__ void route_tokens(const Params& p, RouteShared& rs, int 
     }
     __syncwarp();
     if (lane < K) rs.flag[rs.sel[b][lane]] = 1;
-    if (lane == 0) {  // softmax over the selected logits, sigmoid gate of the shared expert
+    if (lane == 0 && publish) {  // softmax over the selected logits, sigmoid gate of the shared expert
       const float m = rs.selv[b][0];
       float den = 0.f;
       for (int k = 0; k < K; ++k) den += __expf(rs.selv[b][k] - m);
@@ -463,18 +469,25 @@ __device__ __noinline__ void route_tokens(const Params& p, RouteShared& rs, int 
     const unsigned m = __ballot_sync(0xffffffffu, rs.flag[e] != 0);
     const int at = base + __popc(m & ((1u << lane) - 1u));
     rs.pos[e] = at;
-    if (rs.flag[e]) union_ids[at] = e;
+    if (rs.flag[e]) {
+      rs.uid[at] = e;
+      if (publish) union_ids[at] = e;
+    }
   }
   int U = 0;
   for (int q = 0; q < nch; ++q) U += rs.cnt[q];
-  if (tid == 0) *const_cast<int*>(p.n_union) = U;
-  for (int i = tid; i < (kMaxUnion + 1) * kMaxB; i += kCT) slot_of[i] = -1;
-  sync();
-  for (int i = tid; i < p.B * K; i += kCT) {
-    const int b = i / K, k = i % K;
-    slot_of[rs.pos[rs.sel[b][k]] * kMaxB + b] = k;
+  if (tid == 0) rs.U = U;
+  if (publish) {
+    if (tid == 0) *const_cast<int*>(p.n_union) = U;
+    for (int i = tid; i < (kMaxUnion + 1) * kMaxB; i += kCT) slot_of[i] = -1;
+    sync();
+    for (int i = tid; i < p.B * K; i += kCT) {
+      const int b = i / K, k = i % K;
+      slot_of[rs.pos[rs.sel[b][k]] * kMaxB + b] = k;
+    }
+    for (int b = tid; b < kMaxB; b += kCT) slot_of[U * kMaxB + b] = K;
   }
-  for (int b = tid; b < kMaxB; b += kCT) slot_of[U * kMaxB + b] = K;
+  sync();
 }
 
 template <int FMT>
@@ -495,8 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
   float* part = reinterpret_cast<float*>(xs + L.x_parts * kMaxB * L.x_stride);  // [npair][8 warps][16][8]
   uint64_t* full = reinterpret_cast<uint64_t*>(part + npair * kPartFloats);
   uint64_t* empty = full + kMaxStages;
+  uint64_t* rbar = empty + kMaxStages;  // routing done (route_here)
   __shared__ unsigned long long s_key[kMaxB];
   __shared__ int s_last;
+  __shared__ RouteShared s_route;
+  const bool route_here = p.src == kSrcUnionRows && p.route_here;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the unit range of this CTA; for MoE sources it depends on the union the
@@ -504,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
   auto unit_range = [&](int& U, int& t0, int& t1) {
     U = 0;
     if (p.src != kSrcDense) {
-      U = *p.n_union;
+      U = route_here ? s_route.U : *p.n_union;
       if (U < 0 || U > kMaxUnion) {
         set_guard(p.guard, kGuardBadIndex);
         U = 0;
@@ -520,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kWarps);
     }
+    mbar_init(rbar, 1);
     fence_mbar_init();
   }
   if (threadIdx.x < kMaxB) s_key[threadIdx.x] = 0ull;
@@ -531,13 +548,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       if (p.src != kSrcDense) pdl_wait();  // union and expert ids come from the routing kernel
+      if (route_here && !mbar_wait(rbar, 0)) set_guard(p.guard, kGuardWaitTimeout);  // ... or from this CTA
+      const int* uids = route_here ? s_route.uid : p.union_ids;
       int U, t0, t1;
       unit_range(U, t0, t1);
       const uint32_t tx = (uint32_t)(npair * member);
       int n = 0;
       bool alive = true;
       for (int t = t0; t < t1 && alive; ++t) {
-        const UnitSrc us = unit_src(p, t, U);
+        const UnitSrc us = unit_src(p, uids, t, U);
         for (int st = 0; st < spu; ++st, ++n) {
           const int s = n % nst, k = n / nst;
           if (n >= nst && !mbar_wait(&empty[s], (k - 1) & 1)) {
@@ -565,6 +584,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
   const int ctid = threadIdx.x;
   pdl_wait();
   pdl_launch_dependents();
+  if (route_here) {
+    // every CTA routes the batch from the stored router logits (the same
+    // result everywhere) for its copy lane; CTA 0 publishes the routing for
+    // the down projection and the expert sum
+    route_tokens(p, p.r_logits, p.r_ld, s_route, ctid, blockIdx.x == 0);
+    if (ctid == 0) mbar_arrive(rbar);
+  }
+  const int* uids = route_here ? s_route.uid : p.union_ids;
   int U, t0, t1;
   unit_range(U, t0, t1);
   int staged_u = -1;
@@ -580,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
   bool ok = true;
   int n = 0;
   for (int t = t0; t < t1; ++t) {
-    const UnitSrc us = unit_src(p, t, U);
+    const UnitSrc us = unit_src(p, uids, t, U);
     if (p.src == kSrcUnionDown && us.u != staged_u) {  // the unit's expert input, for every token
       named_barrier(1, kCT);
       stage_inputs(p, L, xs, ctid, (long long)us.u * p.C);
@@ -658,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
     named_barrier(1, kCT);
     if (!s_last) return;
     __threadfence();
-    route_tokens(p, *reinterpret_cast<RouteShared*>(stages), ctid);
+    route_tokens(p, p.y, p.ldy, s_route, ctid, true);
     if (ctid == 0) *p.counter = 0u;
     return;
   }
@@ -759,7 +786,7 @@ Plan plan(int R, int C, int fmt, int epi, int nsm, int row_mult) {
   const long long units = (R + TR - 1) / TR;
   pl.ncta = (int)(units < nsm ? units : nsm);
   const int fixed = (fmt == kFmtBf16 ? 2 * kMaxB * (C * 2 + 16) : kMaxB * (C * 2 + 64)) + 4 * npair * kPartFloats +
-                    2 * kMaxStages * 8 +
+                    (2 * kMaxStages + 1) * 8 +
                     1024;  // + alignment of the stages
   int ns = kInFlight / stage_bytes;
   ns = ns < 2 ? 2 : (ns > kMaxStages ? kMaxStages : ns);

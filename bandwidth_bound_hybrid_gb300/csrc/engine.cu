@@ -804,8 +804,8 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
       if ((rc = dense(d, "down")) != HY_OK) return rc;
     } else {
       const int E = cf.n_experts, K = cf.top_k, Fe = cf.expert_ffn;
-      {  // router logits of every token (the router stays bf16); the last CTA routes the batch
-        bgemv::Params r = bparams(bgemv::kFmtBf16, bgemv::kSrcDense, bgemv::kInX, bgemv::kEpiRoute);
+      {  // router logits of every token (the router stays bf16); the expert gate/up kernel routes
+        bgemv::Params r = bparams(bgemv::kFmtBf16, bgemv::kSrcDense, bgemv::kInX, bgemv::kEpiStore);
         r.W[0] = (const uint8_t*)L.router;
         r.R = E + 1;
         r.C = H;
@@ -858,6 +858,12 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
         p.y = c->bh;
         p.ldy = c->bh_len;
         p.n_exp = E;
+        p.route_here = 1;  // every CTA routes the batch from the stored logits; CTA 0 publishes
+        p.r_logits = c->brlog;
+        p.r_ld = E + 1;
+        p.r_ids = c->brids;
+        p.r_w = c->bw;
+        p.r_E = E;
         const bgemv::Plan pl = bgemv::plan(u_exp * Fe, p.C, p.fmt, p.epi, m->nsm, Fe);
         if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no batched plan for the expert gate/up (%d x %d)", Fe, H);
         if ((rc = ck(bgemv::launch(p, pl, st, pdl), "expert gate/up")) != HY_OK) return rc;

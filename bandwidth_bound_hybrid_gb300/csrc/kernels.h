@@ -232,6 +232,12 @@ struct Params {
   int* r_ids;
   float* r_w;
   int r_E;
+  // ---- kSrcUnionRows with route_here: every CTA routes the batch itself from
+  // the stored router logits r_logits [B][r_ld] (same outputs as kEpiRoute,
+  // published by CTA 0) before its copy lane requests expert rows
+  int route_here;
+  const float* r_logits;
+  int r_ld;
   int ncta, nstages;        // from the plan
   int gw, ks;               // row groups of 16 x strip lanes of the 8 compute warps (gw * ks = 8)
   unsigned* guard;
