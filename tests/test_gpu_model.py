@@ -133,12 +133,21 @@ def test_moe_truncated_depth_parity(built, path):
     run_parity(shape, 5, 3, path=path)
 
 
-def test_persistent_and_multi_kernel_steps_agree(built):
+AGREE_SHAPES = {
+    "dense": dataclasses.replace(workloads.DENSE4B, name="dense4b-l4", n_layers=4, attn_layers=(3,), vocab=4096),
+    # the kernel-per-operation step picks the experts in the expert kernel, the
+    # persistent step in the router's epilogue: the same arithmetic either way
+    "moe": dataclasses.replace(workloads.MOE35B, name="moe-l4", n_layers=4, attn_layers=(3,), vocab=4096),
+}
+
+
+@pytest.mark.parametrize("kind", list(AGREE_SHAPES))
+def test_persistent_and_multi_kernel_steps_agree(built, kind):
     """The two ways of running a step compute the same thing: same greedy ids,
     logits within rounding of each other (the persistent step reorders no
     sum, so they are in fact expected to be identical)."""
     import torch
-    shape = dataclasses.replace(workloads.DENSE4B, name="dense4b-l4", n_layers=4, attn_layers=(3,), vocab=4096)
+    shape = AGREE_SHAPES[kind]
     prompt = workloads.host.uniform_ids(9, workloads.PROMPT_TID, 24, shape.vocab)
     outs = []
     for f in PATHS:
