@@ -482,10 +482,13 @@ def gemv_in_roofline(shape, weights, peak, peak_kind, workload):
 
 
 def gemv_batch_roofline(shape, weights, B, peak, peak_kind, workload):
-    """The batched tensor-core GEMV (k_bgemv) timed alone: one graph launches
-    it once per layer over that layer's input projection (every launch
-    streams a fresh matrix from HBM), B token vectors each, RMSNorm fused;
-    average launch duration = graph time / launches."""
+    """The batched tensor-core GEMV (k_bgemv) timed alone on the batch step's
+    largest launch: MoE shapes, the expert gate/up + SwiGLU over the expected
+    union of the batch's picks (round(E (1 - (1 - k/E)^B)) + 1 experts of Fe
+    rows, as one dense view of consecutive experts of each layer's tensors);
+    dense shapes, the input projections.  One graph launches it once per layer
+    (every launch streams fresh weights from HBM); average launch duration =
+    graph time / launches."""
     import torch
 
     from bandwidth_bound_hybrid_gb300 import accounting as acc
@@ -496,16 +499,27 @@ def gemv_batch_roofline(shape, weights, B, peak, peak_kind, workload):
     H = shape.hidden
     x = torch.randn((B, H), device="cuda")
     g = torch.ones(H, device="cuda")
-    layers = [l for l in range(shape.n_layers) if not shape.is_attn(l)]  # one launch shape: the DeltaNet layers'
-    R = shape.gdn_in_rows
+    if shape.ffn == 0:
+        u = int(round(acc.expected_union(shape.n_experts, shape.top_k, B))) + 1
+        R = u * shape.expert_ffn
+        layers = list(range(shape.n_layers))
+        pairs = [(_tensor(weights[f"l{l}.exp_gate"]), _tensor(weights[f"l{l}.exp_up"])) for l in layers]
+        what = f"expert gate/up + SwiGLU over {u} experts, [{R}, {H}] x 2"
+        bytes_launch = 2 * acc.linear_bytes(R, H, fmt) + B * (H + R) * acc.F32
+    else:
+        layers = [l for l in range(shape.n_layers) if not shape.is_attn(l)]
+        R = shape.gdn_in_rows
+        pairs = [(_tensor(weights[f"l{l}.w_in"]), None) for l in layers]
+        what = f"DeltaNet input projections [{R}, {H}]"
+        bytes_launch = acc.gemv_batch_bytes(R, H, B, fmt)
     y = torch.empty((B, R), device="cuda")
-    tens = [_tensor(weights[f"l{l}.w_in"]) for l in layers]
     side = torch.cuda.Stream()
 
     def sweep(stream):
-        for t in tens:
-            capi.check(L.hy_op_gemv_batch(ctypes.byref(t), None, fmt, R, H, B, x.data_ptr(), H, g.data_ptr(), 1e-6,
-                                          y.data_ptr(), R, 0, stream.cuda_stream), "gemv_batch")
+        for w, wu in pairs:
+            capi.check(L.hy_op_gemv_batch(ctypes.byref(w), ctypes.byref(wu) if wu is not None else None, fmt, R, H, B,
+                                          x.data_ptr(), H, g.data_ptr(), 1e-6, y.data_ptr(), R, 0, stream.cuda_stream),
+                       "gemv_batch")
 
     with torch.cuda.stream(side):
         sweep(side)
@@ -523,15 +537,13 @@ def gemv_batch_roofline(shape, weights, B, peak, peak_kind, workload):
         graph.replay()
     b.record(st)
     torch.cuda.synchronize()
-    launch_s = a.elapsed_time(b) / 1e3 / (reps * len(layers))
-    bytes_launch = acc.gemv_batch_bytes(R, H, B, fmt)
+    launch_s = a.elapsed_time(b) / 1e3 / (reps * len(pairs))
     achieved = bytes_launch / launch_s / 1e9
     del graph
-    return {"bound": "hbm",
-            "kernel": f"batched tensor-core GEMV (k_bgemv<{fmt}>), DeltaNet input projections [{R}, {H}], batch {B}",
+    return {"bound": "hbm", "kernel": f"batched tensor-core GEMV (k_bgemv<{fmt}>), {what}, batch {B}",
             "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": load_traffic("gemv_batch", workload), "bytes_per_launch": bytes_launch,
-            "launch_us_mean": launch_s * 1e6, "launches_timed": reps * len(layers),
+            "launch_us_mean": launch_s * 1e6, "launches_timed": reps * len(pairs),
             "peak_source": f"{peak_kind} hbm_gbs"}
 
 
