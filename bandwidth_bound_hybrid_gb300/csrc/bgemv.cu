@@ -478,7 +478,10 @@ __device__ __noinline__ void route_tokens(const Params& p, const float* logits, 
   for (int q = 0; q < nch; ++q) U += rs.cnt[q];
   if (tid == 0) rs.U = U;
   if (publish) {
-    if (tid == 0) *const_cast<int*>(p.n_union) = U;
+    if (tid == 0) {
+      *const_cast<int*>(p.n_union) = U;
+      if (p.union_count) atomicAdd(p.union_count, (unsigned long long)U);
+    }
     for (int i = tid; i < (kMaxUnion + 1) * kMaxB; i += kCT) slot_of[i] = -1;
     sync();
     for (int i = tid; i < p.B * K; i += kCT) {

@@ -144,6 +144,7 @@ struct hy_cache {
   int *btok = nullptr, *bids = nullptr, *bunion = nullptr, *bnu = nullptr, *bslot = nullptr, *bam_idx = nullptr;
   int* brids = nullptr;
   unsigned *bcnt_attn = nullptr, *bcnt_am = nullptr, *bcnt_route = nullptr;
+  unsigned long long* experts_read = nullptr;  // distinct routed experts the batched steps read (hy_experts_read)
   int bh_len = 0;
   size_t bapart_len = 0;
   struct BGraph {
@@ -864,6 +865,7 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
         p.r_ids = c->brids;
         p.r_w = c->bw;
         p.r_E = E;
+        p.union_count = c->experts_read;
         const bgemv::Plan pl = bgemv::plan(u_exp * Fe, p.C, p.fmt, p.epi, m->nsm, Fe);
         if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no batched plan for the expert gate/up (%d x %d)", Fe, H);
         if ((rc = ck(bgemv::launch(p, pl, st, pdl), "expert gate/up")) != HY_OK) return rc;
@@ -1223,7 +1225,7 @@ int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, 
         (rc = dalloc(c, &c->bnu, 1)) || (rc = dalloc(c, &c->bslot, (size_t)(bgemv::kMaxUnion + 1) * B)) ||
         (rc = dalloc(c, &c->brids, (size_t)B * K)) ||
         (rc = dalloc(c, &c->bcnt_attn, (size_t)B * std::max(cf.attn_kv_heads, 1))) || (rc = dalloc(c, &c->bcnt_am, 1)) ||
-        (rc = dalloc(c, &c->bcnt_route, 1))) {
+        (rc = dalloc(c, &c->bcnt_route, 1)) || (rc = dalloc(c, &c->experts_read, 1))) {
       free_cache_mem(c);
       delete c;
       return rc;
@@ -1282,6 +1284,19 @@ int hy_seq_reset(hy_cache* c, int32_t seq, void* stream) {
 int32_t hy_seq_len(const hy_cache* c, int32_t seq) { return valid_seq(c, seq) ? c->len[seq] : -1; }
 int32_t hy_seq_capacity(const hy_cache* c, int32_t seq) { return valid_seq(c, seq) ? c->cap[seq] : -1; }
 int32_t hy_step_kernels(const hy_cache* c) { return c ? c->last_kernels : 0; }
+
+int hy_experts_read(hy_cache* c, void* stream, uint64_t* total_out) {
+  if (!c || !total_out) return fail(HY_ERR_ARG, "null argument");
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned long long v = 0;
+  if (c->experts_read) {
+    HY_CK(cudaMemcpyAsync(&v, c->experts_read, sizeof(v), cudaMemcpyDeviceToHost, st));
+    HY_CK(cudaMemsetAsync(c->experts_read, 0, sizeof(v), st));
+    HY_CK(cudaStreamSynchronize(st));
+  }
+  *total_out = (uint64_t)v;
+  return HY_OK;
+}
 
 int hy_seq_fill_synthetic(hy_cache* c, int32_t seq, int32_t len, uint64_t seed, void* stream) {
   if (!valid_seq(c, seq) || len < 0) return fail(HY_ERR_ARG, "bad argument");

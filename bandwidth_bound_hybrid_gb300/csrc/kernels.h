@@ -238,6 +238,7 @@ struct Params {
   int route_here;
   const float* r_logits;
   int r_ld;
+  unsigned long long* union_count;  // routing publishers add the union size (routed experts read) here (nullable)
   int ncta, nstages;        // from the plan
   int gw, ks;               // row groups of 16 x strip lanes of the 8 compute warps (gw * ks = 8)
   unsigned* guard;

@@ -121,6 +121,13 @@ class HybridModel:
                                              None if logits_host is None else logits_host.data_ptr(),
                                              ids_host.data_ptr(), _stream(stream)), "hy_decode_step_host")
 
+    def experts_read(self, stream=None) -> int:
+        """Distinct routed experts the batched steps read since the last call
+        (summed over layers and steps); resets the count."""
+        v = ctypes.c_uint64(0)
+        check(capi.lib().hy_experts_read(self.c, _stream(stream), ctypes.byref(v)), "hy_experts_read")
+        return int(v.value)
+
     def fill_synthetic(self, seq: int, length: int, seed: int = 0, stream=None) -> None:
         """Give sequence `seq` `length` positions of seeded synthetic cache
         contents (KV rows and recurrent state) without running a prompt."""

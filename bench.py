@@ -152,7 +152,7 @@ def job_throughput(n_ranks: int, units_per_rank: int, seconds: float) -> float:
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_decode_sample(shape, context: int, budget_s: float, max_tokens: int, host_w=None):
+def oracle_decode_sample(shape, context: int, budget_s: float, max_tokens: int, host_w=None, warm=True):
     """Time full-depth oracle decode tokens at position `context` from a seeded
     synthetic cache (random K/V rows and recurrent state: the prompt itself is
     not replayed on the CPU).  Returns (tokens/s, threads, tokens, seconds)."""
@@ -176,15 +176,37 @@ def oracle_decode_sample(shape, context: int, budget_s: float, max_tokens: int, 
         S[:] = (rng.standard_normal(S.shape) * 0.01).astype(np.float32)
     o.cache.len = context
     tok = 17
-    t0 = time.perf_counter()
-    o.forward(tok, want_hidden=False)
-    t1 = time.perf_counter() - t0
-    n = max(1, min(max_tokens, int(math.ceil(budget_s / max(t1, 1e-3)))))
+    n = max_tokens
+    if warm:  # one untimed token, which also sizes the sample to the budget
+        t0 = time.perf_counter()
+        o.forward(tok, want_hidden=False)
+        t1 = time.perf_counter() - t0
+        n = max(1, min(max_tokens, int(math.ceil(budget_s / max(t1, 1e-3)))))
     t0 = time.perf_counter()
     for i in range(n):
         tok = int(orc.argmax(o.forward(tok, want_hidden=False)["logits"]))
     dt = time.perf_counter() - t0
     return n / dt, orc.threads(), n, dt
+
+
+def cpu_baseline_obj(shape, context: int, what: str):
+    """The oracle on this host's cores (all of them, ~12 s) and on one core (one
+    token), at `context` from a seeded synthetic cache."""
+    from oracle import oracle as orc
+    from synth import workloads
+    host_w = workloads.host_weights(shape)
+    tps, cores, ntok, dt = oracle_decode_sample(shape, context, budget_s=12.0, max_tokens=16, host_w=host_w)
+    orc.set_threads(1)
+    try:
+        tps1, _, ntok1, dt1 = oracle_decode_sample(shape, context, budget_s=0.0, max_tokens=1, host_w=host_w,
+                                                   warm=False)
+    finally:
+        orc.set_threads(cores)
+    return {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
+            "value_1_core": tps1,
+            "sample": f"{ntok} full-depth FP64 oracle decode tokens{' ' + what if what else ''} at context {context} "
+                      f"from a seeded "
+                      f"synthetic cache ({dt:.1f} s on {cores} threads; {ntok1} token on 1 thread, {dt1:.1f} s)"}
 
 
 def run_reference(args):
@@ -271,22 +293,9 @@ def run_ours(args):
     ctx0 = model.seq_len(0)
 
     # ---- timed region: K graph launches, inputs resident in HBM
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = Clocks(local)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    ev0.record(st)
-    for _ in range(args.steps):
-        model.decode_step(0, ids, ids)
-    ev1.record(st)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    if dist:
-        dist.barrier()
-    t = ev0.elapsed_time(ev1) / 1e3
-    t = max_over_ranks(t, dist, dev)
+    depth_window = 32 if w.splits else 0  # the long-context workload: tokens/s per 32-token window
+    t, clk, windows, win = timed_region(args, dist, local, st, lambda: model.decode_step(0, ids, ids),
+                                        window=depth_window, warm=False)
     assert model.check_device() == 0, "device guard fired in the timed region"
     n = max(ws, 1)
     value = job_throughput(n, args.steps, t)
@@ -345,7 +354,7 @@ def run_ours(args):
             m2 = HybridModel(shape, weights, [cap], splits=sp, flags=flags)
             m2.fill_synthetic(0, ctx0, seed=1)
             ids2 = ids.clone()
-            t2, _ = timed_region(args, dist, local, st, lambda: m2.decode_step(0, ids2, ids2))
+            t2 = timed_region(args, dist, local, st, lambda: m2.decode_step(0, ids2, ids2))[0]
             assert m2.check_device() == 0
             sweep[str(sp)] = max(ws, 1) * args.steps / t2
             m2.close()
@@ -368,10 +377,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        tps, cores, ntok, dt = oracle_decode_sample(shape, mid_ctx, budget_s=12.0, max_tokens=16)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{ntok} full-depth FP64 oracle decode tokens at context {mid_ctx} from a seeded synthetic "
-                         f"cache ({dt:.1f} s)"}
+        cpu = cpu_baseline_obj(shape, mid_ctx, "")
 
     if rank == 0:
         line = {
@@ -387,6 +393,9 @@ def run_ours(args):
             "roofline": roof,
             "step_roofline": {"bound": "hbm", "bytes_per_step": sb.total, "achieved": step_gbs, "peak": peak,
                               "unit": "GB/s", "frac": step_gbs / peak},
+            "timing": window_stats(windows, win, args.steps),
+            "depth_curve": [{"context_start": ctx0 + i * win, "tokens_per_s": n * win / wt}
+                            for i, wt in enumerate(windows) if (i + 1) * win <= args.steps] if depth_window else None,
             "split_sweep_tokens_per_s": sweep,
             "cpu_baseline": cpu,
             "e2e": {"value": n * e2e_steps / e2e_t, "unit": "tokens/s", "h2d_bytes_per_step": 4,
@@ -404,31 +413,68 @@ def run_ours(args):
     return 0
 
 
-def timed_region(args, dist, local, st, step):
+def timed_region(args, dist, local, st, step, window=0, before_timing=None, warm=True):
     """W warm-up steps, then K timed steps between barriers and device
-    synchronisations, with the clocks sampled meanwhile; returns (seconds,
-    max over ranks; clock record)."""
+    synchronisations, with the clocks sampled meanwhile.  Events are also
+    recorded every `window` steps (default: K / 7) inside the timed region (no
+    synchronisation between them).  Returns (seconds, max over ranks; clock
+    record; per-window seconds of this rank)."""
     import torch
-    for _ in range(args.warmup):
+    for _ in range(args.warmup if warm else 0):
         step()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if before_timing:
+        before_timing()
+    win = window if window > 0 else max(1, args.steps // 7)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps // win + 2)]
     clocks = Clocks(local)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    ev0.record(st)
-    for _ in range(args.steps):
+    evs[0].record(st)
+    n_ev = 1
+    for i in range(args.steps):
         step()
-    ev1.record(st)
+        if (i + 1) % win == 0 and (i + 1) < args.steps:
+            evs[n_ev].record(st)
+            n_ev += 1
+    evs[n_ev].record(st)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if dist:
         dist.barrier()
-    t = ev0.elapsed_time(ev1) / 1e3
+    t = evs[0].elapsed_time(evs[n_ev]) / 1e3
+    windows = [evs[i].elapsed_time(evs[i + 1]) / 1e3 for i in range(n_ev)]
     t = max_over_ranks(t, dist, torch.device("cuda", local))
-    return t, clk
+    return t, clk, windows, win
+
+
+def window_stats(windows, win, steps):
+    """Mean ms per step over the full windows, their coefficient of variation
+    and a Student-t 95% interval of the mean."""
+    full = [w / win * 1e3 for i, w in enumerate(windows) if (i + 1) * win <= steps]
+    n = len(full)
+    if n < 2:
+        return None
+    m = statistics.mean(full)
+    sd = statistics.stdev(full)
+    tq = {2: 12.71, 3: 4.303, 4: 3.182, 5: 2.776, 6: 2.571, 7: 2.447, 8: 2.365, 9: 2.306, 10: 2.262}.get(n, 2.0)
+    h = tq * sd / math.sqrt(n)
+    return {"windows": n, "steps_per_window": win, "ms_per_step_mean": m, "cv": sd / m if m else None,
+            "ci95_ms_per_step": [m - h, m + h], "cv_over_5pct": (sd / m) > 0.05 if m else None}
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part", "hardware")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 def gemv_in_roofline(shape, weights, peak, peak_kind, workload):
@@ -569,35 +615,48 @@ def run_ours_batch(args, w, shape, dist, ws, rank, local):
     for s, c in enumerate(ctx):
         model.fill_synthetic(s, c, seed=s + 1)
     seqs = list(range(B))
-    ids = torch.from_numpy(workloads.host.uniform_ids(w.prompt_seed, workloads.PROMPT_TID, B, shape.vocab)).to(dev)
-    t, clk = timed_region(args, dist, local, st, lambda: model.decode_batch(seqs, ids, ids))
+    # Each sequence is fed its own seeded uniform token every step (teacher
+    # forcing): with synthetic weights, feeding back the greedy ids makes the
+    # sequences converge on one token stream, so the batch would route
+    # identically and read 8 experts per layer instead of a real batch's
+    # union.  A step's work is otherwise the same whichever tokens it gets.
+    n_tok = args.warmup + 2 * args.steps
+    tok_np = workloads.host.uniform_ids(w.prompt_seed, workloads.PROMPT_TID, n_tok * B, shape.vocab).reshape(n_tok, B)
+    tok_dev = torch.from_numpy(tok_np).to(dev)
+    ids = torch.empty(B, dtype=torch.int32, device=dev)
+    cursor = [0]
+
+    def step():
+        model.decode_batch(seqs, tok_dev[cursor[0]], ids)
+        cursor[0] += 1
+
+    t, clk, windows, win = timed_region(args, dist, local, st, step, before_timing=model.experts_read)
+    # distinct routed experts the timed steps read per layer (the union of the batch's picks)
+    moe_layers = shape.n_layers if shape.ffn == 0 else 0
+    realised = model.experts_read() / (moe_layers * args.steps) if moe_layers else None
     assert model.check_device() == 0, "device guard fired"
     n = max(ws, 1)
     value = job_throughput(n, B * args.steps, t)
     mid = [c + args.warmup + args.steps // 2 for c in ctx]
-    sb = acc.batch_step_bytes(shape, mid)
+    sb = acc.batch_step_bytes(shape, mid, realised)
     step_gbs = sb.total * args.steps / t / 1e9
 
     roof = None if args.no_kernel_timing else gemv_batch_roofline(shape, weights, B, peak, peak_kind, args.workload)
 
-    tok_h = torch.zeros(B, dtype=torch.int32).pin_memory()
+    tok_h = torch.from_numpy(tok_np[args.warmup + args.steps:].copy()).pin_memory()  # the next K steps' tokens
     ids_h = torch.zeros(B, dtype=torch.int32).pin_memory()
-    tok_h.copy_(ids.cpu())
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        model.decode_batch_host(seqs, tok_h, ids_h)
-        tok_h.copy_(ids_h)
+    for i in range(args.steps):
+        model.decode_batch_host(seqs, tok_h[i], ids_h)
     e2e_t = time.perf_counter() - t0
     e2e_t = max_over_ranks(e2e_t, dist, dev)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         c0 = int(round(sum(mid) / B))
-        tps, cores, ntok, dt = oracle_decode_sample(shape, c0, budget_s=12.0, max_tokens=16)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{ntok} full-depth FP64 oracle decode tokens of one sequence at the batch's mean context "
-                         f"{c0} from a seeded synthetic cache ({dt:.1f} s; the oracle runs sequences one at a time)"}
+        cpu = cpu_baseline_obj(shape, c0, "of one sequence (the oracle runs sequences one at a time) at the batch's "
+                                          "mean context")
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n, "steps": args.steps,
@@ -605,14 +664,16 @@ def run_ours_batch(args, w, shape, dist, ws, rank, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "shape": shape.name, "batch": B, "contexts": ctx,
                        "context_fill": "seeded synthetic KV rows and recurrent state (no prompt replay)",
+                       "tokens": "seeded uniform ids per sequence and step (teacher forcing)",
                        "weights": "4-bit blocks of 32 + fp16 scale" if getattr(shape, "weight_format", 0) else "bf16",
                        "kv": "bf16", "parallelism": f"replicas x{n}",
                        "l2": "inputs larger than L2: every step streams GBs of weights and KV through the 129 MB L2"},
             "roofline": roof,
             "step_roofline": {"bound": "hbm", "bytes_per_step": sb.total, "achieved": step_gbs, "peak": peak,
-                              "unit": "GB/s", "frac": step_gbs / peak,
-                              "experts_per_layer": acc.expected_union(shape.n_experts, shape.top_k, B)
+                              "unit": "GB/s", "frac": step_gbs / peak, "experts_per_layer": realised,
+                              "experts_per_layer_expected": acc.expected_union(shape.n_experts, shape.top_k, B)
                               if shape.ffn == 0 else None},
+            "timing": window_stats(windows, win, args.steps),
             "cpu_baseline": cpu,
             "e2e": {"value": n * B * args.steps / e2e_t, "unit": "tokens/s", "h2d_bytes_per_step": 4 * B,
                     "d2h_bytes_per_step": 4 * B},

@@ -167,6 +167,14 @@ int32_t hy_seq_capacity(const hy_cache* c, int32_t seq);
  * Stream-ordered. */
 int hy_seq_fill_synthetic(hy_cache* c, int32_t seq, int32_t len, uint64_t seed, void* stream);
 
+/* Distinct routed experts the batched MoE steps (hy_decode_step with several
+ * sequences, or 4-bit weights) read since the last call, summed over layers
+ * and steps: each layer reads the union of its tokens' picks once.  Resets
+ * the count.  Batch-1 bf16 steps read top_k per layer and do not count.
+ * Synchronises `stream`.  [14h] "Eight levers that worked" (expert-gathered
+ * GEMVs read only the selected experts). */
+int hy_experts_read(hy_cache* c, void* stream, uint64_t* total_out);
+
 /* Kernels the last recorded decode step launches: 1 when the whole step runs
  * as one persistent kernel (HY_FLAG_PERSISTENT), else one per operation.  0
  * before any step. */

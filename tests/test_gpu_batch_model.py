@@ -157,3 +157,24 @@ def test_synthetic_fill(built):
     model.fill_synthetic(0, 0)
     assert model.seq_len(0) == 0 and model.check_device() == 0
     model.close()
+
+
+def test_experts_read_counts_the_union(built):
+    """hy_experts_read: per MoE layer a batched step reads the union of its
+    tokens' picks once: between top_k and min(E, B top_k) experts; reading
+    resets the count."""
+    import torch
+
+    from bandwidth_bound_hybrid_gb300.model import HybridModel
+    shape = TINY_MOE_Q4
+    B = 8
+    model = HybridModel(shape, workloads.device_weights(shape), [16] * B, flags=0)
+    toks = torch.tensor(list(range(3, 3 + B)), dtype=torch.int32, device="cuda")
+    ids = torch.empty(B, dtype=torch.int32, device="cuda")
+    model.experts_read()
+    model.decode_batch(list(range(B)), toks, ids)
+    n = model.experts_read()
+    layers = shape.n_layers  # every layer of this shape is MoE
+    assert layers * shape.top_k <= n <= layers * min(shape.n_experts, B * shape.top_k)
+    assert model.experts_read() == 0
+    model.close()
