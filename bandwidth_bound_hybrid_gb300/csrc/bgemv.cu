@@ -640,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
         return;
       }
       float* y = p.y ? p.y + (long long)b * p.ldy + us.a + ri : nullptr;
-      if (p.epi == kEpiStore || p.epi == kEpiRoute) *y = v;
+      if (p.epi == kEpiStore) *y = v;
       else if (p.epi == kEpiResid) *y += v;
       else if (p.epi == kEpiSwiglu) *y = siluf_(v) * vu;
       else {
@@ -678,20 +678,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
     }
   }
   if (named_barrier_or(1, kCT, !ok)) return;  // one decision for all compute threads
-  if (p.epi == kEpiRoute) {
-    // every thread's logits are stored (the barrier above): the last CTA to
-    // arrive routes the batch, in the drained weight ring's shared memory
-    if (ctid == 0) {
-      __threadfence();
-      s_last = (atomicAdd(p.counter, 1u) == (unsigned)(p.ncta - 1));
-    }
-    named_barrier(1, kCT);
-    if (!s_last) return;
-    __threadfence();
-    route_tokens(p, p.y, p.ldy, s_route, ctid, true);
-    if (ctid == 0) *p.counter = 0u;
-    return;
-  }
   if (p.epi != kEpiArgmax) return;
 
   // ------------------------------------------------------------ per-token argmax

@@ -143,7 +143,7 @@ struct hy_cache {
   float *bpart = nullptr, *bapart = nullptr, *bam_val = nullptr;
   int *btok = nullptr, *bids = nullptr, *bunion = nullptr, *bnu = nullptr, *bslot = nullptr, *bam_idx = nullptr;
   int* brids = nullptr;
-  unsigned *bcnt_attn = nullptr, *bcnt_am = nullptr, *bcnt_route = nullptr;
+  unsigned *bcnt_attn = nullptr, *bcnt_am = nullptr;
   unsigned long long* experts_read = nullptr;  // distinct routed experts the batched steps read (hy_experts_read)
   int bh_len = 0;
   size_t bapart_len = 0;
@@ -815,14 +815,6 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
         r.norm_g = L.norm2;
         r.y = c->brlog;
         r.ldy = E + 1;
-        r.counter = c->bcnt_route;
-        r.r_ids = c->brids;
-        r.r_w = c->bw;
-        r.r_E = E;
-        r.top_k = K;
-        r.union_ids = c->bunion;
-        r.n_union = c->bnu;
-        r.slot_of = c->bslot;
         const bgemv::Plan pl = bgemv::plan(r.R, r.C, r.fmt, r.epi, m->nsm);
         if (!pl.ok || E > 511 || B * K > bgemv::kMaxUnion)
           return fail(HY_ERR_UNSUPPORTED, "no batched router for %d experts at hidden %d", E, H);
@@ -1225,7 +1217,7 @@ int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, 
         (rc = dalloc(c, &c->bnu, 1)) || (rc = dalloc(c, &c->bslot, (size_t)(bgemv::kMaxUnion + 1) * B)) ||
         (rc = dalloc(c, &c->brids, (size_t)B * K)) ||
         (rc = dalloc(c, &c->bcnt_attn, (size_t)B * std::max(cf.attn_kv_heads, 1))) || (rc = dalloc(c, &c->bcnt_am, 1)) ||
-        (rc = dalloc(c, &c->bcnt_route, 1)) || (rc = dalloc(c, &c->experts_read, 1))) {
+        (rc = dalloc(c, &c->experts_read, 1))) {
       free_cache_mem(c);
       delete c;
       return rc;

@@ -184,7 +184,7 @@ constexpr int kMaxSmem = 220 * 1024;
 enum Fmt : int { kFmtBf16 = 0, kFmtQ4 = 1 };
 enum Src : int { kSrcDense = 0, kSrcUnionRows = 1, kSrcUnionDown = 2 };
 enum In : int { kInX = 0, kInEmbed = 1 };
-enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiArgmax = 3, kEpiRoute = 4 };
+enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiArgmax = 3 };
 constexpr int kMaxUnion = 64;  // distinct routed experts of one step (top_k * batch at most)
 struct Params {
   int fmt, src, in, epi;
@@ -224,17 +224,15 @@ struct Params {
   int* ids_out;             // [B]
   int* len_inc[kMaxB];      // per token, incremented after the argmax (nullable)
   int n_exp;                // union sources: routed experts in the expert tensors
-  // ---- kEpiRoute (the router: y = logits [B][E + 1]): the last CTA to finish
-  // routes every token (top_k of the E logits, FP32 compare, lowest index on
-  // ties; softmax over the picks; shared gate sigmoid(logit E)) into r_ids
-  // [B][top_k] (nullable), r_w [B][top_k + 1], and the union of the picks
-  // (ascending) with its slot map into union_ids / n_union / slot_of
+  // ---- kSrcUnionRows with route_here: every CTA routes the batch itself from
+  // the stored router logits r_logits [B][r_ld] before its copy lane requests
+  // expert rows (top_k of the r_E logits per token, FP32 compare, lowest index
+  // on ties; softmax over the picks; shared gate sigmoid(logit r_E)); CTA 0
+  // publishes r_ids [B][top_k] (nullable), r_w [B][top_k + 1], and the union
+  // of the picks (ascending) with its slot map in union_ids / n_union / slot_of
   int* r_ids;
   float* r_w;
   int r_E;
-  // ---- kSrcUnionRows with route_here: every CTA routes the batch itself from
-  // the stored router logits r_logits [B][r_ld] (same outputs as kEpiRoute,
-  // published by CTA 0) before its copy lane requests expert rows
   int route_here;
   const float* r_logits;
   int r_ld;
