@@ -54,3 +54,37 @@ def test_moe_step_bytes_counts_selected_experts_only():
 def test_kernels_per_step():
     assert acc.kernels_per_step(workloads.DENSE4B) == 32 * 5 + 1
     assert acc.kernels_per_step(workloads.MOE35B) == 40 * 6 + 1
+
+
+def test_expected_union_against_a_direct_simulation():
+    """E (1 - (1 - k/E)^B): the expected number of distinct experts B tokens
+    pick, each taking k of E uniformly without replacement, checked against
+    sampling (and its end points)."""
+    import numpy as np
+    assert acc.expected_union(256, 8, 1) == 8.0
+    assert abs(acc.expected_union(16, 16, 3) - 16.0) < 1e-12
+    rng = np.random.default_rng(0)
+    E, k, B = 256, 8, 8
+    sizes = [len(set(np.concatenate([rng.choice(E, k, replace=False) for _ in range(B)]))) for _ in range(4000)]
+    assert abs(np.mean(sizes) - acc.expected_union(E, k, B)) < 0.3  # 57.42; sampling error ~0.05
+
+
+def test_batch_step_bytes_count_the_union_once_and_each_sequence_state_and_kv():
+    s = workloads.MOE35B_Q4
+    ctx = [1000, 2000, 3000, 4000]
+    one = acc.step_bytes(s, 0, 10)
+    b = acc.batch_step_bytes(s, ctx, 10)
+    assert b.state == len(ctx) * one.state
+    assert b.kv_read == acc.kv_bytes_per_token(10, s.attn_kv_heads, s.head_dim) * sum(ctx)
+    assert b.kv_write == len(ctx) * one.kv_write
+    # the weights once, plus one embedding row per further token
+    assert b.weights == one.weights + (len(ctx) - 1) * s.hidden * acc.BF16
+    # a fractional union adds that fraction of one expert's three matrices per layer
+    per_exp = 3 * acc.linear_bytes(s.expert_ffn, s.hidden, 1)
+    frac = acc.batch_step_bytes(s, ctx, 10.25)
+    assert frac.weights - b.weights == round(s.n_layers * per_exp * 0.25)
+
+
+def test_batch_gemv_bytes():
+    assert acc.gemv_batch_bytes(16, 256, 8, 0) == 16 * 256 * 2 + 8 * (256 + 16) * 4
+    assert acc.gemv_batch_bytes(16, 256, 8, 1) == 16 * 128 + 16 * 8 * 2 + 8 * (256 + 16) * 4

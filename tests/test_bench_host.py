@@ -1,0 +1,32 @@
+"""Host-side pieces of bench.py: the timing statistics and the bounded oracle
+sample (no GPU)."""
+import math
+
+import bench
+
+
+def test_window_stats_mean_cv_and_interval():
+    w = [0.010, 0.011, 0.0105, 0.0102, 0.0099, 0.0101, 0.0100]  # seconds per 10-step window
+    st = bench.window_stats(w, 10, 70)
+    ms = [x / 10 * 1e3 for x in w]
+    m = sum(ms) / len(ms)
+    sd = math.sqrt(sum((x - m) ** 2 for x in ms) / (len(ms) - 1))
+    assert st["windows"] == 7 and abs(st["ms_per_step_mean"] - m) < 1e-12
+    assert abs(st["cv"] - sd / m) < 1e-12
+    lo, hi = st["ci95_ms_per_step"]
+    assert abs((hi - lo) / 2 - 2.447 * sd / math.sqrt(7)) < 1e-12  # Student t, 6 degrees of freedom
+    assert st["cv_over_5pct"] is False
+
+
+def test_window_stats_drop_a_partial_last_window():
+    st = bench.window_stats([0.01, 0.01, 0.005], 10, 25)  # the third window held 5 steps
+    assert st["windows"] == 2
+
+
+def test_oracle_sample_is_bounded_and_counts_its_tokens():
+    from synth import workloads
+    shape = workloads.WORKLOADS["tiny"].shape
+    tps, cores, n, dt = bench.oracle_decode_sample(shape, 16, budget_s=0.0, max_tokens=3, warm=False)
+    assert n == 3 and cores >= 1 and tps > 0 and abs(tps - n / dt) < 1e-6 * tps
+    tps, cores, n, dt = bench.oracle_decode_sample(shape, 16, budget_s=0.0, max_tokens=5)
+    assert n == 1  # the warm token sizes the sample to the budget: at least one token
