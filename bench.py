@@ -1,12 +1,19 @@
 #!/usr/bin/env python
-"""Decode benchmark: batch-1 greedy decode tokens/s of a hybrid Gated-DeltaNet /
-GQA / MoE model on one GB300, and achieved HBM GB/s as a fraction of the
-measured peak.
+"""Decode benchmark: decode tokens/s of a hybrid Gated-DeltaNet / GQA / MoE
+model on one GB300, and achieved HBM GB/s as a fraction of the measured peak.
 
-Default workload: the dense 4B-shaped hybrid (32 layers, 3:1 DeltaNet:GQA,
-hidden 2560, FFN 9216, vocab 151936) with seeded synthetic bf16 weights and a
-random 4096-token prompt; the timed region is --steps greedy decode steps
-(one CUDA-graph launch each, the argmax fed back on the device).
+Workloads (--workload), seeded synthetic weights and inputs of the configs'
+shapes:
+  dense4b (default)  dense 4B-shaped hybrid (32 layers, 3:1 DeltaNet:GQA, hidden
+                     2560, FFN 9216, vocab 151936), bf16, random 4096-token
+                     prompt, then --steps greedy steps (one CUDA-graph launch
+                     each, the argmax fed back on the device);
+  dense4b-32k        the same at context 32768 (seeded cache fill), with the
+                     split-KV sweep and tokens/s per 32-token window;
+  moe35b             MoE 35B-A3B-shaped hybrid, bf16, 2048-token prompt;
+  moe35b-q4-b8       its 4-bit form at batch 8, ragged contexts 1024..16384
+                     (seeded cache fill), seeded tokens per sequence and step;
+  tiny               the 2-layer test model.
 
 One JSON line on rank 0.  `--impl reference` times the FP64 CPU oracle on the
 same metric and config instead.  With torchrun (N > 1) every rank runs an
