@@ -789,11 +789,11 @@ Plan plan(int R, int C, int fmt, int epi, int nsm, int row_mult) {
 namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-// {128-byte strip, row, strip index} over `rows` rows of a matrix with
-// `row_bytes` bytes per row; box = 16 * GW rows x KS strips.
-bool encode_w(CUtensorMap* m, const void* base, long long rows, int row_bytes, int TR, int KS) {
+// {128-byte strip, row, strip index} over `rows` rows of `width_bytes` of a
+// matrix whose rows are `row_bytes` apart; box = 16 * GW rows x KS strips.
+bool encode_w(CUtensorMap* m, const void* base, long long rows, int row_bytes, int TR, int KS, int width_bytes) {
   if (!base || rows <= 0 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)kStrip, (cuuint64_t)rows, (cuuint64_t)(row_bytes / kStrip)};
+  cuuint64_t dims[3] = {(cuuint64_t)kStrip, (cuuint64_t)rows, (cuuint64_t)(width_bytes / kStrip)};
   cuuint64_t str[2] = {(cuuint64_t)row_bytes, (cuuint64_t)kStrip};
   cuuint32_t box[3] = {(cuuint32_t)kStrip, (cuuint32_t)TR, (cuuint32_t)KS};
   cuuint32_t es[3] = {1, 1, 1};
@@ -801,11 +801,12 @@ bool encode_w(CUtensorMap* m, const void* base, long long rows, int row_bytes, i
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-// The fp16 scales of the same rows: {16 bytes (8 blocks) of a strip, row, strip index}.
-bool encode_s(CUtensorMap* m, const void* base, long long rows, int C, int TR, int KS) {
+// The fp16 scales of the same rows (C columns of a row of ldw):
+// {16 bytes (8 blocks) of a strip, row, strip index}.
+bool encode_s(CUtensorMap* m, const void* base, long long rows, int C, int TR, int KS, int ldw) {
   if (!base || rows <= 0 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
   cuuint64_t dims[3] = {16, (cuuint64_t)rows, (cuuint64_t)(C / 256)};
-  cuuint64_t str[2] = {(cuuint64_t)(C / 16), 16};
+  cuuint64_t str[2] = {(cuuint64_t)(ldw / 16), 16};
   cuuint32_t box[3] = {16, (cuuint32_t)TR, (cuuint32_t)KS};
   cuuint32_t es[3] = {1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, str, box, es,
@@ -837,13 +838,16 @@ cudaError_t launch(const Params& p0, const Plan& pl, cudaStream_t st, bool pdl) 
   p.ks = pl.ks;
   const int TR = kTileRows * pl.gw;
   const int npair = p.epi == kEpiSwiglu ? 2 : 1;
-  const int row_bytes = p.fmt == kFmtQ4 ? p.C / 2 : p.C * 2;
+  const int ldw = p.ldw > 0 ? p.ldw : p.C;  // a dense matrix may be a column slice of a wider one
+  const int width_bytes = p.fmt == kFmtQ4 ? p.C / 2 : p.C * 2;
+  const int row_bytes = p.fmt == kFmtQ4 ? ldw / 2 : ldw * 2;
+  if (ldw < p.C || (p.src != kSrcDense && ldw != p.C) || (p.fmt == kFmtQ4 && ldw % 256)) return cudaErrorInvalidValue;
   alignas(64) Maps mp;
   memset(&mp, 0, sizeof(mp));
   for (int j = 0; j < npair; ++j) {
     if (p.src == kSrcDense) {
-      if (!encode_w(&mp.w[j], p.W[j], p.R, row_bytes, TR, pl.ks)) return cudaErrorInvalidValue;
-      if (p.fmt == kFmtQ4 && !encode_s(&mp.s[j], p.S[j], p.R, p.C, TR, pl.ks)) return cudaErrorInvalidValue;
+      if (!encode_w(&mp.w[j], p.W[j], p.R, row_bytes, TR, pl.ks, width_bytes)) return cudaErrorInvalidValue;
+      if (p.fmt == kFmtQ4 && !encode_s(&mp.s[j], p.S[j], p.R, p.C, TR, pl.ks, ldw)) return cudaErrorInvalidValue;
       continue;
     }
     // union sources: the experts' matrices stacked, and the shared expert's
@@ -851,11 +855,11 @@ cudaError_t launch(const Params& p0, const Plan& pl, cudaStream_t st, bool pdl) 
     if (p.n_exp < 1 || per % TR != 0 || p.exp_stride != per * row_bytes ||
         (p.fmt == kFmtQ4 && p.exp_sstride != per * (p.C / 16)))
       return cudaErrorInvalidValue;
-    if (!encode_w(&mp.ew[j], p.exp_base[j], per * p.n_exp, row_bytes, TR, pl.ks) ||
-        !encode_w(&mp.w[j], p.sh_base[j], per, row_bytes, TR, pl.ks))
+    if (!encode_w(&mp.ew[j], p.exp_base[j], per * p.n_exp, row_bytes, TR, pl.ks, width_bytes) ||
+        !encode_w(&mp.w[j], p.sh_base[j], per, row_bytes, TR, pl.ks, width_bytes))
       return cudaErrorInvalidValue;
-    if (p.fmt == kFmtQ4 && (!encode_s(&mp.es[j], p.exp_scale[j], per * p.n_exp, p.C, TR, pl.ks) ||
-                            !encode_s(&mp.s[j], p.sh_scale[j], per, p.C, TR, pl.ks)))
+    if (p.fmt == kFmtQ4 && (!encode_s(&mp.es[j], p.exp_scale[j], per * p.n_exp, p.C, TR, pl.ks, ldw) ||
+                            !encode_s(&mp.s[j], p.sh_scale[j], per, p.C, TR, pl.ks, ldw)))
       return cudaErrorInvalidValue;
   }
   auto k = p.fmt == kFmtBf16 ? k_bgemv<kFmtBf16> : k_bgemv<kFmtQ4>;

@@ -653,12 +653,37 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
     p.W[j] = (const uint8_t*)t.w;
     p.S[j] = (const uint16_t*)t.scales;
   };
-  // A dense batched GEMV; bf16 matrices too wide for its tiles run per token
-  // through the single-token kernel instead (same epilogue).
+  // A dense batched GEMV.  A bf16 matrix whose token vectors do not fit the
+  // kernel's shared memory, with no RMSNorm on its input (the dense down
+  // projection), runs as column slices of at most 3072 that accumulate into
+  // the output in order; other matrices too wide for it run per token
+  // through the single-token kernel (same epilogue).
   auto dense = [&](bgemv::Params p, const char* what) -> int {
     const bgemv::Plan pl = bgemv::plan(p.R, p.C, p.fmt, p.epi, m->nsm);
     if (pl.ok) return ck(bgemv::launch(p, pl, st, pdl), what);
     if (p.fmt != bgemv::kFmtBf16) return fail(HY_ERR_UNSUPPORTED, "no batched plan for %s (%d x %d)", what, p.R, p.C);
+    if (!p.norm_g && p.in == bgemv::kInX && (p.epi == bgemv::kEpiStore || p.epi == bgemv::kEpiResid) && p.C % 64 == 0) {
+      constexpr int kSlice = 3072;
+      bool slices_ok = true;
+      for (int c0 = 0; c0 < p.C && slices_ok; c0 += kSlice) {
+        const int cc = std::min(kSlice, p.C - c0);
+        slices_ok = bgemv::plan(p.R, cc, p.fmt, bgemv::kEpiResid, m->nsm).ok;
+      }
+      if (slices_ok) {
+        for (int c0 = 0; c0 < p.C; c0 += kSlice) {
+          bgemv::Params q = p;
+          q.C = std::min(kSlice, p.C - c0);
+          q.ldw = p.C;
+          q.W[0] = p.W[0] + (size_t)c0 * 2;
+          q.x = p.x + c0;
+          if (c0 > 0) q.epi = bgemv::kEpiResid;  // later slices add to what the first one stored
+          const bgemv::Plan pq = bgemv::plan(q.R, q.C, q.fmt, q.epi, m->nsm);
+          int rc = ck(bgemv::launch(q, pq, st, pdl), what);
+          if (rc != HY_OK) return rc;
+        }
+        return HY_OK;
+      }
+    }
     for (int b = 0; b < B; ++b) {
       gemv::Params g;
       memset(&g, 0, sizeof(g));

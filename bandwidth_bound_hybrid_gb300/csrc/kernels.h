@@ -207,6 +207,7 @@ struct Params {
   const uint8_t* W[2];      // bf16 [R][C] or packed nibbles [R][C/2] (W[1]: up matrix of a gate/up pair)
   const uint16_t* S[2];     // 4-bit: fp16 scales [R][C/32]
   int R, C, B;
+  int ldw;                  // kSrcDense: elements from one weight row to the next (0: C); C columns are used
   const float* x;           // kInX: [B][ldx]
   int ldx;
   const uint16_t* embed;    // kInEmbed: bf16 [vocab][C]

@@ -178,3 +178,12 @@ def test_experts_read_counts_the_union(built):
     assert layers * shape.top_k <= n <= layers * min(shape.n_experts, B * shape.top_k)
     assert model.experts_read() == 0
     model.close()
+
+
+def test_dense4b_truncated_batch_of_two(built):
+    """bf16 at the dense 4B shape's full widths (hidden 2560, FFN 9216), first
+    2 layers, two sequences: the down projection's 9216-wide token vectors do
+    not fit the kernel's shared memory and run as column slices that
+    accumulate in order."""
+    shape = dataclasses.replace(workloads.DENSE4B, name="dense4b-l2", n_layers=2, attn_layers=(1,), vocab=4096)
+    run(shape, [3, 5], 2)
