@@ -43,7 +43,7 @@ extern "C" {
 #define HY_ERR_CAPACITY 2     /* a sequence would grow past its cache capacity; nothing was launched */
 #define HY_ERR_CUDA 3         /* a CUDA runtime call failed */
 #define HY_ERR_DEVICE_GUARD 4 /* a device-side guard fired (see hy_check_device) */
-#define HY_ERR_UNSUPPORTED 5  /* a shape or option this build does not handle */
+#define HY_ERR_UNSUPPORTED 5  /* a shape or option the library does not handle */
 #define HY_ERR_NOMEM 6        /* device allocation failed */
 
 /* Device guard bits reported by hy_check_device(). */

@@ -1,5 +1,5 @@
 """Byte accounting of a decode step, pinned to the figures the pages print
-(tests/golden/strata_figures.txt) and to the survey's per-config totals."""
+(tests/golden/strata_figures.txt) and to per-config totals worked out from the model shapes."""
 import os
 
 from bandwidth_bound_hybrid_gb300 import accounting as acc
