@@ -117,6 +117,7 @@ struct hy_model {
   bool moe = false, pdl = true, graphs = true, debug = false;
   bool persistent = false;  // the step as one cooperative kernel (when the shape allows it)
   bool q4 = false;          // 4-bit linear weights: every step runs the batched path
+  bool splits_auto = true;  // split-KV count chosen from the SM count (the batched step then scales it down)
 };
 
 struct hy_cache {
@@ -754,7 +755,15 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
       a.nq = cf.attn_q_heads;
       a.nkv = cf.attn_kv_heads;
       a.hd = cf.head_dim;
+      // a batch already spreads over the SMs: fewer splits per sequence (the
+      // largest power of two <= 2 SMs / (kv heads x batch); measured at batch
+      // 8: 16 splits 1903, 32 splits 1884, 8 splits 1845 tokens/s)
       a.nsplit = m->splits;
+      if (m->splits_auto) {
+        int sb = 1;
+        while (2 * sb <= std::max(1, 2 * m->nsm / (cf.attn_kv_heads * B))) sb *= 2;
+        a.nsplit = std::min(m->splits, sb);
+      }
       a.scale = 1.0f / sqrtf((float)cf.head_dim);
       a.part = c->bapart;
       a.counter = c->bcnt_attn;
@@ -1167,6 +1176,7 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
   m->o_len = std::max(m->n_gdn ? c.gdn_heads * c.gdn_dv : 0, m->n_attn ? c.attn_q_heads * c.head_dim : 0);
   m->h_len = m->moe ? (c.top_k + 1) * c.expert_ffn : c.ffn;
   m->splits = c.attn_splits > 0 ? c.attn_splits : attn::auto_splits(c.attn_kv_heads, m->nsm);
+  m->splits_auto = c.attn_splits <= 0;
   m->pdl = !(c.flags & HY_FLAG_NO_PDL);
   m->graphs = !(c.flags & HY_FLAG_NO_GRAPH);
   m->debug = (c.flags & HY_FLAG_DEBUG) != 0;
