@@ -238,12 +238,15 @@ int hy_op_gemv_swiglu(const void* Wg_dev, const void* Wu_dev, int32_t rows, int3
  * y[b] = W * xhat[b] (accumulate != 0: y[b] += ...), or with w_up non-null
  * y[b] = silu(W * xhat[b]) * (W_up * xhat[b]).  xhat[b] = x[b], or its
  * RMSNorm times norm_g.  x_dev [batch][ldx], y_dev [batch][ldy] FP32.
- * weight_format 0: bf16 W.w [rows][cols]; 1: 4-bit blocks of 32 along cols,
- * W.w packed nibbles [rows][cols/2] (byte i of a block holds elements i and
- * i+16 as value+8), W.scales fp16 [rows][cols/32]; cols % 256 == 0.  The
- * products run on the tensor cores with xhat rounded to the MMA operand type
- * (bf16 for bf16 weights, FP16 for 4-bit weights); 4-bit weights are
- * dequantised exactly.  [Strata] "Act 5" (batched decode rows),
+ * weight_format 0: bf16 W.w [rows][cols], cols % 64 == 0; 1: 4-bit blocks of
+ * 32 along cols, W.w packed nibbles [rows][cols/2] (byte i of a block holds
+ * elements i and i+16 as value+8), W.scales fp16 [rows][cols/32],
+ * cols % 256 == 0.  Weight pointers 16-byte aligned.  The products run on the
+ * tensor cores with xhat rounded to the MMA operand type (bf16 hi + lo parts
+ * for bf16 weights, FP16 for 4-bit weights); 4-bit weights are dequantised
+ * exactly.  HY_ERR_UNSUPPORTED (nothing launched) for other cols, or when the
+ * batch's vectors do not fit the kernel's shared memory (bf16 cols above
+ * about 5000).  [Strata] "Act 5" (batched decode rows),
  * [Flash] "Correctness fixes" (the 4-bit block layout). */
 int hy_op_gemv_batch(const hy_tensor* w, const hy_tensor* w_up, int32_t weight_format, int32_t rows, int32_t cols,
                      int32_t batch, const float* x_dev, int32_t ldx, const float* norm_g_dev, float eps, float* y_dev,
