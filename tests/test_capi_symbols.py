@@ -54,3 +54,23 @@ def test_null_arguments_are_rejected_without_a_gpu(built_lib):
     assert b"null" in L.hy_last_error()
     assert L.hy_seq_len(None, 0) == -1
     assert L.hy_decode_step(None, None, None, 1, None, None, None, None) == capi.HY_ERR_ARG
+
+
+def test_new_entry_points_reject_bad_arguments_without_a_gpu(built_lib):
+    """Argument checks come before any device call."""
+    from bandwidth_bound_hybrid_gb300 import capi
+    L = capi.lib()
+    total = ctypes.c_uint64(7)
+    assert L.hy_experts_read(None, None, ctypes.byref(total)) == capi.HY_ERR_ARG
+    assert L.hy_seq_fill_synthetic(None, 0, 16, 1, None) == capi.HY_ERR_ARG
+    assert L.hy_step_kernels(None) == 0
+    w = capi.hy_tensor(None, None)
+    # no weights, batch 0 and 9, a bad format: all refused before a launch
+    args = lambda wt, fmt, batch: (ctypes.byref(wt), None, fmt, 16, 256, batch, None, 256, None, 1e-6, None, 16, 0,
+                                   None)
+    assert L.hy_op_gemv_batch(*args(w, 0, 1)) == capi.HY_ERR_ARG
+    assert L.hy_op_gemv_batch(None, None, 0, 16, 256, 1, None, 256, None, 1e-6, None, 16, 0, None) == capi.HY_ERR_ARG
+    for batch in (0, 9):
+        assert L.hy_op_gemv_batch(*args(w, 0, batch)) == capi.HY_ERR_ARG
+    assert L.hy_op_gemv_batch(*args(w, 2, 1)) == capi.HY_ERR_ARG
+    assert b"batched" in L.hy_last_error()
