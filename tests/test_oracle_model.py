@@ -83,3 +83,26 @@ def test_moe_with_identical_experts_reduces_to_one_ffn():
     rl = r["router_logits"][0][:shape.n_experts]
     np.testing.assert_array_equal(r["router_ids"][0], orc.topk(rl, shape.top_k))
     assert Fe == 32
+
+
+def _unions(shape, n_tok=8):
+    """Distinct experts the router picks per layer for n_tok random tokens
+    (each from an empty cache)."""
+    w = workloads.host_weights(shape)
+    toks = workloads.host.uniform_ids(1, 5, n_tok, shape.vocab)
+    ids = np.array([orc.Oracle(shape, w, 4).forward(int(t), want_hidden=False, want_router=True)["router_ids"]
+                    for t in toks])
+    return [len(set(ids[:, l, :].ravel())) for l in range(shape.n_layers)]
+
+
+def test_4bit_value_distribution_concentrates_routing():
+    """The 4-bit workload's values are uniform in [-8, 7] (mean -0.5), so
+    every 4-bit row carries a common component and the tokens' hidden states
+    come to share a direction: a few layers in, 8 random tokens pick far fewer
+    distinct experts than the 57 of uniform routing.  The bf16 model, whose
+    weights have mean 0, keeps near-uniform routing."""
+    cut = dict(n_layers=5, attn_layers=(3,))
+    q4 = _unions(dataclasses.replace(workloads.MOE35B_Q4, name="q4-l5", **cut))
+    bf = _unions(dataclasses.replace(workloads.MOE35B, name="bf16-l5", **cut))
+    assert min(q4[:2]) >= 45 and max(q4[3:]) <= 25, q4
+    assert min(bf) >= 45, bf
