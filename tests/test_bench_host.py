@@ -30,3 +30,19 @@ def test_oracle_sample_is_bounded_and_counts_its_tokens():
     assert n == 3 and cores >= 1 and tps > 0 and abs(tps - n / dt) < 1e-6 * tps
     tps, cores, n, dt = bench.oracle_decode_sample(shape, 16, budget_s=0.0, max_tokens=5)
     assert n == 1  # the warm token sizes the sample to the budget: at least one token
+
+
+def test_reference_arm_prints_one_contract_line(capsys):
+    """`bench.py --impl reference` (the oracle on the host cores) prints one
+    JSON line with the contract's keys."""
+    import json
+    assert bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "1"]) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["config"]["workload"] and d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
