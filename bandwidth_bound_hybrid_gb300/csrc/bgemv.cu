@@ -102,9 +102,8 @@ __device__ __forceinline__ float4 load4(const float* src, const uint16_t* emb, b
   return make_float4(src[k], src[k + 1], src[k + 2], src[k + 3]);
 }
 
-// Elements k..k+3 (k a multiple of 4) into the staged row: bf16 hi + lo parts,
-// or FP16 at the permuted positions (k -> k/2 and k+2 -> k/2+1 among the evens
-// of the half block, k+1 and k+3 likewise among its odds).
+// Elements k..k+3 (k a multiple of 4) into the staged row: bf16 hi + lo parts
+// in element order, or FP16 in the order the 4-bit B fragments read them.
 __device__ __forceinline__ void store4(int fmt, uint8_t* row, uint8_t* row_lo, int k, float4 v) {
   if (fmt == kFmtBf16) {
     const float f[4] = {v.x, v.y, v.z, v.w};
@@ -131,7 +130,7 @@ __device__ __forceinline__ void store4(int fmt, uint8_t* row, uint8_t* row_lo, i
 }
 
 // Compute warps: token b = warp into xs, RMS-normalised when norm_g is set
-// (FP16, permuted for 4-bit weights; bf16 hi + lo for bf16 weights), zero for
+// (FP16 in fragment order for 4-bit weights; bf16 hi + lo for bf16), zero for
 // padding tokens.  Each warp loads its whole vector at once (up to 2048
 // elements held in registers; longer vectors in two passes), so staging costs
 // about one L2 round trip.  Ends with a barrier of the compute warps.
@@ -377,11 +376,11 @@ __device__ __forceinline__ void am_unkey(unsigned long long k, float& v, int& i)
 }
 
 // Routing of every token of a batch from its router logits (logits [B][ld],
-// row E of a token the shared gate), by the nt = 8 warps' threads tid: warp b
-// picks token b's top_k by repeated warp-wide argmax (largest logit, lowest
-// index on ties: the same set and order as ranking all experts); the union
-// of the picks is an ascending ballot scan over the experts' flags.  `sync`
-// synchronises exactly those threads.
+// row E of a token the shared gate), by the 8 compute warps' threads tid
+// (synchronised with named barrier 1): warp b picks token b's top_k by
+// repeated warp-wide argmax (largest logit, lowest index on ties: the same
+// set and order as ranking all experts); the union of the picks is an
+// ascending ballot scan over the experts' flags.
 constexpr int kRouteMaxE = 512;  // experts + the shared gate per token
 struct RouteShared {
   int sel[kMaxB][16];
@@ -518,8 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
   const bool route_here = p.src == kSrcUnionRows && p.route_here;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // the unit range of this CTA; for MoE sources it depends on the union the
-  // routing kernel wrote, so it is read after griddepcontrol.wait
+  // the unit range of this CTA; for MoE sources it depends on the union: the
+  // one this CTA routed (route_here), or the one the gate/up kernel published,
+  // read after griddepcontrol.wait
   auto unit_range = [&](int& U, int& t0, int& t1) {
     U = 0;
     if (p.src != kSrcDense) {
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bgemv(const __grid_constant__ P
     pdl_launch_dependents();
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      if (p.src != kSrcDense) pdl_wait();  // union and expert ids come from the routing kernel
+      if (p.src != kSrcDense) pdl_wait();  // router logits, union and expert ids come from earlier kernels
       if (route_here && !mbar_wait(rbar, 0)) set_guard(p.guard, kGuardWaitTimeout);  // ... or from this CTA
       const int* uids = route_here ? s_route.uid : p.union_ids;
       int U, t0, t1;
