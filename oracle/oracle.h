@@ -18,8 +18,9 @@
  *
  * Parity pins: every function below is pinned by tests under tests/ against
  * closed forms, invariants, special cases or brute force.  The whole-model
- * composition (orc_forward_token) has no worked example on the pages: beyond
- * its component pins it is parity unpinned.
+ * composition (orc_forward_token) has no worked example on the pages; it is
+ * pinned by a closed form in vectors at the first two positions of a fresh
+ * sequence, and beyond them by its component pins.
  */
 #ifndef HYBRID_ORACLE_H
 #define HYBRID_ORACLE_H
