@@ -125,7 +125,17 @@ def test_4bit_value_distribution_concentrates_routing():
 # and the oracle's whole tokens must equal it.
 
 def _w(b):
-    return gen.bf16_bits_to_f32(np.asarray(b)).astype(np.float64)
+    """Widened weights: bf16 bits, or a 4-bit (packed nibbles, fp16 scale
+    bits) pair: blocks of 32 along the row, byte j of a block holding element
+    j in its low nibble and element j + 16 in its high one, each stored as
+    value + 8, times the block's scale."""
+    if not isinstance(b, tuple):
+        return gen.bf16_bits_to_f32(np.asarray(b)).astype(np.float64)
+    qs, sc = (np.asarray(a) for a in b)
+    blocks = qs.reshape(*qs.shape[:-1], qs.shape[-1] // 16, 16)
+    vals = np.concatenate([blocks & 15, blocks >> 4], axis=-1).astype(np.float64) - 8.0
+    scale = sc.view(np.float16).astype(np.float64)[..., None]
+    return (vals * scale).reshape(*qs.shape[:-1], qs.shape[-1] * 2)
 
 
 def _rms(x, g, eps):
@@ -208,20 +218,22 @@ def _closed_form(shape, w, toks):
             x = x + _w(w[f"l{l}.w_o"]) @ o
             xn = _rms(x, w[f"l{l}.norm2"], eps)
 
-            def ffn(g, u, d, scale=1.0):
-                return scale * (_w(d) @ (_silu(_w(g) @ xn) * (_w(u) @ xn)))
+            def ffn(g, u, d, scale=1.0):  # widened matrices
+                return scale * (d @ (_silu(g @ xn) * (u @ xn)))
 
+            W = lambda n: _w(w[f"l{l}.{n}"])  # noqa: E731
             if shape.ffn > 0:
-                x = x + ffn(w[f"l{l}.w_gate"], w[f"l{l}.w_up"], w[f"l{l}.w_down"])
+                x = x + ffn(W("w_gate"), W("w_up"), W("w_down"))
             else:
                 E, K = shape.n_experts, shape.top_k
-                r = _w(w[f"l{l}.router"]) @ xn
-                ids = np.argsort(-r[:E], kind="stable")[:K]
+                r = W("router") @ xn
+                # the top-k is decided on the logits rounded to FP32, ties to the lower id
+                ids = np.argsort(-r[:E].astype(np.float32), kind="stable")[:K]
                 p = np.exp(r[ids] - r[ids].max())
                 p /= p.sum()
-                d = sum(ffn(w[f"l{l}.exp_gate"][e], w[f"l{l}.exp_up"][e], w[f"l{l}.exp_down"][e], p[t])
-                        for t, e in enumerate(ids))
-                x = x + d + ffn(w[f"l{l}.sh_gate"], w[f"l{l}.sh_up"], w[f"l{l}.sh_down"], _sig(r[E]))
+                eg, eu, ed = W("exp_gate"), W("exp_up"), W("exp_down")
+                d = sum(ffn(eg[e], eu[e], ed[e], p[t]) for t, e in enumerate(ids))
+                x = x + d + ffn(W("sh_gate"), W("sh_up"), W("sh_down"), _sig(r[E]))
             hidden.append(x.copy())
         out.append((np.array(hidden), _w(w["lm_head"]) @ _rms(x, w["final_norm"], eps)))
     return out
@@ -249,3 +261,11 @@ def test_first_two_tokens_moe_match_closed_form():
     shape = dataclasses.replace(TINY, name="moe-tiny-2", vocab=300, ffn=0, n_experts=12, top_k=4,
                                 expert_ffn=64, shared_ffn=96)
     _check_closed_form(shape, ((5, 299), (17, 17)))
+
+
+def test_first_two_tokens_4bit_match_closed_form():
+    dense = dataclasses.replace(TINY, name="tiny-q4", weight_format=1)
+    _check_closed_form(dense, ((0, 77), (9, 9)))
+    moe = dataclasses.replace(dense, name="moe-tiny-q4", vocab=300, ffn=0, n_experts=12, top_k=4, expert_ffn=64,
+                              shared_ffn=96)
+    _check_closed_form(moe, ((5, 299),))
