@@ -164,7 +164,18 @@ int32_t hy_seq_capacity(const hy_cache* c, int32_t seq);
  * cost depends on the lengths only, so benchmarks of long or ragged contexts
  * use this instead of a token-by-token prefill; outputs after it are not
  * those of any prompt.  HY_ERR_CAPACITY if len exceeds the capacity.
- * Stream-ordered. */
+ * Stream-ordered.
+ *
+ * The values, exactly (all integers mod 2^64; mix64 is the SplitMix64 output
+ * function; GOLDEN = 0x9E3779B97F4A7C15): value i of the stream with key k is
+ *   z = mix64(k + (i + 1) * GOLDEN),
+ *   v = (float)(z >> 40) * 2^-23 - 1, times the float scale (FP32 arithmetic).
+ * K (w = 0) and V (w = 1) of attention layer a (0-based among the attention
+ * layers), kv head g: key seed * 1000003 + (2 a + w) * 64 + g, scale 1, element
+ * (row r, column j) is value r * head_dim + j rounded to bf16 (nearest even).
+ * The DeltaNet states of all DeltaNet layers, in the order
+ * [layer][head][dv][dk]: one stream with key seed * 1000003 + 977, scale 0.01.
+ * A host copy of the same values lets a CPU reference start from this state. */
 int hy_seq_fill_synthetic(hy_cache* c, int32_t seq, int32_t len, uint64_t seed, void* stream);
 
 /* Distinct routed experts the batched MoE steps (hy_decode_step with several

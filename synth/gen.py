@@ -132,3 +132,19 @@ def uniform_ids(seed: int, tensor_id: int, n: int, upper: int, start: int = 0) -
 # dequantised weights with RMS ~0.02, like the bfloat16 configurations
 Q4_STD_NIBBLE = math.sqrt(((16 ** 2) - 1) / 12.0 + 0.25)
 Q4_S0 = 0.02 / (1.25 * Q4_STD_NIBBLE)
+
+
+# ------------------------------------------------------ synthetic cache state
+# The generator behind hy_seq_fill_synthetic (a long context without replaying
+# its prompt): value i of the stream keyed by `key` takes the word
+# z = mix64(key + (i + 1) * GOLDEN), keeps its top 24 bits and maps them to
+# (float32(z >> 40) * 2**-23 - 1) * scale, uniform in [-1, 1) * scale.  Every
+# float32 step is exact but the last multiply, one IEEE rounding.
+
+def fill_values(key: int, n: int, scale: float = 1.0) -> np.ndarray:
+    """Values 0 .. n-1 (float32) of the cache-fill stream keyed by ``key``."""
+    i = np.arange(n, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = _mix64_np(np.uint64(key & _MASK) + (i + np.uint64(1)) * np.uint64(GOLDEN))
+    u = (z >> np.uint64(40)).astype(np.float32)
+    return (u * np.float32(2.0 ** -23) - np.float32(1.0)) * np.float32(scale)

@@ -257,5 +257,32 @@ def ragged_contexts(w: Workload) -> np.ndarray:
     return lo + host.uniform_ids(w.context_seed, CONTEXT_TID, w.batch, hi - lo + 1)
 
 
+# Keys of hy_seq_fill_synthetic's streams: K (w = 0) or V (w = 1) of
+# attention layer a, kv head g, rows [0, length) row-major over [length, hd];
+# the DeltaNet states of all layers as one stream [n_gdn][nh][dv][dk] at scale
+# 0.01; conv rings zero.
+FILL_SEED_MULT = 1000003
+FILL_STATE_KEY = 977
+FILL_STATE_SCALE = 0.01
+
+
+def synthetic_cache(s: ModelShape, length: int, seed: int) -> dict:
+    """Host copy of the cache contents hy_seq_fill_synthetic writes: ``k`` and
+    ``v``, one uint16 (bf16 bits) array [nkv, length, hd] per attention layer,
+    and ``state``, float32 [n_gdn, nh, dv, dk]."""
+    n_attn = sum(1 for l in range(s.n_layers) if s.is_attn(l))
+    n_gdn = s.n_layers - n_attn
+    base = seed * FILL_SEED_MULT
+    out = {"k": [], "v": []}
+    for a in range(n_attn):
+        for w, name in ((0, "k"), (1, "v")):
+            heads = [gen.f32_to_bf16_bits(gen.fill_values(base + (a * 2 + w) * 64 + g, length * s.head_dim))
+                     .reshape(length, s.head_dim) for g in range(s.attn_kv_heads)]
+            out[name].append(np.stack(heads) if heads else np.zeros((0, length, s.head_dim), np.uint16))
+    out["state"] = gen.fill_values(base + FILL_STATE_KEY, n_gdn * s.gdn_heads * s.gdn_dv * s.gdn_dk,
+                                   FILL_STATE_SCALE).reshape(n_gdn, s.gdn_heads, s.gdn_dv, s.gdn_dk)
+    return out
+
+
 def param_count(s: ModelShape) -> int:
     return sum(sp.rows * sp.cols for sp in tensor_specs(s))

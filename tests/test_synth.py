@@ -59,3 +59,38 @@ def test_tensor_table_parameter_counts():
     m = workloads.MOE35B
     assert sum(1 for l in range(40) if m.is_attn(l)) == 10
     assert {t.name: t for t in workloads.tensor_specs(m)}["l0.router"].dims == (257, 2048)
+
+
+def test_cache_fill_values_follow_their_definition():
+    """The cache-fill stream: value i is the top 24 bits of the i-th
+    SplitMix64 output of a generator seeded with the key, mapped to
+    [-1, 1) * scale; checked element by element through the scalar
+    SplitMix64 of this module and exact rational arithmetic."""
+    from fractions import Fraction
+    key = 123456789 * workloads.FILL_SEED_MULT + 3 * 64 + 1
+    v = gen.fill_values(key, 4096, 1.0)
+    for i in (0, 1, 2, 77, 4095):
+        z = gen.mix64_int(key + (i + 1) * gen.GOLDEN)
+        assert Fraction(float(v[i])) == Fraction(z >> 40, 1 << 23) - 1
+    assert v.dtype == np.float32 and v.min() >= -1.0 and v.max() < 1.0
+    assert abs(float(v.mean())) < 0.05 and abs(float(v.var()) - 1 / 3) < 0.02
+    s = gen.fill_values(key, 4096, 0.01)
+    np.testing.assert_array_equal(s, v * np.float32(0.01))
+
+
+def test_synthetic_cache_layout():
+    """Host copy of hy_seq_fill_synthetic: one K and one V array per attention
+    layer, [nkv, length, hd] bf16 bits, each kv head its own stream from row
+    0; the DeltaNet states one stream over [n_gdn, nh, dv, dk]."""
+    s = workloads.TINY
+    c = workloads.synthetic_cache(s, 37, seed=5)
+    assert len(c["k"]) == len(c["v"]) == 1
+    assert c["k"][0].shape == (s.attn_kv_heads, 37, s.head_dim) and c["k"][0].dtype == np.uint16
+    base = 5 * workloads.FILL_SEED_MULT
+    np.testing.assert_array_equal(c["v"][0][1].ravel(),
+                                  gen.f32_to_bf16_bits(gen.fill_values(base + 1 * 64 + 1, 37 * s.head_dim)))
+    longer = workloads.synthetic_cache(s, 50, seed=5)
+    np.testing.assert_array_equal(longer["k"][0][:, :37], c["k"][0])  # rows do not depend on the length
+    assert c["state"].shape == (1, s.gdn_heads, s.gdn_dv, s.gdn_dk) and c["state"].dtype == np.float32
+    assert np.abs(c["state"]).max() < workloads.FILL_STATE_SCALE
+    assert not np.array_equal(workloads.synthetic_cache(s, 37, seed=6)["k"][0], c["k"][0])

@@ -7,8 +7,8 @@ a caller workspace.
 Checked through the C ABI against hy_op_attention on the same inputs, on two
 calls in a row with different shapes (the second call finds the first call's
 leftovers in the shared array), plus the size limit.  This file is named to
-be collected last, so that a run stopping at its first failure has run every
-other test before it.
+be collected after the other parity files (only the full-size ones follow),
+so that a run stopping at its first failure has run them before it.
 """
 import numpy as np
 import pytest

@@ -1,0 +1,173 @@
+"""Full-size parity: every model at its full depth, widths and context,
+through the C ABI, against the FP64 oracle, in the launch configuration the
+benchmark times: one kernel per operation in one CUDA graph per step,
+programmatic dependent launch, the automatic split count, no debug copies
+(except in the bf16 MoE test, below).
+
+Both sides start from the same long context without replaying a prompt: the
+device fills its caches with hy_seq_fill_synthetic, and the oracle's caches
+receive the host copy of that generator (``synth.workloads.synthetic_cache``,
+counter-based, bit-identical).  Compared per step and sequence: the final
+logits (relative L2 <= 1e-2) and the greedy id wherever the oracle's top-2
+margin exceeds 0.05.  Every sequence consumes its oracle's greedy token.
+
+Routing near-ties.  Where the k-th and (k+1)-th router logits of a layer lie
+within rounding of each other, either expert set is correct, and the two
+sides may legitimately pick differently.  The bf16 MoE model runs with debug
+copies so that the device's expert set of every layer is visible: a set that
+differs from the oracle's is allowed only at a near-tie (gap <= 1e-3 of the
+largest logit), and ends that sequence's comparison, since its caches may now
+differ.  The 4-bit MoE model routes with frequent near-ties (gaps of 1e-4 to
+1e-3 of the largest logit at full depth) but its outputs hardly depend on
+them: flipping every one of them in the oracle moves the final logits by less
+than 1e-3 relative L2, so its batch is compared at every step as it runs.
+
+The file sorts last so that the quicker parity tests run first.
+"""
+import gc
+
+import numpy as np
+import pytest
+
+from oracle import oracle as orc
+from synth import workloads
+from tests.gpu_util import rel_l2, to_np
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+HIDDEN_TOL, LOGIT_TOL, ID_MARGIN, ROUTER_REL_GAP = 5e-3, 1e-2, 0.05, 1e-3
+START_SEED = 11
+
+
+@pytest.fixture(scope="module")
+def built(gpu):
+    from bandwidth_bound_hybrid_gb300 import build
+    build.build()
+    return True
+
+
+def oracle_at(shape, host_w, capacity, context, seed):
+    """An oracle whose cache holds the synthetic context hy_seq_fill_synthetic
+    writes for (context, seed)."""
+    o = orc.Oracle(shape, host_w, capacity)
+    cache = workloads.synthetic_cache(shape, context, seed)
+    for a, (k, v) in enumerate(zip(cache["k"], cache["v"])):
+        K, V = o.kv_cache(a)
+        K[:, :context] = k
+        V[:, :context] = v
+    for gi in range(cache["state"].shape[0]):
+        o.gdn_state(gi)[:] = cache["state"][gi]
+    o.cache.len = context
+    return o
+
+
+def routing_agrees(out, device_sets, shape) -> bool:
+    """True where the device picked the oracle's expert set in every layer;
+    False where it differs only at near-ties; fails otherwise."""
+    E, K = shape.n_experts, shape.top_k
+    same = True
+    for l, dev in enumerate(device_sets):
+        ref = set(int(i) for i in out["router_ids"][l])
+        if dev == ref:
+            continue
+        srt = np.sort(np.asarray(out["router_logits"][l][:E]))[::-1]
+        gap = srt[K - 1] - srt[K]
+        assert gap <= ROUTER_REL_GAP * max(1.0, abs(srt[0])), \
+            f"layer {l}: device experts {sorted(dev)}, oracle {sorted(ref)}, top-k gap {gap:.3g}"
+        same = False
+    return same
+
+
+def start_tokens(shape, n):
+    return [int(t) for t in workloads.host.uniform_ids(START_SEED, workloads.PROMPT_TID, n, shape.vocab)]
+
+
+def oracle_steps(refs, shape, toks, hidden=False):
+    """One teacher-forced oracle step per sequence; returns the outputs."""
+    return [ref.forward(t, want_hidden=hidden, want_router=shape.is_moe) for ref, t in zip(refs, toks)]
+
+
+def run_full(shape, contexts, steps, batched, debug=False):
+    """Decode `steps` tokens for each of len(contexts) sequences (sequence s
+    filled with seed s + 1); batched: one step for all sequences at once,
+    else one batch-1 step per sequence.  debug (batch-1 steps only): read
+    the device's per-layer hidden states and expert sets after each step.
+    Returns the number of compared (step, sequence) pairs."""
+    import torch
+
+    from bandwidth_bound_hybrid_gb300 import capi
+    from bandwidth_bound_hybrid_gb300.model import HybridModel
+    assert not (batched and debug)
+    B = len(contexts)
+    caps = [c + steps + 1 for c in contexts]
+    model = HybridModel(shape, workloads.device_weights(shape), caps, flags=capi.HY_FLAG_DEBUG if debug else 0)
+    for s, c in enumerate(contexts):
+        model.fill_synthetic(s, c, seed=s + 1)
+    host_w = workloads.host_weights(shape)
+    refs = [oracle_at(shape, host_w, caps[s], c, s + 1) for s, c in enumerate(contexts)]
+    toks = start_tokens(shape, B)
+    logits = torch.empty((B, shape.vocab), dtype=torch.float32, device="cuda")
+    ids = torch.empty(B, dtype=torch.int32, device="cuda")
+    live, compared = [True] * B, 0
+    for step in range(steps):
+        hidden, experts = [None] * B, [None] * B
+        if batched:
+            model.decode_batch(list(range(B)), torch.tensor(toks, dtype=torch.int32, device="cuda"), ids, logits)
+        else:
+            for s in range(B):
+                model.decode_step(s, torch.tensor([toks[s]], dtype=torch.int32, device="cuda"), ids[s:s + 1],
+                                  logits[s])
+                if debug:  # the debug copies hold the last step's; read them before the next sequence's step
+                    hidden[s] = [to_np(model.debug_hidden(l)) for l in range(shape.n_layers)]
+                    if shape.is_moe:
+                        experts[s] = [set(to_np(model.debug_router(l)[1]).tolist()) for l in range(shape.n_layers)]
+        out = oracle_steps(refs, shape, toks, hidden=debug)
+        torch.cuda.synchronize()
+        got, gid = to_np(logits), to_np(ids)
+        for s in range(B):
+            if not live[s]:
+                continue
+            if experts[s] is not None and not routing_agrees(out[s], experts[s], shape):
+                live[s] = False
+                continue
+            if hidden[s] is not None:
+                for l in range(shape.n_layers):
+                    eh = rel_l2(hidden[s][l], out[s]["hidden"][l])
+                    assert eh <= HIDDEN_TOL, f"step {step} sequence {s} layer {l}: hidden rel-L2 {eh:.3g}"
+            e = rel_l2(got[s], out[s]["logits"])
+            assert e <= LOGIT_TOL, f"step {step} sequence {s} (context {contexts[s]}): logits rel-L2 {e:.3g}"
+            srt = np.sort(out[s]["logits"])
+            if srt[-1] - srt[-2] > ID_MARGIN:
+                assert int(gid[s]) == int(orc.argmax(out[s]["logits"])), f"step {step} sequence {s}"
+            compared += 1
+        toks = [int(orc.argmax(o["logits"])) for o in out]
+    for s, c in enumerate(contexts):
+        assert model.seq_len(s) == c + steps
+    assert model.check_device() == 0
+    model.close()
+    del model, refs, host_w
+    gc.collect()
+    torch.cuda.empty_cache()
+    return compared
+
+
+@pytest.mark.parametrize("context", [4096, 32768])
+def test_dense4b_full_size(built, context):
+    """Dense 4B-shaped hybrid, 32 layers, at the context of the benchmark's
+    dense workloads (4096, and 32768 where the split-KV attention dominates)."""
+    assert run_full(workloads.DENSE4B, [context], steps=3, batched=False) == 3
+
+
+def test_moe35b_full_size(built):
+    """MoE 35B-A3B-shaped hybrid, 40 layers, bf16, batch 1 at context 2048:
+    four independent sequences, two steps each, with debug copies (per-layer
+    hidden states and expert sets compared as well)."""
+    assert run_full(workloads.MOE35B, [2048] * 4, steps=2, batched=False, debug=True) >= 1
+
+
+def test_moe35b_q4_batch8_full_size(built):
+    """4-bit MoE, 40 layers, one batched step for the 8 sequences of the
+    benchmark's ragged contexts (1024..16384)."""
+    w = workloads.WORKLOADS["moe35b-q4-b8"]
+    contexts = [int(c) for c in workloads.ragged_contexts(w)]
+    assert run_full(w.shape, contexts, steps=2, batched=True) == 2 * len(contexts)
