@@ -269,3 +269,22 @@ def test_first_two_tokens_4bit_match_closed_form():
     moe = dataclasses.replace(dense, name="moe-tiny-q4", vocab=300, ffn=0, n_experts=12, top_k=4, expert_ffn=64,
                               shared_ffn=96)
     _check_closed_form(moe, ((5, 299),))
+
+
+def test_router_load_is_near_uniform_for_uncorrelated_inputs():
+    """The synthetic router rows (bf16 ~N(0, 0.02) over H = 2048, logit std
+    ~0.9) spread the top-8 picks of uncorrelated inputs evenly: over 4000
+    seeded unit-RMS inputs, the busiest of the 256 experts takes at most 1.5x
+    the mean load, in the first, a middle and the last layer (Poisson noise
+    alone puts the maximum near 1.3x)."""
+    shape = workloads.MOE35B
+    E, K, H = shape.n_experts, shape.top_k, shape.hidden
+    X = np.random.default_rng(2024).standard_normal((4000, H))
+    for l in (0, shape.n_layers // 2, shape.n_layers - 1):
+        name = f"l{l}.router"
+        W = gen.bf16_bits_to_f32(workloads.host_weights(shape, names=[name])[name]).astype(np.float64)
+        logits = X @ W[:E].T
+        assert 0.8 < logits.std() < 1.0
+        counts = np.bincount(np.concatenate([orc.topk(r, K) for r in logits]), minlength=E)
+        assert counts.sum() == 4000 * K and counts.min() > 0
+        assert counts.max() / counts.mean() <= 1.5, (l, counts.max() / counts.mean())
