@@ -25,6 +25,7 @@ than 1e-3 relative L2, so its batch is compared at every step as it runs.
 The file sorts last so that the quicker parity tests run first.
 """
 import gc
+import os
 
 import numpy as np
 import pytest
@@ -44,6 +45,39 @@ def built(gpu):
     from bandwidth_bound_hybrid_gb300 import build
     build.build()
     return True
+
+
+def host_bytes_available() -> int:
+    """Memory this process may still take: the smaller of MemAvailable and
+    the cgroup's limit minus its current use (where a limit is set)."""
+    avail = None
+    with open("/proc/meminfo") as f:
+        for ln in f:
+            if ln.startswith("MemAvailable:"):
+                avail = int(ln.split()[1]) * 1024
+    for lim_p, cur_p in (("/sys/fs/cgroup/memory.max", "/sys/fs/cgroup/memory.current"),
+                         ("/sys/fs/cgroup/memory/memory.limit_in_bytes", "/sys/fs/cgroup/memory/memory.usage_in_bytes")):
+        try:
+            with open(lim_p) as f:
+                lim = f.read().strip()
+            with open(cur_p) as f:
+                cur = int(f.read().strip())
+        except (OSError, ValueError):
+            continue
+        if lim.isdigit() and int(lim) < (1 << 60):
+            room = int(lim) - cur
+            avail = room if avail is None else min(avail, room)
+        break
+    return avail if avail is not None else 1 << 62
+
+
+def need_host_memory(shape):
+    """Skip (rather than be killed) where the host copy of the weights, which
+    the oracle reads, does not fit with a margin."""
+    need = int(1.3 * sum(sp.nbytes() for sp in workloads.tensor_specs(shape))) + (4 << 30)
+    have = host_bytes_available()
+    if have < need:
+        pytest.skip(f"host memory: {have / 2**30:.0f} GiB available, the oracle's weights need {need / 2**30:.0f} GiB")
 
 
 def oracle_at(shape, host_w, capacity, context, seed):
@@ -98,6 +132,7 @@ def run_full(shape, contexts, steps, batched, debug=False):
     from bandwidth_bound_hybrid_gb300 import capi
     from bandwidth_bound_hybrid_gb300.model import HybridModel
     assert not (batched and debug)
+    need_host_memory(shape)
     B = len(contexts)
     caps = [c + steps + 1 for c in contexts]
     model = HybridModel(shape, workloads.device_weights(shape), caps, flags=capi.HY_FLAG_DEBUG if debug else 0)
