@@ -186,6 +186,21 @@ def run_full(shape, contexts, steps, batched, debug=False):
     return compared
 
 
+# a tiny MoE hybrid whose widths suit the 4-bit batched path (multiples of 256)
+TINY_MOE_Q4 = workloads.ModelShape("tiny-moe-q4-fill", n_layers=2, hidden=256, vocab=1024, ffn=0, gdn_heads=4,
+                                   gdn_dk=64, gdn_dv=64, attn_q_heads=4, attn_kv_heads=2, head_dim=64,
+                                   attn_layers=(1,), n_experts=16, top_k=4, expert_ffn=256, shared_ffn=256,
+                                   weight_format=1)
+
+
+def test_synthetic_context_matches_its_host_copy(built):
+    """Seconds-long check of the mechanism the full-size tests rest on: a
+    tiny model decodes from a synthetic context on both sides (batch 1 with
+    per-layer hidden states, and a 4-bit batch of three)."""
+    assert run_full(workloads.TINY, [100], steps=3, batched=False, debug=True) == 3
+    assert run_full(TINY_MOE_Q4, [50, 77, 120], steps=2, batched=True) == 6
+
+
 @pytest.mark.parametrize("context", [4096, 32768])
 def test_dense4b_full_size(built, context):
     """Dense 4B-shaped hybrid, 32 layers, at the context of the benchmark's
