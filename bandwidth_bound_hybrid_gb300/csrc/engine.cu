@@ -1381,6 +1381,12 @@ namespace {
 // Checks of a decode step's sequence list (distinct, valid, not full).
 int check_seqs(hy_cache* c, const int32_t* seqs_host, int32_t nseq, std::vector<int>& seqs) {
   if (nseq < 1 || nseq > bgemv::kMaxB) return fail(HY_ERR_ARG, "nseq must be in 1..%d", bgemv::kMaxB);
+  const hy_model* m = c->m;
+  // the batched MoE step keeps the union of the tokens' picks in kMaxUnion
+  // slots; refuse here, before any launch, rather than part-way through a step
+  if (m->moe && (nseq > 1 || m->q4) && nseq * m->cfg.top_k > bgemv::kMaxUnion)
+    return fail(HY_ERR_UNSUPPORTED, "a batched MoE step holds at most %d routed picks: %d sequences x top_k %d",
+                bgemv::kMaxUnion, nseq, m->cfg.top_k);
   seqs.assign(seqs_host, seqs_host + nseq);
   for (int i = 0; i < nseq; ++i) {
     if (!valid_seq(c, seqs[i])) return fail(HY_ERR_ARG, "bad sequence handle %d", seqs[i]);

@@ -208,7 +208,9 @@ int hy_prefill(hy_model* m, hy_cache* c, int32_t seq, const int32_t* tokens_dev,
  * batched decode rows).  The first call for a given (sequence list,
  * logits_dev, ids_dev) captures a CUDA graph; later calls replay it: one
  * graph launch per step ([Strata] "Act 0", pass 3).  HY_ERR_CAPACITY
- * (nothing launched) if a sequence is full. */
+ * (nothing launched) if a sequence is full; HY_ERR_UNSUPPORTED (nothing
+ * launched) if a batched MoE step would hold more than 64 routed picks
+ * (nseq x top_k > 64). */
 int hy_decode_step(hy_model* m, hy_cache* c, const int32_t* seqs_host, int32_t nseq, const int32_t* tokens_dev,
                    float* logits_dev, int32_t* ids_dev, void* stream);
 
