@@ -259,7 +259,7 @@ int hy_op_gemv_swiglu(const void* Wg_dev, const void* Wu_dev, int32_t rows, int3
  * for bf16 weights, FP16 for 4-bit weights); 4-bit weights are dequantised
  * exactly.  HY_ERR_UNSUPPORTED (nothing launched) for other cols, or when the
  * batch's vectors do not fit the kernel's shared memory (bf16 cols above
- * 5824, or 4672 with w_up).  [Strata] "Act 5" (batched decode rows),
+ * 5824, or 4672 with w_up; 4-bit cols above 11264, or 8704 with w_up).  [Strata] "Act 5" (batched decode rows),
  * [Flash] "Correctness fixes" (the 4-bit block layout). */
 int hy_op_gemv_batch(const hy_tensor* w, const hy_tensor* w_up, int32_t weight_format, int32_t rows, int32_t cols,
                      int32_t batch, const float* x_dev, int32_t ldx, const float* norm_g_dev, float eps, float* y_dev,

@@ -74,3 +74,41 @@ def test_new_entry_points_reject_bad_arguments_without_a_gpu(built_lib):
         assert L.hy_op_gemv_batch(*args(w, 0, batch)) == capi.HY_ERR_ARG
     assert L.hy_op_gemv_batch(*args(w, 2, 1)) == capi.HY_ERR_ARG
     assert b"batched" in L.hy_last_error()
+
+
+def test_config_limits_are_checked_before_any_device_call(built_lib):
+    """hy_model_create checks the config before it looks at weights or the
+    device: a config past a documented limit gets its error code, one at the
+    limit passes on to the weight checks (here: an empty weight table)."""
+    import dataclasses
+
+    from bandwidth_bound_hybrid_gb300 import capi
+    from bandwidth_bound_hybrid_gb300.model import make_config
+    from synth import workloads
+    L = capi.lib()
+    moe = dataclasses.replace(workloads.MOE35B, n_layers=4, attn_layers=(3,))
+
+    def create(shape, **over):
+        cfg = make_config(shape)
+        for k, v in over.items():
+            setattr(cfg, k, v)
+        out = ctypes.c_void_p()
+        rc = L.hy_model_create(ctypes.byref(cfg), ctypes.byref(capi.hy_weights()), ctypes.byref(out))
+        assert not out.value
+        return rc, L.hy_last_error().decode()
+
+    at_limit = (capi.HY_ERR_ARG, "weights.layers is null")
+    assert create(moe, n_experts=511) == at_limit
+    assert create(moe, n_experts=512)[0] == capi.HY_ERR_UNSUPPORTED
+    assert create(moe, top_k=16) == at_limit
+    assert create(moe, top_k=17)[0] == capi.HY_ERR_ARG
+    assert create(moe, shared_ffn=1024)[0] == capi.HY_ERR_UNSUPPORTED
+    dense = workloads.DENSE4B
+    assert create(dense) == at_limit
+    assert create(dense, n_layers=65)[0] == capi.HY_ERR_ARG
+    assert create(dense, head_dim=96)[0] == capi.HY_ERR_UNSUPPORTED
+    assert create(dense, attn_kv_heads=1)[0] == capi.HY_ERR_UNSUPPORTED  # 16 q heads per kv head
+    assert create(dense, gdn_dk=32)[0] == capi.HY_ERR_UNSUPPORTED
+    q4 = dataclasses.replace(dense, weight_format=1)
+    assert create(q4) == at_limit
+    assert create(q4, hidden=2560 + 128)[0] == capi.HY_ERR_UNSUPPORTED
