@@ -46,3 +46,15 @@ def test_reference_arm_prints_one_contract_line(capsys):
     assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
     assert d["config"]["workload"] and d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_traffic_lines_come_only_from_current_captures():
+    """The roofline's DRAM traffic is read from profiles/traffic.txt: comment
+    lines are skipped, the dense and MoE GEMV captures are found, and the
+    batched GEMV, whose counters predate later changes to its kernel, has no
+    line (the bench reports null)."""
+    import bench
+    assert bench.load_traffic("gemv_swiglu", "dense4b") == 94498560
+    assert bench.load_traffic("gemv_in", "moe35b") == 25360128
+    assert bench.load_traffic("gemv_batch", "moe35b-q4-b8") is None
+    assert bench.load_traffic("gemv_swiglu", "no-such-workload") is None
