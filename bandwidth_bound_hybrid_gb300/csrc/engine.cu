@@ -56,7 +56,6 @@ int ensure_init(int dev) {
   if (g_inited[dev]) return HY_OK;
   HY_CK(gemv::init());
   HY_CK(attn::init());
-  HY_CK(step::init());
   HY_CK(bgemv::init());
   g_inited[dev] = true;
   return HY_OK;
@@ -115,7 +114,6 @@ struct hy_model {
   int y_len = 0, o_len = 0, h_len = 0;
   int splits = 1;
   bool moe = false, pdl = true, graphs = true, debug = false;
-  bool persistent = false;  // the step as one cooperative kernel (when the shape allows it)
   bool q4 = false;          // 4-bit linear weights: every step runs the batched path
   bool splits_auto = true;  // split-KV count chosen from the SM count (the batched step then scales it down)
 };
@@ -132,13 +130,12 @@ struct hy_cache {
   float *x = nullptr, *y = nullptr, *o = nullptr, *h = nullptr, *part = nullptr, *am_val = nullptr;
   float *rlog = nullptr, *moe_w = nullptr, *logits_buf = nullptr;
   int *am_idx = nullptr, *tok = nullptr, *ids = nullptr, *moe_ids = nullptr;
-  unsigned *cnt_attn = nullptr, *cnt_am = nullptr, *cnt_router = nullptr, *guard = nullptr;
+  unsigned *cnt_attn = nullptr, *cnt_am = nullptr, *guard = nullptr;
   float2* rope = nullptr;
   float *dbg_hidden = nullptr, *dbg_rlog = nullptr;
   int* dbg_rids = nullptr;
   std::vector<void*> allocs;
   cudaStream_t cap_stream = nullptr;
-  unsigned* step_bar = nullptr;  // grid barrier of the persistent step kernel
   // batched steps (several sequences, or 4-bit weights): per-token scratch
   float *bx = nullptr, *by = nullptr, *bo = nullptr, *bh = nullptr, *brlog = nullptr, *bw = nullptr;
   float *bpart = nullptr, *bapart = nullptr, *bam_val = nullptr;
@@ -156,14 +153,6 @@ struct hy_cache {
   };
   std::vector<BGraph> bgraphs;
   int last_kernels = 0;          // kernels of the last recorded step
-  struct Prog {
-    int seq;
-    float* logits;
-    int* ids;
-    step::Phase* dev;
-    step::Program pr;
-  };
-  std::vector<Prog> progs;
   struct Graph {
     int seq;
     float* logits;
@@ -262,11 +251,10 @@ int launch_ops(hy_model* m, std::vector<StepOp>& ops, cudaStream_t st) {
   return HY_OK;
 }
 
-// The operations of one decode step for sequence `seq`, in order.
-// route_in_experts: the router GEMV only stores its logits and the expert
-// gate/up kernel's CTAs pick the experts themselves (kernel-per-operation
-// steps); otherwise the router's last CTA picks them (persistent step).
-int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepOp>& ops, bool route_in_experts) {
+// The operations of one decode step for sequence `seq`, in order.  The MoE
+// router GEMV only stores its logits; the expert gate/up kernel's CTAs pick
+// the experts themselves.
+int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepOp>& ops) {
   hy_model* m = c->m;
   const hy_config& cf = m->cfg;
   const int H = cf.hidden;
@@ -393,24 +381,8 @@ int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepO
       r.C = H;
       r.x = c->x;
       r.norm_g = L.norm2;
-      r.router_logits = c->rlog;
-      r.out_ids = c->moe_ids;
-      r.out_w = c->moe_w;
-      r.counter = c->cnt_router;
-      r.n_experts = E;
-      r.top_k = K;
-      if (m->debug) {
-        r.dbg_ids = c->dbg_rids + (size_t)l * K;
-        r.dbg_logits = c->dbg_rlog + (size_t)l * (E + 1);
-      }
-      if (route_in_experts) {
-        r.y = c->rlog;
-        r.dbg_ids = nullptr;
-        r.dbg_logits = nullptr;
-        if ((rc = run(r, gemv::kSrcDense, gemv::kInX, gemv::kEpiStore, "router")) != HY_OK) return rc;
-      } else if ((rc = run(r, gemv::kSrcDense, gemv::kInX, gemv::kEpiRouter, "router")) != HY_OK) {
-        return rc;
-      }
+      r.y = c->rlog;
+      if ((rc = run(r, gemv::kSrcDense, gemv::kInX, gemv::kEpiStore, "router")) != HY_OK) return rc;
       gemv::Params gu = gemv_base();
       gu.exp_base[0] = (const uint8_t*)L.exp_gate.w;
       gu.exp_base[1] = (const uint8_t*)L.exp_up.w;
@@ -427,15 +399,13 @@ int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepO
       gu.x = c->x;
       gu.norm_g = L.norm2;
       gu.y = c->h;
-      if (route_in_experts) {
-        gu.route_here = 1;
-        gu.router_logits = c->rlog;
-        gu.out_ids = c->moe_ids;
-        gu.out_w = c->moe_w;
-        if (m->debug) {
-          gu.dbg_ids = c->dbg_rids + (size_t)l * K;
-          gu.dbg_logits = c->dbg_rlog + (size_t)l * (E + 1);
-        }
+      gu.route_here = 1;
+      gu.router_logits = c->rlog;
+      gu.out_ids = c->moe_ids;
+      gu.out_w = c->moe_w;
+      if (m->debug) {
+        gu.dbg_ids = c->dbg_rids + (size_t)l * K;
+        gu.dbg_logits = c->dbg_rlog + (size_t)l * (E + 1);
       }
       if ((rc = run(gu, gemv::kSrcExpertRows, gemv::kInX, gemv::kEpiSwiglu, "expert gate/up")) != HY_OK) return rc;
       gemv::Params dn = gemv_base();
@@ -482,143 +452,11 @@ int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepO
   return HY_OK;
 }
 
-int env_kb(const char* name, int dflt_kb) {
-  const char* v = getenv(name);
-  return ((v && *v) ? atoi(v) : dflt_kb) * 1024;
-}
-
-// The step's operations as phases of the persistent kernel; false when some
-// operation has no persistent form (the step then runs one kernel per
-// operation).
-bool build_program(hy_cache* c, const std::vector<StepOp>& ops, std::vector<step::Phase>& phases,
-                   step::Program& pr) {
-  hy_model* m = c->m;
-  const hy_config& cf = m->cfg;
-  memset(&pr, 0, sizeof(pr));
-  pr.hd = m->n_attn ? cf.head_dim : 64;
-  pr.G = m->n_attn ? cf.attn_q_heads / cf.attn_kv_heads : 2;
-  pr.epl = m->n_gdn ? cf.gdn_dk / 32 : (pr.hd == 64 ? 2 : 4);
-  if (!step::supported(pr.hd, pr.G, pr.epl)) return false;
-  const int pf = env_kb("HY_STEP_PREFETCH_KB", 128);
-  size_t region = 0, scratch = 1;
-  int stage = 0;
-  int routed_after = 0;  // phases up to the last router: the routed experts' rows depend on them
-  phases.assign(ops.size(), step::Phase());
-  for (size_t i = 0; i < ops.size(); ++i) {
-    const StepOp& o = ops[i];
-    step::Phase& ph = phases[i];
-    memset(&ph, 0, sizeof(ph));
-    if (o.kind == StepOp::kGemv) {
-      const int npair = o.epi == gemv::kEpiSwiglu ? 2 : 1;
-      const gemv::Plan pl = gemv::plan(o.g.R, o.g.C, npair, m->nsm, o.g.norm_g != nullptr);
-      if (!pl.ok || pl.vpl > 5 || !pl.full) return false;
-      ph.kind = step::kGemv;
-      ph.src = o.src;
-      ph.in = o.in;
-      ph.epi = o.epi;
-      ph.vpl = pl.vpl;
-      ph.full = 1;
-      if (o.epi == gemv::kEpiRouter) routed_after = (int)i + 1;
-      if (o.src != gemv::kSrcDense) ph.after = routed_after;
-      ph.g = o.g;
-      ph.g.n_nx = 0;
-      ph.g.ncta = pl.ncta;
-      ph.g.tile_rows = pl.tile_rows;
-      ph.g.nchunk = pl.nchunk;
-      ph.g.chunk_vecs = pl.chunk_vecs;
-      ph.g.stage_bytes = pl.stage_bytes;
-      ph.g.nstages = 0;
-      ph.g.rows_cta_max = pl.rows_cta_max;
-      ph.g.xs_floats = pl.xs_floats;
-      ph.g.gs_floats = pl.gs_floats;
-      ph.g.pre_stages = 0;
-      ph.g.pf_ahead = 0;
-      ph.g.npair = npair;
-      stage = std::max(stage, pl.stage_bytes);
-      region = std::max(region, (size_t)4 * (pl.xs_floats + pl.gs_floats +
-                                              ((pl.rows_cta_max * npair * pl.nchunk + 1) & ~1)));
-      if (o.epi == gemv::kEpiRouter) scratch = std::max(scratch, (size_t)o.g.n_experts + 1);
-    } else if (o.kind == StepOp::kGdn) {
-      if (o.d.dk != 32 * pr.epl) return false;
-      ph.kind = step::kGdn;
-      ph.d = o.d;
-      ph.pf_bytes = pf;
-      region = std::max(region, step::gdn_work_bytes(pr.epl));
-    } else if (o.kind == StepOp::kAttn) {
-      if (o.a.hd != pr.hd || o.a.nq / o.a.nkv != pr.G) return false;
-      ph.kind = step::kAttn;
-      ph.a = o.a;
-      region = std::max(region, step::attn_work_bytes(pr.hd, pr.G));
-      stage = std::max(stage, step::attn_stage_bytes(pr.hd));
-      scratch = std::max(scratch, (size_t)o.a.nsplit * pr.G + pr.G);
-    } else {
-      ph.kind = step::kCopy;
-      ph.csrc = o.csrc;
-      ph.cdst = o.cdst;
-      ph.cn = o.cn;
-    }
-  }
-  pr.nphases = (int)phases.size();
-  pr.bar = c->step_bar;
-  pr.guard = c->guard;
-  pr.stage_bytes = stage;
-  pr.region_bytes = (int)((region + 15) & ~(size_t)15);
-  pr.scratch_floats = (int)scratch;
-  int ns = env_kb("HY_STEP_INFLIGHT_KB", 180) / std::max(stage, 1);
-  ns = std::max(2, std::min(ns, step::kMaxStagesStep));
-  for (pr.nstages = ns; pr.nstages >= 2 && !step::smem_bytes(pr); --pr.nstages) {
-  }
-  if (pr.nstages < 2 || !step::smem_bytes(pr)) return false;
-  return step::blocks_per_sm(pr) >= 1;
-}
-
-// The persistent program of (seq, logits, ids): built and copied to the
-// device on first use.  Allocates, so never call it while capturing.
-int get_program(hy_cache* c, int seq, float* logits, int* ids, const step::Program** out) {
-  *out = nullptr;
-  for (auto& p : c->progs)
-    if (p.seq == seq && p.logits == logits && p.ids == ids) {
-      *out = &p.pr;
-      return HY_OK;
-    }
-  std::vector<StepOp> ops;
-  int rc = collect_ops(c, seq, logits, ids, ops, false);
-  if (rc != HY_OK) return rc;
-  std::vector<step::Phase> phases;
-  step::Program pr;
-  if (!build_program(c, ops, phases, pr)) {
-    c->m->persistent = false;  // this shape runs one kernel per operation
-    return HY_OK;
-  }
-  void* dev = nullptr;
-  HY_CK(cudaMalloc(&dev, phases.size() * sizeof(step::Phase)));
-  cudaError_t e = cudaMemcpy(dev, phases.data(), phases.size() * sizeof(step::Phase), cudaMemcpyHostToDevice);
-  if (e != cudaSuccess) {
-    cudaFree(dev);
-    return fail(HY_ERR_CUDA, "program upload: %s", cudaGetErrorString(e));
-  }
-  pr.phases = reinterpret_cast<step::Phase*>(dev);
-  c->progs.push_back({seq, logits, ids, reinterpret_cast<step::Phase*>(dev), pr});
-  *out = &c->progs.back().pr;
-  return HY_OK;
-}
-
-// Issue one decode step for sequence `seq` on `st`: the persistent kernel
-// (its program must exist), or one kernel per operation.
+// Issue one decode step for sequence `seq` on `st`, one kernel per operation.
 int record_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) {
   hy_model* m = c->m;
-  if (m->persistent) {
-    for (auto& p : c->progs)
-      if (p.seq == seq && p.logits == logits && p.ids == ids) {
-        cudaError_t e = step::launch(p.pr, m->nsm, st);
-        if (e != cudaSuccess) return fail(HY_ERR_CUDA, "step launch: %s", cudaGetErrorString(e));
-        c->last_kernels = 1;
-        return HY_OK;
-      }
-    return fail(HY_ERR_ARG, "no step program for sequence %d", seq);
-  }
   std::vector<StepOp> ops;
-  int rc = collect_ops(c, seq, logits, ids, ops, true);
+  int rc = collect_ops(c, seq, logits, ids, ops);
   if (rc != HY_OK) return rc;
   c->last_kernels = (int)ops.size();
   return launch_ops(m, ops, st);
@@ -992,11 +830,6 @@ int get_graph(hy_cache* c, int seq, float* logits, int* ids, cudaGraphExec_t* ou
     cudaGraphExecDestroy(c->graphs.front().exec);
     c->graphs.erase(c->graphs.begin());
   }
-  if (c->m->persistent) {
-    const step::Program* pr = nullptr;
-    int rc0 = get_program(c, seq, logits, ids, &pr);
-    if (rc0 != HY_OK) return rc0;
-  }
   HY_CK(cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
   int rc = record_step(c, seq, logits, ids, c->cap_stream);
   cudaGraph_t graph = nullptr;
@@ -1017,14 +850,7 @@ int get_graph(hy_cache* c, int seq, float* logits, int* ids, cudaGraphExec_t* ou
 
 // one step of sequence `seq` whose token id is already in c->tok
 int run_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) {
-  if (!c->m->graphs) {
-    if (c->m->persistent) {
-      const step::Program* pr = nullptr;
-      int rc0 = get_program(c, seq, logits, ids, &pr);
-      if (rc0 != HY_OK) return rc0;
-    }
-    return record_step(c, seq, logits, ids, st);
-  }
+  if (!c->m->graphs) return record_step(c, seq, logits, ids, st);
   cudaGraphExec_t exec;
   int rc = get_graph(c, seq, logits, ids, &exec);
   if (rc != HY_OK) return rc;
@@ -1033,6 +859,8 @@ int run_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) {
 }
 
 int check_model_cfg(const hy_config* c) {
+  if (c->flags & ~(uint32_t)(HY_FLAG_DEBUG | HY_FLAG_NO_GRAPH | HY_FLAG_NO_PDL))
+    return fail(HY_ERR_ARG, "unknown flag bits 0x%x", c->flags & ~(uint32_t)(HY_FLAG_DEBUG | HY_FLAG_NO_GRAPH | HY_FLAG_NO_PDL));
   if (c->n_layers < 1 || c->n_layers > 64) return fail(HY_ERR_ARG, "n_layers must be in 1..64");
   if (c->hidden <= 0 || c->hidden % 8 || c->vocab <= 0) return fail(HY_ERR_ARG, "hidden must be a positive multiple of 8");
   if (c->weight_format != 0 && c->weight_format != 1) return fail(HY_ERR_ARG, "weight_format must be 0 or 1");
@@ -1075,8 +903,6 @@ void free_cache_mem(hy_cache* c) {
   c->graphs.clear();
   for (auto& g : c->bgraphs) cudaGraphExecDestroy(g.exec);
   c->bgraphs.clear();
-  for (auto& p : c->progs) cudaFree(p.dev);
-  c->progs.clear();
   for (void* p : c->allocs) cudaFree(p);
   c->allocs.clear();
   for (uint8_t* p : c->mem) cudaFree(p);
@@ -1180,7 +1006,6 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
   m->pdl = !(c.flags & HY_FLAG_NO_PDL);
   m->graphs = !(c.flags & HY_FLAG_NO_GRAPH);
   m->debug = (c.flags & HY_FLAG_DEBUG) != 0;
-  m->persistent = (c.flags & HY_FLAG_PERSISTENT) != 0;
   m->q4 = c.weight_format == 1;
   *out = m;
   g_err.clear();
@@ -1235,7 +1060,7 @@ int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, 
       (rc = dalloc(c, &c->rlog, std::max(cf.n_experts + 1, 1))) || (rc = dalloc(c, &c->moe_w, gemv::kMaxTopK + 4)) ||
       (rc = dalloc(c, &c->moe_ids, 16)) || (rc = dalloc(c, &c->tok, max_seqs)) || (rc = dalloc(c, &c->ids, max_seqs)) ||
       (rc = dalloc(c, &c->cnt_attn, std::max(cf.attn_kv_heads, 1))) || (rc = dalloc(c, &c->cnt_am, 1)) ||
-      (rc = dalloc(c, &c->cnt_router, 1)) || (rc = dalloc(c, &c->guard, 1)) || (rc = dalloc(c, &c->step_bar, 1)) ||
+      (rc = dalloc(c, &c->guard, 1)) ||
       (rc = dalloc(c, &c->logits_buf, (size_t)cf.vocab * bgemv::kMaxB))) {
     free_cache_mem(c);
     delete c;

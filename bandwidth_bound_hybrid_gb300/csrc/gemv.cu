@@ -14,7 +14,7 @@
 //     in registers, read 16-byte bf16 vectors from shared memory, accumulate
 //     in FP32, and reduce with warp shuffles;
 //   * fused prologues (RMSNorm, embedding gather, MoE weighted activations) and
-//     epilogues (store, residual add, SwiGLU, argmax, router top-k).
+//     epilogues (store, residual add, SwiGLU, argmax).
 #include <cstdlib>
 
 #include "common.cuh"
@@ -164,7 +164,7 @@ __global__ void __maxnreg__(kMaxRegs) k_gemv(const Params p) {
   }
   named_barrier(1, kCT);
   if (abort) return;
-  epilogue(p, EPI, red, r0, rows_cta, esh, reinterpret_cast<float*>(stages), ctid);
+  epilogue(p, EPI, red, r0, rows_cta, esh, ctid);
 }
 
 template <int SRC, int IN, int EPI, bool FULL>
@@ -192,7 +192,6 @@ void* pick(int src, int in, int epi, int vpl, bool full) {
   if (src == kSrcDense && in == kInX && epi == kEpiResid) return pick_vpl<kSrcDense, kInX, kEpiResid>(vpl, full);
   if (src == kSrcDense && in == kInX && epi == kEpiSwiglu) return pick_vpl<kSrcDense, kInX, kEpiSwiglu>(vpl, full);
   if (src == kSrcDense && in == kInX && epi == kEpiArgmax) return pick_vpl<kSrcDense, kInX, kEpiArgmax>(vpl, full);
-  if (src == kSrcDense && in == kInX && epi == kEpiRouter) return pick_vpl<kSrcDense, kInX, kEpiRouter>(vpl, full);
   if (src == kSrcExpertRows && in == kInX && epi == kEpiSwiglu) return pick_vpl<kSrcExpertRows, kInX, kEpiSwiglu>(vpl, full);
   if (src == kSrcExpertSegs && in == kInMoeZ && epi == kEpiResid) return pick_vpl<kSrcExpertSegs, kInMoeZ, kEpiResid>(vpl, full);
   return nullptr;
@@ -200,7 +199,7 @@ void* pick(int src, int in, int epi, int vpl, bool full) {
 
 const int kCombos[][3] = {
     {kSrcDense, kInX, kEpiStore},   {kSrcDense, kInEmbed, kEpiStore},      {kSrcDense, kInX, kEpiResid},
-    {kSrcDense, kInX, kEpiSwiglu},  {kSrcDense, kInX, kEpiArgmax},         {kSrcDense, kInX, kEpiRouter},
+    {kSrcDense, kInX, kEpiSwiglu},  {kSrcDense, kInX, kEpiArgmax},
     {kSrcExpertRows, kInX, kEpiSwiglu}, {kSrcExpertSegs, kInMoeZ, kEpiResid},
 };
 

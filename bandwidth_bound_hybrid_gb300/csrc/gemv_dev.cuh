@@ -373,12 +373,10 @@ __device__ __forceinline__ void route_weights(const Params& p, const int* sel, c
 }
 
 // Epilogue over the CTA's rows (after all tiles): store, residual add,
-// SwiGLU, or argmax / router top-k finished by the last CTA to arrive (an
-// atomic ticket: no CTA waits for another).
-// scratch: >= n_experts + 1 floats of shared memory no longer in use (the
-// drained weight ring).
+// SwiGLU, or argmax finished by the last CTA to arrive (an atomic ticket: no
+// CTA waits for another).
 __device__ __forceinline__ void epilogue(const Params& p, int epi, const float* red, int r0, int rows_cta,
-                                         EpiShared& sh, float* scratch, int ctid) {
+                                         EpiShared& sh, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   auto row_val = [&](int jj, int i) {
     float v = 0.f;
@@ -397,37 +395,29 @@ __device__ __forceinline__ void epilogue(const Params& p, int epi, const float* 
     for (int i = ctid; i < rows_cta; i += kCT) p.y[r0 + i] = siluf_(row_val(0, i)) * row_val(1, i);
     return;
   }
+  // argmax: per-CTA best (row value, lowest index on ties), then the last CTA merges
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   for (int i = ctid; i < rows_cta; i += kCT) {
     const float v = row_val(0, i);
-    if (epi == kEpiArgmax) {
-      if (p.y) p.y[r0 + i] = v;
-      argmax_merge(bv, bi, v, r0 + i);
-    } else {
-      p.router_logits[r0 + i] = v;
-    }
+    if (p.y) p.y[r0 + i] = v;
+    argmax_merge(bv, bi, v, r0 + i);
   }
-  if (epi == kEpiRouter) named_barrier(1, kCT);  // every thread's logits stored before the ticket's fence
-  if (epi == kEpiArgmax) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      argmax_merge(bv, bi, ov, oi);
-    }
-    if (lane == 0) {
-      sh.red[warp] = bv;
-      sh.redi[warp] = bi;
-    }
-    named_barrier(1, kCT);
-    if (ctid == 0) {
-      for (int w = 1; w < kConsumerWarps; ++w) argmax_merge(bv, bi, sh.red[w], sh.redi[w]);
-      p.part_val[blockIdx.x] = bv;
-      p.part_idx[blockIdx.x] = bi;
-    }
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    argmax_merge(bv, bi, ov, oi);
   }
+  if (lane == 0) {
+    sh.red[warp] = bv;
+    sh.redi[warp] = bi;
+  }
+  named_barrier(1, kCT);
   if (ctid == 0) {
+    for (int w = 1; w < kConsumerWarps; ++w) argmax_merge(bv, bi, sh.red[w], sh.redi[w]);
+    p.part_val[blockIdx.x] = bv;
+    p.part_idx[blockIdx.x] = bi;
     __threadfence();
     const unsigned ticket = atomicAdd(p.counter, 1u);
     sh.last = (ticket == (unsigned)(p.ncta - 1));
@@ -435,44 +425,22 @@ __device__ __forceinline__ void epilogue(const Params& p, int epi, const float* 
   named_barrier(1, kCT);
   if (!sh.last) return;
   __threadfence();
-  if (epi == kEpiArgmax) {
-    if (warp == 0) {
-      float v = -INFINITY;
-      int vi = 0x7fffffff;
-      for (int c = lane; c < p.ncta; c += 32) argmax_merge(v, vi, __ldcg(p.part_val + c), __ldcg(p.part_idx + c));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, vi, o);
-        argmax_merge(v, vi, ov, oi);
-      }
-      if (lane == 0) {
-        *p.ids_out = vi;
-        *p.counter = 0u;
-        if (p.len_inc) *p.len_inc += 1;
-      }
-    }
-    return;
-  }
-  // router: top-k over the E expert logits (FP32 compare, lowest index on
-  // ties), softmax over the selected logits, sigmoid gate of the shared
-  // expert's row ("Fourteen hours to 100 tokens per second", "The router with
-  // 257 rows").  This is the step's critical path (every other CTA waits for
-  // it), so one warp does it: each lane holds E/32 logits and top_k rounds of
-  // a warp-wide argmax (largest logit, lowest index on ties) pick the
-  // selection in order.
-  const int E = p.n_experts;
-  for (int e = ctid; e <= E; e += kCT) scratch[e] = __ldcg(p.router_logits + e);
-  named_barrier(1, kCT);
   if (warp == 0) {
-    warp_topk([&](int e) { return scratch[e]; }, E, p.top_k, sh.sel, sh.selv, lane);
+    float v = -INFINITY;
+    int vi = 0x7fffffff;
+    for (int c = lane; c < p.ncta; c += 32) argmax_merge(v, vi, __ldcg(p.part_val + c), __ldcg(p.part_idx + c));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, vi, o);
+      argmax_merge(v, vi, ov, oi);
+    }
     if (lane == 0) {
-      route_weights(p, sh.sel, sh.selv, scratch[E]);
+      *p.ids_out = vi;
       *p.counter = 0u;
+      if (p.len_inc) *p.len_inc += 1;
     }
   }
-  if (p.dbg_logits)
-    for (int e = ctid; e <= E; e += kCT) p.dbg_logits[e] = scratch[e];
 }
 
 }  // namespace gemv

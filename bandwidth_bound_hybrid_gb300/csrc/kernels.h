@@ -14,7 +14,7 @@ namespace gemv {
 
 enum Src : int { kSrcDense = 0, kSrcExpertRows = 1, kSrcExpertSegs = 2 };
 enum In : int { kInX = 0, kInEmbed = 1, kInMoeZ = 2 };
-enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiArgmax = 3, kEpiRouter = 4 };
+enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiArgmax = 3 };
 
 #ifndef HY_GEMV_WARPS
 #define HY_GEMV_WARPS 12
@@ -82,10 +82,10 @@ struct Params {
   unsigned* counter;            // last-CTA ticket (zero between launches)
   int* ids_out;                 // argmax result
   int* len_inc;                 // incremented once after the argmax (nullable)
-  float* router_logits;         // kEpiRouter: [n_experts + 1] scratch, always written
-  int* out_ids;                 // kEpiRouter: [top_k]
-  float* out_w;                 // kEpiRouter: [top_k + 1]
-  int* dbg_ids;                 // kEpiRouter debug copies (nullable)
+  float* router_logits;         // route_here: the router's stored logits [n_experts + 1]
+  int* out_ids;                 // route_here: selected experts [top_k] (CTA 0 writes them)
+  float* out_w;                 // route_here: routing weights [top_k + 1]
+  int* dbg_ids;                 // route_here debug copies (nullable)
   float* dbg_logits;
   int route_here;               // kSrcExpertRows: every CTA picks the experts itself from router_logits (the
                                 //   router kernel only stored them); CTA 0 writes out_ids / out_w (and dbg_ids)
@@ -258,54 +258,6 @@ cudaError_t launch(const Params& p, const Plan& pl, cudaStream_t st, bool pdl);
 cudaError_t moe_reduce(float* y, int ldy, const float* part, const float* w, int R, int B, int top_k, cudaStream_t st,
                        bool pdl);
 }  // namespace bgemv
-
-// ---------------------------------------------------------------- persistent step
-// The whole decode step as one cooperative kernel: one CTA per SM runs the
-// step's kernels as phases separated by grid barriers, and its copy lane keeps
-// streaming across phase boundaries.
-namespace step {
-enum Kind : int { kGemv = 0, kGdn = 1, kAttn = 2, kCopy = 3 };
-struct alignas(16) Phase {
-  int kind;
-  int src, in, epi, vpl, full;  // GEMV launch variant (full: every lane's vectors inside its chunk)
-  int pf_bytes;                 // DeltaNet: L2 prefetch of the state rows, issued while earlier phases run
-  int after;                    // the copy lane issues this phase's tiles once this many phases are
-                                // complete grid-wide (0: as soon as ring slots free up)
-  gemv::Params g;  // plan fields filled for ncta = the grid (CTAs past g.ncta idle in this phase)
-  gdn::Params d;
-  attn::Params a;
-  const float* csrc;  // kCopy: csrc[0, cn) -> cdst
-  float* cdst;
-  int cn, pad2_;
-};
-struct Program {
-  const Phase* phases;  // device array
-  int nphases;
-  unsigned* bar;        // grid-barrier arrivals; zero at launch, reset by the last arrival of the step
-  unsigned* guard;
-  int stage_bytes, nstages;
-  int region_bytes;     // per-phase working area (input vector, gain, partial sums / attention / DeltaNet)
-  int scratch_floats;   // router logits or split-merge weights
-  int hd, G, epl;       // attention and DeltaNet shapes the kernel is instantiated for
-};
-constexpr int kNW = gemv::kConsumerWarps;   // compute warps
-constexpr int kThreads = (kNW + 1) * 32;
-constexpr int kMaxSmem = 226 * 1024;  // dynamic; the rest is static shared data
-constexpr int kMaxStagesStep = 8;
-// Shared memory of a program, or 0 when it does not fit.
-size_t smem_bytes(const Program& pr);
-// Whether a kernel is instantiated for (hd, G, epl).
-bool supported(int hd, int G, int epl);
-// Working-area bytes of an attention item and of a DeltaNet item, and the
-// ring stage an attention tile needs.
-size_t attn_work_bytes(int hd, int G);
-size_t gdn_work_bytes(int epl);
-int attn_stage_bytes(int hd);
-// CTAs of the program's kernel that fit on one SM (0: none).
-int blocks_per_sm(const Program& pr);
-cudaError_t init();
-cudaError_t launch(const Program& pr, int nctas, cudaStream_t st);
-}  // namespace step
 
 // Record `msg` as the calling thread's last error (hy_last_error) and return
 // `code`; for C-ABI entry points defined outside engine.cu.

@@ -141,7 +141,7 @@ class HybridModel:
         return int(capi.lib().hy_seq_capacity(self.c, seq))
 
     def step_kernels(self) -> int:
-        """Kernels the last recorded decode step launches (1: the persistent step)."""
+        """Kernels the last recorded decode step launches (one per operation)."""
         return int(capi.lib().hy_step_kernels(self.c))
 
     def reset(self, seq: int, stream=None) -> None:

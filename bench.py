@@ -58,7 +58,6 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernel-timing", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="no programmatic dependent launch between kernels")
-    ap.add_argument("--persistent", action="store_true", help="run the step as one persistent cooperative kernel")
     return ap.parse_args(argv)
 
 
@@ -282,7 +281,7 @@ def run_ours(args):
     weights = workloads.device_weights(shape)
     cap = prompt + args.warmup + 2 * args.steps + 16
     from bandwidth_bound_hybrid_gb300 import capi as _capi
-    flags = (_capi.HY_FLAG_NO_PDL if args.no_pdl else 0) | (_capi.HY_FLAG_PERSISTENT if args.persistent else 0)
+    flags = _capi.HY_FLAG_NO_PDL if args.no_pdl else 0
     model = HybridModel(shape, weights, [cap], splits=args.splits, flags=flags)
     toks = torch.from_numpy(workloads.prompt_ids(w, n=prompt)).to(dev) if prompt else None
     ids = torch.zeros(1, dtype=torch.int32, device=dev)

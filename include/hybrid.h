@@ -55,7 +55,7 @@ extern "C" {
 #define HY_FLAG_DEBUG 1u    /* keep per-layer hidden states and router results of the last step */
 #define HY_FLAG_NO_GRAPH 2u /* launch kernels one by one instead of replaying a CUDA graph */
 #define HY_FLAG_NO_PDL 4u   /* no programmatic dependent launch between kernels */
-#define HY_FLAG_PERSISTENT 8u /* run the step as one persistent cooperative kernel (phases and grid barriers) */
+/* Other flag bits are refused (HY_ERR_ARG). */
 
 /* Model shape.  [Strata] "The Beast: Qwen 3.5 Hybrid Architecture": Gated
  * DeltaNet layers with a fixed FP32 state plus full GQA layers with a bf16 KV
@@ -186,8 +186,7 @@ int hy_seq_fill_synthetic(hy_cache* c, int32_t seq, int32_t len, uint64_t seed, 
  * GEMVs read only the selected experts). */
 int hy_experts_read(hy_cache* c, void* stream, uint64_t* total_out);
 
-/* Kernels the last recorded decode step launches: 1 when the whole step runs
- * as one persistent kernel (HY_FLAG_PERSISTENT), else one per operation.  0
+/* Kernels the last recorded decode step launches (one per operation); 0
  * before any step. */
 int32_t hy_step_kernels(const hy_cache* c);
 

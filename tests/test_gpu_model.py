@@ -21,10 +21,6 @@ pytestmark = pytest.mark.gpu
 
 HIDDEN_TOL, LOGIT_TOL, ID_MARGIN, ROUTER_GAP = 5e-3, 1e-2, 0.05, 1e-3
 
-# one kernel per operation (default) and the persistent single-kernel step
-PATHS = [0, capi.HY_FLAG_PERSISTENT]
-PATH_IDS = ["multi-kernel", "persistent"]
-
 
 @pytest.fixture(scope="module")
 def built(gpu):
@@ -67,10 +63,10 @@ def greedy_ok(gpu_id, ref_logits):
     return True
 
 
-def run_parity(shape, prompt_len, n_decode, capacity=None, prefill_path=True, seed_seq=0, path=0):
+def run_parity(shape, prompt_len, n_decode, capacity=None, prefill_path=True, seed_seq=0):
     import torch
     capacity = capacity or prompt_len + n_decode + 1
-    model, ref = make(shape, capacity, flags=capi.HY_FLAG_DEBUG | path)
+    model, ref = make(shape, capacity, flags=capi.HY_FLAG_DEBUG)
     prompt = workloads.host.uniform_ids(1 + seed_seq, workloads.PROMPT_TID, prompt_len, shape.vocab)
     logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
     ids = torch.empty(1, dtype=torch.int32, device="cuda")
@@ -96,76 +92,34 @@ def run_parity(shape, prompt_len, n_decode, capacity=None, prefill_path=True, se
         matched += int(int(ids.item()) == int(orc.argmax(r["logits"])))
     assert model.seq_len(0) == prompt_len + n_decode
     assert model.check_device() == 0
-    if path == capi.HY_FLAG_PERSISTENT:
-        assert model.step_kernels() == 1, "the step did not run as one persistent kernel"
-    else:
-        assert model.step_kernels() > 1
+    assert model.step_kernels() > 1
     model.close()
     return matched
 
 
-@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
-def test_tiny_full_parity(built, path):
+def test_tiny_full_parity(built):
     """Tiny hybrid: 128-token prompt, then 16 greedy decode steps."""
     w = workloads.WORKLOADS["tiny"]
-    run_parity(w.shape, w.prompt_len, w.decode_steps, path=path)
+    run_parity(w.shape, w.prompt_len, w.decode_steps)
 
 
-@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
-def test_tiny_per_token_parity_through_decode_steps(built, path):
-    run_parity(workloads.TINY, 40, 4, prefill_path=False, path=path)
+def test_tiny_per_token_parity_through_decode_steps(built):
+    run_parity(workloads.TINY, 40, 4, prefill_path=False)
 
 
-@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
-def test_dense4b_truncated_depth_parity(built, path):
+def test_dense4b_truncated_depth_parity(built):
     """Full widths of the dense 4B-shaped model (hidden 2560, FFN 9216, vocab
     151936, 16x128 DeltaNet heads, 16/4x128 GQA), first 4 layers (3 DeltaNet +
     1 attention)."""
     shape = dataclasses.replace(workloads.DENSE4B, name="dense4b-l4", n_layers=4, attn_layers=(3,))
-    run_parity(shape, 6, 3, path=path)
+    run_parity(shape, 6, 3)
 
 
-@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
-def test_moe_truncated_depth_parity(built, path):
+def test_moe_truncated_depth_parity(built):
     """Full widths of the MoE 35B-A3B-shaped model (256 experts of 512, top-8
     + shared, 16/2x256 GQA), first 4 layers."""
     shape = dataclasses.replace(workloads.MOE35B, name="moe-l4", n_layers=4, attn_layers=(3,))
-    run_parity(shape, 5, 3, path=path)
-
-
-AGREE_SHAPES = {
-    "dense": dataclasses.replace(workloads.DENSE4B, name="dense4b-l4", n_layers=4, attn_layers=(3,), vocab=4096),
-    # the kernel-per-operation step picks the experts in the expert kernel, the
-    # persistent step in the router's epilogue: the same arithmetic either way
-    "moe": dataclasses.replace(workloads.MOE35B, name="moe-l4", n_layers=4, attn_layers=(3,), vocab=4096),
-}
-
-
-@pytest.mark.parametrize("kind", list(AGREE_SHAPES))
-def test_persistent_and_multi_kernel_steps_agree(built, kind):
-    """The two ways of running a step compute the same thing: same greedy ids,
-    logits within rounding of each other (the persistent step reorders no
-    sum, so they are in fact expected to be identical)."""
-    import torch
-    shape = AGREE_SHAPES[kind]
-    prompt = workloads.host.uniform_ids(9, workloads.PROMPT_TID, 24, shape.vocab)
-    outs = []
-    for f in PATHS:
-        model, _ = make(shape, 40, flags=f, host=False)
-        logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
-        ids = torch.empty(1, dtype=torch.int32, device="cuda")
-        model.prefill(0, torch.from_numpy(prompt).cuda())
-        seq = []
-        for _ in range(6):
-            model.decode_step(0, ids if seq else torch.tensor([3], dtype=torch.int32, device="cuda"), ids, logits)
-            torch.cuda.synchronize()
-            seq.append((int(ids.item()), to_np(logits).copy()))
-        outs.append(seq)
-        assert model.check_device() == 0
-        model.close()
-    for (a, la), (b, lb) in zip(*outs):
-        assert a == b
-        np.testing.assert_array_equal(la, lb)
+    run_parity(shape, 5, 3)
 
 
 @pytest.mark.parametrize("flags", [capi.HY_FLAG_NO_GRAPH, capi.HY_FLAG_NO_PDL, capi.HY_FLAG_NO_GRAPH | capi.HY_FLAG_NO_PDL])
