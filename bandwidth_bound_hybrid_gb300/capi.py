@@ -76,6 +76,7 @@ SIGNATURES = {
     "hy_check_device": (ctypes.c_int, [vp, vp, P(u32)]),
     "hy_debug_hidden": (ctypes.c_int, [vp, i32, vp, vp]),
     "hy_debug_router": (ctypes.c_int, [vp, i32, vp, vp, vp]),
+    "hy_op_check_device": (ctypes.c_int, [vp, P(u32)]),
     "hy_op_gemv": (ctypes.c_int, [vp, i32, i32, vp, vp, f32, vp, i32, vp]),
     "hy_op_gemv_swiglu": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, f32, vp, vp]),
     "hy_op_gemv_batch": (ctypes.c_int, [P(hy_tensor), P(hy_tensor), i32, i32, i32, i32, vp, i32, vp, f32, vp, i32, i32,

@@ -1418,6 +1418,29 @@ int hy_op_gemv_batch(const hy_tensor* w, const hy_tensor* w_up, int32_t weight_f
   return HY_OK;
 }
 
+int hy_op_check_device(void* stream, uint32_t* bits_out) {
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned* words[2] = {nullptr, hy::noalloc_guard()};
+  {
+    int dev = 0;
+    HY_CK(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(g_init_mu);
+    auto it = g_op_guard.find(dev);  // never created here: this call allocates nothing
+    if (it != g_op_guard.end()) words[0] = it->second;
+  }
+  unsigned got[2] = {0u, 0u};
+  for (int i = 0; i < 2; ++i)
+    if (words[i]) HY_CK(cudaMemcpyAsync(&got[i], words[i], sizeof(unsigned), cudaMemcpyDeviceToHost, st));
+  HY_CK(cudaStreamSynchronize(st));
+  const unsigned bits = got[0] | got[1];
+  if (bits_out) *bits_out = bits;
+  if (!bits) return HY_OK;
+  for (int i = 0; i < 2; ++i)
+    if (got[i]) HY_CK(cudaMemsetAsync(words[i], 0, sizeof(unsigned), st));
+  HY_CK(cudaStreamSynchronize(st));
+  return fail(HY_ERR_DEVICE_GUARD, "device guard bits 0x%x", bits);
+}
+
 size_t hy_op_argmax_workspace(void) { return 256 + 1024 * 8; }
 
 int hy_op_gemv_argmax(const void* W_dev, int32_t rows, int32_t cols, const float* x_dev, const float* norm_g_dev,

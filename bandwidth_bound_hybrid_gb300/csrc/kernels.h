@@ -259,6 +259,10 @@ cudaError_t moe_reduce(float* y, int ldy, const float* part, const float* w, int
                        bool pdl);
 }  // namespace bgemv
 
+// Guard word of the allocation-free attention call on the current device
+// (null before its first call there); read by hy_op_check_device.
+unsigned* noalloc_guard();
+
 // Record `msg` as the calling thread's last error (hy_last_error) and return
 // `code`; for C-ABI entry points defined outside engine.cu.
 int set_error(int code, const char* msg);

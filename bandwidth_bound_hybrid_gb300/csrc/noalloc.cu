@@ -71,11 +71,20 @@ int setup(uint8_t** addr, int* nsm) {
 
 }  // namespace
 
+// Device address of the guard word in this device's array, or null before the
+// first hy_op_attention_noalloc call on it (nothing to report then).
+unsigned* hy::noalloc_guard() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return reinterpret_cast<unsigned*>(g_addr[dev]);
+}
+
 extern "C" int hy_op_attention_noalloc(const float* y_dev, void* K_dev, void* V_dev, int32_t cap, int32_t nq,
                                        int32_t nkv, int32_t hd, const int32_t* len_dev, const float* rope_table_dev,
                                        int32_t nsplit, float* o_dev, void* stream) {
   if (!y_dev || !K_dev || !V_dev || ((uintptr_t)K_dev & 15u) || ((uintptr_t)V_dev & 15u) || !len_dev ||
-      !rope_table_dev || !o_dev || cap <= 0 || nkv <= 0 || nq <= 0 || nq % nkv || nsplit < 0)
+      !rope_table_dev || !o_dev || cap <= 0 || nkv <= 0 || nq <= 0 || nq % nkv)
     return err(HY_ERR_ARG, "bad attention arguments");
   if ((hd != 64 && hd != 128 && hd != 256) || nq / nkv > 8 || ((nq / nkv) & (nq / nkv - 1)))
     return err(HY_ERR_UNSUPPORTED, "attention: head_dim 64/128/256 and nq/nkv in {1,2,4,8}");
@@ -83,7 +92,7 @@ extern "C" int hy_op_attention_noalloc(const float* y_dev, void* K_dev, void* V_
   int nsm = 0;
   int rc = setup(&base, &nsm);
   if (rc != HY_OK) return rc;
-  if (nsplit == 0) nsplit = attn::auto_splits(nkv, nsm);
+  if (nsplit <= 0) nsplit = attn::auto_splits(nkv, nsm);
   // layout: [guard | pad to 256] [tickets, nkv words, padded to 256] [partials]
   const size_t tickets = ((size_t)nkv * 4 + 255) / 256 * 256;
   const size_t need = kHeaderBytes + tickets + attn::part_floats(nq, nkv, hd, nsplit) * 4;

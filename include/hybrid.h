@@ -233,7 +233,19 @@ int hy_debug_router(hy_cache* c, int32_t layer, float* logits_dev, int32_t* ids_
 
 /* ------------------------------------------------------------- single ops
  * The kernels of the decode step, callable on their own (used by tests and
- * measurements).  All device pointers, stream-ordered. */
+ * measurements).  All device pointers, stream-ordered.  Their kernels report
+ * device-side refusals (a position at or past the cache capacity, a bounded
+ * wait that gave up) in a guard word, not in the return code, which only
+ * covers what the host checks before launching: read it with
+ * hy_op_check_device. */
+
+/* Synchronise `stream`, then read and clear the guard words of the single-op
+ * calls on the current device (every hy_op_* call, and the allocation-free
+ * attention, whose word each of its calls clears first, so that it reports
+ * that call's refusals only).  *bits_out (nullable) receives the HY_GUARD_*
+ * bits.  Returns HY_ERR_DEVICE_GUARD when any bit was set.  Allocates
+ * nothing. */
+int hy_op_check_device(void* stream, uint32_t* bits_out);
 
 /* y = W * xhat, xhat = x (norm_g == NULL) or RMSNorm(x) * norm_g with eps:
  * W bf16 [rows][cols], x, y FP32.  accumulate != 0: y += W * xhat.
@@ -303,11 +315,15 @@ int hy_op_attention(const float* y_dev, void* K_dev, void* V_dev, int32_t cap, i
  * allocations outside its allocator.  The pages have no counterpart of this
  * call; it exists only for such callers.
  *
- * Same arguments, layout and results as hy_op_attention; the scratch (guard
+ * Same arguments, layout and results as hy_op_attention (nsplit <= 0 selects
+ * the automatic split count); the scratch (guard
  * word, per-kv-head tickets, per-split partials) lives instead in one fixed
  * device array of HY_NOALLOC_SCRATCH_BYTES that every GPU loading this
  * library holds until the process exits.  The call makes no allocation: it
- * clears the guard word and the tickets on `stream`, then launches.
+ * clears the guard word and the tickets on `stream`, then launches.  A
+ * position at or past `cap` is refused on the device: the kernel returns
+ * without touching o_dev or the cache and sets HY_GUARD_BAD_POSITION, which
+ * hy_op_check_device reports until the next call clears it.
  *   - Returns HY_ERR_UNSUPPORTED, launching nothing, when the scratch this
  *     shape needs (hy_op_attention_workspace(nq, nkv, hd, nsplit) bytes, with
  *     nsplit = 0 resolved as hy_op_attention resolves it) exceeds

@@ -160,3 +160,11 @@ def test_batch_of_one_equals_each_token_alone(L):
         torch.cuda.synchronize()
         np.testing.assert_array_equal(to_np(y1)[0], to_np(yb)[b])
     del keep
+
+
+@pytest.mark.parametrize("fmt,C,swiglu", [(0, 5824, False), (0, 4672, True), (1, 11264, False), (1, 8704, True)])
+def test_batch_gemv_at_the_documented_column_limits(L, fmt, C, swiglu):
+    """The widest inputs include/hybrid.h promises for hy_op_gemv_batch (bf16
+    5824, or 4672 with an up matrix; 4-bit 11264, or 8704 with an up matrix),
+    a full batch of 8, where the token vectors take the most shared memory."""
+    run(L, fmt, 160, C, 8, True, swiglu=swiglu)

@@ -187,3 +187,11 @@ def test_dense4b_truncated_batch_of_two(built):
     accumulate in order."""
     shape = dataclasses.replace(workloads.DENSE4B, name="dense4b-l2", n_layers=2, attn_layers=(1,), vocab=4096)
     run(shape, [3, 5], 2)
+
+
+def test_moe_top16_batch_of_four_at_the_pick_limit(built):
+    """top_k 16 (the largest the header allows) for four sequences in one
+    batched step: 64 routed picks, the most a batched MoE step holds."""
+    shape = dataclasses.replace(workloads.TINY, name="tiny-moe-k16", vocab=512, ffn=0, n_experts=64, top_k=16,
+                                expert_ffn=64, shared_ffn=64)
+    run(shape, [5, 9, 12, 7], 2)

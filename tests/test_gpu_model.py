@@ -212,3 +212,11 @@ def test_host_buffer_step_matches_device_step(built):
         tok_h[0] = int(ids_h.item())
     a.close()
     b.close()
+
+
+def test_moe_with_511_experts(built):
+    """511 routed experts (the header's limit: the router's 512th row gates the
+    shared expert) at batch 1, against the oracle with the router ids checked."""
+    shape = dataclasses.replace(workloads.TINY, name="tiny-moe-e511", vocab=512, ffn=0, n_experts=511, top_k=8,
+                                expert_ffn=64, shared_ffn=64)
+    run_parity(shape, 8, 3)

@@ -212,7 +212,12 @@ def test_moe35b_full_size(built):
     """MoE 35B-A3B-shaped hybrid, 40 layers, bf16, batch 1 at context 2048:
     four independent sequences, two steps each, with debug copies (per-layer
     hidden states and expert sets compared as well)."""
-    assert run_full(workloads.MOE35B, [2048] * 4, steps=2, batched=False, debug=True) >= 1
+    compared = run_full(workloads.MOE35B, [2048] * 4, steps=2, batched=False, debug=True)
+    print(f"moe35b full size: {compared} of 8 (sequence, step) pairs compared")
+    # a sequence stops being compared at its first allowed routing near-tie
+    # (gap <= 1e-3 of the largest logit, both expert sets correct); the bar
+    # keeps such ties rare enough that most pairs are checked
+    assert compared >= 6, f"only {compared} of 8 (sequence, step) pairs compared"
 
 
 def test_moe35b_q4_batch8_full_size(built):
