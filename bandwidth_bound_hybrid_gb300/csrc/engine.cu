@@ -57,6 +57,7 @@ int ensure_init(int dev) {
   HY_CK(gemv::init());
   HY_CK(attn::init());
   HY_CK(bgemv::init());
+  HY_CK(gemm::init());
   g_inited[dev] = true;
   return HY_OK;
 }
@@ -1439,6 +1440,67 @@ int hy_op_check_device(void* stream, uint32_t* bits_out) {
     if (got[i]) HY_CK(cudaMemsetAsync(words[i], 0, sizeof(unsigned), st));
   HY_CK(cudaStreamSynchronize(st));
   return fail(HY_ERR_DEVICE_GUARD, "device guard bits 0x%x", bits);
+}
+
+namespace {
+size_t split_part_bytes(int32_t M, int32_t K) { return ((size_t)M * K * 2 + 255) / 256 * 256; }
+
+// The activations of a prompt GEMM op: RMSNorm (optional) and the bf16 hi / lo
+// split into the workspace, then the GEMM.
+int op_gemm_run(gemm::Params& p, const void* W0, const void* W1, const float* x_dev, int32_t ldx,
+                const float* norm_g_dev, float eps, void* workspace_dev, void* stream) {
+  unsigned* guard = nullptr;
+  int rc = op_guard(&guard);
+  if (rc != HY_OK) return rc;
+  p.guard = guard;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint16_t* hi = (uint16_t*)workspace_dev;
+  uint16_t* lo = (uint16_t*)((uint8_t*)workspace_dev + split_part_bytes(p.M, p.K));
+  cudaError_t e = gemm::norm_split(x_dev, ldx, norm_g_dev, eps, p.M, p.K, hi, lo, p.K, st);
+  if (e == cudaSuccess) e = gemm::launch(p, hi, lo, p.K, (const uint16_t*)W0, (const uint16_t*)W1, p.K, st);
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "prompt GEMM launch: %s", cudaGetErrorString(e));
+  return HY_OK;
+}
+}  // namespace
+
+size_t hy_op_gemm_workspace(int32_t M, int32_t K) {
+  if (M <= 0 || K <= 0) return 0;
+  return 2 * split_part_bytes(M, K);
+}
+
+int hy_op_gemm(const void* W_dev, int32_t N, int32_t K, int32_t M, const float* x_dev, int32_t ldx,
+               const float* norm_g_dev, float eps, float* y_dev, int32_t ldy, int32_t accumulate, void* workspace_dev,
+               void* stream) {
+  if (!aligned16(W_dev) || !x_dev || !y_dev || !aligned16(workspace_dev) || N <= 0 || M <= 0 || K <= 0 || K % 8 ||
+      ldx < K || ldy < N)
+    return fail(HY_ERR_ARG, "bad prompt GEMM arguments");
+  gemm::Params p;
+  memset(&p, 0, sizeof(p));
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.epi = accumulate ? gemm::kEpiResid : gemm::kEpiStore;
+  p.y = y_dev;
+  p.ldy = ldy;
+  return op_gemm_run(p, W_dev, nullptr, x_dev, ldx, norm_g_dev, eps, workspace_dev, stream);
+}
+
+int hy_op_gemm_swiglu(const void* Wg_dev, const void* Wu_dev, int32_t N, int32_t K, int32_t M, const float* x_dev,
+                      int32_t ldx, const float* norm_g_dev, float eps, uint16_t* h_hi_dev, uint16_t* h_lo_dev,
+                      int32_t ldh, void* workspace_dev, void* stream) {
+  if (!aligned16(Wg_dev) || !aligned16(Wu_dev) || !x_dev || !h_hi_dev || !h_lo_dev || !aligned16(workspace_dev) ||
+      N <= 0 || M <= 0 || K <= 0 || K % 8 || ldx < K || ldh < N)
+    return fail(HY_ERR_ARG, "bad prompt GEMM arguments");
+  gemm::Params p;
+  memset(&p, 0, sizeof(p));
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.epi = gemm::kEpiSwigluSplit;
+  p.h_hi = h_hi_dev;
+  p.h_lo = h_lo_dev;
+  p.ldh = ldh;
+  return op_gemm_run(p, Wg_dev, Wu_dev, x_dev, ldx, norm_g_dev, eps, workspace_dev, stream);
 }
 
 size_t hy_op_argmax_workspace(void) { return 256 + 1024 * 8; }

@@ -259,6 +259,72 @@ cudaError_t moe_reduce(float* y, int ldy, const float* part, const float* w, int
                        bool pdl);
 }  // namespace bgemv
 
+// ---------------------------------------------------------------- prompt GEMM
+// Y[m][n] = sum_k A[m][k] W[n][k] on the tensor cores (tcgen05), with the
+// FP32 activations as two bf16 parts A_hi + A_lo (gemm.cu).
+namespace gemm {
+enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwigluSplit = 2 };
+struct Params {
+  int M, N, K, epi;
+  float* y;             // store / residual: FP32 [M][ldy]
+  int ldy;
+  uint16_t* h_hi;       // SwiGLU: silu(A Wg^T) * (A Wu^T) as bf16 hi / lo parts [M][ldh]
+  uint16_t* h_lo;
+  int ldh;
+  unsigned* guard;
+};
+cudaError_t init();
+bool supported(int M, int N, int K);
+// a_hi, a_lo: bf16 [M][lda]; w0 (and the up matrix w1 for SwiGLU): bf16 [N][ldw].
+cudaError_t launch(const Params& p, const uint16_t* a_hi, const uint16_t* a_lo, int lda, const uint16_t* w0,
+                   const uint16_t* w1, int ldw, cudaStream_t st);
+// rows of x -> RMSNorm with gain g (or none when g is null) -> bf16 hi / lo parts.
+cudaError_t norm_split(const float* x, int ld_x, const float* g, float eps, int rows, int cols, uint16_t* hi,
+                       uint16_t* lo, int ld_out, cudaStream_t st);
+}  // namespace gemm
+
+// ---------------------------------------------------------------- prompt mixers
+// The chunk of n prompt tokens at positions t0 .. t0+n-1 of one sequence
+// (prefill.cu).  Mixer outputs are written as bf16 hi / lo parts [n][ldo], the
+// A operand of the output projection's GEMM.
+namespace prefill {
+struct GdnArgs {
+  const float* Y;          // projection rows q|k|v|a|b of the chunk [n][ldy]
+  int ldy;
+  const uint16_t* conv_w;  // bf16 [channels][conv_k]
+  float* ring;             // conv ring [conv_k][channels] (inputs of the positions before t0; updated)
+  float* S;                // state [nh][dv][dk], updated in place
+  float* Qn;               // scratch: normalised, scaled q [n][nh][dk]
+  float* Kn;               // scratch: normalised k [n][nh][dk]
+  float* V;                // scratch: conv outputs of v [n][nh][dv]
+  float* AB;               // scratch: alpha, beta [n][nh][2]
+  uint16_t* O_hi;
+  uint16_t* O_lo;
+  int ldo;
+  int n, t0, nh, dk, dv, conv_k;
+};
+struct AttnArgs {
+  const float* Y;          // projection rows q|k|v of the chunk [n][ldy]
+  int ldy;
+  uint16_t* K;             // bf16 cache [nkv][cap][hd]; rows t0 .. t0+n-1 are written
+  uint16_t* V;
+  int cap;
+  const float2* rope;      // (cos, sin) [>= t0 + n][hd/2]
+  float* Qr;               // scratch: rotated, scaled queries [n][nq][hd]
+  uint16_t* O_hi;
+  uint16_t* O_lo;
+  int ldo;
+  int n, t0, nq, nkv, hd;
+  float scale;
+};
+cudaError_t init();
+cudaError_t embed_rows(const uint16_t* embed, const int* tok, int n, int H, int vocab, float* X, unsigned* guard,
+                       cudaStream_t st);
+cudaError_t gdn(const GdnArgs& a, cudaStream_t st);
+cudaError_t attention(const AttnArgs& a, cudaStream_t st);
+cudaError_t set_len(int* len, int value, cudaStream_t st);
+}  // namespace prefill
+
 // Guard word of the allocation-free attention call on the current device
 // (null before its first call there); read by hy_op_check_device.
 unsigned* noalloc_guard();

@@ -276,6 +276,26 @@ int hy_op_gemv_batch(const hy_tensor* w, const hy_tensor* w_up, int32_t weight_f
                      int32_t batch, const float* x_dev, int32_t ldx, const float* norm_g_dev, float eps, float* y_dev,
                      int32_t ldy, int32_t accumulate, void* stream);
 
+/* Prompt GEMM on the tensor cores: for the M token rows of x (FP32
+ * [M][ldx], K columns used), xhat = x or its RMSNorm times norm_g (eps), and
+ * y[m][n] = sum_k xhat[m][k] W[n][k] (accumulate != 0: y += ...), W bf16
+ * [N][K], y FP32 [M][ldy].  xhat reaches the tensor cores as two bf16 parts
+ * hi + lo (relative error ~2^-16) written to workspace_dev
+ * (hy_op_gemm_workspace(M, K) bytes, caller-owned, no zeroing needed); the
+ * products accumulate in FP32 in tensor memory.  K % 8 == 0.  [Strata]
+ * "Act 1" (the prompt through batched kernels, one launch per layer). */
+size_t hy_op_gemm_workspace(int32_t M, int32_t K);
+int hy_op_gemm(const void* W_dev, int32_t N, int32_t K, int32_t M, const float* x_dev, int32_t ldx,
+               const float* norm_g_dev, float eps, float* y_dev, int32_t ldy, int32_t accumulate, void* workspace_dev,
+               void* stream);
+/* The gate/up pair of the same: h = silu(xhat Wg^T) * (xhat Wu^T), returned
+ * as its bf16 hi and lo parts (h ~ hi + lo, relative error ~2^-16) in
+ * h_hi_dev, h_lo_dev [M][ldh] (the form the down projection's GEMM takes).
+ * [14h] "Eight levers that worked" (silu(gate) * up fused into the GEMM). */
+int hy_op_gemm_swiglu(const void* Wg_dev, const void* Wu_dev, int32_t N, int32_t K, int32_t M, const float* x_dev,
+                      int32_t ldx, const float* norm_g_dev, float eps, uint16_t* h_hi_dev, uint16_t* h_lo_dev,
+                      int32_t ldh, void* workspace_dev, void* stream);
+
 /* Greedy head: logits = W * xhat (logits_dev nullable), *id_dev = argmax
  * (lowest index on ties).  workspace_dev: hy_op_argmax_workspace() bytes,
  * zeroed before its first use and left zeroed after each call.
