@@ -27,6 +27,7 @@ HY_GUARD_BAD_POSITION = 4
 HY_FLAG_DEBUG = 1
 HY_FLAG_NO_GRAPH = 2
 HY_FLAG_NO_PDL = 4
+HY_FLAG_TOKEN_PREFILL = 16
 
 HY_NOALLOC_SCRATCH_BYTES = 1 << 20
 

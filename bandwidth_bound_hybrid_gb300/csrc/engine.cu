@@ -58,6 +58,7 @@ int ensure_init(int dev) {
   HY_CK(attn::init());
   HY_CK(bgemv::init());
   HY_CK(gemm::init());
+  HY_CK(prefill::init());
   g_inited[dev] = true;
   return HY_OK;
 }
@@ -117,6 +118,7 @@ struct hy_model {
   bool moe = false, pdl = true, graphs = true, debug = false;
   bool q4 = false;          // 4-bit linear weights: every step runs the batched path
   bool splits_auto = true;  // split-KV count chosen from the SM count (the batched step then scales it down)
+  bool chunk_prefill = false;  // prompts run as chunks through the tensor-core GEMMs (else token by token)
 };
 
 struct hy_cache {
@@ -154,6 +156,11 @@ struct hy_cache {
   };
   std::vector<BGraph> bgraphs;
   int last_kernels = 0;          // kernels of the last recorded step
+  // chunked prompt (prefill) buffers, allocated at the first chunked prefill for pf_rows tokens
+  int pf_rows = 0, pf_ka = 0;
+  float *pf_x = nullptr, *pf_y = nullptr, *pf_qn = nullptr, *pf_kn = nullptr, *pf_v = nullptr, *pf_ab = nullptr;
+  float* pf_qr = nullptr;
+  uint16_t *pf_ahi = nullptr, *pf_alo = nullptr, *pf_hhi = nullptr, *pf_hlo = nullptr;
   struct Graph {
     int seq;
     float* logits;
@@ -860,8 +867,8 @@ int run_step(hy_cache* c, int seq, float* logits, int* ids, cudaStream_t st) {
 }
 
 int check_model_cfg(const hy_config* c) {
-  if (c->flags & ~(uint32_t)(HY_FLAG_DEBUG | HY_FLAG_NO_GRAPH | HY_FLAG_NO_PDL))
-    return fail(HY_ERR_ARG, "unknown flag bits 0x%x", c->flags & ~(uint32_t)(HY_FLAG_DEBUG | HY_FLAG_NO_GRAPH | HY_FLAG_NO_PDL));
+  const uint32_t known = HY_FLAG_DEBUG | HY_FLAG_NO_GRAPH | HY_FLAG_NO_PDL | HY_FLAG_TOKEN_PREFILL;
+  if (c->flags & ~known) return fail(HY_ERR_ARG, "unknown flag bits 0x%x", c->flags & ~known);
   if (c->n_layers < 1 || c->n_layers > 64) return fail(HY_ERR_ARG, "n_layers must be in 1..64");
   if (c->hidden <= 0 || c->hidden % 8 || c->vocab <= 0) return fail(HY_ERR_ARG, "hidden must be a positive multiple of 8");
   if (c->weight_format != 0 && c->weight_format != 1) return fail(HY_ERR_ARG, "weight_format must be 0 or 1");
@@ -927,6 +934,154 @@ int dalloc(hy_cache* c, T** p, size_t count) {
 int valid_seq(const hy_cache* c, int seq) { return c && seq >= 0 && seq < c->max_seqs; }
 
 }  // namespace
+
+// ---------------------------------------------------------------- chunked prompt
+// Prompt tokens per chunk (the GEMMs' M); HY_PREFILL_CHUNK overrides.
+int prefill_chunk_rows() {
+  const char* v = getenv("HY_PREFILL_CHUNK");
+  const int r = (v && *v) ? atoi(v) : 2048;
+  return r > 0 ? r : 2048;
+}
+
+// Buffers of a chunk of `rows` prompt tokens (grown when a longer chunk comes).
+int prefill_buffers(hy_cache* c, int rows) {
+  if (c->pf_rows >= rows) return HY_OK;
+  hy_model* m = c->m;
+  const hy_config& cf = m->cfg;
+  const int H = cf.hidden;
+  const int ka = std::max(H, std::max(m->o_len, 8));
+  for (void* p : {(void*)c->pf_x, (void*)c->pf_y, (void*)c->pf_qn, (void*)c->pf_kn, (void*)c->pf_v, (void*)c->pf_ab,
+                  (void*)c->pf_qr, (void*)c->pf_ahi, (void*)c->pf_alo, (void*)c->pf_hhi, (void*)c->pf_hlo})
+    if (p) {
+      c->allocs.erase(std::remove(c->allocs.begin(), c->allocs.end(), p), c->allocs.end());
+      cudaFree(p);
+    }
+  c->pf_x = c->pf_y = c->pf_qn = c->pf_kn = c->pf_v = c->pf_ab = c->pf_qr = nullptr;
+  c->pf_ahi = c->pf_alo = c->pf_hhi = c->pf_hlo = nullptr;
+  c->pf_rows = 0;
+  const size_t R = (size_t)rows;
+  const size_t gq = m->n_gdn ? R * cf.gdn_heads * cf.gdn_dk : 1;
+  int rc;
+  if ((rc = dalloc(c, &c->pf_x, R * H)) || (rc = dalloc(c, &c->pf_y, R * m->y_len)) ||
+      (rc = dalloc(c, &c->pf_ahi, R * ka)) || (rc = dalloc(c, &c->pf_alo, R * ka)) ||
+      (rc = dalloc(c, &c->pf_hhi, R * std::max(cf.ffn, 8))) || (rc = dalloc(c, &c->pf_hlo, R * std::max(cf.ffn, 8))) ||
+      (rc = dalloc(c, &c->pf_qn, gq)) || (rc = dalloc(c, &c->pf_kn, gq)) ||
+      (rc = dalloc(c, &c->pf_v, m->n_gdn ? R * cf.gdn_heads * cf.gdn_dv : 1)) ||
+      (rc = dalloc(c, &c->pf_ab, m->n_gdn ? R * cf.gdn_heads * 2 : 1)) ||
+      (rc = dalloc(c, &c->pf_qr, m->n_attn ? R * cf.attn_q_heads * cf.head_dim : 1)))
+    return rc;
+  c->pf_rows = rows;
+  c->pf_ka = ka;
+  return HY_OK;
+}
+
+// One chunk of n prompt tokens of sequence `seq` at positions t0 .. t0+n-1
+// through every layer; `last`: also the final norm, the LM head and argmax of
+// its last token (logits nullable, id to c->ids) and the debug copies.
+int prefill_chunk(hy_cache* c, int seq, const int* tok, int n, int t0, bool last, float* logits, cudaStream_t st) {
+  hy_model* m = c->m;
+  const hy_config& cf = m->cfg;
+  const int H = cf.hidden, ka = c->pf_ka;
+  cudaError_t e = prefill::embed_rows((const uint16_t*)m->w.embed, tok, n, H, cf.vocab, c->pf_x, c->guard, st);
+  auto gemm_run = [&](int N, int K, int epi, const uint16_t* ahi, const uint16_t* alo, int lda, const void* w0,
+                      const void* w1, float* y, int ldy) {
+    gemm::Params g;
+    memset(&g, 0, sizeof(g));
+    g.M = n;
+    g.N = N;
+    g.K = K;
+    g.epi = epi;
+    g.y = y;
+    g.ldy = ldy;
+    g.h_hi = c->pf_hhi;
+    g.h_lo = c->pf_hlo;
+    g.ldh = cf.ffn;
+    g.guard = c->guard;
+    return gemm::launch(g, ahi, alo, lda, (const uint16_t*)w0, (const uint16_t*)w1, K, st);
+  };
+  for (int l = 0; l < cf.n_layers && e == cudaSuccess; ++l) {
+    const hy_layer_weights& L = m->layers[l];
+    const bool attn_l = m->is_attn[l];
+    const int rows = attn_l ? m->attn_rows : m->gdn_rows;
+    const int od = attn_l ? cf.attn_q_heads * cf.head_dim : cf.gdn_heads * cf.gdn_dv;
+    e = gemm::norm_split(c->pf_x, H, L.norm1, cf.rms_eps, n, H, c->pf_ahi, c->pf_alo, ka, st);
+    if (e == cudaSuccess)
+      e = gemm_run(rows, H, gemm::kEpiStore, c->pf_ahi, c->pf_alo, ka, L.w_in.w, nullptr, c->pf_y, m->y_len);
+    if (e == cudaSuccess && attn_l) {
+      prefill::AttnArgs a;
+      memset(&a, 0, sizeof(a));
+      a.Y = c->pf_y;
+      a.ldy = m->y_len;
+      a.K = kv_cache(c, seq, m->sub[l], 0);
+      a.V = kv_cache(c, seq, m->sub[l], 1);
+      a.cap = c->cap[seq];
+      a.rope = c->rope;
+      a.Qr = c->pf_qr;
+      a.O_hi = c->pf_ahi;
+      a.O_lo = c->pf_alo;
+      a.ldo = ka;
+      a.n = n;
+      a.t0 = t0;
+      a.nq = cf.attn_q_heads;
+      a.nkv = cf.attn_kv_heads;
+      a.hd = cf.head_dim;
+      a.scale = 1.0f / sqrtf((float)cf.head_dim);
+      e = prefill::attention(a, st);
+    } else if (e == cudaSuccess) {
+      prefill::GdnArgs g;
+      memset(&g, 0, sizeof(g));
+      g.Y = c->pf_y;
+      g.ldy = m->y_len;
+      g.conv_w = (const uint16_t*)L.conv_w;
+      g.ring = conv_state(c, seq, m->sub[l]);
+      g.S = gdn_state(c, seq, m->sub[l]);
+      g.Qn = c->pf_qn;
+      g.Kn = c->pf_kn;
+      g.V = c->pf_v;
+      g.AB = c->pf_ab;
+      g.O_hi = c->pf_ahi;
+      g.O_lo = c->pf_alo;
+      g.ldo = ka;
+      g.n = n;
+      g.t0 = t0;
+      g.nh = cf.gdn_heads;
+      g.dk = cf.gdn_dk;
+      g.dv = cf.gdn_dv;
+      g.conv_k = cf.conv_k;
+      e = prefill::gdn(g, st);
+    }
+    if (e == cudaSuccess) e = gemm_run(H, od, gemm::kEpiResid, c->pf_ahi, c->pf_alo, ka, L.w_o.w, nullptr, c->pf_x, H);
+    if (e == cudaSuccess) e = gemm::norm_split(c->pf_x, H, L.norm2, cf.rms_eps, n, H, c->pf_ahi, c->pf_alo, ka, st);
+    if (e == cudaSuccess)
+      e = gemm_run(cf.ffn, H, gemm::kEpiSwigluSplit, c->pf_ahi, c->pf_alo, ka, L.w_gate.w, L.w_up.w, nullptr, 0);
+    if (e == cudaSuccess)
+      e = gemm_run(H, cf.ffn, gemm::kEpiResid, c->pf_hhi, c->pf_hlo, cf.ffn, L.w_down.w, nullptr, c->pf_x, H);
+    if (e == cudaSuccess && last && m->debug)
+      e = cudaMemcpyAsync(c->dbg_hidden + (size_t)l * H, c->pf_x + (size_t)(n - 1) * H, sizeof(float) * H,
+                          cudaMemcpyDeviceToDevice, st);
+  }
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "prompt chunk launch: %s", cudaGetErrorString(e));
+  if (!last) return HY_OK;
+  gemv::Params p;  // final RMSNorm + LM head + argmax of the last token
+  memset(&p, 0, sizeof(p));
+  p.guard = c->guard;
+  p.eps = cf.rms_eps;
+  p.W[0] = (const uint8_t*)m->w.lm_head.w;
+  p.R = cf.vocab;
+  p.C = H;
+  p.x = c->pf_x + (size_t)(n - 1) * H;
+  p.norm_g = m->w.final_norm;
+  p.y = logits;
+  p.part_val = c->am_val;
+  p.part_idx = c->am_idx;
+  p.counter = c->cnt_am;
+  p.ids_out = c->ids;
+  const gemv::Plan pl = gemv::plan(p.R, p.C, 1, m->nsm, true);
+  if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no GEMV plan for the LM head");
+  e = gemv::launch(p, pl, gemv::kSrcDense, gemv::kInX, gemv::kEpiArgmax, st, false);
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "LM head launch: %s", cudaGetErrorString(e));
+  return HY_OK;
+}
 
 // ====================================================================== C ABI
 
@@ -1008,6 +1163,11 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
   m->graphs = !(c.flags & HY_FLAG_NO_GRAPH);
   m->debug = (c.flags & HY_FLAG_DEBUG) != 0;
   m->q4 = c.weight_format == 1;
+  {  // the chunked prompt path: bf16 dense models whose GEMM widths suit the tensor copies
+    const int od = std::max(m->n_gdn ? c.gdn_heads * c.gdn_dv : 8, m->n_attn ? c.attn_q_heads * c.head_dim : 8);
+    m->chunk_prefill = !m->q4 && !m->moe && !(c.flags & HY_FLAG_TOKEN_PREFILL) && H % 8 == 0 && c.ffn % 8 == 0 &&
+                       od % 8 == 0;
+  }
   *out = m;
   g_err.clear();
   return HY_OK;
@@ -1186,6 +1346,21 @@ int hy_prefill(hy_model* m, hy_cache* c, int32_t seq, const int32_t* tokens_dev,
   if ((long long)c->len[seq] + n > c->cap[seq])
     return fail(HY_ERR_CAPACITY, "sequence %d: %d + %d tokens exceed capacity %d", seq, c->len[seq], n, c->cap[seq]);
   cudaStream_t st = (cudaStream_t)stream;
+  if (m->chunk_prefill && n > 0) {
+    const int P = std::min(n, prefill_chunk_rows());
+    int rc = prefill_buffers(c, P);
+    if (rc != HY_OK) return rc;
+    const int t_start = c->len[seq];
+    for (int i0 = 0; i0 < n; i0 += P) {
+      const int cn = std::min(P, n - i0);
+      rc = prefill_chunk(c, seq, tokens_dev + i0, cn, t_start + i0, i0 + cn == n, logits_dev, st);
+      if (rc != HY_OK) return rc;
+    }
+    cudaError_t e = prefill::set_len(c->d_len + seq, t_start + n, st);
+    if (e != cudaSuccess) return fail(HY_ERR_CUDA, "position update: %s", cudaGetErrorString(e));
+    c->len[seq] = t_start + n;
+    return HY_OK;
+  }
   const std::vector<int> one{seq};
   for (int i = 0; i < n; ++i) {
     float* lg = (i == n - 1) ? logits_dev : nullptr;

@@ -55,6 +55,7 @@ extern "C" {
 #define HY_FLAG_DEBUG 1u    /* keep per-layer hidden states and router results of the last step */
 #define HY_FLAG_NO_GRAPH 2u /* launch kernels one by one instead of replaying a CUDA graph */
 #define HY_FLAG_NO_PDL 4u   /* no programmatic dependent launch between kernels */
+#define HY_FLAG_TOKEN_PREFILL 16u /* run prompts token by token through the decode step (no chunked prefill) */
 /* Other flag bits are refused (HY_ERR_ARG). */
 
 /* Model shape.  [Strata] "The Beast: Qwen 3.5 Hybrid Architecture": Gated
@@ -191,9 +192,18 @@ int hy_experts_read(hy_cache* c, void* stream, uint64_t* total_out);
 int32_t hy_step_kernels(const hy_cache* c);
 
 /* Run the n prompt tokens tokens_dev[0..n) of sequence `seq` through the
- * model one position at a time, filling its caches.  logits_dev (nullable)
- * receives the FP32 logits [V] of the last token.  HY_ERR_CAPACITY (nothing
- * launched) if len + n > capacity. */
+ * model at positions len .. len+n-1, filling its caches.  logits_dev
+ * (nullable) receives the FP32 logits [V] of the last token.
+ * HY_ERR_CAPACITY (nothing launched) if len + n > capacity.  bf16 dense
+ * models run the prompt in chunks of up to 2048 tokens (HY_PREFILL_CHUNK in
+ * the environment overrides) through tensor-core GEMMs (tcgen05, the
+ * activations as bf16 hi + lo parts, FP32 accumulation) and prompt kernels
+ * of the mixers, with buffers the library allocates at the first such call;
+ * the caches it leaves equal those of a token-by-token prefill within
+ * rounding.  MoE and 4-bit models, and models created with
+ * HY_FLAG_TOKEN_PREFILL, run the prompt one position at a time through the
+ * decode step.  [Strata] "Act 1" (batched chunk kernels: one launch per layer
+ * for all prompt tokens). */
 int hy_prefill(hy_model* m, hy_cache* c, int32_t seq, const int32_t* tokens_dev, int32_t n, float* logits_dev,
                void* stream);
 
