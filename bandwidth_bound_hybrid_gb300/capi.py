@@ -85,6 +85,8 @@ SIGNATURES = {
     "hy_op_gemm_workspace": (sz, [i32, i32]),
     "hy_op_gemm": (ctypes.c_int, [vp, i32, i32, i32, vp, i32, vp, f32, vp, i32, i32, vp, vp]),
     "hy_op_gemm_swiglu": (ctypes.c_int, [vp, vp, i32, i32, i32, vp, i32, vp, f32, vp, vp, i32, vp, vp]),
+    "hy_op_moe_gateup": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, f32, vp, vp, vp, vp]),
+    "hy_op_moe_down": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]),
     "hy_op_argmax_workspace": (sz, []),
     "hy_op_gemv_argmax": (ctypes.c_int, [vp, i32, i32, vp, vp, f32, vp, vp, vp, vp]),
     "hy_op_gdn_step": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp]),

@@ -1678,6 +1678,80 @@ int hy_op_gemm_swiglu(const void* Wg_dev, const void* Wu_dev, int32_t N, int32_t
   return op_gemm_run(p, Wg_dev, Wu_dev, x_dev, ldx, norm_g_dev, eps, workspace_dev, stream);
 }
 
+int hy_op_moe_gateup(const void* exp_gate_dev, const void* exp_up_dev, const void* sh_gate_dev, const void* sh_up_dev,
+                     int32_t n_experts, int32_t top_k, int32_t expert_ffn, int32_t hidden,
+                     const float* router_logits_dev, const float* x_dev, const float* norm_g_dev, float eps,
+                     float* h_dev, int32_t* ids_dev, float* w_dev, void* stream) {
+  if (!aligned16(exp_gate_dev) || !aligned16(exp_up_dev) || !aligned16(sh_gate_dev) || !aligned16(sh_up_dev) ||
+      !router_logits_dev || !aligned16(x_dev) || !h_dev || !ids_dev || !w_dev || n_experts < 1 || top_k < 1 ||
+      top_k > gemv::kMaxTopK || top_k > n_experts || expert_ffn <= 0 || hidden <= 0 || hidden % 8)
+    return fail(HY_ERR_ARG, "bad MoE gate/up arguments");
+  if (n_experts > gemv::kMaxExperts - 1) return fail(HY_ERR_UNSUPPORTED, "at most %d routed experts", gemv::kMaxExperts - 1);
+  gemv::Params p;
+  memset(&p, 0, sizeof(p));
+  p.exp_base[0] = (const uint8_t*)exp_gate_dev;
+  p.exp_base[1] = (const uint8_t*)exp_up_dev;
+  p.sh_base[0] = (const uint8_t*)sh_gate_dev;
+  p.sh_base[1] = (const uint8_t*)sh_up_dev;
+  p.exp_stride = (long long)expert_ffn * hidden * 2;
+  p.moe_ids = ids_dev;
+  p.top_k = top_k;
+  p.n_experts = n_experts;
+  p.slot_rows = expert_ffn;
+  p.sh_rows = expert_ffn;
+  p.R = (top_k + 1) * expert_ffn;
+  p.C = hidden;
+  p.x = x_dev;
+  p.norm_g = norm_g_dev;
+  p.eps = eps;
+  p.y = h_dev;
+  p.route_here = 1;
+  p.router_logits = router_logits_dev;
+  p.out_ids = ids_dev;
+  p.out_w = w_dev;
+  unsigned* guard = nullptr;
+  int rc = op_guard(&guard);
+  if (rc != HY_OK) return rc;
+  p.guard = guard;
+  const gemv::Plan pl = gemv::plan(p.R, p.C, 2, op_nsm(), norm_g_dev != nullptr);
+  if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no GEMV plan for the expert gate/up (%d x %d)", p.R, p.C);
+  cudaError_t e = gemv::launch(p, pl, gemv::kSrcExpertRows, gemv::kInX, gemv::kEpiSwiglu, (cudaStream_t)stream, false);
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "expert gate/up launch: %s", cudaGetErrorString(e));
+  return HY_OK;
+}
+
+int hy_op_moe_down(const void* exp_down_dev, const void* sh_down_dev, int32_t n_experts, int32_t top_k,
+                   int32_t expert_ffn, int32_t hidden, const int32_t* ids_dev, const float* w_dev, const float* h_dev,
+                   float* y_dev, void* stream) {
+  if (!aligned16(exp_down_dev) || !aligned16(sh_down_dev) || !ids_dev || !aligned16(w_dev) || !aligned16(h_dev) ||
+      !y_dev || n_experts < 1 || top_k < 1 || top_k > gemv::kMaxTopK || expert_ffn <= 0 || expert_ffn % 8 ||
+      hidden <= 0)
+    return fail(HY_ERR_ARG, "bad MoE down arguments");
+  gemv::Params p;
+  memset(&p, 0, sizeof(p));
+  p.exp_base[0] = (const uint8_t*)exp_down_dev;
+  p.sh_base[0] = (const uint8_t*)sh_down_dev;
+  p.exp_stride = (long long)hidden * expert_ffn * 2;
+  p.moe_ids = ids_dev;
+  p.moe_w = w_dev;
+  p.top_k = top_k;
+  p.n_experts = n_experts;
+  p.seg_cols = expert_ffn;
+  p.R = hidden;
+  p.C = (top_k + 1) * expert_ffn;
+  p.x = h_dev;
+  p.y = y_dev;
+  unsigned* guard = nullptr;
+  int rc = op_guard(&guard);
+  if (rc != HY_OK) return rc;
+  p.guard = guard;
+  const gemv::Plan pl = gemv::plan(p.R, p.C, 1, op_nsm(), false);
+  if (!pl.ok) return fail(HY_ERR_UNSUPPORTED, "no GEMV plan for the expert down (%d x %d)", p.R, p.C);
+  cudaError_t e = gemv::launch(p, pl, gemv::kSrcExpertSegs, gemv::kInMoeZ, gemv::kEpiResid, (cudaStream_t)stream, false);
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "expert down launch: %s", cudaGetErrorString(e));
+  return HY_OK;
+}
+
 size_t hy_op_argmax_workspace(void) { return 256 + 1024 * 8; }
 
 int hy_op_gemv_argmax(const void* W_dev, int32_t rows, int32_t cols, const float* x_dev, const float* norm_g_dev,

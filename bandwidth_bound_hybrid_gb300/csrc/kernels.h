@@ -9,6 +9,30 @@
 
 namespace hy {
 
+// ---------------------------------------------------------------- GDN
+namespace gdn {
+constexpr int kRowsPerCta = 16;
+constexpr int kThreads = 128;
+constexpr int kMaxB = 8;
+struct Params {
+  const float* y;          // projection output: q|k|v|a|b  (conv_channels + 2*nh)
+  const uint16_t* conv_w;  // bf16 [channels][conv_k]
+  float* conv_state;       // ring of conv_k slots [conv_k][channels]; slot t % conv_k holds input t
+  float* S;                // [nh][dv][dk]
+  const int* pos;          // position t of the token
+  float* o;                // [nh*dv]
+  int nh, dk, dv, conv_k;
+  unsigned* guard;
+  // batch (nb > 0): token z = blockIdx.z uses y + z*ld_y, o + z*ld_o and its
+  // own sequence's state, conv ring and position
+  int nb, ld_y, ld_o;
+  float* S_b[kMaxB];
+  float* conv_b[kMaxB];
+  const int* pos_b[kMaxB];
+};
+cudaError_t launch(const Params& p, cudaStream_t st, bool pdl);
+}  // namespace gdn
+
 // ---------------------------------------------------------------- GEMV
 namespace gemv {
 
@@ -82,7 +106,7 @@ struct Params {
   unsigned* counter;            // last-CTA ticket (zero between launches)
   int* ids_out;                 // argmax result
   int* len_inc;                 // incremented once after the argmax (nullable)
-  float* router_logits;         // route_here: the router's stored logits [n_experts + 1]
+  const float* router_logits;   // route_here: the router's stored logits [n_experts + 1]
   int* out_ids;                 // route_here: selected experts [top_k] (CTA 0 writes them)
   float* out_w;                 // route_here: routing weights [top_k + 1]
   int* dbg_ids;                 // route_here debug copies (nullable)
@@ -114,29 +138,6 @@ cudaError_t launch(const Params& p, const Plan& pl, int src, int in, int epi, cu
 
 }  // namespace gemv
 
-// ---------------------------------------------------------------- GDN
-namespace gdn {
-constexpr int kRowsPerCta = 16;
-constexpr int kThreads = 128;
-constexpr int kMaxB = 8;
-struct Params {
-  const float* y;          // projection output: q|k|v|a|b  (conv_channels + 2*nh)
-  const uint16_t* conv_w;  // bf16 [channels][conv_k]
-  float* conv_state;       // ring of conv_k slots [conv_k][channels]; slot t % conv_k holds input t
-  float* S;                // [nh][dv][dk]
-  const int* pos;          // position t of the token
-  float* o;                // [nh*dv]
-  int nh, dk, dv, conv_k;
-  unsigned* guard;
-  // batch (nb > 0): token z = blockIdx.z uses y + z*ld_y, o + z*ld_o and its
-  // own sequence's state, conv ring and position
-  int nb, ld_y, ld_o;
-  float* S_b[kMaxB];
-  float* conv_b[kMaxB];
-  const int* pos_b[kMaxB];
-};
-cudaError_t launch(const Params& p, cudaStream_t st, bool pdl);
-}  // namespace gdn
 
 // ---------------------------------------------------------------- attention
 namespace attn {

@@ -306,6 +306,29 @@ int hy_op_gemm_swiglu(const void* Wg_dev, const void* Wu_dev, int32_t N, int32_t
                       int32_t ldx, const float* norm_g_dev, float eps, uint16_t* h_hi_dev, uint16_t* h_lo_dev,
                       int32_t ldh, void* workspace_dev, void* stream);
 
+/* MoE FFN of one token in two kernels ([14h] "Eight levers that worked":
+ * router top-k fused into the expert-gathered GEMV; "The router with 257
+ * rows": the shared expert's sigmoid gate as the router's extra row).
+ * hy_op_moe_gateup: from the router logits [n_experts + 1] (the last is the
+ * shared expert's gate), every CTA picks the top_k experts (largest logit,
+ * lowest index on ties), then h[s * Fe + r] = silu(g) * u of the picked
+ * experts' gate / up rows (slots 0..top_k-1, in selection order) and of the
+ * shared expert (slot top_k), with xhat = x or RMSNorm(x) * norm_g.  ids_dev
+ * [top_k] receives the picks, w_dev [top_k + 1] the softmax over the picked
+ * logits and sigmoid of the shared gate.  Expert tensors bf16: exp_gate /
+ * exp_up [n_experts][Fe][hidden], sh_gate / sh_up [Fe][hidden]; h FP32
+ * [(top_k + 1) * Fe].
+ * hy_op_moe_down: y[H] += sum_s w[s] * Wd_s h_s over the picked experts'
+ * down matrices (exp_down [n_experts][hidden][Fe]) and the shared expert's
+ * (sh_down [hidden][Fe]).  top_k <= 16, n_experts <= 511. */
+int hy_op_moe_gateup(const void* exp_gate_dev, const void* exp_up_dev, const void* sh_gate_dev, const void* sh_up_dev,
+                     int32_t n_experts, int32_t top_k, int32_t expert_ffn, int32_t hidden,
+                     const float* router_logits_dev, const float* x_dev, const float* norm_g_dev, float eps,
+                     float* h_dev, int32_t* ids_dev, float* w_dev, void* stream);
+int hy_op_moe_down(const void* exp_down_dev, const void* sh_down_dev, int32_t n_experts, int32_t top_k,
+                   int32_t expert_ffn, int32_t hidden, const int32_t* ids_dev, const float* w_dev, const float* h_dev,
+                   float* y_dev, void* stream);
+
 /* Greedy head: logits = W * xhat (logits_dev nullable), *id_dev = argmax
  * (lowest index on ties).  workspace_dev: hy_op_argmax_workspace() bytes,
  * zeroed before its first use and left zeroed after each call.

@@ -189,6 +189,69 @@ void orc_gdn_step(float* S, int32_t dk, int32_t dv, const double* q, const doubl
   free(M);
 }
 
+/* int8 quantisation of one cached vector x[0..n) with one FP32 scale:
+ * "hanzo-engine: A Portable Single-Binary LLM Inference Engine...", section
+ * "System Architecture" (an int8 KV cache with one f32 scale per cached
+ * vector) and "Results" ("int8 KV").  The pages name only the format; the
+ * rule is the plainest symmetric one: with a = max_i |x_i| (x taken in FP32,
+ * where the decisions are made), scale = a / 127 and q_i = round-half-even(x_i
+ * * (127 / a)) in FP32, clamped to [-127, 127]; a = 0 gives codes 0 and scale
+ * 0.  The stored value of element i is q_i * scale. */
+void orc_quant_i8(const double* x, int32_t n, int8_t* q, float* scale) {
+  float amax = 0.0f;
+  for (int32_t i = 0; i < n; ++i) {
+    float f = fabsf((float)x[i]);
+    if (f > amax) amax = f;
+  }
+  if (amax == 0.0f) {
+    for (int32_t i = 0; i < n; ++i) q[i] = 0;
+    *scale = 0.0f;
+    return;
+  }
+  volatile float inv = 127.0f / amax; /* FP32 division, as the kernel's */
+  for (int32_t i = 0; i < n; ++i) {
+    volatile float prod = (float)x[i] * inv; /* one FP32 rounding of the product */
+    float r = rintf(prod);
+    if (r > 127.0f) r = 127.0f;
+    if (r < -127.0f) r = -127.0f;
+    q[i] = (int8_t)r;
+  }
+  *scale = amax / 127.0f;
+}
+
+/* Attention of orc_attention over an int8 cache: K and V values are the
+ * stored codes times their vector's scale. */
+void orc_attention_i8(const double* q, const int8_t* Kq, const float* Ks, const int8_t* Vq, const float* Vs,
+                      int32_t nq, int32_t nkv, int32_t hd, int32_t cap, int32_t npos, double* o) {
+  int32_t group = nq / nkv;
+  double scale = 1.0 / sqrt((double)hd);
+  double* s = (double*)malloc(sizeof(double) * (size_t)(npos > 0 ? npos : 1));
+  for (int32_t j = 0; j < nq; ++j) {
+    int32_t g = j / group;
+    double mx = -INFINITY;
+    for (int32_t p = 0; p < npos; ++p) {
+      const int8_t* kr = Kq + ((int64_t)g * cap + p) * hd;
+      double ks = (double)Ks[(int64_t)g * cap + p];
+      double acc = 0.0;
+      for (int32_t d = 0; d < hd; ++d) acc += q[(int64_t)j * hd + d] * ((double)kr[d] * ks);
+      s[p] = acc * scale;
+      if (s[p] > mx) mx = s[p];
+    }
+    double den = 0.0;
+    for (int32_t p = 0; p < npos; ++p) {
+      s[p] = exp(s[p] - mx);
+      den += s[p];
+    }
+    for (int32_t d = 0; d < hd; ++d) {
+      double acc = 0.0;
+      for (int32_t p = 0; p < npos; ++p)
+        acc += s[p] * ((double)Vq[((int64_t)g * cap + p) * hd + d] * (double)Vs[(int64_t)g * cap + p]);
+      o[(int64_t)j * hd + d] = npos > 0 ? acc / den : 0.0;
+    }
+  }
+  free(s);
+}
+
 /* Single-pass softmax attention of nq query heads over positions [0, npos) of
  * a bf16 cache [nkv][cap][hd]; query head j reads kv head j / (nq / nkv).
  * [Strata] "The Beast" (GQA layers, bf16 KV cache [kv_heads, seq_len, dim]);
@@ -348,6 +411,17 @@ int orc_cache_create(const orc_config* cfg, int32_t capacity, orc_cache* out) {
   out->conv_state = (double*)calloc((size_t)(cs > 0 ? cs : 1), sizeof(double));
   out->k_cache = (uint16_t*)calloc((size_t)(kv > 0 ? kv : 1), sizeof(uint16_t));
   out->v_cache = (uint16_t*)calloc((size_t)(kv > 0 ? kv : 1), sizeof(uint16_t));
+  if (cfg->kv_format == 1) {
+    int64_t ns = na * (int64_t)cfg->attn_kv_heads * capacity;
+    out->k_q = (int8_t*)calloc((size_t)(kv > 0 ? kv : 1), 1);
+    out->v_q = (int8_t*)calloc((size_t)(kv > 0 ? kv : 1), 1);
+    out->k_s = (float*)calloc((size_t)(ns > 0 ? ns : 1), sizeof(float));
+    out->v_s = (float*)calloc((size_t)(ns > 0 ? ns : 1), sizeof(float));
+    if (!out->k_q || !out->v_q || !out->k_s || !out->v_s) {
+      orc_cache_destroy(out);
+      return -1;
+    }
+  }
   if (!out->gdn_state || !out->conv_state || !out->k_cache || !out->v_cache) {
     orc_cache_destroy(out);
     return -1;
@@ -360,6 +434,10 @@ void orc_cache_destroy(orc_cache* c) {
   free(c->conv_state);
   free(c->k_cache);
   free(c->v_cache);
+  free(c->k_q);
+  free(c->v_q);
+  free(c->k_s);
+  free(c->v_s);
   memset(c, 0, sizeof(*c));
 }
 
@@ -369,6 +447,13 @@ void orc_cache_reset(const orc_config* cfg, orc_cache* c) {
   memset(c->conv_state, 0, sizeof(double) * (size_t)(ng * (int64_t)(cfg->conv_k - 1) * conv_channels(cfg)));
   memset(c->k_cache, 0, sizeof(uint16_t) * (size_t)(na * (int64_t)cfg->attn_kv_heads * c->capacity * cfg->head_dim));
   memset(c->v_cache, 0, sizeof(uint16_t) * (size_t)(na * (int64_t)cfg->attn_kv_heads * c->capacity * cfg->head_dim));
+  if (c->k_q) {
+    size_t nkv = (size_t)(na * (int64_t)cfg->attn_kv_heads * c->capacity);
+    memset(c->k_q, 0, nkv * (size_t)cfg->head_dim);
+    memset(c->v_q, 0, nkv * (size_t)cfg->head_dim);
+    memset(c->k_s, 0, nkv * sizeof(float));
+    memset(c->v_s, 0, nkv * sizeof(float));
+  }
   c->len = 0;
 }
 
@@ -424,14 +509,28 @@ int orc_forward_token(const orc_config* cfg, const orc_weights* w, orc_cache* c,
       double* v = y + (int64_t)(nq + nkv) * hd;
       for (int32_t j = 0; j < nq; ++j) orc_rope(q + (int64_t)j * hd, hd, pos, cfg->rope_theta);
       for (int32_t g = 0; g < nkv; ++g) orc_rope(k + (int64_t)g * hd, hd, pos, cfg->rope_theta);
-      uint16_t* Kc = c->k_cache + (int64_t)ai * nkv * c->capacity * hd;
-      uint16_t* Vc = c->v_cache + (int64_t)ai * nkv * c->capacity * hd;
-      for (int32_t g = 0; g < nkv; ++g)
-        for (int32_t e = 0; e < hd; ++e) {
-          Kc[((int64_t)g * c->capacity + pos) * hd + e] = orc_to_bf16(k[(int64_t)g * hd + e]);
-          Vc[((int64_t)g * c->capacity + pos) * hd + e] = orc_to_bf16(v[(int64_t)g * hd + e]);
+      if (cfg->kv_format == 1) {
+        /* int8 cache: each new k and v vector quantised with its own scale */
+        int8_t* Kq = c->k_q + (int64_t)ai * nkv * c->capacity * hd;
+        int8_t* Vq = c->v_q + (int64_t)ai * nkv * c->capacity * hd;
+        float* Ks = c->k_s + (int64_t)ai * nkv * c->capacity;
+        float* Vs = c->v_s + (int64_t)ai * nkv * c->capacity;
+        for (int32_t g = 0; g < nkv; ++g) {
+          int64_t row = (int64_t)g * c->capacity + pos;
+          orc_quant_i8(k + (int64_t)g * hd, hd, Kq + row * hd, Ks + row);
+          orc_quant_i8(v + (int64_t)g * hd, hd, Vq + row * hd, Vs + row);
         }
-      orc_attention(q, Kc, Vc, nq, nkv, hd, c->capacity, pos + 1, o);
+        orc_attention_i8(q, Kq, Ks, Vq, Vs, nq, nkv, hd, c->capacity, pos + 1, o);
+      } else {
+        uint16_t* Kc = c->k_cache + (int64_t)ai * nkv * c->capacity * hd;
+        uint16_t* Vc = c->v_cache + (int64_t)ai * nkv * c->capacity * hd;
+        for (int32_t g = 0; g < nkv; ++g)
+          for (int32_t e = 0; e < hd; ++e) {
+            Kc[((int64_t)g * c->capacity + pos) * hd + e] = orc_to_bf16(k[(int64_t)g * hd + e]);
+            Vc[((int64_t)g * c->capacity + pos) * hd + e] = orc_to_bf16(v[(int64_t)g * hd + e]);
+          }
+        orc_attention(q, Kc, Vc, nq, nkv, hd, c->capacity, pos + 1, o);
+      }
       ++ai;
     } else {
       /* Gated DeltaNet layer: conv over q|k|v, per-head gates, delta rule. */

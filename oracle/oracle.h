@@ -48,6 +48,7 @@ typedef struct {
   int32_t n_experts, top_k, expert_ffn, shared_ffn;
   double rms_eps, rope_theta;
   const uint8_t* is_attn; /* [n_layers]: 1 = GQA attention layer, 0 = Gated DeltaNet */
+  int32_t kv_format;      /* 0: bf16 KV cache; 1: int8 codes with one FP32 scale per cached vector */
 } orc_config;
 
 typedef struct {
@@ -75,8 +76,12 @@ typedef struct {
   int32_t len, capacity;
   float* gdn_state;    /* per GDN layer: [nh][dv][dk] FP32 */
   double* conv_state;  /* per GDN layer: [conv_k-1][channels], oldest first */
-  uint16_t* k_cache;   /* per attention layer: [nkv][capacity][hd] bf16 */
+  uint16_t* k_cache;   /* per attention layer: [nkv][capacity][hd] bf16 (kv_format 0) */
   uint16_t* v_cache;
+  int8_t* k_q;         /* kv_format 1, per attention layer: codes [nkv][capacity][hd] */
+  int8_t* v_q;
+  float* k_s;          /* kv_format 1, per attention layer: scales [nkv][capacity] */
+  float* v_s;
 } orc_cache;
 
 /* --- scalar formats ------------------------------------------------------ */
@@ -100,6 +105,9 @@ void orc_attention(const double* q, const uint16_t* K, const uint16_t* V, int32_
                    int32_t cap, int32_t npos, double* o);
 void orc_attention_split(const double* q, const uint16_t* K, const uint16_t* V, int32_t nq, int32_t nkv,
                          int32_t hd, int32_t cap, int32_t npos, int32_t nsplit, double* o);
+void orc_quant_i8(const double* x, int32_t n, int8_t* q, float* scale);
+void orc_attention_i8(const double* q, const int8_t* Kq, const float* Ks, const int8_t* Vq, const float* Vs,
+                      int32_t nq, int32_t nkv, int32_t hd, int32_t cap, int32_t npos, double* o);
 int32_t orc_argmax(const double* v, int64_t n);
 void orc_topk(const double* r, int32_t n, int32_t k, int32_t* ids);
 void orc_softmax(const double* x, int32_t n, double* p);

@@ -33,7 +33,7 @@ class OrcConfig(ctypes.Structure):
     _fields_ = [(n, c_i32) for n in ("n_layers", "hidden", "vocab", "ffn", "gdn_heads", "gdn_dk", "gdn_dv", "conv_k",
                                      "attn_q_heads", "attn_kv_heads", "head_dim", "n_experts", "top_k",
                                      "expert_ffn", "shared_ffn")] + [
-        ("rms_eps", c_f64), ("rope_theta", c_f64), ("is_attn", c_vp)]
+        ("rms_eps", c_f64), ("rope_theta", c_f64), ("is_attn", c_vp), ("kv_format", c_i32)]
 
 
 class OrcLayer(ctypes.Structure):
@@ -49,7 +49,7 @@ class OrcWeights(ctypes.Structure):
 
 class OrcCache(ctypes.Structure):
     _fields_ = [("len", c_i32), ("capacity", c_i32), ("gdn_state", c_vp), ("conv_state", c_vp),
-                ("k_cache", c_vp), ("v_cache", c_vp)]
+                ("k_cache", c_vp), ("v_cache", c_vp), ("k_q", c_vp), ("v_q", c_vp), ("k_s", c_vp), ("v_s", c_vp)]
 
 
 _lib = None
@@ -76,6 +76,8 @@ def lib():
         L.orc_gdn_step.argtypes = [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_f64, c_f64, c_vp]
         L.orc_attention.argtypes = [c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp]
         L.orc_attention_split.argtypes = [c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp]
+        L.orc_quant_i8.argtypes = [c_vp, c_i32, c_vp, c_vp]
+        L.orc_attention_i8.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp]
         L.orc_argmax.argtypes, L.orc_argmax.restype = [c_vp, c_i64], c_i32
         L.orc_topk.argtypes = [c_vp, c_i32, c_i32, c_vp]
         L.orc_softmax.argtypes = [c_vp, c_i32, c_vp]
@@ -88,6 +90,7 @@ def lib():
         L.orc_set_threads.argtypes = [ctypes.c_int]
         for f in (L.orc_mat_row, L.orc_gemv, L.orc_rmsnorm, L.orc_l2norm, L.orc_rope, L.orc_conv_step,
                   L.orc_gdn_step, L.orc_attention, L.orc_attention_split, L.orc_topk, L.orc_softmax,
+                  L.orc_quant_i8, L.orc_attention_i8,
                   L.orc_cache_destroy, L.orc_cache_reset, L.orc_set_threads):
             f.restype = None
     return _lib
@@ -196,6 +199,27 @@ def attention(q, K, V, npos: int, nsplit: int = 0) -> np.ndarray:
     return o
 
 
+def quant_i8(x):
+    """(int8 codes, FP32 scale) of one cached vector."""
+    x = f64(x)
+    q = np.zeros(x.size, dtype=np.int8)
+    sc = np.zeros(1, dtype=np.float32)
+    lib().orc_quant_i8(_p(x), x.size, _p(q), _p(sc))
+    return q, float(sc[0])
+
+
+def attention_i8(q, Kq, Ks, Vq, Vs, npos: int) -> np.ndarray:
+    """q: [nq][hd]; Kq, Vq: int8 codes [nkv][cap][hd]; Ks, Vs: FP32 scales [nkv][cap]."""
+    q = f64(q)
+    nq, hd = q.shape
+    Kq, Vq = np.ascontiguousarray(Kq, dtype=np.int8), np.ascontiguousarray(Vq, dtype=np.int8)
+    Ks, Vs = np.ascontiguousarray(Ks, dtype=np.float32), np.ascontiguousarray(Vs, dtype=np.float32)
+    nkv, cap, _ = Kq.shape
+    o = np.zeros_like(q)
+    lib().orc_attention_i8(_p(q), _p(Kq), _p(Ks), _p(Vq), _p(Vs), nq, nkv, hd, cap, npos, _p(o))
+    return o
+
+
 def argmax(v) -> int:
     v = f64(v)
     return int(lib().orc_argmax(_p(v), v.size))
@@ -257,6 +281,7 @@ class Oracle:
                   "attn_kv_heads", "head_dim", "n_experts", "top_k", "expert_ffn", "shared_ffn"):
             setattr(cfg, n, int(getattr(s, n)))
         cfg.rms_eps, cfg.rope_theta = float(s.rms_eps), float(s.rope_theta)
+        cfg.kv_format = int(getattr(s, "kv_format", 0))
         self._is_attn = np.array([1 if s.is_attn(l) else 0 for l in range(s.n_layers)], dtype=np.uint8)
         cfg.is_attn = _p(self._is_attn)
         self.cfg = cfg
@@ -329,6 +354,19 @@ class Oracle:
         k = np.ctypeslib.as_array(base, shape=(n * (attn_index + 1),))[n * attn_index:]
         v = np.ctypeslib.as_array(vbase, shape=(n * (attn_index + 1),))[n * attn_index:]
         return k.reshape(s.attn_kv_heads, cap, s.head_dim), v.reshape(s.attn_kv_heads, cap, s.head_dim)
+
+    def kv_cache_i8(self, attn_index: int):
+        """(K codes, K scales, V codes, V scales) of an int8 cache layer."""
+        s, cap = self.shape, self.cache.capacity
+        n, ns = s.attn_kv_heads * cap * s.head_dim, s.attn_kv_heads * cap
+        out = []
+        for ptr, cnt, ty, shp in ((self.cache.k_q, n, ctypes.c_int8, (s.attn_kv_heads, cap, s.head_dim)),
+                                  (self.cache.k_s, ns, ctypes.c_float, (s.attn_kv_heads, cap)),
+                                  (self.cache.v_q, n, ctypes.c_int8, (s.attn_kv_heads, cap, s.head_dim)),
+                                  (self.cache.v_s, ns, ctypes.c_float, (s.attn_kv_heads, cap))):
+            base = ctypes.cast(ptr, ctypes.POINTER(ty))
+            out.append(np.ctypeslib.as_array(base, shape=(cnt * (attn_index + 1),))[cnt * attn_index:].reshape(shp))
+        return tuple(out)
 
     def gdn_state(self, gdn_index: int) -> np.ndarray:
         s = self.shape

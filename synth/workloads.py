@@ -72,6 +72,7 @@ class ModelShape:
     rms_eps: float = 1e-6
     rope_theta: float = 1e4
     weight_format: int = 0        # 0 bf16, 1 4-bit blocks of 32
+    kv_format: int = 0            # 0 bf16 KV cache, 1 int8 codes with one FP32 scale per cached vector
     seed: int = 0
 
     @property

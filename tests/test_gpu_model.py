@@ -220,3 +220,4 @@ def test_moe_with_511_experts(built):
     shape = dataclasses.replace(workloads.TINY, name="tiny-moe-e511", vocab=512, ffn=0, n_experts=511, top_k=8,
                                 expert_ffn=64, shared_ffn=64)
     run_parity(shape, 8, 3)
+

@@ -157,6 +157,25 @@ def _bf16_round(x):
     return np.ldexp(np.rint(m * 256.0), e - 8)
 
 
+def _i8_round(rows):
+    """Each row as its int8 cache value: codes round-half-even(x * (127 / a))
+    with a = max |x| (FP32 decisions), times the scale a / 127."""
+    out = np.empty_like(rows)
+    for i, r in enumerate(np.atleast_2d(rows)):
+        xf = r.astype(np.float32)
+        a = np.float32(np.abs(xf).max())
+        if a == 0:
+            out[i] = 0.0
+            continue
+        codes = np.clip(np.rint(xf * (np.float32(127.0) / a)), -127, 127)
+        out[i] = codes.astype(np.float64) * float(a / np.float32(127.0))
+    return out
+
+
+def _kv_round(shape, x):
+    return _i8_round(x) if getattr(shape, "kv_format", 0) == 1 else _bf16_round(x)
+
+
 def _rope_complex(v, pos, theta):
     h = v.shape[-1] // 2
     z = (v[..., :h] + 1j * v[..., h:]) * np.exp(1j * pos * theta ** (-2.0 * np.arange(h) / (2 * h)))
@@ -178,8 +197,8 @@ def _closed_form(shape, w, toks):
             if shape.is_attn(l):
                 nq, nkv, hd = shape.attn_q_heads, shape.attn_kv_heads, shape.head_dim
                 q = _rope_complex(y[:nq * hd].reshape(nq, hd), pos, shape.rope_theta)
-                k = _bf16_round(_rope_complex(y[nq * hd:(nq + nkv) * hd].reshape(nkv, hd), pos, shape.rope_theta))
-                v = _bf16_round(y[(nq + nkv) * hd:]).reshape(nkv, hd)
+                k = _kv_round(shape, _rope_complex(y[nq * hd:(nq + nkv) * hd].reshape(nkv, hd), pos, shape.rope_theta))
+                v = _kv_round(shape, y[(nq + nkv) * hd:].reshape(nkv, hd))
                 Ks = mem.get(l, ([], []))[0] + [k]
                 Vs = mem.get(l, ([], []))[1] + [v]
                 mem[l] = (Ks, Vs)
@@ -288,3 +307,8 @@ def test_router_load_is_near_uniform_for_uncorrelated_inputs():
         counts = np.bincount(np.concatenate([orc.topk(r, K) for r in logits]), minlength=E)
         assert counts.sum() == 4000 * K and counts.min() > 0
         assert counts.max() / counts.mean() <= 1.5, (l, counts.max() / counts.mean())
+
+
+def test_first_two_tokens_int8_kv_match_closed_form():
+    """The int8 KV cache (one FP32 scale per cached vector) in the whole model."""
+    _check_closed_form(dataclasses.replace(TINY, name="tiny-kv8", kv_format=1), ((0, 77), (1023, 1023), (5, 6)))

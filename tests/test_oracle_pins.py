@@ -341,3 +341,66 @@ def test_softmax_over_selected_equals_renormalised_full_softmax():
     full = scipy.special.softmax(r)
     np.testing.assert_allclose(p_sel, full[ids] / full[ids].sum(), rtol=1e-13)
     np.testing.assert_allclose(orc.softmax(r), full, rtol=1e-13)
+
+
+# ------------------------------------------------------------------ int8 KV cache
+# One cached vector -> int8 codes and one FP32 scale ("hanzo-engine...",
+# "System Architecture": int8 KV with one f32 scale per vector).
+
+def test_int8_quant_worked_example():
+    """amax 1: scale 1/127; -0.5 * 127 = -63.5 is a tie and goes to the even
+    -64; 0.25 * 127 = 31.75 rounds to 32."""
+    q, s = orc.quant_i8([1.0, -0.5, 0.25, 0.0])
+    np.testing.assert_array_equal(q, [127, -64, 32, 0])
+    assert s == float(np.float32(1.0) / np.float32(127.0))
+
+
+def test_int8_quant_invariants():
+    rng = np.random.default_rng(12)
+    for n in (1, 7, 64, 128, 256):
+        x = rng.standard_normal(n) * rng.uniform(1e-3, 30)
+        q, s = orc.quant_i8(x)
+        i = int(np.argmax(np.abs(x)))
+        assert abs(int(q[i])) == 127 and np.sign(q[i]) == np.sign(x[i])
+        assert np.all(np.abs(q.astype(np.int32)) <= 127)
+        # every element within half a step of its code (plus the FP32 rounding of the inputs)
+        assert np.all(np.abs(x - q.astype(np.float64) * s) <= s * (0.5 + 1e-5) + 1e-6 * np.abs(x))
+        qn, sn = orc.quant_i8(-x)
+        np.testing.assert_array_equal(qn, -q)
+        assert sn == s
+    q, s = orc.quant_i8(np.zeros(16))
+    assert s == 0.0 and not q.any()
+
+
+def test_int8_attention_equals_bf16_attention_on_exact_values():
+    """Codes with scale 2^-7 give values code / 128, exact in bf16: the int8
+    attention then equals the bf16 one."""
+    rng = np.random.default_rng(3)
+    nq, nkv, hd, cap, npos = 4, 2, 16, 9, 7
+    Kq = rng.integers(-127, 128, (nkv, cap, hd)).astype(np.int8)
+    Vq = rng.integers(-127, 128, (nkv, cap, hd)).astype(np.int8)
+    Ks = np.full((nkv, cap), 2.0 ** -7, dtype=np.float32)
+    Vs = np.full((nkv, cap), 2.0 ** -7, dtype=np.float32)
+    q = rng.standard_normal((nq, hd))
+    Kb = gen.f32_to_bf16_bits((Kq.astype(np.float32) / 128.0))
+    Vb = gen.f32_to_bf16_bits((Vq.astype(np.float32) / 128.0))
+    np.testing.assert_allclose(orc.attention_i8(q, Kq, Ks, Vq, Vs, npos), orc.attention(q, Kb, Vb, npos),
+                               rtol=1e-12, atol=1e-14)
+
+
+def test_int8_attention_brute_force():
+    rng = np.random.default_rng(4)
+    nq, nkv, hd, cap, npos = 6, 3, 8, 6, 5
+    Kq = rng.integers(-127, 128, (nkv, cap, hd)).astype(np.int8)
+    Vq = rng.integers(-127, 128, (nkv, cap, hd)).astype(np.int8)
+    Ks = rng.uniform(0.001, 0.02, (nkv, cap)).astype(np.float32)
+    Vs = rng.uniform(0.001, 0.02, (nkv, cap)).astype(np.float32)
+    q = rng.standard_normal((nq, hd))
+    got = orc.attention_i8(q, Kq, Ks, Vq, Vs, npos)
+    for j in range(nq):
+        g = j // (nq // nkv)
+        K = Kq[g, :npos].astype(np.float64) * Ks[g, :npos, None]
+        V = Vq[g, :npos].astype(np.float64) * Vs[g, :npos, None]
+        sc = K @ q[j] / np.sqrt(hd)
+        p = np.exp(sc - sc.max())
+        np.testing.assert_allclose(got[j], (p / p.sum()) @ V, rtol=1e-12, atol=1e-14)
