@@ -32,8 +32,11 @@ def gdn_state_bytes_per_layer(nh: int, dk: int, dv: int) -> int:
     return nh * dv * dk * F32
 
 
-def kv_bytes_per_token(n_attn: int, nkv: int, hd: int, elem: int = BF16) -> int:
-    """K and V of one position over all attention layers."""
+def kv_bytes_per_token(n_attn: int, nkv: int, hd: int, elem: int = BF16, kv_format: int = 0) -> int:
+    """K and V of one position over all attention layers: bf16 elements, or
+    int8 codes plus one FP32 scale per cached vector (kv_format 1)."""
+    if kv_format == 1:
+        return n_attn * 2 * nkv * (hd + F32)
     return n_attn * 2 * nkv * hd * elem
 
 
@@ -74,8 +77,9 @@ def step_bytes(shape, context: int, experts_touched: int | None = None) -> StepB
                            + 2 * linear_bytes(s.shared_ffn, H, fmt) + linear_bytes(H, s.shared_ffn, fmt))
     w += H * BF16 + H * F32 + linear_bytes(s.vocab, H, fmt)  # embedding row, final norm, LM head
     state = n_gdn * (2 * gdn_state_bytes_per_layer(s.gdn_heads, s.gdn_dk, s.gdn_dv) + s.conv_k * CC * F32)
-    kv_read = kv_bytes_per_token(n_attn, s.attn_kv_heads, s.head_dim) * context
-    kv_write = kv_bytes_per_token(n_attn, s.attn_kv_heads, s.head_dim)
+    kvf = getattr(s, "kv_format", 0)
+    kv_read = kv_bytes_per_token(n_attn, s.attn_kv_heads, s.head_dim, kv_format=kvf) * context
+    kv_write = kv_bytes_per_token(n_attn, s.attn_kv_heads, s.head_dim, kv_format=kvf)
     return StepBytes(weights=w, state=state, kv_read=kv_read, kv_write=kv_write, activations=0)
 
 
@@ -100,7 +104,7 @@ def batch_step_bytes(shape, contexts, experts_touched: float | None = None) -> S
         per_exp = 2 * linear_bytes(shape.expert_ffn, shape.hidden, fmt) + linear_bytes(shape.hidden, shape.expert_ffn, fmt)
         w += int(round(shape.n_layers * per_exp * (experts_touched - round(experts_touched))))
     n_attn = sum(1 for l in range(shape.n_layers) if shape.is_attn(l))
-    kv1 = kv_bytes_per_token(n_attn, shape.attn_kv_heads, shape.head_dim)
+    kv1 = kv_bytes_per_token(n_attn, shape.attn_kv_heads, shape.head_dim, kv_format=getattr(shape, "kv_format", 0))
     return StepBytes(weights=w, state=B * one.state, kv_read=kv1 * int(sum(contexts)), kv_write=B * kv1,
                      activations=0)
 

@@ -40,7 +40,7 @@ class hy_config(ctypes.Structure):
                 ("gdn_dk", i32), ("gdn_dv", i32), ("conv_k", i32), ("attn_q_heads", i32), ("attn_kv_heads", i32),
                 ("head_dim", i32), ("attn_layer_mask", u64), ("n_experts", i32), ("top_k", i32),
                 ("expert_ffn", i32), ("shared_ffn", i32), ("rms_eps", f32), ("rope_theta", f32),
-                ("weight_format", i32), ("attn_splits", i32), ("flags", u32)]
+                ("weight_format", i32), ("attn_splits", i32), ("flags", u32), ("kv_format", i32)]
 
 
 class hy_tensor(ctypes.Structure):
@@ -94,6 +94,7 @@ SIGNATURES = {
     "hy_op_attention_workspace": (sz, [i32, i32, i32, i32]),
     "hy_op_attention": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, i32, vp, vp, vp]),
     "hy_op_attention_noalloc": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, i32, vp, vp]),
+    "hy_op_attention_i8": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32, vp, vp, vp]),
 }
 
 _lib = None

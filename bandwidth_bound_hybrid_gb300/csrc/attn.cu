@@ -36,7 +36,7 @@ struct Smem {
   static constexpr size_t total = stages + ((work + 15) & ~(size_t)15) + bars + 64;
 };
 
-template <int HD, int G>
+template <int HD, int G, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p0) {
   Params p = p0;
   if (p0.nb > 0) {  // token blockIdx.z of a batch: its sequence's cache and scratch
@@ -47,8 +47,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p0) {
     p.counter = p0.counter + z * p0.nkv;
     p.K = p0.K_b[z];
     p.V = p0.V_b[z];
+    p.Ks = p0.Ks_b[z];
+    p.Vs = p0.Vs_b[z];
     p.len = p0.len_b[z];
     p.cap = p0.cap_b[z];
+    p.cap_s = p0.cap_s_b[z];
   }
   using S_ = Smem<HD, G>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p0) {
           set_guard(p.guard, kGuardWaitTimeout);
           break;
         }
-        issue_tile<HD>(p, g, it, t, stages + s * Tile<HD>::kStageBytes, &full[s], pol);
+        issue_tile<HD, KV8>(p, g, it, t, stages + s * Tile<HD>::kStageBytes, &full[s], pol);
       }
       for (int u = (t > kStages ? t - kStages : 0); u < t; ++u)
         if (!mbar_wait(&full[u % kStages], (u / kStages) & 1)) set_guard(p.guard, kGuardWaitTimeout);
@@ -101,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p0) {
   pdl_wait();
   pdl_launch_dependents();
   Acc<HD, G> A;
-  begin_item<HD, G>(p, g, T, it, w, A, ctid);
+  begin_item<HD, G, KV8>(p, g, T, it, w, A, ctid);
   for (int t = 0; t < it.ntiles; ++t) {
     const int s = t % kStages, k = t / kStages;
     if (!mbar_wait(&full[s], k & 1)) {
@@ -109,24 +112,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p0) {
       return;
     }
     const uint8_t* st = stages + s * Tile<HD>::kStageBytes;
-    process_tile<HD, G>(reinterpret_cast<const uint16_t*>(st), reinterpret_cast<const uint16_t*>(st + Tile<HD>::kBytesKV),
-                        tile_rows<HD>(it, t), w, A, ctid);
+    if (KV8) {
+      const int r0 = it.p0 + t * Tile<HD>::TP, pad = r0 - (r0 & ~3);
+      const float* ks = reinterpret_cast<const float*>(st + scale_off<HD>()) + pad;
+      const float* vs = reinterpret_cast<const float*>(st + scale_off<HD>() + scale_span<HD>()) + pad;
+      process_tile<HD, G, true>(reinterpret_cast<const uint16_t*>(st),
+                                reinterpret_cast<const uint16_t*>(st + Tile<HD>::TP * HD), tile_rows<HD>(it, t), w, A,
+                                ctid, ks, vs);
+    } else {
+      process_tile<HD, G>(reinterpret_cast<const uint16_t*>(st),
+                          reinterpret_cast<const uint16_t*>(st + Tile<HD>::kBytesKV), tile_rows<HD>(it, t), w, A,
+                          ctid);
+    }
     if (ctid == 0) mbar_arrive(&empty[s]);
   }
-  if (it.has_new) process_tile<HD, G>(w.kn, w.vn, 1, w, A, ctid);
+  if (it.has_new) process_tile<HD, G, KV8>(w.kn, w.vn, 1, w, A, ctid, w.kvs, w.kvs + 1);
   end_item<HD, G>(p, g, sp, w, A, reinterpret_cast<float*>(stages), ctid);
 }
 
 template <int HD, int G>
-void* kern() {
-  return (void*)k_attn<HD, G>;
+void* kern(bool kv8) {
+  return kv8 ? (void*)k_attn<HD, G, true> : (void*)k_attn<HD, G, false>;
 }
 
-void* pick(int hd, int G, size_t* smem) {
+void* pick(int hd, int G, size_t* smem, bool kv8) {
 #define HY_ATTN_CASE(H_, G_)            \
   if (hd == H_ && G == G_) {            \
     *smem = Smem<H_, G_>::total;        \
-    return kern<H_, G_>();              \
+    return kern<H_, G_>(kv8);           \
   }
   HY_ATTN_CASE(64, 1) HY_ATTN_CASE(64, 2) HY_ATTN_CASE(64, 4) HY_ATTN_CASE(64, 8)
   HY_ATTN_CASE(128, 1) HY_ATTN_CASE(128, 2) HY_ATTN_CASE(128, 4) HY_ATTN_CASE(128, 8)
@@ -164,20 +177,22 @@ cudaError_t init() {
   const int hds[] = {64, 128, 256};
   const int gs[] = {1, 2, 4, 8};
   for (int h : hds)
-    for (int gg : gs) {
-      size_t smem = 0;
-      void* k = pick(h, gg, &smem);
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-    }
+    for (int gg : gs)
+      for (int kv8 = 0; kv8 < 2; ++kv8) {
+        size_t smem = 0;
+        void* k = pick(h, gg, &smem, kv8 != 0);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+      }
   return cudaSuccess;
 }
 
 cudaError_t launch(const Params& p, cudaStream_t st, bool pdl) {
   if (p.nkv <= 0 || p.nq % p.nkv != 0 || p.nsplit < 1) return cudaErrorInvalidValue;
   size_t smem = 0;
-  void* k = pick(p.hd, p.nq / p.nkv, &smem);
+  void* k = pick(p.hd, p.nq / p.nkv, &smem, p.kv8 != 0);
   if (!k) return cudaErrorInvalidValue;
+  if (p.kv8 && (p.cap_s % 4 || p.cap_s < p.cap)) return cudaErrorInvalidValue;
   if (p.nb < 0 || p.nb > 8) return cudaErrorInvalidValue;
   return launch_k(reinterpret_cast<void (*)(Params)>(k), dim3(p.nkv, p.nsplit, p.nb > 0 ? p.nb : 1), dim3(kThreads),
                   smem, st, pdl, p);

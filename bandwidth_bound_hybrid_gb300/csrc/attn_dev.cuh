@@ -37,7 +37,7 @@ struct Work {
   static constexpr size_t sc = (size_t)G * TP * 4;
   static constexpr size_t ored = (size_t)NG * G * HD * 4;
   static constexpr size_t kvnew = 2 * HD * 2;
-  static constexpr size_t small = 3 * G * 4 + 16;  // m, l, corr, last
+  static constexpr size_t small = 3 * G * 4 + 16 + 64;  // m, l, corr, last; int8 cache: the new row's scales, amax
   static constexpr size_t total = q + sc + ored + kvnew + small;
 };
 
@@ -52,6 +52,7 @@ struct WorkPtrs {
   float* l;
   float* corr;
   int* last;
+  float* kvs;  // int8 cache: the new row's k and v scales [2], then amax scratch [8]
   __device__ __forceinline__ void carve(uint8_t* base) {
     using W = Work<HD, G>;
     q_s = reinterpret_cast<float*>(base);
@@ -63,6 +64,7 @@ struct WorkPtrs {
     l = m + G;
     corr = l + G;
     last = reinterpret_cast<int*>(corr + G);
+    kvs = reinterpret_cast<float*>(last + 4);
   }
 };
 
@@ -84,17 +86,68 @@ __device__ __forceinline__ Item item_of(const Params& p, int T, int sp) {
   return it;
 }
 
-// Copy lane: K and V rows of tile t of the item into dst (K at 0, V at kBytesKV).
+// Copy lane: K and V rows of tile t of the item into dst (K at 0, V at
+// kBytesKV).  int8 cache: the code rows at 0 and TP * HD, then the rows'
+// scales from the 16-byte boundary at or before the tile's first row (so that
+// the copy starts aligned): K scales at scale_off(), V scales 128 floats later.
 template <int HD>
+__device__ __forceinline__ int scale_off() {
+  return 2 * Tile<HD>::TP * HD;
+}
+template <int HD>
+__device__ __forceinline__ int scale_span() {  // bytes between the K and the V scales of a tile
+  return ((Tile<HD>::TP + 8) * 4 + 15) & ~15;
+}
+template <int HD, bool KV8>
 __device__ __forceinline__ void issue_tile(const Params& p, int g, const Item& it, int t, uint8_t* dst, uint64_t* bar,
                                            uint64_t pol) {
   constexpr int TP = Tile<HD>::TP;
   const int r0 = it.p0 + t * TP;
   const int rows = (it.pc1 - r0) < TP ? (it.pc1 - r0) : TP;
+  if (KV8) {
+    const uint32_t bytes = (uint32_t)rows * HD;
+    const int ra = r0 & ~3, n4 = ((r0 + rows + 3) & ~3) - ra;
+    mbar_arrive_expect_tx(bar, 2 * bytes + 2 * n4 * 4);
+    const uint8_t* K8 = reinterpret_cast<const uint8_t*>(p.K);
+    const uint8_t* V8 = reinterpret_cast<const uint8_t*>(p.V);
+    bulk_g2s(dst, K8 + ((long long)g * p.cap + r0) * HD, bytes, bar, pol);
+    bulk_g2s(dst + TP * HD, V8 + ((long long)g * p.cap + r0) * HD, bytes, bar, pol);
+    bulk_g2s(dst + scale_off<HD>(), p.Ks + (long long)g * p.cap_s + ra, n4 * 4, bar, pol);
+    bulk_g2s(dst + scale_off<HD>() + scale_span<HD>(), p.Vs + (long long)g * p.cap_s + ra, n4 * 4, bar, pol);
+    return;
+  }
   const uint32_t bytes = (uint32_t)rows * HD * 2;
   mbar_arrive_expect_tx(bar, 2 * bytes);
   bulk_g2s(dst, p.K + ((long long)g * p.cap + r0) * HD, bytes, bar, pol);
   bulk_g2s(dst + Tile<HD>::kBytesKV, p.V + ((long long)g * p.cap + r0) * HD, bytes, bar, pol);
+}
+
+// Eight int8 codes (one 8-byte word) as floats.
+__device__ __forceinline__ void i8x8(uint2 u, float* f) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[i] = (float)(int)(int8_t)(u.x >> (8 * i));
+    f[4 + i] = (float)(int)(int8_t)(u.y >> (8 * i));
+  }
+}
+
+// int8 quantisation of a vector held by the compute threads (the same rule as
+// the oracle's: amax in FP32, codes round-half-even of x * (127 / amax),
+// scale amax / 127).  Every compute thread calls it; `red` >= 8 floats.
+__device__ __forceinline__ float block_amax(float local, float* red, int ctid) {
+  local = warp_max(local);
+  if ((ctid & 31) == 0) red[ctid >> 5] = local;
+  named_barrier(1, kCT);
+  float a = 0.f;
+#pragma unroll
+  for (int w2 = 0; w2 < kCWarps; ++w2) a = fmaxf(a, red[w2]);
+  named_barrier(1, kCT);
+  return a;
+}
+__device__ __forceinline__ int8_t quant_code(float x, float inv) {
+  float r = rintf(__fmul_rn(x, inv));
+  r = fminf(fmaxf(r, -127.f), 127.f);
+  return (int8_t)(int)r;
 }
 
 template <int HD>
@@ -112,7 +165,7 @@ struct Acc {
 
 // Compute threads: rotated, scaled queries; the new row (rotated k and v in
 // bf16, also appended to the cache) when the item holds position T.
-template <int HD, int G>
+template <int HD, int G, bool KV8 = false>
 __device__ __forceinline__ void begin_item(const Params& p, int g, int T, const Item& it, const WorkPtrs<HD, G>& w,
                                            Acc<HD, G>& A, int ctid) {
   const int lane = ctid & 31;
@@ -125,7 +178,45 @@ __device__ __forceinline__ void begin_item(const Params& p, int g, int T, const 
     w.q_s[j * HD + i] = (a * cs.x - b * cs.y) * p.scale;
     w.q_s[j * HD + i + HD / 2] = (b * cs.x + a * cs.y) * p.scale;
   }
-  if (it.has_new) {
+  if (KV8 && it.has_new) {
+    // int8 cache: the new k and v vectors quantised with their own scales
+    const float* kh = p.y + (long long)(p.nq + g) * HD;
+    const float* vh = p.y + (long long)(p.nq + p.nkv + g) * HD;
+    int8_t* K8 = reinterpret_cast<int8_t*>(p.K) + ((long long)g * p.cap + T) * HD;
+    int8_t* V8 = reinterpret_cast<int8_t*>(p.V) + ((long long)g * p.cap + T) * HD;
+    int8_t* kn8 = reinterpret_cast<int8_t*>(w.kn);
+    int8_t* vn8 = reinterpret_cast<int8_t*>(w.vn);
+    float k0 = 0.f, k1 = 0.f, v0 = 0.f;
+    if (ctid < HD / 2) {
+      const float2 cs = rope[ctid];
+      const float a = kh[ctid], b = kh[ctid + HD / 2];
+      k0 = a * cs.x - b * cs.y;
+      k1 = b * cs.x + a * cs.y;
+    }
+    if (ctid < HD) v0 = vh[ctid];
+    const float ka = block_amax(fmaxf(fabsf(k0), fabsf(k1)), w.kvs + 2, ctid);
+    const float va = block_amax(fabsf(v0), w.kvs + 2, ctid);
+    const float kinv = ka > 0.f ? 127.0f / ka : 0.f, vinv = va > 0.f ? 127.0f / va : 0.f;
+    if (ctid < HD / 2) {
+      const int8_t c0 = quant_code(k0, kinv), c1 = quant_code(k1, kinv);
+      kn8[ctid] = c0;
+      kn8[ctid + HD / 2] = c1;
+      K8[ctid] = c0;
+      K8[ctid + HD / 2] = c1;
+    }
+    if (ctid < HD) {
+      const int8_t c = quant_code(v0, vinv);
+      vn8[ctid] = c;
+      V8[ctid] = c;
+    }
+    if (ctid == 0) {
+      w.kvs[0] = ka / 127.0f;
+      w.kvs[1] = va / 127.0f;
+      p.Ks[(long long)g * p.cap_s + T] = ka / 127.0f;
+      p.Vs[(long long)g * p.cap_s + T] = va / 127.0f;
+    }
+  }
+  if (!KV8 && it.has_new) {
     const float* kh = p.y + (long long)(p.nq + g) * HD;
     const float* vh = p.y + (long long)(p.nq + p.nkv + g) * HD;
     uint16_t* Kw = p.K + ((long long)g * p.cap + T) * HD;
@@ -161,9 +252,10 @@ __device__ __forceinline__ void begin_item(const Params& p, int g, int T, const 
 }
 
 // One tile of rows: scores -> online softmax (one warp per head) -> P V.
-template <int HD, int G>
+template <int HD, int G, bool KV8 = false>
 __device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t* tv, int rows,
-                                             const WorkPtrs<HD, G>& w, Acc<HD, G>& A, int ctid) {
+                                             const WorkPtrs<HD, G>& w, Acc<HD, G>& A, int ctid,
+                                             const float* ks = nullptr, const float* vs = nullptr) {
   using W = Work<HD, G>;
   constexpr int TP = W::TP;
   constexpr int LPR = HD / 8, RPW = 32 / LPR;
@@ -175,9 +267,23 @@ __device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t*
 #pragma unroll
     for (int j = 0; j < G; ++j) d[j] = 0.f;
     if (row < rows) {
-      const uint4 kv = *reinterpret_cast<const uint4*>(tk + row * HD + li * 8);
+      if (KV8) {
+        const uint2 k8 = *reinterpret_cast<const uint2*>(reinterpret_cast<const int8_t*>(tk) + row * HD + li * 8);
+        float kf[8];
+        i8x8(k8, kf);
+        const float sk = ks[row];
 #pragma unroll
-      for (int j = 0; j < G; ++j) d[j] = dot8(kv, A.qr[j]);
+        for (int j = 0; j < G; ++j) {
+          float a = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) a = fmaf(kf[e], A.qr[j][e], a);
+          d[j] = a * sk;
+        }
+      } else {
+        const uint4 kv = *reinterpret_cast<const uint4*>(tk + row * HD + li * 8);
+#pragma unroll
+        for (int j = 0; j < G; ++j) d[j] = dot8(kv, A.qr[j]);
+      }
     }
 #pragma unroll
     for (int o = LPR / 2; o > 0; o >>= 1)
@@ -218,9 +324,19 @@ __device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t*
     A.acc[j][1] *= c;
   }
   const uint32_t* tv32 = reinterpret_cast<const uint32_t*>(tv);
+  const uint16_t* tv16 = reinterpret_cast<const uint16_t*>(tv);  // int8 cache: two codes
   for (int r = pg; r < rows; r += W::NG) {
-    const uint32_t v2 = tv32[r * W::NP + dp];
-    const float vx = bf16_lo(v2), vy = bf16_hi(v2);
+    float vx, vy;
+    if (KV8) {
+      const uint16_t c2 = tv16[r * W::NP + dp];
+      const float sv = vs[r];
+      vx = (float)(int)(int8_t)(c2 & 0xFF) * sv;
+      vy = (float)(int)(int8_t)(c2 >> 8) * sv;
+    } else {
+      const uint32_t v2 = tv32[r * W::NP + dp];
+      vx = bf16_lo(v2);
+      vy = bf16_hi(v2);
+    }
 #pragma unroll
     for (int j = 0; j < G; ++j) {
       const float pj = w.sc[j * TP + r];

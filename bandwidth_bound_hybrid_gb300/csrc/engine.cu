@@ -87,6 +87,26 @@ __global__ void k_fill_bf16(uint16_t* dst, long long rows, int row_len, long lon
   }
 }
 
+// int8 cache rows: the same seeded values as k_fill_bf16 (in FP32), each row
+// quantised with its own scale (amax / 127, codes round-half-even of
+// x * (127 / amax)).  One warp per row.
+__global__ void k_fill_i8(int8_t* dst, float* scales, long long rows, int row_len, uint64_t seed) {
+  const int lane = threadIdx.x & 31;
+  for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; r < rows;
+       r += ((long long)gridDim.x * blockDim.x) >> 5) {
+    float a = 0.f;
+    for (int k = lane; k < row_len; k += 32) a = fmaxf(a, fabsf(synth_value(seed, (uint64_t)(r * row_len + k), 1.0f)));
+    a = warp_max(a);
+    const float inv = a > 0.f ? 127.0f / a : 0.f;
+    for (int k = lane; k < row_len; k += 32) {
+      float q = rintf(__fmul_rn(synth_value(seed, (uint64_t)(r * row_len + k), 1.0f), inv));
+      q = fminf(fmaxf(q, -127.f), 127.f);
+      dst[r * row_len + k] = (int8_t)(int)q;
+    }
+    if (lane == 0) scales[r] = a / 127.0f;
+  }
+}
+
 __global__ void k_fill_f32(float* dst, long long n, uint64_t seed, float scale) {
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x)
     dst[e] = synth_value(seed, (uint64_t)e, scale);
@@ -180,10 +200,28 @@ float* conv_state(hy_cache* c, int seq, int gi) {
   const hy_model* m = c->m;
   return reinterpret_cast<float*>(c->mem[seq] + c->off_conv) + (size_t)gi * m->cfg.conv_k * m->CC;
 }
+// Scale row stride of an int8 cache (a multiple of 4, so that every kv
+// head's scales start 16-byte aligned).
+int cap_scales(int cap) { return (cap + 3) & ~3; }
+
+// K (which = 0) or V rows of attention layer ai: bf16 [nkv][cap][hd], or with
+// the int8 cache the codes [nkv][cap][hd] (bytes, returned as uint16_t*).
 uint16_t* kv_cache(hy_cache* c, int seq, int ai, int which) {
   const hy_model* m = c->m;
   const size_t per = (size_t)m->cfg.attn_kv_heads * c->cap[seq] * m->cfg.head_dim;
-  return reinterpret_cast<uint16_t*>(c->mem[seq] + c->off_kv[seq]) + ((size_t)ai * 2 + which) * per;
+  const size_t esz = m->cfg.kv_format == 1 ? 1 : 2;
+  return reinterpret_cast<uint16_t*>(c->mem[seq] + c->off_kv[seq] + ((size_t)ai * 2 + which) * per * esz);
+}
+
+// int8 cache: the FP32 scales [nkv][cap_scales(cap)] of K (which = 0) or V of
+// attention layer ai, after every layer's codes.
+float* kv_scales(hy_cache* c, int seq, int ai, int which) {
+  const hy_model* m = c->m;
+  if (m->cfg.kv_format != 1) return nullptr;
+  const size_t codes = (size_t)m->n_attn * 2 * m->cfg.attn_kv_heads * c->cap[seq] * m->cfg.head_dim;
+  const size_t base = c->off_kv[seq] + ((codes + 255) & ~(size_t)255);
+  const size_t per = (size_t)m->cfg.attn_kv_heads * cap_scales(c->cap[seq]);
+  return reinterpret_cast<float*>(c->mem[seq] + base) + ((size_t)ai * 2 + which) * per;
 }
 
 // One kernel of the decode step, recorded before any is launched so that each
@@ -318,6 +356,10 @@ int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepO
       a.y = c->y;
       a.K = kv_cache(c, seq, m->sub[l], 0);
       a.V = kv_cache(c, seq, m->sub[l], 1);
+      a.kv8 = cf.kv_format == 1;
+      a.Ks = kv_scales(c, seq, m->sub[l], 0);
+      a.Vs = kv_scales(c, seq, m->sub[l], 1);
+      a.cap_s = cap_scales(c->cap[seq]);
       a.len = pos;
       a.rope = c->rope;
       a.cap = c->cap[seq];
@@ -622,11 +664,18 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
       for (int b = 0; b < B; ++b) {
         a.K_b[b] = kv_cache(c, seqs[b], m->sub[l], 0);
         a.V_b[b] = kv_cache(c, seqs[b], m->sub[l], 1);
+        a.Ks_b[b] = kv_scales(c, seqs[b], m->sub[l], 0);
+        a.Vs_b[b] = kv_scales(c, seqs[b], m->sub[l], 1);
+        a.cap_s_b[b] = cap_scales(c->cap[seqs[b]]);
         a.len_b[b] = c->d_len + seqs[b];
         a.cap_b[b] = c->cap[seqs[b]];
       }
       a.K = a.K_b[0];
       a.V = a.V_b[0];
+      a.kv8 = cf.kv_format == 1;
+      a.Ks = a.Ks_b[0];
+      a.Vs = a.Vs_b[0];
+      a.cap_s = a.cap_s_b[0];
       a.len = a.len_b[0];
       a.cap = a.cap_b[0];
       if ((rc = ck(attn::launch(a, st, pdl), "attention")) != HY_OK) return rc;
@@ -893,6 +942,7 @@ int check_model_cfg(const hy_config* c) {
     if ((c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) || (G != 1 && G != 2 && G != 4 && G != 8))
       return fail(HY_ERR_UNSUPPORTED, "attention: head_dim must be 64/128/256 and nq/nkv in {1,2,4,8}");
   }
+  if (c->kv_format != 0 && c->kv_format != 1) return fail(HY_ERR_ARG, "kv_format must be 0 or 1");
   if (c->ffn < 0) return fail(HY_ERR_ARG, "ffn < 0");
   if (c->ffn == 0) {
     if (c->n_experts <= 0 || c->top_k <= 0 || c->top_k > 16 || c->top_k > c->n_experts || c->expert_ffn <= 0 ||
@@ -1165,8 +1215,8 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
   m->q4 = c.weight_format == 1;
   {  // the chunked prompt path: bf16 dense models whose GEMM widths suit the tensor copies
     const int od = std::max(m->n_gdn ? c.gdn_heads * c.gdn_dv : 8, m->n_attn ? c.attn_q_heads * c.head_dim : 8);
-    m->chunk_prefill = !m->q4 && !m->moe && !(c.flags & HY_FLAG_TOKEN_PREFILL) && H % 8 == 0 && c.ffn % 8 == 0 &&
-                       od % 8 == 0;
+    m->chunk_prefill = !m->q4 && !m->moe && c.kv_format == 0 && !(c.flags & HY_FLAG_TOKEN_PREFILL) && H % 8 == 0 &&
+                       c.ffn % 8 == 0 && od % 8 == 0;
   }
   *out = m;
   g_err.clear();
@@ -1195,7 +1245,11 @@ int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, 
   c->off_conv = (state_b + 255) & ~(size_t)255;
   const size_t off_kv = (c->off_conv + conv_b + 255) & ~(size_t)255;
   for (int s = 0; s < max_seqs; ++s) {
-    const size_t kv_b = (size_t)m->n_attn * 2 * cf.attn_kv_heads * c->cap[s] * cf.head_dim * 2;
+    size_t kv_b = (size_t)m->n_attn * 2 * cf.attn_kv_heads * c->cap[s] * cf.head_dim * 2;
+    if (cf.kv_format == 1) {  // int8 codes, then the per-vector scales
+      const size_t codes = (size_t)m->n_attn * 2 * cf.attn_kv_heads * c->cap[s] * cf.head_dim;
+      kv_b = ((codes + 255) & ~(size_t)255) + (size_t)m->n_attn * 2 * cf.attn_kv_heads * cap_scales(c->cap[s]) * 4;
+    }
     void* p = nullptr;
     cudaError_t e = cudaMalloc(&p, off_kv + kv_b + 256);
     if (e != cudaSuccess) {
@@ -1323,9 +1377,15 @@ int hy_seq_fill_synthetic(hy_cache* c, int32_t seq, int32_t len, uint64_t seed, 
   for (int a = 0; a < m->n_attn; ++a)
     for (int w = 0; w < 2; ++w)
       for (int g = 0; g < cf.attn_kv_heads && len > 0; ++g) {
-        uint16_t* base = kv_cache(c, seq, a, w) + (size_t)g * c->cap[seq] * cf.head_dim;
-        k_fill_bf16<<<1024, 256, 0, st>>>(base, len, cf.head_dim, cf.head_dim,
-                                          seed * 1000003ull + (uint64_t)((a * 2 + w) * 64 + g));
+        const uint64_t key = seed * 1000003ull + (uint64_t)((a * 2 + w) * 64 + g);
+        if (cf.kv_format == 1) {
+          int8_t* base = reinterpret_cast<int8_t*>(kv_cache(c, seq, a, w)) + (size_t)g * c->cap[seq] * cf.head_dim;
+          float* sc = kv_scales(c, seq, a, w) + (size_t)g * cap_scales(c->cap[seq]);
+          k_fill_i8<<<1024, 256, 0, st>>>(base, sc, len, cf.head_dim, key);
+        } else {
+          uint16_t* base = kv_cache(c, seq, a, w) + (size_t)g * c->cap[seq] * cf.head_dim;
+          k_fill_bf16<<<1024, 256, 0, st>>>(base, len, cf.head_dim, cf.head_dim, key);
+        }
       }
   if (m->n_gdn) {
     const long long n = (long long)m->n_gdn * cf.gdn_heads * cf.gdn_dv * cf.gdn_dk;
@@ -1807,6 +1867,45 @@ int hy_op_rope_table(float* table_dev, int32_t cap, int32_t hd, float theta, voi
   if (!table_dev || cap <= 0 || hd <= 0 || hd % 2) return fail(HY_ERR_ARG, "bad RoPE table arguments");
   cudaError_t e = attn::rope_table((float2*)table_dev, cap, hd, (double)theta, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(HY_ERR_CUDA, "RoPE table: %s", cudaGetErrorString(e));
+  return HY_OK;
+}
+
+int hy_op_attention_i8(const float* y_dev, void* Kq_dev, float* Ks_dev, void* Vq_dev, float* Vs_dev, int32_t cap,
+                       int32_t nq, int32_t nkv, int32_t hd, const int32_t* len_dev, const float* rope_table_dev,
+                       int32_t nsplit, float* o_dev, void* workspace_dev, void* stream) {
+  if (!y_dev || !aligned16(Kq_dev) || !aligned16(Vq_dev) || !aligned16(Ks_dev) || !aligned16(Vs_dev) || !len_dev ||
+      !rope_table_dev || !o_dev || !aligned16(workspace_dev) || cap <= 0 || nkv <= 0 || nq <= 0 || nq % nkv)
+    return fail(HY_ERR_ARG, "bad attention arguments");
+  if ((hd != 64 && hd != 128 && hd != 256) || nq / nkv > 8 || ((nq / nkv) & (nq / nkv - 1)))
+    return fail(HY_ERR_UNSUPPORTED, "attention: head_dim 64/128/256 and nq/nkv in {1,2,4,8}");
+  unsigned* guard = nullptr;
+  int rc = op_guard(&guard);
+  if (rc != HY_OK) return rc;
+  if (nsplit <= 0) nsplit = attn::auto_splits(nkv, op_nsm());
+  uint8_t* ws = (uint8_t*)workspace_dev;
+  attn::Params a;
+  memset(&a, 0, sizeof(a));
+  a.y = y_dev;
+  a.K = (uint16_t*)Kq_dev;
+  a.V = (uint16_t*)Vq_dev;
+  a.kv8 = 1;
+  a.Ks = Ks_dev;
+  a.Vs = Vs_dev;
+  a.cap_s = cap_scales(cap);
+  a.len = len_dev;
+  a.rope = (const float2*)rope_table_dev;
+  a.cap = cap;
+  a.nq = nq;
+  a.nkv = nkv;
+  a.hd = hd;
+  a.nsplit = nsplit;
+  a.scale = 1.0f / sqrtf((float)hd);
+  a.counter = (unsigned*)ws;
+  a.part = (float*)(ws + 256 + ((size_t)nkv * 4 + 255) / 256 * 256);
+  a.o = o_dev;
+  a.guard = guard;
+  cudaError_t e = attn::launch(a, (cudaStream_t)stream, false);
+  if (e != cudaSuccess) return fail(HY_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
   return HY_OK;
 }
 

@@ -145,8 +145,12 @@ constexpr int kThreads = 288;  // 8 compute warps + 1 copy warp
 constexpr int kStages = 3;
 struct Params {
   const float* y;          // projection output: q|k|v
-  uint16_t* K;             // bf16 [nkv][cap][hd]
+  uint16_t* K;             // bf16 [nkv][cap][hd]; with kv8: int8 codes [nkv][cap][hd] (bytes)
   uint16_t* V;
+  int kv8;                 // int8 cache: one FP32 scale per cached vector in Ks / Vs [nkv][cap_s]
+  float* Ks;
+  float* Vs;
+  int cap_s;               // scale row stride (a multiple of 4)
   const int* len;          // position of the new token (= cached rows)
   const float2* rope;      // [>= cap][hd/2] (cos, sin) of position * theta^(-2i/hd)
   int cap, nq, nkv, hd, nsplit;
@@ -161,8 +165,11 @@ struct Params {
   long long ld_part;
   uint16_t* K_b[8];
   uint16_t* V_b[8];
+  float* Ks_b[8];
+  float* Vs_b[8];
   const int* len_b[8];
   int cap_b[8];
+  int cap_s_b[8];
 };
 size_t part_floats(int nq, int nkv, int hd, int nsplit);
 int auto_splits(int nkv, int nsm);

@@ -41,6 +41,7 @@ def make_config(shape, splits: int = 0, flags: int = 0) -> hy_config:
     c.rms_eps = float(shape.rms_eps)
     c.rope_theta = float(shape.rope_theta)
     c.weight_format = int(getattr(shape, "weight_format", 0))
+    c.kv_format = int(getattr(shape, "kv_format", 0))
     c.attn_splits = int(splits)
     c.flags = int(flags)
     return c

@@ -84,6 +84,7 @@ typedef struct {
   int32_t weight_format;   /* 0 = bf16; 1 = 4-bit blocks of 32 for the linear weights (see hy_tensor) */
   int32_t attn_splits;     /* split-KV chunks per kv head; 0 = chosen from the SM count */
   uint32_t flags;          /* HY_FLAG_* */
+  int32_t kv_format;       /* 0 = bf16 KV cache; 1 = int8 codes with one FP32 scale per cached k or v vector */
 } hy_config;
 
 /* One linear weight [rows][cols]: bf16 in `w` (`scales` unused), or with
@@ -360,6 +361,20 @@ size_t hy_op_attention_workspace(int32_t nq, int32_t nkv, int32_t hd, int32_t ns
 int hy_op_attention(const float* y_dev, void* K_dev, void* V_dev, int32_t cap, int32_t nq, int32_t nkv, int32_t hd,
                     const int32_t* len_dev, const float* rope_table_dev, int32_t nsplit, float* o_dev,
                     void* workspace_dev, void* stream);
+
+/* hy_op_attention over an int8 cache ("hanzo-engine: A Portable Single-Binary
+ * LLM Inference Engine...", sections "System Architecture" and "Results":
+ * int8 KV, one f32 scale per cached vector).  Kq_dev, Vq_dev: int8 codes
+ * [nkv][cap][hd]; Ks_dev, Vs_dev: FP32 scales [nkv][cap4], cap4 = cap rounded
+ * up to a multiple of 4 (all four 16-byte aligned).  A cached value is code *
+ * scale.  The new k (after RoPE) and v vectors at row T = *len_dev are
+ * quantised on the device: a = max |x| (FP32), scale = a / 127, code =
+ * round-half-even(x * (127 / a)) clamped to [-127, 127] (a = 0: codes 0,
+ * scale 0); they are attended to as stored.  Other arguments as for
+ * hy_op_attention (same workspace size). */
+int hy_op_attention_i8(const float* y_dev, void* Kq_dev, float* Ks_dev, void* Vq_dev, float* Vs_dev, int32_t cap,
+                       int32_t nq, int32_t nkv, int32_t hd, const int32_t* len_dev, const float* rope_table_dev,
+                       int32_t nsplit, float* o_dev, void* workspace_dev, void* stream);
 
 /* hy_op_attention without a caller-provided workspace, for callers that
  * cannot allocate device memory: a host framework that owns the whole memory

@@ -135,6 +135,8 @@ WORKLOADS = {
     "dense4b": Workload("dense 4B-shaped hybrid, prompt 4096 + 256 decode", DENSE4B, 4096, 256),
     "dense4b-32k": Workload("dense 4B-shaped hybrid, prompt 32768 + 128 decode", DENSE4B, 32768, 128,
                             splits=(1, 2, 4, 8, 16)),
+    "dense4b-32k-kv8": Workload("dense 4B-shaped hybrid, int8 KV cache, prompt 32768 + 128 decode",
+                                dataclasses.replace(DENSE4B, name="dense-4b-kv8", kv_format=1), 32768, 128),
     "moe35b": Workload("MoE 35B-A3B-shaped hybrid, prompt 2048 + 256 decode", MOE35B, 2048, 256),
     "moe35b-q4-b8": Workload("MoE 35B-A3B-shaped hybrid, 4-bit, batch 8, ragged context 1024..16384, 128 decode",
                              MOE35B_Q4, 0, 128, batch=8, ragged_context=(1024, 16384)),
