@@ -50,7 +50,7 @@ def linear_bytes(rows: int, cols: int, weight_format: int) -> int:
     return rows * cols * BF16
 
 
-def step_bytes(shape, context: int, experts_touched: int | None = None) -> StepBytes:
+def step_bytes(shape, context: int, experts_touched: int | None = None, logits: bool = False) -> StepBytes:
     """Bytes one decode step at position ``context`` must move.
 
     ``shape`` has the model-shape attributes; ``experts_touched`` (MoE) is
@@ -80,7 +80,34 @@ def step_bytes(shape, context: int, experts_touched: int | None = None) -> StepB
     kvf = getattr(s, "kv_format", 0)
     kv_read = kv_bytes_per_token(n_attn, s.attn_kv_heads, s.head_dim, kv_format=kvf) * context
     kv_write = kv_bytes_per_token(n_attn, s.attn_kv_heads, s.head_dim, kv_format=kvf)
-    return StepBytes(weights=w, state=state, kv_read=kv_read, kv_write=kv_write, activations=0)
+    return StepBytes(weights=w, state=state, kv_read=kv_read, kv_write=kv_write,
+                     activations=s.vocab * F32 if logits else 0)
+
+
+def prefill_flops(shape, n: int, t0: int = 0) -> dict:
+    """FLOPs of a prompt chunk of n tokens at positions t0 .. t0+n-1: the
+    linear projections (2 per weight and token; the LM head for the last token
+    only), the causal attention (scores and P V: 4 nq hd per (query, key)
+    pair), the DeltaNet recurrence (about 6 dk dv per head and token), and the
+    tensor-core share (the projections; they run as two bf16 parts of the
+    activations, so the tensor pipe executes twice their FLOPs)."""
+    H = shape.hidden
+    n_attn = sum(1 for l in range(shape.n_layers) if shape.is_attn(l))
+    n_gdn = shape.n_layers - n_attn
+    lin = n_gdn * (shape.gdn_in_rows * H + H * shape.gdn_heads * shape.gdn_dv)
+    lin += n_attn * ((shape.attn_q_heads + 2 * shape.attn_kv_heads) * shape.head_dim * H +
+                     H * shape.attn_q_heads * shape.head_dim)
+    if shape.ffn > 0:
+        lin += shape.n_layers * 3 * shape.ffn * H
+    else:
+        lin += shape.n_layers * ((shape.n_experts + 1) * H + (shape.top_k + 1) * 3 * shape.expert_ffn * H)
+    gemm = 2.0 * lin * n
+    pairs = n * t0 + n * (n + 1) / 2.0
+    attn = 4.0 * n_attn * shape.attn_q_heads * shape.head_dim * pairs
+    gdn = 6.0 * n_gdn * shape.gdn_heads * shape.gdn_dk * shape.gdn_dv * n
+    head = 2.0 * shape.vocab * H
+    return {"gemm": gemm, "attention": attn, "deltanet": gdn, "lm_head": head, "total": gemm + attn + gdn + head,
+            "tensor_executed": 2 * gemm}
 
 
 def expected_union(n_experts: int, top_k: int, batch: int) -> float:

@@ -65,6 +65,8 @@ SIGNATURES = {
     "hy_model_free": (None, [vp]),
     "hy_cache_alloc": (ctypes.c_int, [vp, i32, P(i32), P(vp)]),
     "hy_cache_free": (None, [vp]),
+    "hy_cache_alloc_paged": (ctypes.c_int, [vp, i32, P(i32), i32, i32, P(vp)]),
+    "hy_cache_free_pages": (i32, [vp]),
     "hy_seq_reset": (ctypes.c_int, [vp, i32, vp]),
     "hy_seq_len": (i32, [vp, i32]),
     "hy_seq_capacity": (i32, [vp, i32]),

@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p0) {
     p.len = p0.len_b[z];
     p.cap = p0.cap_b[z];
     p.cap_s = p0.cap_s_b[z];
+    p.pages = p0.pages_b[z];
   }
   using S_ = Smem<HD, G>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -193,6 +194,7 @@ cudaError_t launch(const Params& p, cudaStream_t st, bool pdl) {
   void* k = pick(p.hd, p.nq / p.nkv, &smem, p.kv8 != 0);
   if (!k) return cudaErrorInvalidValue;
   if (p.kv8 && (p.cap_s % 4 || p.cap_s < p.cap)) return cudaErrorInvalidValue;
+  if (p.pages && (p.kv8 || p.page_tokens <= 0 || p.page_tokens % 128)) return cudaErrorInvalidValue;
   if (p.nb < 0 || p.nb > 8) return cudaErrorInvalidValue;
   return launch_k(reinterpret_cast<void (*)(Params)>(k), dim3(p.nkv, p.nsplit, p.nb > 0 ? p.nb : 1), dim3(kThreads),
                   smem, st, pdl, p);

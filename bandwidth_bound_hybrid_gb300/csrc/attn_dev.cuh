@@ -73,12 +73,26 @@ struct Item {
   bool has_new;
 };
 
+// Element offset of cached row r of kv head g: contiguous [nkv][cap][HD], or
+// through the sequence's page table.
+template <int HD>
+__device__ __forceinline__ long long kv_row(const Params& p, int g, int r) {
+  if (p.pages)
+    return (long long)p.pages[r / p.page_tokens] * p.page_elems + ((long long)g * p.page_tokens + r % p.page_tokens) * HD;
+  return ((long long)g * p.cap + r) * HD;
+}
+
 template <int HD>
 __device__ __forceinline__ Item item_of(const Params& p, int T, int sp) {
   Item it;
   const long long L = (long long)T + 1;
   it.p0 = (int)((long long)sp * L / p.nsplit);
   it.p1 = (int)((long long)(sp + 1) * L / p.nsplit);
+  if (p.pages) {  // paged cache: split boundaries on tile multiples, so that no tile straddles a page
+    constexpr int TP = Tile<HD>::TP;
+    it.p0 &= ~(TP - 1);
+    it.p1 = (sp == p.nsplit - 1) ? (int)L : (it.p1 & ~(TP - 1));
+  }
   it.pc1 = it.p1 < T ? it.p1 : T;  // cached rows [p0, pc1)
   const int nc = it.pc1 > it.p0 ? it.pc1 - it.p0 : 0;
   it.ntiles = (nc + Tile<HD>::TP - 1) / Tile<HD>::TP;
@@ -118,8 +132,9 @@ __device__ __forceinline__ void issue_tile(const Params& p, int g, const Item& i
   }
   const uint32_t bytes = (uint32_t)rows * HD * 2;
   mbar_arrive_expect_tx(bar, 2 * bytes);
-  bulk_g2s(dst, p.K + ((long long)g * p.cap + r0) * HD, bytes, bar, pol);
-  bulk_g2s(dst + Tile<HD>::kBytesKV, p.V + ((long long)g * p.cap + r0) * HD, bytes, bar, pol);
+  const long long off = kv_row<HD>(p, g, r0);
+  bulk_g2s(dst, p.K + off, bytes, bar, pol);
+  bulk_g2s(dst + Tile<HD>::kBytesKV, p.V + off, bytes, bar, pol);
 }
 
 // Eight int8 codes (one 8-byte word) as floats.
@@ -219,8 +234,8 @@ __device__ __forceinline__ void begin_item(const Params& p, int g, int T, const 
   if (!KV8 && it.has_new) {
     const float* kh = p.y + (long long)(p.nq + g) * HD;
     const float* vh = p.y + (long long)(p.nq + p.nkv + g) * HD;
-    uint16_t* Kw = p.K + ((long long)g * p.cap + T) * HD;
-    uint16_t* Vw = p.V + ((long long)g * p.cap + T) * HD;
+    uint16_t* Kw = p.K + kv_row<HD>(p, g, T);
+    uint16_t* Vw = p.V + kv_row<HD>(p, g, T);
     for (int i = ctid; i < HD / 2; i += kCT) {
       const float2 cs = rope[i];
       const float a = kh[i], b = kh[i + HD / 2];

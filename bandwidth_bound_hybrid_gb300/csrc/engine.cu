@@ -79,11 +79,14 @@ __device__ __forceinline__ float synth_value(uint64_t seed, uint64_t i, float sc
   return ((float)(uint32_t)(z >> 40) * (1.0f / 8388608.0f) - 1.0f) * scale;
 }
 
-__global__ void k_fill_bf16(uint16_t* dst, long long rows, int row_len, long long stride, uint64_t seed) {
+// Rows [first_row, first_row + rows) of a seeded bf16 stream (value index
+// row * row_len + column) into dst (row stride `stride`).
+__global__ void k_fill_bf16(uint16_t* dst, long long rows, int row_len, long long stride, uint64_t seed,
+                            long long first_row = 0) {
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < rows * row_len;
        e += (long long)gridDim.x * blockDim.x) {
     const long long r = e / row_len, k = e % row_len;
-    dst[r * stride + k] = f32_to_bf16_rne(synth_value(seed, (uint64_t)e, 1.0f));
+    dst[r * stride + k] = f32_to_bf16_rne(synth_value(seed, (uint64_t)(e + first_row * row_len), 1.0f));
   }
 }
 
@@ -188,6 +191,14 @@ struct hy_cache {
     cudaGraphExec_t exec;
   };
   std::vector<Graph> graphs;
+  // paged KV cache (page_tokens > 0): pages of page_tokens positions (every
+  // attention layer's K and V of one sequence) drawn from one pool on demand
+  int page_tokens = 0, max_pages = 0;
+  long long page_elems = 0;
+  uint16_t* pool = nullptr;
+  int* d_pages = nullptr;  // [max_seqs][max_pages]: the page of each block of page_tokens positions
+  std::vector<int> free_pages;
+  std::vector<std::vector<int>> seq_pages;
 };
 
 namespace {
@@ -208,9 +219,15 @@ int cap_scales(int cap) { return (cap + 3) & ~3; }
 // the int8 cache the codes [nkv][cap][hd] (bytes, returned as uint16_t*).
 uint16_t* kv_cache(hy_cache* c, int seq, int ai, int which) {
   const hy_model* m = c->m;
+  if (c->page_tokens)  // this layer's K or V block in page 0 of the pool; kv rows then go through the page table
+    return c->pool + ((size_t)ai * 2 + which) * m->cfg.attn_kv_heads * c->page_tokens * m->cfg.head_dim;
   const size_t per = (size_t)m->cfg.attn_kv_heads * c->cap[seq] * m->cfg.head_dim;
   const size_t esz = m->cfg.kv_format == 1 ? 1 : 2;
   return reinterpret_cast<uint16_t*>(c->mem[seq] + c->off_kv[seq] + ((size_t)ai * 2 + which) * per * esz);
+}
+
+const int* seq_page_table(hy_cache* c, int seq) {
+  return c->page_tokens ? c->d_pages + (size_t)seq * c->max_pages : nullptr;
 }
 
 // int8 cache: the FP32 scales [nkv][cap_scales(cap)] of K (which = 0) or V of
@@ -360,6 +377,9 @@ int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepO
       a.Ks = kv_scales(c, seq, m->sub[l], 0);
       a.Vs = kv_scales(c, seq, m->sub[l], 1);
       a.cap_s = cap_scales(c->cap[seq]);
+      a.pages = seq_page_table(c, seq);
+      a.page_tokens = c->page_tokens;
+      a.page_elems = c->page_elems;
       a.len = pos;
       a.rope = c->rope;
       a.cap = c->cap[seq];
@@ -667,6 +687,7 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
         a.Ks_b[b] = kv_scales(c, seqs[b], m->sub[l], 0);
         a.Vs_b[b] = kv_scales(c, seqs[b], m->sub[l], 1);
         a.cap_s_b[b] = cap_scales(c->cap[seqs[b]]);
+        a.pages_b[b] = seq_page_table(c, seqs[b]);
         a.len_b[b] = c->d_len + seqs[b];
         a.cap_b[b] = c->cap[seqs[b]];
       }
@@ -676,6 +697,9 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
       a.Ks = a.Ks_b[0];
       a.Vs = a.Vs_b[0];
       a.cap_s = a.cap_s_b[0];
+      a.pages = a.pages_b[0];
+      a.page_tokens = c->page_tokens;
+      a.page_elems = c->page_elems;
       a.len = a.len_b[0];
       a.cap = a.cap_b[0];
       if ((rc = ck(attn::launch(a, st, pdl), "attention")) != HY_OK) return rc;
@@ -985,6 +1009,34 @@ int valid_seq(const hy_cache* c, int seq) { return c && seq >= 0 && seq < c->max
 
 }  // namespace
 
+// ---------------------------------------------------------------- page pool
+// Pages so that each (sequence, length) of `need` holds `length` positions:
+// taken from the pool and entered in the device page table on `st` before
+// any launch that reads them.  HY_ERR_CAPACITY, with nothing taken, when the
+// pool is short.
+int ensure_pages(hy_cache* c, const std::vector<std::pair<int, int>>& need, cudaStream_t st) {
+  if (!c->page_tokens) return HY_OK;
+  const int P = c->page_tokens;
+  size_t want = 0;
+  for (const auto& sl : need) {
+    const size_t np = (size_t)(sl.second + P - 1) / P;
+    if (np > c->seq_pages[sl.first].size()) want += np - c->seq_pages[sl.first].size();
+  }
+  if (want > c->free_pages.size())
+    return fail(HY_ERR_CAPACITY, "page pool: %zu more pages needed, %zu free", want, c->free_pages.size());
+  for (const auto& sl : need) {
+    auto& pages = c->seq_pages[sl.first];
+    while ((long long)pages.size() * P < sl.second) {
+      const int pg = c->free_pages.back();
+      c->free_pages.pop_back();
+      cudaError_t e = prefill::set_len(c->d_pages + (size_t)sl.first * c->max_pages + pages.size(), pg, st);
+      if (e != cudaSuccess) return fail(HY_ERR_CUDA, "page table update: %s", cudaGetErrorString(e));
+      pages.push_back(pg);
+    }
+  }
+  return HY_OK;
+}
+
 // ---------------------------------------------------------------- chunked prompt
 // Prompt tokens per chunk (the GEMMs' M); HY_PREFILL_CHUNK overrides.
 int prefill_chunk_rows() {
@@ -1067,6 +1119,9 @@ int prefill_chunk(hy_cache* c, int seq, const int* tok, int n, int t0, bool last
       a.cap = c->cap[seq];
       a.rope = c->rope;
       a.Qr = c->pf_qr;
+      a.pages = seq_page_table(c, seq);
+      a.page_tokens = c->page_tokens;
+      a.page_elems = c->page_elems;
       a.O_hi = c->pf_ahi;
       a.O_lo = c->pf_alo;
       a.ldo = ka;
@@ -1225,10 +1280,15 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
 
 void hy_model_free(hy_model* m) { delete m; }
 
-int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, hy_cache** out) {
+static int cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, int32_t page_tokens,
+                       int32_t pool_pages, hy_cache** out) {
   if (!m || !out || max_seqs <= 0 || !capacity_host) return fail(HY_ERR_ARG, "bad argument");
   *out = nullptr;
   const hy_config& cf = m->cfg;
+  const bool paged = page_tokens > 0;
+  if (paged && (page_tokens % 128 || pool_pages <= 0))
+    return fail(HY_ERR_ARG, "page_tokens must be a positive multiple of 128 and pool_pages positive");
+  if (paged && cf.kv_format != 0) return fail(HY_ERR_UNSUPPORTED, "paged caches hold bf16 K/V only");
   auto* c = new hy_cache();
   c->m = m;
   c->max_seqs = max_seqs;
@@ -1245,7 +1305,7 @@ int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, 
   c->off_conv = (state_b + 255) & ~(size_t)255;
   const size_t off_kv = (c->off_conv + conv_b + 255) & ~(size_t)255;
   for (int s = 0; s < max_seqs; ++s) {
-    size_t kv_b = (size_t)m->n_attn * 2 * cf.attn_kv_heads * c->cap[s] * cf.head_dim * 2;
+    size_t kv_b = paged ? 0 : (size_t)m->n_attn * 2 * cf.attn_kv_heads * c->cap[s] * cf.head_dim * 2;
     if (cf.kv_format == 1) {  // int8 codes, then the per-vector scales
       const size_t codes = (size_t)m->n_attn * 2 * cf.attn_kv_heads * c->cap[s] * cf.head_dim;
       kv_b = ((codes + 255) & ~(size_t)255) + (size_t)m->n_attn * 2 * cf.attn_kv_heads * cap_scales(c->cap[s]) * 4;
@@ -1301,6 +1361,19 @@ int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, 
       return rc;
     }
   }
+  if (paged) {  // the page pool and the page tables
+    c->page_tokens = page_tokens;
+    c->max_pages = (max_cap + page_tokens - 1) / page_tokens;
+    c->page_elems = (long long)std::max(m->n_attn, 1) * 2 * cf.attn_kv_heads * page_tokens * cf.head_dim;
+    if ((rc = dalloc(c, &c->pool, (size_t)pool_pages * c->page_elems)) ||
+        (rc = dalloc(c, &c->d_pages, (size_t)max_seqs * c->max_pages))) {
+      free_cache_mem(c);
+      delete c;
+      return rc;
+    }
+    for (int pg = pool_pages - 1; pg >= 0; --pg) c->free_pages.push_back(pg);
+    c->seq_pages.assign(max_seqs, {});
+  }
   if (m->n_attn) {
     if ((rc = dalloc(c, &c->rope, (size_t)max_cap * (cf.head_dim / 2)))) {
       free_cache_mem(c);
@@ -1335,6 +1408,20 @@ int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, 
   return HY_OK;
 }
 
+int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, hy_cache** out) {
+  return cache_alloc(m, max_seqs, capacity_host, 0, 0, out);
+}
+
+int hy_cache_alloc_paged(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, int32_t page_tokens,
+                         int32_t pool_pages, hy_cache** out) {
+  if (page_tokens <= 0) return fail(HY_ERR_ARG, "page_tokens must be a positive multiple of 128");
+  return cache_alloc(m, max_seqs, capacity_host, page_tokens, pool_pages, out);
+}
+
+int32_t hy_cache_free_pages(const hy_cache* c) {
+  return (c && c->page_tokens) ? (int32_t)c->free_pages.size() : -1;
+}
+
 void hy_cache_free(hy_cache* c) {
   if (!c) return;
   cudaDeviceSynchronize();
@@ -1348,6 +1435,10 @@ int hy_seq_reset(hy_cache* c, int32_t seq, void* stream) {
   HY_CK(cudaMemsetAsync(c->mem[seq], 0, c->off_kv[seq], st));
   HY_CK(cudaMemsetAsync(c->d_len + seq, 0, sizeof(int), st));
   c->len[seq] = 0;
+  if (c->page_tokens) {  // the sequence's pages go back to the pool
+    for (int pg : c->seq_pages[seq]) c->free_pages.push_back(pg);
+    c->seq_pages[seq].clear();
+  }
   return HY_OK;
 }
 
@@ -1374,6 +1465,10 @@ int hy_seq_fill_synthetic(hy_cache* c, int32_t seq, int32_t len, uint64_t seed, 
   const hy_model* m = c->m;
   const hy_config& cf = m->cfg;
   cudaStream_t st = (cudaStream_t)stream;
+  {
+    int rc = ensure_pages(c, {{seq, len}}, st);
+    if (rc != HY_OK) return rc;
+  }
   for (int a = 0; a < m->n_attn; ++a)
     for (int w = 0; w < 2; ++w)
       for (int g = 0; g < cf.attn_kv_heads && len > 0; ++g) {
@@ -1382,6 +1477,14 @@ int hy_seq_fill_synthetic(hy_cache* c, int32_t seq, int32_t len, uint64_t seed, 
           int8_t* base = reinterpret_cast<int8_t*>(kv_cache(c, seq, a, w)) + (size_t)g * c->cap[seq] * cf.head_dim;
           float* sc = kv_scales(c, seq, a, w) + (size_t)g * cap_scales(c->cap[seq]);
           k_fill_i8<<<1024, 256, 0, st>>>(base, sc, len, cf.head_dim, key);
+        } else if (c->page_tokens) {  // block by block through the sequence's pages
+          const int P = c->page_tokens;
+          for (int j = 0; j * P < len; ++j) {
+            uint16_t* base = kv_cache(c, seq, a, w) + (size_t)c->seq_pages[seq][j] * c->page_elems +
+                             (size_t)g * P * cf.head_dim;
+            k_fill_bf16<<<256, 256, 0, st>>>(base, std::min(P, len - j * P), cf.head_dim, cf.head_dim, key,
+                                             (long long)j * P);
+          }
         } else {
           uint16_t* base = kv_cache(c, seq, a, w) + (size_t)g * c->cap[seq] * cf.head_dim;
           k_fill_bf16<<<1024, 256, 0, st>>>(base, len, cf.head_dim, cf.head_dim, key);
@@ -1406,6 +1509,10 @@ int hy_prefill(hy_model* m, hy_cache* c, int32_t seq, const int32_t* tokens_dev,
   if ((long long)c->len[seq] + n > c->cap[seq])
     return fail(HY_ERR_CAPACITY, "sequence %d: %d + %d tokens exceed capacity %d", seq, c->len[seq], n, c->cap[seq]);
   cudaStream_t st = (cudaStream_t)stream;
+  {
+    int rc = ensure_pages(c, {{seq, c->len[seq] + n}}, st);
+    if (rc != HY_OK) return rc;
+  }
   if (m->chunk_prefill && n > 0) {
     const int P = std::min(n, prefill_chunk_rows());
     int rc = prefill_buffers(c, P);
@@ -1467,6 +1574,11 @@ int hy_decode_step(hy_model* m, hy_cache* c, const int32_t* seqs_host, int32_t n
   int rc = check_seqs(c, seqs_host, nseq, seqs);
   if (rc != HY_OK) return rc;
   cudaStream_t st = (cudaStream_t)stream;
+  {
+    std::vector<std::pair<int, int>> need;
+    for (int s_ : seqs) need.push_back({s_, c->len[s_] + 1});
+    if ((rc = ensure_pages(c, need, st)) != HY_OK) return rc;
+  }
   if (nseq == 1 && !m->q4) {
     HY_CK(cudaMemcpyAsync(c->tok, tokens_dev, sizeof(int), cudaMemcpyDeviceToDevice, st));
     rc = run_step(c, seqs[0], logits_dev, ids_dev, st);
@@ -1486,6 +1598,11 @@ int hy_decode_step_host(hy_model* m, hy_cache* c, const int32_t* seqs_host, int3
   int rc = check_seqs(c, seqs_host, nseq, seqs);
   if (rc != HY_OK) return rc;
   cudaStream_t st = (cudaStream_t)stream;
+  {
+    std::vector<std::pair<int, int>> need;
+    for (int s_ : seqs) need.push_back({s_, c->len[s_] + 1});
+    if ((rc = ensure_pages(c, need, st)) != HY_OK) return rc;
+  }
   float* lg = logits_host ? c->logits_buf : nullptr;
   int* ids = nullptr;
   if (nseq == 1 && !m->q4) {

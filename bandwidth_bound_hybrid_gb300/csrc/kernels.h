@@ -151,6 +151,11 @@ struct Params {
   float* Ks;
   float* Vs;
   int cap_s;               // scale row stride (a multiple of 4)
+  // paged cache (pages != null): row r of kv head g is at K + pages[r / page_tokens] * page_elems
+  // + (g * page_tokens + r % page_tokens) * hd; K, V point at this layer's K or V block of page 0
+  const int* pages;
+  int page_tokens;
+  long long page_elems;
   const int* len;          // position of the new token (= cached rows)
   const float2* rope;      // [>= cap][hd/2] (cos, sin) of position * theta^(-2i/hd)
   int cap, nq, nkv, hd, nsplit;
@@ -167,6 +172,7 @@ struct Params {
   uint16_t* V_b[8];
   float* Ks_b[8];
   float* Vs_b[8];
+  const int* pages_b[8];
   const int* len_b[8];
   int cap_b[8];
   int cap_s_b[8];
@@ -319,6 +325,9 @@ struct AttnArgs {
   int cap;
   const float2* rope;      // (cos, sin) [>= t0 + n][hd/2]
   float* Qr;               // scratch: rotated, scaled queries [n][nq][hd]
+  const int* pages;        // paged cache (as attn::Params), else null
+  int page_tokens;
+  long long page_elems;
   uint16_t* O_hi;
   uint16_t* O_lo;
   int ldo;

@@ -198,6 +198,13 @@ __global__ void k_gdn_ring(GdnArgs a) {
 }
 
 // ------------------------------------------------------------------ attention
+// Element offset of cached row r of kv head g (contiguous, or through the page table).
+__device__ __forceinline__ long long kv_off(const AttnArgs& a, int g, int r) {
+  if (a.pages)
+    return (long long)a.pages[r / a.page_tokens] * a.page_elems + ((long long)g * a.page_tokens + r % a.page_tokens) * a.hd;
+  return ((long long)g * a.cap + r) * a.hd;
+}
+
 __global__ void k_attn_prep(AttnArgs a) {
   const int i = blockIdx.x;
   const int t = a.t0 + i;
@@ -216,13 +223,13 @@ __global__ void k_attn_prep(AttnArgs a) {
     const int g = e / half, d = e % half;
     const float2 cs = rope[d];
     const float x0 = yi[(a.nq + g) * hd + d], x1 = yi[(a.nq + g) * hd + d + half];
-    uint16_t* kr = a.K + ((long long)g * a.cap + t) * hd;
+    uint16_t* kr = a.K + kv_off(a, g, t);
     kr[d] = f32_to_bf16_rne(x0 * cs.x - x1 * cs.y);
     kr[d + half] = f32_to_bf16_rne(x1 * cs.x + x0 * cs.y);
   }
   for (int e = threadIdx.x; e < a.nkv * hd; e += blockDim.x) {
     const int g = e / hd, d = e % hd;
-    a.V[((long long)g * a.cap + t) * hd + d] = f32_to_bf16_rne(yi[(a.nq + a.nkv + g) * hd + d]);
+    a.V[kv_off(a, g, t) + d] = f32_to_bf16_rne(yi[(a.nq + a.nkv + g) * hd + d]);
   }
 }
 
@@ -275,8 +282,7 @@ __global__ void __launch_bounds__(kCausalThreads) k_attn_causal(AttnArgs a) {
   }
   const int last = a.t0 + i0 + nvalid - 1;  // last key position any query of the CTA sees
   const int ntiles = last / kTK + 1;
-  const uint16_t* Kg = a.K + (long long)g * a.cap * HD;
-  const uint16_t* Vg = a.V + (long long)g * a.cap * HD;
+
   for (int tt = 0; tt < ntiles; ++tt) {
     const int p0 = tt * kTK;
     __syncthreads();  // the previous tile's K, V and P are no longer read
@@ -284,8 +290,9 @@ __global__ void __launch_bounds__(kCausalThreads) k_attn_causal(AttnArgs a) {
       const int r = e / (HD / 8), c = e % (HD / 8);
       uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
       if (p0 + r <= last) {
-        kv = *reinterpret_cast<const uint4*>(Kg + (long long)(p0 + r) * HD + c * 8);
-        vv = *reinterpret_cast<const uint4*>(Vg + (long long)(p0 + r) * HD + c * 8);
+        const long long off = kv_off(a, g, p0 + r);
+        kv = *reinterpret_cast<const uint4*>(a.K + off + c * 8);
+        vv = *reinterpret_cast<const uint4*>(a.V + off + c * 8);
       }
       *reinterpret_cast<uint4*>(Ks + r * SM::kRow + c * 16) = kv;
       *reinterpret_cast<uint4*>(Vs + r * SM::kRow + c * 16) = vv;

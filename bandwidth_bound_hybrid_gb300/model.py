@@ -56,7 +56,8 @@ class HybridModel:
     referenced by this object.
     """
 
-    def __init__(self, shape, weights: dict, capacities, splits: int = 0, flags: int = 0):
+    def __init__(self, shape, weights: dict, capacities, splits: int = 0, flags: int = 0, pages=None):
+        """pages: (page_tokens, pool_pages) for a paged KV cache (hy_cache_alloc_paged)."""
         L = capi.lib()
         self.shape = shape
         self._weights = weights
@@ -84,7 +85,10 @@ class HybridModel:
         self.m = m
         caps = (ctypes.c_int32 * len(capacities))(*[int(x) for x in capacities])
         c = ctypes.c_void_p()
-        rc = L.hy_cache_alloc(m, len(capacities), caps, ctypes.byref(c))
+        if pages:
+            rc = L.hy_cache_alloc_paged(m, len(capacities), caps, int(pages[0]), int(pages[1]), ctypes.byref(c))
+        else:
+            rc = L.hy_cache_alloc(m, len(capacities), caps, ctypes.byref(c))
         if rc != capi.HY_OK:
             L.hy_model_free(m)
             self.m = None
@@ -144,6 +148,10 @@ class HybridModel:
     def step_kernels(self) -> int:
         """Kernels the last recorded decode step launches (one per operation)."""
         return int(capi.lib().hy_step_kernels(self.c))
+
+    def free_pages(self) -> int:
+        """Pages left in the pool of a paged cache (-1 without pages)."""
+        return int(capi.lib().hy_cache_free_pages(self.c))
 
     def reset(self, seq: int, stream=None) -> None:
         check(capi.lib().hy_seq_reset(self.c, seq, _stream(stream)), "hy_seq_reset")

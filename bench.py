@@ -58,6 +58,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernel-timing", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="no programmatic dependent launch between kernels")
+    ap.add_argument("--kernel-table", action="store_true",
+                    help="time every decode kernel kind on its own (CUDA graphs over every layer's own buffers) and "
+                         "print one JSON line of rows instead of the benchmark line")
+    ap.add_argument("--paged", action="store_true", help="batch workloads: a paged KV cache sized to the contexts")
     return ap.parse_args(argv)
 
 
@@ -208,7 +212,8 @@ def cpu_baseline_obj(shape, context: int, what: str):
                                                    warm=False)
     finally:
         orc.set_threads(cores)
-    return {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
+    return {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "oracle": "FP64 throughout, the DeltaNet step with its explicit dk x dk matrix",
+            "cpu_model": cpu_model(),
             "value_1_core": tps1,
             "sample": f"{ntok} full-depth FP64 oracle decode tokens{' ' + what if what else ''} at context {context} "
                       f"from a seeded "
@@ -239,6 +244,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "context": prompt, "batch": w.batch},
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "oracle": "FP64 throughout, the DeltaNet step with its explicit dk x dk matrix",
                          "sample": f"{n} full-depth FP64 oracle decode tokens ({dt:.1f} s) at context {prompt} from a "
                                    f"seeded synthetic cache (prompt not replayed on the CPU)"},
         "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -285,28 +291,30 @@ def run_ours(args):
     model = HybridModel(shape, weights, [cap], splits=args.splits, flags=flags)
     toks = torch.from_numpy(workloads.prompt_ids(w, n=prompt)).to(dev) if prompt else None
     ids = torch.zeros(1, dtype=torch.int32, device=dev)
+    logits = torch.empty(shape.vocab, dtype=torch.float32, device=dev)  # the step returns logits and the greedy id
     synthetic_fill = prompt > SYNTHETIC_FILL_ABOVE
+    pre = None
     if synthetic_fill:  # a step's cost depends on the context length, not on what the cache holds
         model.fill_synthetic(0, prompt, seed=1)
         ids.copy_(toks[-1:])
     elif prompt:
-        model.prefill(0, toks)
+        pre = timed_prefill(model, toks, shape, logits)
         ids.copy_(toks[-1:])
     for _ in range(args.warmup):
-        model.decode_step(0, ids, ids)
+        model.decode_step(0, ids, ids, logits)
     torch.cuda.synchronize()
     assert model.check_device() == 0, "device guard fired during warm-up"
     ctx0 = model.seq_len(0)
 
     # ---- timed region: K graph launches, inputs resident in HBM
     depth_window = 32 if w.splits else 0  # the long-context workload: tokens/s per 32-token window
-    t, clk, windows, win = timed_region(args, dist, local, st, lambda: model.decode_step(0, ids, ids),
+    t, clk, windows, win = timed_region(args, dist, local, st, lambda: model.decode_step(0, ids, ids, logits),
                                         window=depth_window, warm=False)
     assert model.check_device() == 0, "device guard fired in the timed region"
     n = max(ws, 1)
     value = job_throughput(n, args.steps, t)
     mid_ctx = ctx0 + args.steps // 2
-    sb = acc.step_bytes(shape, mid_ctx)
+    sb = acc.step_bytes(shape, mid_ctx, logits=True)
     step_gbs = sb.total * args.steps / t / 1e9
 
     # ---- dominant kernel: the gate/up SwiGLU GEMV.  One CUDA graph launches
@@ -360,13 +368,13 @@ def run_ours(args):
             m2 = HybridModel(shape, weights, [cap], splits=sp, flags=flags)
             m2.fill_synthetic(0, ctx0, seed=1)
             ids2 = ids.clone()
-            t2 = timed_region(args, dist, local, st, lambda: m2.decode_step(0, ids2, ids2))[0]
+            t2 = timed_region(args, dist, local, st, lambda: m2.decode_step(0, ids2, ids2, logits))[0]
             assert m2.check_device() == 0
             sweep[str(sp)] = max(ws, 1) * args.steps / t2
             m2.close()
 
     if not args.no_kernel_timing and shape.ffn == 0:
-        roof = gemv_in_roofline(shape, weights, peak, peak_kind, args.workload)
+        roof = moe_gateup_roofline(shape, weights, peak, peak_kind, args.workload)
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
     tok_h = torch.zeros(1, dtype=torch.int32).pin_memory()
@@ -391,7 +399,9 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "shape": shape.name, "batch": 1, "prompt": prompt,
-                       "context_timed": [ctx0, ctx0 + args.steps], "weights": "bf16", "kv": "bf16",
+                       "context_timed": [ctx0, ctx0 + args.steps], "weights": "bf16",
+                       "kv": "int8 + FP32 scale per vector" if getattr(shape, "kv_format", 0) else "bf16",
+                       "outputs": "FP32 logits [V] and the greedy id per step",
                        "context_fill": "seeded synthetic KV rows and recurrent state (no prompt replay)"
                        if synthetic_fill else "prefill of the prompt",
                        "splits": model_splits(args, shape), "parallelism": f"replicas x{n}",
@@ -403,6 +413,7 @@ def run_ours(args):
             "depth_curve": [{"context_start": ctx0 + i * win, "tokens_per_s": n * win / wt}
                             for i, wt in enumerate(windows) if (i + 1) * win <= args.steps] if depth_window else None,
             "split_sweep_tokens_per_s": sweep,
+            "prefill": pre,
             "cpu_baseline": cpu,
             "e2e": {"value": n * e2e_steps / e2e_t, "unit": "tokens/s", "h2d_bytes_per_step": 4,
                     "d2h_bytes_per_step": 4},
@@ -533,6 +544,276 @@ def gemv_in_roofline(shape, weights, peak, peak_kind, workload):
             "peak_source": f"{peak_kind} hbm_gbs"}
 
 
+def load_tensor_peak():
+    """Measured dense bf16 tensor throughput (TFLOP/s): (burst, sustained, kind)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    return 1900.0, 1700.0, "fallback"
+
+
+def timed_prefill(model, toks, shape, logits):
+    """The prompt through hy_prefill, timed with CUDA events on the launching
+    stream: time to the first token's logits, tokens/s, and FLOP rates
+    (prompt GEMMs at bf16 hi + lo on the tensor cores, the rest on the CUDA
+    cores) against the measured sustained bf16 tensor peak."""
+    import torch
+
+    from bandwidth_bound_hybrid_gb300 import accounting as acc
+    st = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(st)
+    model.prefill(0, toks, logits)
+    b.record(st)
+    torch.cuda.synchronize()
+    t = a.elapsed_time(b) / 1e3
+    n = int(toks.numel())
+    fl = acc.prefill_flops(shape, n)
+    _, sustained, kind = load_tensor_peak()
+    chunked = shape.ffn > 0 and getattr(shape, "weight_format", 0) == 0 and getattr(shape, "kv_format", 0) == 0
+    return {"tokens": n, "ttft_ms": t * 1e3, "tokens_per_s": n / t,
+            "path": "chunks of up to 2048 tokens: tcgen05 GEMMs + prompt mixer kernels" if chunked
+            else "token by token through the decode step",
+            "flops_total": fl["total"], "tflops_total": fl["total"] / t / 1e12,
+            "tensor_tflops_executed": fl["tensor_executed"] / t / 1e12, "peak_tflops_sustained": sustained,
+            "frac_of_tensor_peak_whole_prefill": fl["tensor_executed"] / t / 1e12 / sustained,
+            "peak_source": f"{kind} bf16_tflops_sustained"}
+
+
+def graph_us_per_launch(launches, reps=5):
+    """Mean microseconds per launch of one CUDA graph that makes every call of
+    `launches` (functions of a stream handle) once, replayed `reps` times."""
+    import torch
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        for f in launches:
+            f(side.cuda_stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for f in launches:
+            f(side.cuda_stream)
+    graph.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(reps):
+        graph.replay()
+    b.record(st)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / (reps * len(launches))
+    del graph
+    return us
+
+
+def moe_gateup_roofline(shape, weights, peak, peak_kind, workload):
+    """The MoE step's dominant kernel timed alone: the expert gate/up + SwiGLU
+    (k_gemv over the routed experts' rows, routing in every CTA), one graph
+    launching it once per layer over that layer's expert tensors from fixed
+    router logits (top_k + 1 slots of Fe gate and up rows each launch: fresh
+    weights from HBM every launch); average launch duration = graph time /
+    launches."""
+    import torch
+
+    from bandwidth_bound_hybrid_gb300 import capi
+    L = capi.lib()
+    H, E, K, Fe = shape.hidden, shape.n_experts, shape.top_k, shape.expert_ffn
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    rl = torch.randn(E + 1, device="cuda", generator=gen)
+    x = torch.randn(H, device="cuda", generator=gen)
+    g = torch.ones(H, device="cuda")
+    h = torch.empty((K + 1) * Fe, device="cuda")
+    ids = torch.empty(K, dtype=torch.int32, device="cuda")
+    wts = torch.empty(K + 1, device="cuda")
+
+    def one(l):
+        return lambda s: capi.check(L.hy_op_moe_gateup(
+            weights[f"l{l}.exp_gate"].data_ptr(), weights[f"l{l}.exp_up"].data_ptr(),
+            weights[f"l{l}.sh_gate"].data_ptr(), weights[f"l{l}.sh_up"].data_ptr(), E, K, Fe, H, rl.data_ptr(),
+            x.data_ptr(), g.data_ptr(), 1e-6, h.data_ptr(), ids.data_ptr(), wts.data_ptr(), s), "moe_gateup")
+
+    layers = list(range(shape.n_layers))
+    us = graph_us_per_launch([one(l) for l in layers])
+    bytes_launch = (K + 1) * 2 * Fe * H * 2 + (E + 1 + 2 * H + (K + 1) * Fe) * 4
+    achieved = bytes_launch / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "kernel": f"expert gate/up + SwiGLU with in-kernel top-{K} routing (k_gemv, expert rows), "
+                                      f"{K} routed + 1 shared experts x 2 x [{Fe}, {H}]",
+            "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": load_traffic("moe_gateup", workload), "bytes_per_launch": bytes_launch,
+            "launch_us_mean": us, "launches_timed": 5 * len(layers), "peak_source": f"{peak_kind} hbm_gbs"}
+
+
+def kernel_table(args):
+    """Every decode kernel kind of the workload timed on its own: one CUDA
+    graph launches it once per layer over that layer's own weights, states or
+    caches (distinct buffers cycled so that no launch finds its bytes in L2),
+    replayed 5 times; bytes are the algorithmic bytes of one launch.  Plus the
+    prompt GEMM (tcgen05) on a 2048-token chunk, in executed TFLOP/s."""
+    import torch
+
+    from bandwidth_bound_hybrid_gb300 import accounting as acc
+    from bandwidth_bound_hybrid_gb300 import build as hb
+    from bandwidth_bound_hybrid_gb300 import capi
+    from synth import workloads
+    torch.cuda.set_device(0)
+    hb.build()
+    L = capi.lib()
+    w, shape, prompt = workload_of(args)
+    peak, peak_kind = load_peaks()
+    burst, sustained, tkind = load_tensor_peak()
+    weights = workloads.device_weights(shape)
+    H, F4 = shape.hidden, acc.F32
+    gen = torch.Generator(device="cuda").manual_seed(3)
+    rows = []
+    gdn_l = [l for l in range(shape.n_layers) if not shape.is_attn(l)]
+    att_l = [l for l in range(shape.n_layers) if shape.is_attn(l)]
+    x = torch.randn(max(H, 16384), device="cuda", generator=gen)
+    g = torch.ones(max(H, 16384), device="cuda")
+    y = torch.empty(200000, device="cuda")
+
+    def add(name, kernel, launches, nbytes, note=""):
+        us = graph_us_per_launch(launches)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        rows.append({"kernel": name, "impl": kernel, "launches_in_graph": len(launches), "bytes_per_launch": nbytes,
+                     "us_per_launch": us, "gbs": gbs, "frac": gbs / peak, "note": note})
+
+    def gemv(l, name, R, C, norm, acc_):
+        return lambda s: capi.check(L.hy_op_gemv(weights[f"l{l}.{name}"].data_ptr(), R, C, x.data_ptr(),
+                                                 g.data_ptr() if norm else None, 1e-6, y.data_ptr(), acc_, s), "gemv")
+
+    R = shape.gdn_in_rows
+    add(f"input projection, DeltaNet layers [{R}, {H}]", "k_gemv (RMSNorm prologue)",
+        [gemv(l, "w_in", R, H, True, 0) for l in gdn_l], acc.linear_bytes(R, H, 0) + (2 * H + R) * F4)
+    Ra = (shape.attn_q_heads + 2 * shape.attn_kv_heads) * shape.head_dim
+    add(f"input projection, attention layers [{Ra}, {H}]", "k_gemv (RMSNorm prologue)",
+        [gemv(l, "w_in", Ra, H, True, 0) for l in att_l], acc.linear_bytes(Ra, H, 0) + (2 * H + Ra) * F4)
+    Cg = shape.gdn_heads * shape.gdn_dv
+    add(f"output projection + residual, DeltaNet layers [{H}, {Cg}]", "k_gemv (residual epilogue)",
+        [gemv(l, "w_o", H, Cg, False, 1) for l in gdn_l], acc.linear_bytes(H, Cg, 0) + (Cg + 2 * H) * F4)
+    Ca = shape.attn_q_heads * shape.head_dim
+    add(f"output projection + residual, attention layers [{H}, {Ca}]", "k_gemv (residual epilogue)",
+        [gemv(l, "w_o", H, Ca, False, 1) for l in att_l], acc.linear_bytes(H, Ca, 0) + (Ca + 2 * H) * F4)
+    if shape.ffn > 0:
+        Fd = shape.ffn
+        hbuf = torch.empty(Fd, device="cuda")
+
+        def gu(l):
+            return lambda s: capi.check(L.hy_op_gemv_swiglu(weights[f"l{l}.w_gate"].data_ptr(),
+                                                            weights[f"l{l}.w_up"].data_ptr(), Fd, H, x.data_ptr(),
+                                                            g.data_ptr(), 1e-6, hbuf.data_ptr(), s), "swiglu")
+        lay = list(range(shape.n_layers))
+        add(f"RMSNorm + gate/up + SwiGLU 2 x [{Fd}, {H}]", "k_gemv (SwiGLU epilogue)", [gu(l) for l in lay],
+            acc.gemv_swiglu_bytes(Fd, H))
+        add(f"down projection + residual [{H}, {Fd}]", "k_gemv (residual epilogue)",
+            [gemv(l, "w_down", H, Fd, False, 1) for l in lay], acc.linear_bytes(H, Fd, 0) + (Fd + 2 * H) * F4)
+    else:
+        E, K, Fe = shape.n_experts, shape.top_k, shape.expert_ffn
+        lay = list(range(shape.n_layers))
+        add(f"router logits [{E + 1}, {H}]", "k_gemv (RMSNorm prologue)",
+            [gemv(l, "router", E + 1, H, True, 0) for l in lay], (E + 1) * H * 2 + (2 * H + E + 1) * F4)
+        roof = moe_gateup_roofline(shape, weights, peak, peak_kind, args.workload)
+        rows.append({"kernel": f"expert gate/up + SwiGLU, {K} routed + shared x 2 x [{Fe}, {H}]",
+                     "impl": "k_gemv (expert rows, in-kernel top-k)", "launches_in_graph": len(lay),
+                     "bytes_per_launch": roof["bytes_per_launch"], "us_per_launch": roof["launch_us_mean"],
+                     "gbs": roof["achieved"], "frac": roof["frac"], "note": ""})
+        rl = torch.randn(E + 1, device="cuda", generator=gen)
+        hb_ = torch.randn((K + 1) * Fe, device="cuda", generator=gen)
+        ids = torch.empty(K, dtype=torch.int32, device="cuda")
+        wts = torch.empty(K + 1, device="cuda")
+        capi.check(L.hy_op_moe_gateup(weights["l0.exp_gate"].data_ptr(), weights["l0.exp_up"].data_ptr(),
+                                      weights["l0.sh_gate"].data_ptr(), weights["l0.sh_up"].data_ptr(), E, K, Fe, H,
+                                      rl.data_ptr(), x.data_ptr(), g.data_ptr(), 1e-6, hb_.data_ptr(), ids.data_ptr(),
+                                      wts.data_ptr(), None), "moe_gateup")
+
+        def dn(l):
+            return lambda s: capi.check(L.hy_op_moe_down(weights[f"l{l}.exp_down"].data_ptr(),
+                                                         weights[f"l{l}.sh_down"].data_ptr(), E, K, Fe, H,
+                                                         ids.data_ptr(), wts.data_ptr(), hb_.data_ptr(),
+                                                         y.data_ptr(), s), "moe_down")
+        add(f"expert down + weighted sum + residual, {K} routed + shared x [{H}, {Fe}]",
+            "k_gemv (expert segments)", [dn(l) for l in lay],
+            (K + 1) * H * Fe * 2 + ((K + 1) * Fe + K + 1 + 2 * H) * F4)
+    ws = torch.zeros(L.hy_op_argmax_workspace(), dtype=torch.uint8, device="cuda")
+    lg = torch.empty(shape.vocab, device="cuda")
+    oid = torch.empty(1, dtype=torch.int32, device="cuda")
+    head = lambda s: capi.check(L.hy_op_gemv_argmax(weights["lm_head"].data_ptr(), shape.vocab, H, x.data_ptr(),  # noqa
+                                                    g.data_ptr(), 1e-6, lg.data_ptr(), oid.data_ptr(),
+                                                    ws.data_ptr(), s), "argmax")
+    add(f"final RMSNorm + LM head [{shape.vocab}, {H}] + argmax", "k_gemv (argmax epilogue)", [head] * 4,
+        acc.linear_bytes(shape.vocab, H, 0) + (2 * H + shape.vocab) * F4)
+    # DeltaNet update: 160 distinct states, more than L2 holds
+    nh, dk, dv, K4 = shape.gdn_heads, shape.gdn_dk, shape.gdn_dv, shape.conv_k
+    CC = 2 * nh * dk + nh * dv
+    ns = max(8, (160 << 20) // (nh * dv * dk * 4))
+    S = torch.randn((ns, nh, dv, dk), device="cuda", generator=gen) * 0.01
+    ring = torch.zeros((ns, K4, CC), device="cuda")
+    cw = weights[f"l{gdn_l[0]}.conv_w"]
+    yg = torch.randn(CC + 2 * nh, device="cuda", generator=gen)
+    og = torch.empty(nh * dv, device="cuda")
+    pos = torch.tensor([5], dtype=torch.int32, device="cuda")
+
+    def gd(i):
+        return lambda s: capi.check(L.hy_op_gdn_step(yg.data_ptr(), cw.data_ptr(), ring[i].data_ptr(),
+                                                     S[i].data_ptr(), og.data_ptr(), nh, dk, dv, K4, pos.data_ptr(),
+                                                     s), "gdn")
+    add(f"DeltaNet conv + gates + in-place delta rule, {nh} x {dv} x {dk} FP32 state", "k_gdn",
+        [gd(i) for i in range(ns)],
+        2 * nh * dv * dk * 4 + (K4 - 1) * CC * 4 + CC * 4 + CC * K4 * 2 + (CC + 2 * nh + nh * dv) * 4)
+    del S, ring
+    # attention at the workload's context: distinct caches, more than L2 holds
+    nq, nkv, hd = shape.attn_q_heads, shape.attn_kv_heads, shape.head_dim
+    T = max(prompt, 1)
+    cap = T + 8
+    per = nkv * cap * hd * 2
+    nc = max(4, min(64, (400 << 20) // (2 * per)))
+    Kc = torch.randn((nc, nkv, cap, hd), device="cuda", generator=gen).to(torch.bfloat16)
+    Vc = torch.randn((nc, nkv, cap, hd), device="cuda", generator=gen).to(torch.bfloat16)
+    table = torch.empty((cap, hd // 2, 2), device="cuda")
+    capi.check(L.hy_op_rope_table(table.data_ptr(), cap, hd, 1e4, None), "rope")
+    ya = torch.randn((nq + 2 * nkv) * hd, device="cuda", generator=gen)
+    oa = torch.empty(nq * hd, device="cuda")
+    ln = torch.tensor([T], dtype=torch.int32, device="cuda")
+    wsa = torch.zeros(L.hy_op_attention_workspace(nq, nkv, hd, args.splits), dtype=torch.uint8, device="cuda")
+
+    def at(i):
+        return lambda s: capi.check(L.hy_op_attention(ya.data_ptr(), Kc[i].data_ptr(), Vc[i].data_ptr(), cap, nq, nkv,
+                                                      hd, ln.data_ptr(), table.data_ptr(), args.splits, oa.data_ptr(),
+                                                      wsa.data_ptr(), s), "attention")
+    add(f"split-KV GQA attention {nq}/{nkv} x {hd} at context {T} (RoPE, bf16 KV append, LSE combine)", "k_attn",
+        [at(i) for i in range(nc)], 2 * nkv * (T + 1) * hd * 2 + ((nq + 2 * nkv) * hd + nq * hd) * 4)
+    del Kc, Vc
+    # the prompt GEMM on a 2048-token chunk: the largest projection of the model
+    M = 2048
+    if shape.ffn > 0:
+        N, Kd = shape.ffn, H
+        hh = torch.empty((M, N), dtype=torch.int16, device="cuda")
+        hl = torch.empty((M, N), dtype=torch.int16, device="cuda")
+        xm = torch.randn((M, Kd), device="cuda", generator=gen)
+        wsg = torch.empty(L.hy_op_gemm_workspace(M, Kd), dtype=torch.uint8, device="cuda")
+        lay = list(range(shape.n_layers))
+
+        def gm(l):
+            return lambda s: capi.check(L.hy_op_gemm_swiglu(weights[f"l{l}.w_gate"].data_ptr(),
+                                                            weights[f"l{l}.w_up"].data_ptr(), N, Kd, M, xm.data_ptr(),
+                                                            Kd, g.data_ptr(), 1e-6, hh.data_ptr(), hl.data_ptr(), N,
+                                                            wsg.data_ptr(), s), "gemm")
+        us = graph_us_per_launch([gm(l) for l in lay])
+        alg = 2.0 * M * (2 * N) * Kd
+        rows.append({"kernel": f"prompt GEMM, RMSNorm + gate/up + SwiGLU, {M} tokens x 2 x [{N}, {Kd}] "
+                               f"(plus the norm/split pass of the chunk)",
+                     "impl": "k_norm_split + k_gemm (tcgen05, TMEM accumulator, TMA tiles)",
+                     "launches_in_graph": len(lay), "us_per_launch": us, "tflops_algorithmic": alg / us / 1e6,
+                     "tflops_executed": 2 * alg / us / 1e6, "frac_executed_of_sustained": 2 * alg / us / 1e6 / sustained,
+                     "note": "activations as bf16 hi + lo parts: the tensor pipe executes twice the algorithmic FLOPs"})
+    print(json.dumps({"kernel_table": rows, "workload": w.name, "hbm_peak_gbs": peak, "hbm_peak_source": peak_kind,
+                      "bf16_tflops_sustained": sustained, "tensor_peak_source": tkind}), flush=True)
+    return 0
+
+
 def gemv_batch_roofline(shape, weights, B, peak, peak_kind, workload):
     """The batched tensor-core GEMV (k_bgemv) timed alone on the batch step's
     largest launch: MoE shapes, the expert gate/up + SwiGLU over the expected
@@ -617,7 +898,11 @@ def run_ours_batch(args, w, shape, dist, ws, rank, local):
     weights = workloads.device_weights(shape)
     caps = [c + args.warmup + 2 * args.steps + 16 for c in ctx]
     flags = capi.HY_FLAG_NO_PDL if args.no_pdl else 0
-    model = HybridModel(shape, weights, caps, splits=args.splits, flags=flags)
+    pages = None
+    if args.paged:  # a pool of 128-token pages holding what the contexts and steps need, not B maximal slabs
+        pool = sum((c + args.warmup + 2 * args.steps + 127) // 128 for c in ctx)
+        pages = (128, pool)
+    model = HybridModel(shape, weights, caps, splits=args.splits, flags=flags, pages=pages)
     for s, c in enumerate(ctx):
         model.fill_synthetic(s, c, seed=s + 1)
     seqs = list(range(B))
@@ -673,6 +958,8 @@ def run_ours_batch(args, w, shape, dist, ws, rank, local):
                        "tokens": "seeded uniform ids per sequence and step (teacher forcing)",
                        "weights": "4-bit blocks of 32 + fp16 scale" if getattr(shape, "weight_format", 0) else "bf16",
                        "kv": "bf16", "parallelism": f"replicas x{n}",
+                       "kv_layout": f"paged: {pages[1]} pages of 128 positions shared by the batch" if pages
+                       else "one slab of its capacity per sequence",
                        "l2": "inputs larger than L2: every step streams GBs of weights and KV through the 129 MB L2"},
             "roofline": roof,
             "step_roofline": {"bound": "hbm", "bytes_per_step": sb.total, "achieved": step_gbs, "peak": peak,
@@ -708,6 +995,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel_table:
+        return kernel_table(args)
     return run_ours(args)
 
 

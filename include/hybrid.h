@@ -149,6 +149,25 @@ void hy_model_free(hy_model* m);
 int hy_cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, hy_cache** out);
 void hy_cache_free(hy_cache* c);
 
+/* hy_cache_alloc with a paged KV cache ("hanzo-engine: A Portable Single-Binary
+ * LLM Inference Engine...", section "System Architecture": paged KV cache and
+ * continuous batching).  Instead of a slab of capacity_host[s] positions per
+ * sequence, K and V live in one pool of pool_pages pages of page_tokens
+ * positions (a positive multiple of 128), each holding every attention
+ * layer's K and V of page_tokens consecutive positions of one sequence.  A
+ * sequence takes pages as it grows (hy_prefill, hy_decode_step and
+ * hy_seq_fill_synthetic take them, on `stream`, before they launch anything;
+ * HY_ERR_CAPACITY, with nothing launched and no page taken, when the pool is
+ * short) and gives them back on hy_seq_reset, so sequences of any mix of
+ * lengths share the pool and may join or leave a batch between steps.
+ * capacity_host[s] still bounds each sequence's length.  Recurrent state and
+ * scratch are as for hy_cache_alloc.  bf16 K/V only (HY_ERR_UNSUPPORTED with
+ * kv_format 1). */
+int hy_cache_alloc_paged(hy_model* m, int32_t max_seqs, const int32_t* capacity_host, int32_t page_tokens,
+                         int32_t pool_pages, hy_cache** out);
+/* Pages left in the pool of a paged cache, or -1 for a cache without pages. */
+int32_t hy_cache_free_pages(const hy_cache* c);
+
 /* Forget sequence `seq`: length 0, recurrent and conv state zeroed
  * (stream-ordered). */
 int hy_seq_reset(hy_cache* c, int32_t seq, void* stream);
