@@ -17,9 +17,11 @@
 //   shuffles) -> online softmax per head -> P V with each thread owning two
 //   output dims.  The CTA holding position T rotates and rounds the new k/v
 //   to bf16, appends them to the cache and attends to them from shared memory.
-//   Partials (m, l, o) go to a scratch buffer; the last CTA of a kv head to
-//   finish (atomic ticket, nobody waits) merges them:
-//     m = max_s m_s,  o = sum_s e^{m_s - m} o_s / sum_s e^{m_s - m} l_s.
+//   Partials (m, l, o) go to a scratch buffer and are merged
+//     m = max_s m_s,  o = sum_s e^{m_s - m} o_s / sum_s e^{m_s - m} l_s
+//   by the last few CTAs of a kv head to finish, each a slice of the outputs
+//   (a ticket counter: earlier CTAs exit at once, the last ones wait for the
+//   very last, bounded, then merge together).
 #include "attn_dev.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p0) {
     if (ctid == 0) mbar_arrive(&empty[s]);
   }
   if (it.has_new) process_tile<HD, G, KV8>(w.kn, w.vn, 1, w, A, ctid, w.kvs, w.kvs + 1);
-  end_item<HD, G>(p, g, sp, w, A, reinterpret_cast<float*>(stages), ctid);
+  end_item<HD, G>(p, g, sp, w, A, ctid);
 }
 
 template <int HD, int G>
@@ -195,9 +197,31 @@ cudaError_t launch(const Params& p, cudaStream_t st, bool pdl) {
   if (!k) return cudaErrorInvalidValue;
   if (p.kv8 && (p.cap_s % 4 || p.cap_s < p.cap)) return cudaErrorInvalidValue;
   if (p.pages && (p.kv8 || p.page_tokens <= 0 || p.page_tokens % 128)) return cudaErrorInvalidValue;
-  if (p.nb < 0 || p.nb > 8) return cudaErrorInvalidValue;
+  if (p.nb < 0 || p.nb > 8 || p.nsplit > 0xFFFF) return cudaErrorInvalidValue;
+  // Mergers per kv head: enough that each merges about 16 partial values
+  // per thread; while they wait, at most (mergers - 1) CTAs per head and
+  // token hold an SM, which must leave at least one SM for the CTAs they wait
+  // for (every SM holds at least one CTA).
+  static int nsm_of[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (nsm_of[dev] == 0) {
+    int n = 0;
+    if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    nsm_of[dev] = n;
+  }
+  Params q = p;
+  const long long values = (long long)p.nq * p.hd * p.nsplit / p.nkv;  // partial o values of one kv head
+  long long K = (values + 16 * kCT - 1) / (16 * kCT);
+  const long long groups = (long long)p.nkv * (p.nb > 0 ? p.nb : 1);
+  const long long kmax = (nsm_of[dev] - 1) / groups + 1;
+  if (K > kmax) K = kmax;
+  if (K > p.nsplit) K = p.nsplit;
+  q.mergers = K < 1 ? 1 : (int)K;
   return launch_k(reinterpret_cast<void (*)(Params)>(k), dim3(p.nkv, p.nsplit, p.nb > 0 ? p.nb : 1), dim3(kThreads),
-                  smem, st, pdl, p);
+                  smem, st, pdl, q);
 }
 
 cudaError_t rope_table(float2* tab, int cap, int hd, double theta, cudaStream_t st) {

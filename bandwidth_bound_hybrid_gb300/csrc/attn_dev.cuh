@@ -4,8 +4,9 @@
 // of the L = T + 1 keys.  Its cached K/V rows arrive as shared-memory tiles
 // (copied by the TMA engine); the new row T (rotated, rounded to bf16 and
 // appended to the cache by the item that holds it) is attended from shared
-// memory.  The item leaves (m, l, o) partials for its G query heads; the last
-// item of kv head g to finish merges them with log-sum-exp weights
+// memory.  The item leaves (m, l, o) partials for its G query heads, merged
+// with log-sum-exp weights by the last few items of kv head g to finish, each
+// a slice of the outputs
 // ("Beating llama.cpp from Scratch on Consumer AMD", Act 4 and "What Broke"
 // section 1: partial sums over segments of the KV cache, combined across
 // separate workgroups).
@@ -266,21 +267,54 @@ __device__ __forceinline__ void begin_item(const Params& p, int g, int T, const 
   }
 }
 
+// Reduce-scatter of C per-head partial sums over the lanes of a row: at
+// each halving of the lane distance O a lane keeps half of its heads (the
+// upper half if bit O of its lane index is set) and adds its partner's sums
+// of them; once one head is left the remaining levels are a plain all-reduce.
+// On return v[0] is the full sum of head li / (lanes per row / heads).
+template <int C, int O>
+__device__ __forceinline__ void head_scatter(float* v, int li) {
+  if constexpr (O > 0) {
+    if constexpr (C > 1) {
+      const bool up = (li & O) != 0;
+#pragma unroll
+      for (int i = 0; i < C / 2; ++i) {
+        const float send = up ? v[i] : v[i + C / 2];
+        const float keep = up ? v[i + C / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      head_scatter<C / 2, O / 2>(v, li);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      head_scatter<1, O / 2>(v, li);
+    }
+  }
+}
+
 // One tile of rows: scores -> online softmax (one warp per head) -> P V.
+// Scores: a row is read by HD / 8 lanes (8 dims each, one 16-byte shared
+// load), every warp takes its rows of all passes at once (independent loads
+// and shuffles in flight), and the head sums are reduce-scattered.  The
+// probabilities are kept row-major [row][G] so that P V reads a row's G
+// weights with vector loads.
 template <int HD, int G, bool KV8 = false>
 __device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t* tv, int rows,
                                              const WorkPtrs<HD, G>& w, Acc<HD, G>& A, int ctid,
                                              const float* ks = nullptr, const float* vs = nullptr) {
   using W = Work<HD, G>;
   constexpr int TP = W::TP;
-  constexpr int LPR = HD / 8, RPW = 32 / LPR;
+  constexpr int LPR = HD / 8, RPW = 32 / LPR, RSTEP = kCWarps * RPW;
+  constexpr int NPASS = (TP + RSTEP - 1) / RSTEP;
+  constexpr int GL = LPR / G;  // lanes left per head after the scatter
+  static_assert(G <= LPR, "heads per group above lanes per row");
   const int warp = ctid >> 5, lane = ctid & 31;
   const int sub = lane / LPR, li = lane % LPR;
-  for (int base = warp * RPW; base < rows; base += kCWarps * RPW) {
-    const int row = base + sub;
-    float d[G];
+  float d[NPASS][G];
 #pragma unroll
-    for (int j = 0; j < G; ++j) d[j] = 0.f;
+  for (int ps = 0; ps < NPASS; ++ps) {
+    const int row = ps * RSTEP + warp * RPW + sub;
+#pragma unroll
+    for (int j = 0; j < G; ++j) d[ps][j] = 0.f;
     if (row < rows) {
       if (KV8) {
         const uint2 k8 = *reinterpret_cast<const uint2*>(reinterpret_cast<const int8_t*>(tk) + row * HD + li * 8);
@@ -292,34 +326,33 @@ __device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t*
           float a = 0.f;
 #pragma unroll
           for (int e = 0; e < 8; ++e) a = fmaf(kf[e], A.qr[j][e], a);
-          d[j] = a * sk;
+          d[ps][j] = a * sk;
         }
       } else {
         const uint4 kv = *reinterpret_cast<const uint4*>(tk + row * HD + li * 8);
 #pragma unroll
-        for (int j = 0; j < G; ++j) d[j] = dot8(kv, A.qr[j]);
+        for (int j = 0; j < G; ++j) d[ps][j] = dot8(kv, A.qr[j]);
       }
     }
+  }
 #pragma unroll
-    for (int o = LPR / 2; o > 0; o >>= 1)
-#pragma unroll
-      for (int j = 0; j < G; ++j) d[j] += __shfl_xor_sync(0xffffffffu, d[j], o);
-    if (li == 0 && row < rows)
-#pragma unroll
-      for (int j = 0; j < G; ++j) w.sc[j * TP + row] = d[j];
+  for (int ps = 0; ps < NPASS; ++ps) {
+    head_scatter<G, LPR / 2>(d[ps], li);
+    const int row = ps * RSTEP + warp * RPW + sub;
+    if (li % GL == 0 && row < rows) w.sc[row * G + li / GL] = d[ps][0];
   }
   named_barrier(1, kCT);
   if (warp < G) {
     const int j = warp;
     float mx = -INFINITY;
-    for (int r = lane; r < rows; r += 32) mx = fmaxf(mx, w.sc[j * TP + r]);
+    for (int r = lane; r < rows; r += 32) mx = fmaxf(mx, w.sc[r * G + j]);
     mx = warp_max(mx);
     const float m_old = w.m[j];
     const float m_new = fmaxf(m_old, mx);
     float sum = 0.f;
     for (int r = lane; r < rows; r += 32) {
-      const float e = __expf(w.sc[j * TP + r] - m_new);
-      w.sc[j * TP + r] = e;
+      const float e = __expf(w.sc[r * G + j] - m_new);
+      w.sc[r * G + j] = e;
       sum += e;
     }
     sum = warp_sum(sum);
@@ -340,6 +373,7 @@ __device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t*
   }
   const uint32_t* tv32 = reinterpret_cast<const uint32_t*>(tv);
   const uint16_t* tv16 = reinterpret_cast<const uint16_t*>(tv);  // int8 cache: two codes
+#pragma unroll 4
   for (int r = pg; r < rows; r += W::NG) {
     float vx, vy;
     if (KV8) {
@@ -352,21 +386,164 @@ __device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t*
       vx = bf16_lo(v2);
       vy = bf16_hi(v2);
     }
+    float pj[G];
+    if constexpr (G % 4 == 0) {
+#pragma unroll
+      for (int j = 0; j < G; j += 4) {
+        const float4 q4 = *reinterpret_cast<const float4*>(w.sc + r * G + j);
+        pj[j] = q4.x;
+        pj[j + 1] = q4.y;
+        pj[j + 2] = q4.z;
+        pj[j + 3] = q4.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < G; ++j) pj[j] = w.sc[r * G + j];
+    }
 #pragma unroll
     for (int j = 0; j < G; ++j) {
-      const float pj = w.sc[j * TP + r];
-      A.acc[j][0] = fmaf(pj, vx, A.acc[j][0]);
-      A.acc[j][1] = fmaf(pj, vy, A.acc[j][1]);
+      A.acc[j][0] = fmaf(pj[j], vx, A.acc[j][0]);
+      A.acc[j][1] = fmaf(pj[j], vy, A.acc[j][1]);
     }
   }
   named_barrier(1, kCT);
 }
 
-// Partials of the item, then (last item of kv head g only) the merge.
-// scratch: >= nsplit * G + G floats of shared memory that no tile uses.
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* a) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+
+// Merge of the partials of kv head g by the last p.mergers items to finish.
+// The head's counter holds arrivals in its low 16 bits and a generation
+// above them.  Every item arrives once its partials are written; items that
+// arrive before the last p.mergers exit at once (their SMs go to the next
+// kernel).  Each of the last p.mergers waits for the generation to step: the
+// very last one clears the count and steps it, which releases the others.
+// Merger r then merges slice r of the G * HD outputs,
+//   M = max_s m_s,  o = sum_s e^{m_s - M} o_s / sum_s e^{m_s - M} l_s,
+// up to 32 splits at a time (lane u holds m, l of split u and its weight).  At most p.mergers - 1 items of a head wait at a time and the
+// launch keeps that below the SM count over all heads and tokens, so the
+// items they wait for always find an SM.
+template <int HD, int G>
+__device__ __forceinline__ void merge(const Params& p, int g, const WorkPtrs<HD, G>& w, int ctid) {
+  unsigned* ctr = p.counter + g;
+  const int K = p.mergers;
+  if (ctid == 0) {
+    __threadfence();
+    const unsigned old = atomicAdd(ctr, 1u);
+    const int ticket = (int)(old & 0xFFFFu);
+    int role = ticket - (p.nsplit - K);
+    if (role >= 0) {
+      if (ticket == p.nsplit - 1) {
+        atomicAdd(ctr, 0x10000u - (unsigned)p.nsplit);
+      } else {
+        uint64_t t0 = 0;
+        for (uint32_t i = 0; (ld_acquire_gpu(ctr) >> 16) == (old >> 16); ++i) {
+          if ((i & 255u) == 255u) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+              t0 = now;
+            } else if (now - t0 > kWaitLimitNs) {
+              set_guard(p.guard, kGuardWaitTimeout);
+              role = -1;
+              break;
+            }
+          }
+        }
+      }
+    }
+    *w.last = role;
+  }
+  named_barrier(1, kCT);
+  const int role = *w.last;
+  if (role < 0) return;
+  // merger `role` takes its share of the G * HD / 32 groups of 32 outputs
+  // (one head each, since 32 divides HD); a group's outputs are one warp's
+  // lanes, so that each load of a split's o values is 128 contiguous bytes,
+  // and when groups are few several warps share a group's splits
+  constexpr int NGR = G * HD / 32;
+  const int gpm = (NGR + K - 1) / K;
+  const int ga = role * gpm, gb = (ga + gpm < NGR) ? ga + gpm : NGR;
+  if (ga >= gb) return;
+  const int ng = gb - ga;
+  const int wpg = ng >= kCWarps ? 1 : kCWarps / ng;  // warps per group
+  const int gstep = kCWarps / wpg;                    // groups per round
+  const int spw = (p.nsplit + wpg - 1) / wpg;         // splits per warp
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int wg = warp / wpg, wsp = warp % wpg;
+  const float* pg0 = p.part + (long long)g * p.nsplit * G * (HD + 2);
+  float* s_num = w.ored;  // [kCWarps][32], then M and den per warp
+  float* s_M = s_num + kCWarps * 32;
+  float* s_den = s_M + kCWarps;
+  const int rounds = (ng + gstep - 1) / gstep;
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int gi = ga + rd * gstep + wg;
+    const bool vg = (wg < gstep) && gi < gb;  // warp-uniform
+    const int e = (vg ? gi : ga) * 32 + lane;
+    const int j = e / HD, d = e % HD;
+    float M = -INFINITY, den = 0.f, num = 0.f;
+    if (vg) {
+      const int sa = wsp * spw, se = (sa + spw < p.nsplit) ? sa + spw : p.nsplit;
+      for (int s0 = sa; s0 < se; s0 += 32) {
+        const int ns = (se - s0 < 32) ? se - s0 : 32;
+        float mi = -INFINITY, lv = 0.f;
+        if (lane < ns) {
+          const float* ps = pg0 + ((long long)(s0 + lane) * G + j) * (HD + 2);
+          mi = __ldcg(ps + HD);
+          lv = __ldcg(ps + HD + 1);
+        }
+        float ov[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+          ov[u] = (u < ns) ? __ldcg(pg0 + ((long long)(s0 + u) * G + j) * (HD + 2) + d) : 0.f;
+        const float bm = warp_max(lv > 0.f ? mi : -INFINITY);
+        if (bm > -INFINITY) {
+          const float nm = fmaxf(M, bm);
+          const float c = (M == -INFINITY) ? 0.f : __expf(M - nm);
+          const float wt = (lv > 0.f) ? __expf(mi - nm) : 0.f;  // lane u: weight of split s0 + u
+          den = den * c + warp_sum(wt * lv);
+          num *= c;
+#pragma unroll
+          for (int u = 0; u < 32; ++u) num = fmaf(__shfl_sync(0xffffffffu, wt, u), ov[u], num);
+          M = nm;
+        }
+      }
+    }
+    if (wpg > 1) {
+      // the wpg warps of a group combine through shared memory
+      s_num[warp * 32 + lane] = num;
+      if (lane == 0) {
+        s_M[warp] = M;
+        s_den[warp] = den;
+      }
+      named_barrier(1, kCT);
+      if (vg && wsp == 0) {
+        for (int q = 1; q < wpg; ++q) {
+          const float Mq = s_M[warp + q];
+          const float nm = fmaxf(M, Mq);
+          if (nm == -INFINITY) continue;
+          const float c0 = (M == -INFINITY) ? 0.f : __expf(M - nm);
+          const float c1 = (Mq == -INFINITY) ? 0.f : __expf(Mq - nm);
+          den = den * c0 + s_den[warp + q] * c1;
+          num = num * c0 + s_num[(warp + q) * 32 + lane] * c1;
+          M = nm;
+        }
+        p.o[(long long)g * G * HD + e] = num / den;
+      }
+      named_barrier(1, kCT);
+    } else if (vg) {
+      p.o[(long long)g * G * HD + e] = num / den;
+    }
+  }
+}
+
+// Partials of the item (o reduced over the position groups, then m and l),
+// then the merge.
 template <int HD, int G>
 __device__ __forceinline__ void end_item(const Params& p, int g, int sp, const WorkPtrs<HD, G>& w, Acc<HD, G>& A,
-                                         float* scratch, int ctid) {
+                                         int ctid) {
   using W = Work<HD, G>;
   const int pg = ctid / W::NP, dp = ctid % W::NP;
 #pragma unroll
@@ -388,75 +565,7 @@ __device__ __forceinline__ void end_item(const Params& p, int g, int sp, const W
     part[ctid * (HD + 2) + HD + 1] = w.l[ctid];
   }
   named_barrier(1, kCT);
-  if (ctid == 0) {
-    __threadfence();
-    const unsigned ticket = atomicAdd(p.counter + g, 1u);
-    *w.last = (ticket == (unsigned)(p.nsplit - 1));
-  }
-  named_barrier(1, kCT);
-  if (!*w.last) return;
-  __threadfence();
-  // merge: split weights first (all loads in flight together), then each
-  // thread merges its (head, dim) outputs with batches of independent loads
-  const float* pg0 = p.part + (long long)g * p.nsplit * G * (HD + 2);
-  float* s_w = scratch;                  // [nsplit][G]: m_s, then e^{m_s - M}
-  float* s_den = scratch + p.nsplit * G; // [G]
-  float* s_l = w.ored;                   // [nsplit][G]
-  for (int e = ctid; e < p.nsplit * G; e += kCT) {
-    const float* ps = pg0 + (long long)e * (HD + 2);
-    s_w[e] = __ldcg(ps + HD);
-    s_l[e] = __ldcg(ps + HD + 1);
-  }
-  named_barrier(1, kCT);
-  if (ctid < G) {
-    const int j = ctid;
-    float M = -INFINITY;
-    for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, s_w[s * G + j]);
-    float den = 0.f;
-    for (int s = 0; s < p.nsplit; ++s) {
-      const float l = s_l[s * G + j];
-      const float wt = (l > 0.f) ? __expf(s_w[s * G + j] - M) : 0.f;
-      s_w[s * G + j] = wt;
-      den = fmaf(wt, l, den);
-    }
-    s_den[j] = den;
-  }
-  named_barrier(1, kCT);
-  // each thread merges its NE (head, dim) outputs; every load of a batch of
-  // eight splits is in flight at once
-  constexpr int NE = (G * HD + kCT - 1) / kCT;
-  float num[NE];
-#pragma unroll
-  for (int q = 0; q < NE; ++q) num[q] = 0.f;
-  for (int s0 = 0; s0 < p.nsplit; s0 += 8) {
-    float v[NE][8];
-#pragma unroll
-    for (int q = 0; q < NE; ++q) {
-      const int e = ctid + q * kCT;
-      const int j = e / HD, d = e % HD;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        v[q][u] = (e < G * HD && s0 + u < p.nsplit) ? __ldcg(pg0 + ((long long)(s0 + u) * G + j) * (HD + 2) + d) : 0.f;
-    }
-#pragma unroll
-    for (int q = 0; q < NE; ++q) {
-      const int e = ctid + q * kCT;
-      const int j = (e < G * HD) ? e / HD : 0;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (s0 + u < p.nsplit) num[q] = fmaf(s_w[(s0 + u) * G + j], v[q][u], num[q]);
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < NE; ++q) {
-    const int e = ctid + q * kCT;
-    if (e < G * HD) {
-      const int j = e / HD, d = e % HD;
-      p.o[(long long)(g * G + j) * HD + d] = num[q] / s_den[j];
-    }
-  }
-  if (ctid == 0) p.counter[g] = 0u;
-  named_barrier(1, kCT);
+  merge<HD, G>(p, g, w, ctid);
 }
 
 }  // namespace attn

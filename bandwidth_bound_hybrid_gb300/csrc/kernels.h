@@ -161,7 +161,8 @@ struct Params {
   int cap, nq, nkv, hd, nsplit;
   float scale;
   float* part;             // [nkv][nsplit][G][hd + 2]
-  unsigned* counter;       // [nkv], zero between launches
+  unsigned* counter;       // [nkv]: arrivals in bits 0-15 (zero between launches), a generation above
+  int mergers;            // set by launch(): the last `mergers` CTAs of a kv head merge its partials
   float* o;                // [nq*hd]
   unsigned* guard;
   // batch (nb > 0): token z = blockIdx.z uses y + z*ld_y, o + z*ld_o,

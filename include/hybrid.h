@@ -374,8 +374,9 @@ int hy_op_rope_table(float* table_dev, int32_t cap, int32_t hd, float theta, voi
  * the new k with rope_table_dev, appends bf16 k, v at row T of K_dev, V_dev
  * (bf16 [nkv][cap][hd]), attends over rows [0, T], writes o_dev FP32
  * [nq*hd].  nsplit chunks per kv head (0 = automatic).  workspace_dev:
- * hy_op_attention_workspace() bytes, zeroed before first use, left zeroed.
- * [Strata] "Act 4" and "What Broke" section 1. */
+ * hy_op_attention_workspace() bytes, zeroed before its first use and then
+ * passed unmodified to later calls (its counters carry a generation number
+ * from call to call).  [Strata] "Act 4" and "What Broke" section 1. */
 size_t hy_op_attention_workspace(int32_t nq, int32_t nkv, int32_t hd, int32_t nsplit);
 int hy_op_attention(const float* y_dev, void* K_dev, void* V_dev, int32_t cap, int32_t nq, int32_t nkv, int32_t hd,
                     const int32_t* len_dev, const float* rope_table_dev, int32_t nsplit, float* o_dev,
