@@ -8,15 +8,18 @@
 // going further needs partial sums combined across separate workgroups).
 // Here each split is its own CTA with no length-dependent shared memory:
 //   grid (kv_heads, splits); CTA (g, s) owns positions [s L / S, (s+1) L / S)
-//   of kv head g (L = T + 1 keys), streams its K/V rows HBM -> shared memory
-//   with bulk copies (one copy warp, 3 stages, started before
-//   griddepcontrol.wait since earlier positions were written by earlier
-//   steps), and serves all G = nq / nkv query heads of the group from one
-//   read of each K/V row.
-//   Per tile: scores (8 bf16 per lane, reduced across the lanes of a row with
-//   shuffles) -> online softmax per head -> P V with each thread owning two
-//   output dims.  The CTA holding position T rotates and rounds the new k/v
-//   to bf16, appends them to the cache and attends to them from shared memory.
+//   of kv head g (L = T + 1 keys), streams its K and V rows HBM -> shared
+//   memory as separate tiles with bulk copies (one copy warp, a 6-stage ring,
+//   started before griddepcontrol.wait since earlier positions were written
+//   by earlier steps), and serves all G = nq / nkv query heads of the group
+//   from one read of each K/V row.
+//   Per chunk of up to 512 positions: scores of all its K tiles (8 bf16 per
+//   lane, head sums reduce-scattered across the lanes of a row), one online
+//   softmax pass per head, then P V over its V tiles with each thread owning
+//   two output dims; warps release tiles one by one, so a chunk costs three
+//   block barriers whatever its tile count.  The CTA holding position T
+//   rotates and rounds the new k/v to bf16, appends them to the cache and
+//   attends to them from shared memory as the chunk's last row.
 //   Partials (m, l, o) go to a scratch buffer and are merged
 //     m = max_s m_s,  o = sum_s e^{m_s - m} o_s / sum_s e^{m_s - m} l_s
 //   by the last few CTAs of a kv head to finish, each a slice of the outputs
@@ -32,9 +35,9 @@ namespace {
 
 template <int HD, int G>
 struct Smem {
-  static constexpr size_t stages = (size_t)kStages * Tile<HD>::kStageBytes;
+  static constexpr size_t stages = (size_t)kRing * Tile<HD>::kBytes;
   static constexpr size_t work = Work<HD, G>::total;
-  static constexpr size_t bars = 2 * kStages * 8;
+  static constexpr size_t bars = 2 * kRing * 8;
   static constexpr size_t total = stages + ((work + 15) & ~(size_t)15) + bars + 64;
 };
 
@@ -62,7 +65,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p0) {
   WorkPtrs<HD, G> w;
   w.carve(smem + S_::stages);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S_::stages + ((S_::work + 15) & ~(size_t)15));
-  uint64_t* empty = full + kStages;
+  uint64_t* empty = full + kRing;
 
   const int g = blockIdx.x, sp = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -74,9 +77,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p0) {
   const Item it = item_of<HD>(p, T, sp);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kRing; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kCWarps);  // one arrival per compute warp
     }
     fence_mbar_init();
   }
@@ -86,50 +89,82 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const Params p0) {
   if (warp == kCWarps) {
     pdl_launch_dependents();  // the CTA's trigger needs every thread (or its exit)
     if (lane == 0) {
+      // issue order = consumption order: per chunk its K tiles, then its V tiles
       const uint64_t pol = l2_evict_first_policy();
-      int t = 0;
-      for (; t < it.ntiles; ++t) {
-        const int s = t % kStages, k = t / kStages;
-        if (t >= kStages && !mbar_wait(&empty[s], (k - 1) & 1)) {
-          set_guard(p.guard, kGuardWaitTimeout);
-          break;
-        }
-        issue_tile<HD, KV8>(p, g, it, t, stages + s * Tile<HD>::kStageBytes, &full[s], pol);
+      constexpr int CH = Tile<HD>::CH;
+      int q = 0;
+      bool ok = true;
+      for (int t0 = 0; ok && t0 < it.ntiles; t0 += CH) {
+        const int t1 = (t0 + CH < it.ntiles) ? t0 + CH : it.ntiles;
+        for (int kv = 0; ok && kv < 2; ++kv)
+          for (int t = t0; t < t1; ++t, ++q) {
+            const int s = q % kRing;
+            if (q >= kRing && !mbar_wait(&empty[s], ((q / kRing) - 1) & 1)) {
+              set_guard(p.guard, kGuardWaitTimeout);
+              ok = false;
+              break;
+            }
+            issue_tile<HD, KV8>(p, g, it, t, kv, stages + s * Tile<HD>::kBytes, &full[s], pol);
+          }
       }
-      for (int u = (t > kStages ? t - kStages : 0); u < t; ++u)
-        if (!mbar_wait(&full[u % kStages], (u / kStages) & 1)) set_guard(p.guard, kGuardWaitTimeout);
+      for (int u = (q > kRing ? q - kRing : 0); u < q; ++u)
+        if (!mbar_wait(&full[u % kRing], (u / kRing) & 1)) set_guard(p.guard, kGuardWaitTimeout);
     }
     return;
   }
 
   // ------------------------------------------------------------ compute warps
+  // Per chunk: scores of its K tiles (each warp releases a tile as it is
+  // done), one softmax pass, then P V over its V tiles.  The new row (held in
+  // shared memory) is the last row of the last chunk.
   const int ctid = threadIdx.x;
   pdl_wait();
   pdl_launch_dependents();
   Acc<HD, G> A;
   begin_item<HD, G, KV8>(p, g, T, it, w, A, ctid);
-  for (int t = 0; t < it.ntiles; ++t) {
-    const int s = t % kStages, k = t / kStages;
-    if (!mbar_wait(&full[s], k & 1)) {
-      if (ctid == 0) set_guard(p.guard, kGuardWaitTimeout);
-      return;
+  constexpr int TP = Tile<HD>::TP, CH = Tile<HD>::CH;
+  const int nchunks = it.ntiles > 0 ? (it.ntiles + CH - 1) / CH : 1;
+  int q = 0;
+  for (int c = 0; c < nchunks; ++c) {
+    const int t0 = c * CH, t1 = (t0 + CH < it.ntiles) ? t0 + CH : it.ntiles;
+    const bool last = (c == nchunks - 1);
+    int rows_c = 0;
+    for (int t = t0; t < t1; ++t, ++q) {
+      const int s = q % kRing;
+      if (!mbar_wait(&full[s], (q / kRing) & 1)) {
+        if (ctid == 0) set_guard(p.guard, kGuardWaitTimeout);
+        return;
+      }
+      const uint8_t* st = stages + s * Tile<HD>::kBytes;
+      const int rows = tile_rows<HD>(it, t);
+      const float* ks = KV8 ? reinterpret_cast<const float*>(st + scale_off<HD>()) + ((it.p0 + t * TP) & 3) : nullptr;
+      tile_scores<HD, G, KV8>(reinterpret_cast<const uint16_t*>(st), rows, rows_c, w, A, ctid, ks);
+      rows_c += rows;
+      __syncwarp();
+      if ((ctid & 31) == 0) mbar_arrive(&empty[s]);
     }
-    const uint8_t* st = stages + s * Tile<HD>::kStageBytes;
-    if (KV8) {
-      const int r0 = it.p0 + t * Tile<HD>::TP, pad = r0 - (r0 & ~3);
-      const float* ks = reinterpret_cast<const float*>(st + scale_off<HD>()) + pad;
-      const float* vs = reinterpret_cast<const float*>(st + scale_off<HD>() + scale_span<HD>()) + pad;
-      process_tile<HD, G, true>(reinterpret_cast<const uint16_t*>(st),
-                                reinterpret_cast<const uint16_t*>(st + Tile<HD>::TP * HD), tile_rows<HD>(it, t), w, A,
-                                ctid, ks, vs);
-    } else {
-      process_tile<HD, G>(reinterpret_cast<const uint16_t*>(st),
-                          reinterpret_cast<const uint16_t*>(st + Tile<HD>::kBytesKV), tile_rows<HD>(it, t), w, A,
-                          ctid);
+    const bool with_new = last && it.has_new;
+    if (with_new) tile_scores<HD, G, KV8>(w.kn, 1, rows_c, w, A, ctid, w.kvs);
+    named_barrier(1, kCT);
+    chunk_softmax<HD, G>(rows_c + (with_new ? 1 : 0), w, A, ctid);
+    int rb = 0;
+    for (int t = t0; t < t1; ++t, ++q) {
+      const int s = q % kRing;
+      if (!mbar_wait(&full[s], (q / kRing) & 1)) {
+        if (ctid == 0) set_guard(p.guard, kGuardWaitTimeout);
+        return;
+      }
+      const uint8_t* st = stages + s * Tile<HD>::kBytes;
+      const int rows = tile_rows<HD>(it, t);
+      const float* vs = KV8 ? reinterpret_cast<const float*>(st + scale_off<HD>()) + ((it.p0 + t * TP) & 3) : nullptr;
+      tile_pv<HD, G, KV8>(reinterpret_cast<const uint16_t*>(st), rows, rb, w, A, ctid, vs);
+      rb += rows;
+      __syncwarp();
+      if ((ctid & 31) == 0) mbar_arrive(&empty[s]);
     }
-    if (ctid == 0) mbar_arrive(&empty[s]);
+    if (with_new) tile_pv<HD, G, KV8>(w.vn, 1, rows_c, w, A, ctid, w.kvs + 1);
+    if (!last) named_barrier(1, kCT);  // the next chunk's scores overwrite w.sc
   }
-  if (it.has_new) process_tile<HD, G, KV8>(w.kn, w.vn, 1, w, A, ctid, w.kvs, w.kvs + 1);
   end_item<HD, G>(p, g, sp, w, A, ctid);
 }
 

@@ -21,11 +21,14 @@ namespace attn {
 constexpr int kCWarps = 8;
 constexpr int kCT = kCWarps * 32;
 
+// A tile is TP cached rows of K or of V (one ring stage); a chunk is CH
+// tiles (CP positions) whose scores are all formed before one softmax pass.
 template <int HD>
 struct Tile {
   static constexpr int TP = HD >= 256 ? 32 : (HD >= 128 ? 64 : 128);  // positions per tile
-  static constexpr int kBytesKV = TP * HD * 2;                          // one of K or V
-  static constexpr int kStageBytes = 2 * kBytesKV;
+  static constexpr int kBytes = TP * HD * 2;                            // one K or V tile
+  static constexpr int CP = 512;                                        // positions per chunk
+  static constexpr int CH = CP / TP;                                    // tiles per chunk
 };
 
 // Shared memory a work item uses besides its tiles (floats unless noted).
@@ -35,7 +38,7 @@ struct Work {
   static constexpr int NG = kCT / NP;        // position groups in P V
   static constexpr int TP = Tile<HD>::TP;
   static constexpr size_t q = (size_t)G * HD * 4;
-  static constexpr size_t sc = (size_t)G * TP * 4;
+  static constexpr size_t sc = (size_t)G * Tile<HD>::CP * 4;  // chunk scores / probabilities [row][G]
   static constexpr size_t ored = (size_t)NG * G * HD * 4;
   static constexpr size_t kvnew = 2 * HD * 2;
   static constexpr size_t small = 3 * G * 4 + 16 + 64;  // m, l, corr, last; int8 cache: the new row's scales, amax
@@ -101,41 +104,33 @@ __device__ __forceinline__ Item item_of(const Params& p, int T, int sp) {
   return it;
 }
 
-// Copy lane: K and V rows of tile t of the item into dst (K at 0, V at
-// kBytesKV).  int8 cache: the code rows at 0 and TP * HD, then the rows'
-// scales from the 16-byte boundary at or before the tile's first row (so that
-// the copy starts aligned): K scales at scale_off(), V scales 128 floats later.
+// Copy lane: the K (kv = 0) or V (kv = 1) rows of tile t of the item into
+// dst.  int8 cache: the code rows at 0, then the rows' scales from the
+// 16-byte boundary at or before the tile's first row (so that the copy starts
+// aligned) at scale_off(); row r's scale is float (r0 & 3) + r there.
 template <int HD>
 __device__ __forceinline__ int scale_off() {
-  return 2 * Tile<HD>::TP * HD;
-}
-template <int HD>
-__device__ __forceinline__ int scale_span() {  // bytes between the K and the V scales of a tile
-  return ((Tile<HD>::TP + 8) * 4 + 15) & ~15;
+  return Tile<HD>::TP * HD;
 }
 template <int HD, bool KV8>
-__device__ __forceinline__ void issue_tile(const Params& p, int g, const Item& it, int t, uint8_t* dst, uint64_t* bar,
-                                           uint64_t pol) {
+__device__ __forceinline__ void issue_tile(const Params& p, int g, const Item& it, int t, int kv, uint8_t* dst,
+                                           uint64_t* bar, uint64_t pol) {
   constexpr int TP = Tile<HD>::TP;
   const int r0 = it.p0 + t * TP;
   const int rows = (it.pc1 - r0) < TP ? (it.pc1 - r0) : TP;
   if (KV8) {
     const uint32_t bytes = (uint32_t)rows * HD;
     const int ra = r0 & ~3, n4 = ((r0 + rows + 3) & ~3) - ra;
-    mbar_arrive_expect_tx(bar, 2 * bytes + 2 * n4 * 4);
-    const uint8_t* K8 = reinterpret_cast<const uint8_t*>(p.K);
-    const uint8_t* V8 = reinterpret_cast<const uint8_t*>(p.V);
-    bulk_g2s(dst, K8 + ((long long)g * p.cap + r0) * HD, bytes, bar, pol);
-    bulk_g2s(dst + TP * HD, V8 + ((long long)g * p.cap + r0) * HD, bytes, bar, pol);
-    bulk_g2s(dst + scale_off<HD>(), p.Ks + (long long)g * p.cap_s + ra, n4 * 4, bar, pol);
-    bulk_g2s(dst + scale_off<HD>() + scale_span<HD>(), p.Vs + (long long)g * p.cap_s + ra, n4 * 4, bar, pol);
+    mbar_arrive_expect_tx(bar, bytes + n4 * 4);
+    const uint8_t* C8 = reinterpret_cast<const uint8_t*>(kv ? p.V : p.K);
+    const float* S = kv ? p.Vs : p.Ks;
+    bulk_g2s(dst, C8 + ((long long)g * p.cap + r0) * HD, bytes, bar, pol);
+    bulk_g2s(dst + scale_off<HD>(), S + (long long)g * p.cap_s + ra, n4 * 4, bar, pol);
     return;
   }
   const uint32_t bytes = (uint32_t)rows * HD * 2;
-  mbar_arrive_expect_tx(bar, 2 * bytes);
-  const long long off = kv_row<HD>(p, g, r0);
-  bulk_g2s(dst, p.K + off, bytes, bar, pol);
-  bulk_g2s(dst + Tile<HD>::kBytesKV, p.V + off, bytes, bar, pol);
+  mbar_arrive_expect_tx(bar, bytes);
+  bulk_g2s(dst, (kv ? p.V : p.K) + kv_row<HD>(p, g, r0), bytes, bar, pol);
 }
 
 // Eight int8 codes (one 8-byte word) as floats.
@@ -291,18 +286,15 @@ __device__ __forceinline__ void head_scatter(float* v, int li) {
   }
 }
 
-// One tile of rows: scores -> online softmax (one warp per head) -> P V.
-// Scores: a row is read by HD / 8 lanes (8 dims each, one 16-byte shared
-// load), every warp takes its rows of all passes at once (independent loads
-// and shuffles in flight), and the head sums are reduce-scattered.  The
-// probabilities are kept row-major [row][G] so that P V reads a row's G
-// weights with vector loads.
+// Scores of one K tile (rows rows, chunk rows row_base ..): a row is read by
+// HD / 8 lanes (8 dims each, one 16-byte shared load), every warp takes its
+// rows of all passes at once (independent loads and shuffles in flight), and
+// the head sums are reduce-scattered.  Written to w.sc row-major [row][G].
+// int8 cache: ks[row] is the row's scale.
 template <int HD, int G, bool KV8 = false>
-__device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t* tv, int rows,
-                                             const WorkPtrs<HD, G>& w, Acc<HD, G>& A, int ctid,
-                                             const float* ks = nullptr, const float* vs = nullptr) {
-  using W = Work<HD, G>;
-  constexpr int TP = W::TP;
+__device__ __forceinline__ void tile_scores(const uint16_t* tk, int rows, int row_base, const WorkPtrs<HD, G>& w,
+                                            const Acc<HD, G>& A, int ctid, const float* ks = nullptr) {
+  constexpr int TP = Tile<HD>::TP;
   constexpr int LPR = HD / 8, RPW = 32 / LPR, RSTEP = kCWarps * RPW;
   constexpr int NPASS = (TP + RSTEP - 1) / RSTEP;
   constexpr int GL = LPR / G;  // lanes left per head after the scatter
@@ -339,9 +331,17 @@ __device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t*
   for (int ps = 0; ps < NPASS; ++ps) {
     head_scatter<G, LPR / 2>(d[ps], li);
     const int row = ps * RSTEP + warp * RPW + sub;
-    if (li % GL == 0 && row < rows) w.sc[row * G + li / GL] = d[ps][0];
+    if (li % GL == 0 && row < rows) w.sc[(row_base + row) * G + li / GL] = d[ps][0];
   }
-  named_barrier(1, kCT);
+}
+
+// Online softmax over the chunk's rows (one warp per head; every compute
+// thread calls it after the chunk's scores are in w.sc): new running max,
+// probabilities in place, running sum; then every thread rescales its
+// accumulators by e^{m_old - m_new}.
+template <int HD, int G>
+__device__ __forceinline__ void chunk_softmax(int rows, const WorkPtrs<HD, G>& w, Acc<HD, G>& A, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
   if (warp < G) {
     const int j = warp;
     float mx = -INFINITY;
@@ -364,13 +364,22 @@ __device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t*
     }
   }
   named_barrier(1, kCT);
-  const int pg = ctid / W::NP, dp = ctid % W::NP;
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     const float c = w.corr[j];
     A.acc[j][0] *= c;
     A.acc[j][1] *= c;
   }
+}
+
+// P V of one V tile (rows rows, chunk rows row_base ..): each thread owns two
+// output dims and a position group; a row's G probabilities are vector loads.
+// int8 cache: vs[row] is the row's scale.
+template <int HD, int G, bool KV8 = false>
+__device__ __forceinline__ void tile_pv(const uint16_t* tv, int rows, int row_base, const WorkPtrs<HD, G>& w,
+                                        Acc<HD, G>& A, int ctid, const float* vs = nullptr) {
+  using W = Work<HD, G>;
+  const int pg = ctid / W::NP, dp = ctid % W::NP;
   const uint32_t* tv32 = reinterpret_cast<const uint32_t*>(tv);
   const uint16_t* tv16 = reinterpret_cast<const uint16_t*>(tv);  // int8 cache: two codes
 #pragma unroll 4
@@ -386,11 +395,12 @@ __device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t*
       vx = bf16_lo(v2);
       vy = bf16_hi(v2);
     }
+    const float* pr = w.sc + (row_base + r) * G;
     float pj[G];
     if constexpr (G % 4 == 0) {
 #pragma unroll
       for (int j = 0; j < G; j += 4) {
-        const float4 q4 = *reinterpret_cast<const float4*>(w.sc + r * G + j);
+        const float4 q4 = *reinterpret_cast<const float4*>(pr + j);
         pj[j] = q4.x;
         pj[j + 1] = q4.y;
         pj[j + 2] = q4.z;
@@ -398,7 +408,7 @@ __device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t*
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < G; ++j) pj[j] = w.sc[r * G + j];
+      for (int j = 0; j < G; ++j) pj[j] = pr[j];
     }
 #pragma unroll
     for (int j = 0; j < G; ++j) {
@@ -406,7 +416,6 @@ __device__ __forceinline__ void process_tile(const uint16_t* tk, const uint16_t*
       A.acc[j][1] = fmaf(pj[j], vy, A.acc[j][1]);
     }
   }
-  named_barrier(1, kCT);
 }
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* a) {

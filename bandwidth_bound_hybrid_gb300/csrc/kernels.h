@@ -142,7 +142,7 @@ cudaError_t launch(const Params& p, const Plan& pl, int src, int in, int epi, cu
 // ---------------------------------------------------------------- attention
 namespace attn {
 constexpr int kThreads = 288;  // 8 compute warps + 1 copy warp
-constexpr int kStages = 3;
+constexpr int kRing = 6;       // ring stages, one K or V tile each
 struct Params {
   const float* y;          // projection output: q|k|v
   uint16_t* K;             // bf16 [nkv][cap][hd]; with kv8: int8 codes [nkv][cap][hd] (bytes)
