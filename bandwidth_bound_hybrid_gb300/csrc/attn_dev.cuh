@@ -181,18 +181,44 @@ __device__ __forceinline__ void begin_item(const Params& p, int g, int T, const 
                                            Acc<HD, G>& A, int ctid) {
   const int lane = ctid & 31;
   const float2* rope = p.rope + (long long)T * (HD / 2);
-  for (int e = ctid; e < G * (HD / 2); e += kCT) {
-    const int j = e / (HD / 2), i = e % (HD / 2);
-    const float* qh = p.y + (long long)(g * G + j) * HD;
-    const float2 cs = rope[i];
-    const float a = qh[i], b = qh[i + HD / 2];
-    w.q_s[j * HD + i] = (a * cs.x - b * cs.y) * p.scale;
-    w.q_s[j * HD + i + HD / 2] = (b * cs.x + a * cs.y) * p.scale;
+  static_assert(kCT >= HD, "one new-row element per thread");
+  // the new row's k and v inputs are loaded with the queries (one round trip)
+  float nk0 = 0.f, nk1 = 0.f, nv = 0.f;
+  if (it.has_new) {
+    const float* kh = p.y + (long long)(p.nq + g) * HD;
+    const float* vh = p.y + (long long)(p.nq + p.nkv + g) * HD;
+    if (ctid < HD / 2) {
+      nk0 = kh[ctid];
+      nk1 = kh[ctid + HD / 2];
+    }
+    if (ctid < HD) nv = vh[ctid];
+  }
+  // all query pairs of this thread are loaded before any is stored
+  constexpr int NQ = (G * (HD / 2) + kCT - 1) / kCT;
+  float qa[NQ], qb[NQ];
+  float2 qc[NQ];
+#pragma unroll
+  for (int u = 0; u < NQ; ++u) {
+    const int e = ctid + u * kCT;
+    if (e < G * (HD / 2)) {
+      const int j = e / (HD / 2), i = e % (HD / 2);
+      const float* qh = p.y + (long long)(g * G + j) * HD;
+      qc[u] = rope[i];
+      qa[u] = qh[i];
+      qb[u] = qh[i + HD / 2];
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < NQ; ++u) {
+    const int e = ctid + u * kCT;
+    if (e < G * (HD / 2)) {
+      const int j = e / (HD / 2), i = e % (HD / 2);
+      w.q_s[j * HD + i] = (qa[u] * qc[u].x - qb[u] * qc[u].y) * p.scale;
+      w.q_s[j * HD + i + HD / 2] = (qb[u] * qc[u].x + qa[u] * qc[u].y) * p.scale;
+    }
   }
   if (KV8 && it.has_new) {
     // int8 cache: the new k and v vectors quantised with their own scales
-    const float* kh = p.y + (long long)(p.nq + g) * HD;
-    const float* vh = p.y + (long long)(p.nq + p.nkv + g) * HD;
     int8_t* K8 = reinterpret_cast<int8_t*>(p.K) + ((long long)g * p.cap + T) * HD;
     int8_t* V8 = reinterpret_cast<int8_t*>(p.V) + ((long long)g * p.cap + T) * HD;
     int8_t* kn8 = reinterpret_cast<int8_t*>(w.kn);
@@ -200,11 +226,10 @@ __device__ __forceinline__ void begin_item(const Params& p, int g, int T, const 
     float k0 = 0.f, k1 = 0.f, v0 = 0.f;
     if (ctid < HD / 2) {
       const float2 cs = rope[ctid];
-      const float a = kh[ctid], b = kh[ctid + HD / 2];
-      k0 = a * cs.x - b * cs.y;
-      k1 = b * cs.x + a * cs.y;
+      k0 = nk0 * cs.x - nk1 * cs.y;
+      k1 = nk1 * cs.x + nk0 * cs.y;
     }
-    if (ctid < HD) v0 = vh[ctid];
+    if (ctid < HD) v0 = nv;
     const float ka = block_amax(fmaxf(fabsf(k0), fabsf(k1)), w.kvs + 2, ctid);
     const float va = block_amax(fabsf(v0), w.kvs + 2, ctid);
     const float kinv = ka > 0.f ? 127.0f / ka : 0.f, vinv = va > 0.f ? 127.0f / va : 0.f;
@@ -227,24 +252,21 @@ __device__ __forceinline__ void begin_item(const Params& p, int g, int T, const 
       p.Vs[(long long)g * p.cap_s + T] = va / 127.0f;
     }
   }
-  if (!KV8 && it.has_new) {
-    const float* kh = p.y + (long long)(p.nq + g) * HD;
-    const float* vh = p.y + (long long)(p.nq + p.nkv + g) * HD;
+  if (!KV8 && it.has_new) {  // kCT >= HD: one k pair and one v element per thread at most
     uint16_t* Kw = p.K + kv_row<HD>(p, g, T);
     uint16_t* Vw = p.V + kv_row<HD>(p, g, T);
-    for (int i = ctid; i < HD / 2; i += kCT) {
-      const float2 cs = rope[i];
-      const float a = kh[i], b = kh[i + HD / 2];
-      const uint16_t k0 = f32_to_bf16_rne(a * cs.x - b * cs.y), k1 = f32_to_bf16_rne(b * cs.x + a * cs.y);
-      w.kn[i] = k0;
-      w.kn[i + HD / 2] = k1;
-      Kw[i] = k0;
-      Kw[i + HD / 2] = k1;
+    if (ctid < HD / 2) {
+      const float2 cs = rope[ctid];
+      const uint16_t k0 = f32_to_bf16_rne(nk0 * cs.x - nk1 * cs.y), k1 = f32_to_bf16_rne(nk1 * cs.x + nk0 * cs.y);
+      w.kn[ctid] = k0;
+      w.kn[ctid + HD / 2] = k1;
+      Kw[ctid] = k0;
+      Kw[ctid + HD / 2] = k1;
     }
-    for (int i = ctid; i < HD; i += kCT) {
-      const uint16_t v = f32_to_bf16_rne(vh[i]);
-      w.vn[i] = v;
-      Vw[i] = v;
+    if (ctid < HD) {
+      const uint16_t v = f32_to_bf16_rne(nv);
+      w.vn[ctid] = v;
+      Vw[ctid] = v;
     }
   }
   if (ctid < G) {

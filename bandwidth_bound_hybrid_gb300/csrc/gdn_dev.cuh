@@ -127,6 +127,8 @@ __device__ __forceinline__ void run_item(const Params& p, int h, int rc, Rows<EP
   // conv + SiLU over this item's channels (q and k of head h, its v rows):
   // only the new input comes from the projection output
   const int nqk = 2 * dk;
+  // the gate inputs go out with the conv inputs: one round trip for all
+  const float a_in = p.y[CC + h], b_in = p.y[CC + nh + h];
   float u[kChanPerThread];
 #pragma unroll
   for (int q = 0; q < kChanPerThread; ++q) u[q] = V.ch[q] >= 0 ? p.y[V.ch[q]] : 0.f;
@@ -170,8 +172,8 @@ __device__ __forceinline__ void run_item(const Params& p, int h, int rc, Rows<EP
     kq[e] = sh.k[lane * EPL + e] * ks;
     qq[e] = sh.q[lane * EPL + e] * qs;
   }
-  const float alpha = sigmoidf_(p.y[CC + h]);
-  const float beta = sigmoidf_(p.y[CC + nh + h]);
+  const float alpha = sigmoidf_(a_in);
+  const float beta = sigmoidf_(b_in);
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
     const int li = warp * RPW + r;
