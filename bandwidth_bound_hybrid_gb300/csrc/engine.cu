@@ -141,6 +141,7 @@ struct hy_model {
   bool moe = false, pdl = true, graphs = true, debug = false;
   bool q4 = false;          // 4-bit linear weights: every step runs the batched path
   bool splits_auto = true;  // split-KV count chosen from the SM count (the batched step then scales it down)
+  int splits_long = 0;      // splits of a single sequence whose cache holds attn::kLongContext positions or more
   bool chunk_prefill = false;  // prompts run as chunks through the tensor-core GEMMs (else token by token)
 };
 
@@ -386,7 +387,7 @@ int collect_ops(hy_cache* c, int seq, float* logits, int* ids, std::vector<StepO
       a.nq = cf.attn_q_heads;
       a.nkv = cf.attn_kv_heads;
       a.hd = cf.head_dim;
-      a.nsplit = m->splits;
+      a.nsplit = c->cap[seq] >= attn::kLongContext ? m->splits_long : m->splits;
       a.scale = 1.0f / sqrtf((float)cf.head_dim);
       a.part = c->part;
       a.counter = c->cnt_attn;
@@ -1264,6 +1265,7 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
   m->h_len = m->moe ? (c.top_k + 1) * c.expert_ffn : c.ffn;
   m->splits = c.attn_splits > 0 ? c.attn_splits : attn::auto_splits(c.attn_kv_heads, m->nsm);
   m->splits_auto = c.attn_splits <= 0;
+  m->splits_long = m->splits_auto ? attn::long_context_splits(c.attn_q_heads, c.attn_kv_heads, m->nsm) : m->splits;
   m->pdl = !(c.flags & HY_FLAG_NO_PDL);
   m->graphs = !(c.flags & HY_FLAG_NO_GRAPH);
   m->debug = (c.flags & HY_FLAG_DEBUG) != 0;
@@ -1326,7 +1328,8 @@ static int cache_alloc(hy_model* m, int32_t max_seqs, const int32_t* capacity_ho
     }
   }
   const int G = cf.attn_kv_heads > 0 ? cf.attn_q_heads / cf.attn_kv_heads : 1;
-  const size_t part = m->n_attn ? attn::part_floats(cf.attn_q_heads, cf.attn_kv_heads, cf.head_dim, m->splits) : 1;
+  const size_t part = m->n_attn ? attn::part_floats(cf.attn_q_heads, cf.attn_kv_heads, cf.head_dim,
+                                                   std::max(m->splits, m->splits_long)) : 1;
   (void)G;
   if ((rc = dalloc(c, &c->d_len, max_seqs)) || (rc = dalloc(c, &c->x, cf.hidden)) ||
       (rc = dalloc(c, &c->y, m->y_len)) || (rc = dalloc(c, &c->o, std::max(m->o_len, 1))) ||

@@ -180,6 +180,8 @@ struct Params {
 };
 size_t part_floats(int nq, int nkv, int hd, int nsplit);
 int auto_splits(int nkv, int nsm);
+int long_context_splits(int nq, int nkv, int nsm);  // for caches of kLongContext positions or more
+constexpr int kLongContext = 16384;
 cudaError_t init();
 cudaError_t launch(const Params& p, cudaStream_t st, bool pdl);
 cudaError_t rope_table(float2* tab, int cap, int hd, double theta, cudaStream_t st);

@@ -48,7 +48,8 @@ def flip_candidates(x):
 
 
 @pytest.mark.parametrize("nq,nkv,hd,T,nsplit", [(4, 2, 64, 0, 1), (4, 2, 64, 200, 3), (16, 4, 128, 1000, 16),
-                                                 (16, 4, 128, 4095, 0), (16, 2, 256, 2303, 32), (8, 8, 128, 37, 4)])
+                                                 (16, 4, 128, 4095, 0), (16, 2, 256, 2303, 32), (8, 8, 128, 37, 4),
+                                                 (16, 4, 128, 3000, 64)])
 def test_attention_int8_cache(L, nq, nkv, hd, T, nsplit):
     torch = _torch()
     rng = np.random.default_rng(T * 7 + hd + nsplit)

@@ -270,7 +270,7 @@ ATTN_CASES = [(4, 2, 64, 0), (4, 2, 64, 1), (4, 2, 64, 127), (4, 2, 64, 128), (4
 
 
 @pytest.mark.parametrize("nq,nkv,hd,T", ATTN_CASES)
-@pytest.mark.parametrize("nsplit", [1, 3, 16, 32, 0])
+@pytest.mark.parametrize("nsplit", [1, 3, 16, 32, 64, 0])
 def test_attention_parity(L, nq, nkv, hd, T, nsplit):
     rng = np.random.default_rng(T * 31 + hd + nsplit)
     cap = T + 3

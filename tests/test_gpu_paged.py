@@ -172,3 +172,38 @@ def test_continuous_batching_over_a_shared_pool(W):
     steps([1, 2, 3], 5)
     assert model.check_device() == 0
     model.close()
+
+
+def test_long_context_paged_equals_contiguous(gpu):
+    """Four layers of the dense 4B shape from a 16384-token synthetic context
+    on a paged and on a contiguous cache: the long-context split count runs
+    the attention as CTA pairs, on both layouts; the logits agree to
+    rounding (the paged scan splits at tile boundaries)."""
+    import dataclasses
+
+    import torch
+
+    from bandwidth_bound_hybrid_gb300.model import HybridModel
+    shape = dataclasses.replace(workloads.DENSE4B, name="dense4b-l4-long", n_layers=4, attn_layers=(3,))
+    dev_w = workloads.device_weights(shape)
+    cap, ctx = 16384 + 128, 16384
+    got = []
+    for pages in (None, (128, cap // 128)):
+        m = HybridModel(shape, dev_w, [cap], pages=pages)
+        m.fill_synthetic(0, ctx, seed=3)
+        lg = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+        ids = torch.empty(1, dtype=torch.int32, device="cuda")
+        tok = _t([7])
+        seq = []
+        for _ in range(3):
+            m.decode_step(0, tok, ids, lg)
+            torch.cuda.synchronize()
+            seq.append((int(ids.item()), to_np(lg).copy()))
+            tok = ids.clone()
+        assert m.check_device() == 0
+        m.close()
+        got.append(seq)
+    del dev_w
+    for (a, la), (b, lb) in zip(*got):
+        assert a == b
+        assert rel_l2(lb, la) < 1e-5

@@ -24,6 +24,7 @@ than 1e-3 relative L2, so its batch is compared at every step as it runs.
 
 The file sorts last so that the quicker parity tests run first.
 """
+import dataclasses
 import gc
 import os
 
@@ -199,6 +200,15 @@ def test_synthetic_context_matches_its_host_copy(built):
     per-layer hidden states, and a 4-bit batch of three)."""
     assert run_full(workloads.TINY, [100], steps=3, batched=False, debug=True) == 3
     assert run_full(TINY_MOE_Q4, [50, 77, 120], steps=2, batched=True) == 6
+
+
+def test_dense4b_truncated_long_context(built):
+    """Four layers of the dense 4B shape (one attention layer) from a
+    16384-token synthetic context: a cache of that capacity takes the
+    long-context split count, whose grid exceeds the SM count and runs as
+    CTA pairs."""
+    shape = dataclasses.replace(workloads.DENSE4B, name="dense4b-l4-long", n_layers=4, attn_layers=(3,))
+    assert run_full(shape, [16384], steps=3, batched=False) == 3
 
 
 @pytest.mark.parametrize("context", [4096, 32768])
