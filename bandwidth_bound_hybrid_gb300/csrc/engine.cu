@@ -1263,7 +1263,7 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
   m->y_len = y;
   m->o_len = std::max(m->n_gdn ? c.gdn_heads * c.gdn_dv : 0, m->n_attn ? c.attn_q_heads * c.head_dim : 0);
   m->h_len = m->moe ? (c.top_k + 1) * c.expert_ffn : c.ffn;
-  m->splits = c.attn_splits > 0 ? c.attn_splits : attn::auto_splits(c.attn_kv_heads, m->nsm);
+  m->splits = c.attn_splits > 0 ? c.attn_splits : attn::step_splits(c.attn_kv_heads, m->nsm);
   m->splits_auto = c.attn_splits <= 0;
   m->splits_long = m->splits_auto ? attn::long_context_splits(c.attn_q_heads, c.attn_kv_heads, m->nsm) : m->splits;
   m->pdl = !(c.flags & HY_FLAG_NO_PDL);

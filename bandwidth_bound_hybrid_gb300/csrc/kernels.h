@@ -179,7 +179,8 @@ struct Params {
   int cap_s_b[8];
 };
 size_t part_floats(int nq, int nkv, int hd, int nsplit);
-int auto_splits(int nkv, int nsm);
+int auto_splits(int nkv, int nsm);   // the single ops' automatic count
+int step_splits(int nkv, int nsm);   // the decode step's
 int long_context_splits(int nq, int nkv, int nsm);  // for caches of kLongContext positions or more
 constexpr int kLongContext = 16384;
 cudaError_t init();
