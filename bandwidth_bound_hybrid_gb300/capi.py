@@ -71,6 +71,7 @@ SIGNATURES = {
     "hy_seq_len": (i32, [vp, i32]),
     "hy_seq_capacity": (i32, [vp, i32]),
     "hy_step_kernels": (i32, [vp]),
+    "hy_step_splits": (i32, [vp, i32]),
     "hy_experts_read": (ctypes.c_int, [vp, vp, vp]),
     "hy_seq_fill_synthetic": (ctypes.c_int, [vp, i32, i32, u64, vp]),
     "hy_prefill": (ctypes.c_int, [vp, vp, i32, vp, i32, vp, vp]),

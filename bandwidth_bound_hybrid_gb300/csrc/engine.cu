@@ -1448,6 +1448,10 @@ int hy_seq_reset(hy_cache* c, int32_t seq, void* stream) {
 int32_t hy_seq_len(const hy_cache* c, int32_t seq) { return valid_seq(c, seq) ? c->len[seq] : -1; }
 int32_t hy_seq_capacity(const hy_cache* c, int32_t seq) { return valid_seq(c, seq) ? c->cap[seq] : -1; }
 int32_t hy_step_kernels(const hy_cache* c) { return c ? c->last_kernels : 0; }
+int32_t hy_step_splits(const hy_cache* c, int32_t seq) {
+  if (!c || seq < 0 || seq >= (int32_t)c->cap.size() || !c->m->n_attn) return 0;
+  return c->cap[seq] >= attn::kLongContext ? c->m->splits_long : c->m->splits;
+}
 
 int hy_experts_read(hy_cache* c, void* stream, uint64_t* total_out) {
   if (!c || !total_out) return fail(HY_ERR_ARG, "null argument");

@@ -149,6 +149,10 @@ class HybridModel:
         """Kernels the last recorded decode step launches (one per operation)."""
         return int(capi.lib().hy_step_kernels(self.c))
 
+    def step_splits(self, seq: int = 0) -> int:
+        """Split-KV chunks per kv head of sequence `seq`'s batch-1 step."""
+        return int(capi.lib().hy_step_splits(self.c, seq))
+
     def free_pages(self) -> int:
         """Pages left in the pool of a paged cache (-1 without pages)."""
         return int(capi.lib().hy_cache_free_pages(self.c))

@@ -404,7 +404,7 @@ def run_ours(args):
                        "outputs": "FP32 logits [V] and the greedy id per step",
                        "context_fill": "seeded synthetic KV rows and recurrent state (no prompt replay)"
                        if synthetic_fill else "prefill of the prompt",
-                       "splits": model_splits(args, shape), "parallelism": f"replicas x{n}",
+                       "splits": model.step_splits(0), "parallelism": f"replicas x{n}",
                        "l2": "inputs larger than L2: every step streams all weights (GBs) through the 129 MB L2"},
             "roofline": roof,
             "step_roofline": {"bound": "hbm", "bytes_per_step": sb.total, "achieved": step_gbs, "peak": peak,
@@ -981,14 +981,6 @@ def run_ours_batch(args, w, shape, dist, ws, rank, local):
         dist.barrier()
         dist.destroy_process_group()
     return 0
-
-
-def model_splits(args, shape):
-    if args.splits:
-        return args.splits
-    import torch
-    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    return max(1, min(32, (2 * nsm) // max(shape.attn_kv_heads, 1)))
 
 
 def main(argv=None):

@@ -211,6 +211,13 @@ int hy_experts_read(hy_cache* c, void* stream, uint64_t* total_out);
  * before any step. */
 int32_t hy_step_kernels(const hy_cache* c);
 
+/* Split-KV chunks per kv head that a batch-1 decode step of sequence `seq`
+ * uses: hy_config.attn_splits when set, else one CTA per SM across the kv
+ * heads, or, for a cache of 16384 positions or more with up to 4 query heads
+ * per kv head, 64 splits run as two CTAs per SM.  0 for a bad sequence index
+ * or a model without attention layers. */
+int32_t hy_step_splits(const hy_cache* c, int32_t seq);
+
 /* Run the n prompt tokens tokens_dev[0..n) of sequence `seq` through the
  * model at positions len .. len+n-1, filling its caches.  logits_dev
  * (nullable) receives the FP32 logits [V] of the last token.
