@@ -377,10 +377,10 @@ __device__ __forceinline__ void am_unkey(unsigned long long k, float& v, int& i)
 
 // Routing of every token of a batch from its router logits (logits [B][ld],
 // row E of a token the shared gate), by the 8 compute warps' threads tid
-// (synchronised with named barrier 1): warp b picks token b's top_k by
-// repeated warp-wide argmax (largest logit, lowest index on ties: the same
-// set and order as ranking all experts); the union of the picks is an
-// ascending ballot scan over the experts' flags.
+// (synchronised with named barrier 1): warp b picks token b's top_k with
+// warp_topk (largest logit, lowest index on ties: the same set and order as
+// ranking all experts); the union of the picks is an ascending ballot scan
+// over the experts' flags.
 constexpr int kRouteMaxE = 512;  // experts + the shared gate per token
 struct RouteShared {
   int sel[kMaxB][16];
@@ -406,41 +406,13 @@ __device__ __noinline__ void route_tokens(const Params& p, const float* logits, 
   sync();
   if (warp < p.B) {
     const int b = warp;
-    constexpr int kPer = kRouteMaxE / 32;
-    float v[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane + 32 * i;
-      const float x = e < E ? __ldcg(logits + (long long)b * ld + e) : -INFINITY;
-      v[i] = x == x ? x : -INFINITY;  // a NaN logit ranks last
-    }
-    uint32_t taken = 0u;
-    for (int k = 0; k < K; ++k) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !(taken >> i & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-          bv = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == 0) {
-        rs.sel[b][k] = bi;
-        rs.selv[b][k] = bv;
-      }
-    }
+    auto logit = [&](int e) { return __ldcg(logits + (long long)b * ld + e); };
+    if (E <= 128)
+      warp_topk<4>(logit, E, K, rs.sel[b], rs.selv[b], lane);
+    else if (E <= 256)
+      warp_topk<8>(logit, E, K, rs.sel[b], rs.selv[b], lane);
+    else
+      warp_topk<kRouteMaxE / 32>(logit, E, K, rs.sel[b], rs.selv[b], lane);
     __syncwarp();
     if (lane < K) rs.flag[rs.sel[b][lane]] = 1;
     if (lane == 0 && publish) {  // softmax over the selected logits, sigmoid gate of the shared expert

@@ -96,6 +96,78 @@ __device__ __forceinline__ float warp_max(float v) {
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
 __device__ __forceinline__ float siluf_(float x) { return x / (1.0f + __expf(-x)); }
 
+// ------------------------------------------------------------ top-k
+// Unsigned key with the order of the FP32 value (-0 taken as +0, as an FP32
+// compare does), and back.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t u = __float_as_uint(x == 0.f ? 0.f : x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// top_k of E logits (FP32 compare, lowest index on ties; a NaN ranks last) by
+// one warp, in order (the same set and order as ranking all experts), E <=
+// 32 * kPer.  Each lane holds logits lane, lane + 32, ... as order keys (slots past E get key
+// 0, below every logit) and sorts them once, best first, with a bitonic
+// network in registers; then each round takes the warp's best with two
+// reductions (the largest key, then the lowest index holding it) and the
+// winning lane shifts its list by one.  sel / selv (shared) receive ids and
+// logits.
+template <int kPer, typename Load>
+__device__ __forceinline__ void warp_topk(Load load, int E, int K, int* sel, float* selv, int lane) {
+  uint32_t key[kPer];
+  uint32_t idx[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    const float x = e < E ? load(e) : -INFINITY;
+    key[i] = e < E ? order_key(x == x ? x : -INFINITY) : 0u;
+    idx[i] = (uint32_t)e;
+  }
+  // bitonic sort, best first: a larger key, or an equal key and a lower index
+#pragma unroll
+  for (int k = 2; k <= kPer; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          const bool i_better = key[i] > key[l] || (key[i] == key[l] && idx[i] < idx[l]);
+          const bool want_i_first = (i & k) == 0;
+          if (i_better != want_i_first) {
+            const uint32_t tk = key[i], ti = idx[i];
+            key[i] = key[l];
+            idx[i] = idx[l];
+            key[l] = tk;
+            idx[l] = ti;
+          }
+        }
+      }
+    }
+  }
+  for (int q = 0; q < K; ++q) {
+    const uint32_t gk = __reduce_max_sync(0xffffffffu, key[0]);
+    const uint32_t gi = __reduce_min_sync(0xffffffffu, key[0] == gk ? idx[0] : 0xffffffffu);
+    if (lane == 0) {
+      sel[q] = (int)gi;
+      selv[q] = key_value(gk);
+    }
+    if (idx[0] == gi) {
+#pragma unroll
+      for (int i = 0; i + 1 < kPer; ++i) {
+        key[i] = key[i + 1];
+        idx[i] = idx[i + 1];
+      }
+      key[kPer - 1] = 0u;
+      idx[kPer - 1] = 0xffffffffu;
+    }
+  }
+  __syncwarp();
+}
+
 // ------------------------------------------------------------ mbarrier / bulk copy
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 

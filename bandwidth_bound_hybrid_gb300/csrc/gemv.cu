@@ -134,7 +134,14 @@ __global__ void __maxnreg__(kMaxRegs) k_gemv(const Params p) {
     // every CTA picks the experts from the stored router logits (the same
     // result everywhere) and hands the ids to its copy lane; CTA 0 publishes
     // them and the routing weights for the down projection
-    warp_topk([&](int e) { return __ldcg(p.router_logits + e); }, p.n_experts, p.top_k, esh.sel, esh.selv, lane);
+    // the smallest per-lane list that holds the experts (its sort is the cost)
+    auto logit = [&](int e) { return __ldcg(p.router_logits + e); };
+    if (p.n_experts <= 128)
+      warp_topk<4>(logit, p.n_experts, p.top_k, esh.sel, esh.selv, lane);
+    else if (p.n_experts <= 256)
+      warp_topk<8>(logit, p.n_experts, p.top_k, esh.sel, esh.selv, lane);
+    else
+      warp_topk<kMaxExperts / 32>(logit, p.n_experts, p.top_k, esh.sel, esh.selv, lane);
     if (blockIdx.x == 0 && p.dbg_logits)
       for (int e = lane; e <= p.n_experts; e += 32) p.dbg_logits[e] = __ldcg(p.router_logits + e);
     if (lane == 0) {

@@ -316,47 +316,6 @@ __device__ __forceinline__ void argmax_merge(float& bv, int& bi, float ov, int o
   }
 }
 
-// top_k of E logits (FP32 compare, lowest index on ties) by one warp: each
-// lane holds E/32 logits (load(e) reads logit e) and top_k rounds of a
-// warp-wide argmax pick the selection in order (the same set and order as
-// ranking all experts).  sel / selv (shared) receive ids and logits.
-template <typename Load>
-__device__ __forceinline__ void warp_topk(Load load, int E, int K, int* sel, float* selv, int lane) {
-  constexpr int kPer = kMaxExperts / 32;
-  float v[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = lane + 32 * i;
-    const float x = e < E ? load(e) : -INFINITY;
-    v[i] = x == x ? x : -INFINITY;  // a NaN logit ranks last
-  }
-  uint32_t taken = 0u;
-  for (int q = 0; q < K; ++q) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !(taken >> i & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      argmax_merge(bv, bi, ov, oi);
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == 0) {
-      sel[q] = bi;
-      selv[q] = bv;
-    }
-  }
-  __syncwarp();
-}
-
 // One thread: softmax over the selected logits and the shared expert's gate
 // sigmoid(gate_logit) into out_w [top_k + 1], the ids into out_ids (and the
 // debug copy).
