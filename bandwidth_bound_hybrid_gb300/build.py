@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 SO = os.path.join(HERE, "libhybrid.so")
-SOURCES = ["gemv.cu", "bgemv.cu", "gdn.cu", "attn.cu", "attn_pair.cu", "gemm.cu", "prefill.cu", "engine.cu", "noalloc.cu"]
+SOURCES = ["gemv.cu", "bgemv.cu", "gdn.cu", "attn.cu", "attn_pair.cu", "gemm.cu", "prefill.cu", "moe_prefill.cu", "engine.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "kernels.h", "gemv_dev.cuh", "attn_dev.cuh", "attn_kernel.cuh", "gdn_dev.cuh", "tc05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "--extended-lambda"]

@@ -185,6 +185,12 @@ struct hy_cache {
   float *pf_x = nullptr, *pf_y = nullptr, *pf_qn = nullptr, *pf_kn = nullptr, *pf_v = nullptr, *pf_ab = nullptr;
   float* pf_qr = nullptr;
   uint16_t *pf_ahi = nullptr, *pf_alo = nullptr, *pf_hhi = nullptr, *pf_hlo = nullptr;
+  // MoE models: router logits, routing, the picks grouped by expert, their gathered activations, expert
+  // outputs, and the shared expert's
+  float *pf_rlog = nullptr, *pf_rw = nullptr, *pf_ye = nullptr, *pf_ysh = nullptr;
+  int *pf_ids = nullptr, *pf_pos = nullptr, *pf_tok = nullptr, *pf_tiles = nullptr, *pf_ntiles = nullptr;
+  uint16_t *pf_ghi = nullptr, *pf_glo = nullptr, *pf_ehi = nullptr, *pf_elo = nullptr, *pf_shi = nullptr,
+           *pf_slo = nullptr;
   struct Graph {
     int seq;
     float* logits;
@@ -1054,13 +1060,19 @@ int prefill_buffers(hy_cache* c, int rows) {
   const int H = cf.hidden;
   const int ka = std::max(H, std::max(m->o_len, 8));
   for (void* p : {(void*)c->pf_x, (void*)c->pf_y, (void*)c->pf_qn, (void*)c->pf_kn, (void*)c->pf_v, (void*)c->pf_ab,
-                  (void*)c->pf_qr, (void*)c->pf_ahi, (void*)c->pf_alo, (void*)c->pf_hhi, (void*)c->pf_hlo})
+                  (void*)c->pf_qr, (void*)c->pf_ahi, (void*)c->pf_alo, (void*)c->pf_hhi, (void*)c->pf_hlo,
+                  (void*)c->pf_rlog, (void*)c->pf_rw, (void*)c->pf_ye, (void*)c->pf_ysh, (void*)c->pf_ids,
+                  (void*)c->pf_pos, (void*)c->pf_tok, (void*)c->pf_tiles, (void*)c->pf_ntiles, (void*)c->pf_ghi,
+                  (void*)c->pf_glo, (void*)c->pf_ehi, (void*)c->pf_elo, (void*)c->pf_shi, (void*)c->pf_slo})
     if (p) {
       c->allocs.erase(std::remove(c->allocs.begin(), c->allocs.end(), p), c->allocs.end());
       cudaFree(p);
     }
   c->pf_x = c->pf_y = c->pf_qn = c->pf_kn = c->pf_v = c->pf_ab = c->pf_qr = nullptr;
   c->pf_ahi = c->pf_alo = c->pf_hhi = c->pf_hlo = nullptr;
+  c->pf_rlog = c->pf_rw = c->pf_ye = c->pf_ysh = nullptr;
+  c->pf_ids = c->pf_pos = c->pf_tok = c->pf_tiles = c->pf_ntiles = nullptr;
+  c->pf_ghi = c->pf_glo = c->pf_ehi = c->pf_elo = c->pf_shi = c->pf_slo = nullptr;
   c->pf_rows = 0;
   const size_t R = (size_t)rows;
   const size_t gq = m->n_gdn ? R * cf.gdn_heads * cf.gdn_dk : 1;
@@ -1073,9 +1085,89 @@ int prefill_buffers(hy_cache* c, int rows) {
       (rc = dalloc(c, &c->pf_ab, m->n_gdn ? R * cf.gdn_heads * 2 : 1)) ||
       (rc = dalloc(c, &c->pf_qr, m->n_attn ? R * cf.attn_q_heads * cf.head_dim : 1)))
     return rc;
+  if (m->moe) {
+    const size_t E = cf.n_experts, K = cf.top_k, Fe = cf.expert_ffn, Fs = cf.shared_ffn, P = R * K;
+    if ((rc = dalloc(c, &c->pf_rlog, R * (E + 1))) || (rc = dalloc(c, &c->pf_rw, R * (K + 1))) ||
+        (rc = dalloc(c, &c->pf_ye, P * H)) || (rc = dalloc(c, &c->pf_ysh, R * H)) || (rc = dalloc(c, &c->pf_ids, P)) ||
+        (rc = dalloc(c, &c->pf_pos, P)) || (rc = dalloc(c, &c->pf_tok, P)) ||
+        (rc = dalloc(c, &c->pf_tiles, (size_t)3 * moepf::max_tiles(rows, (int)E, (int)K))) ||
+        (rc = dalloc(c, &c->pf_ntiles, 1)) || (rc = dalloc(c, &c->pf_ghi, P * H)) ||
+        (rc = dalloc(c, &c->pf_glo, P * H)) || (rc = dalloc(c, &c->pf_ehi, P * Fe)) ||
+        (rc = dalloc(c, &c->pf_elo, P * Fe)) || (rc = dalloc(c, &c->pf_shi, R * Fs)) ||
+        (rc = dalloc(c, &c->pf_slo, R * Fs)))
+      return rc;
+  }
   c->pf_rows = rows;
   c->pf_ka = ka;
   return HY_OK;
+}
+
+// The MoE FFN of a chunk of n tokens whose normalised activations are in
+// pf_ahi / pf_alo: router GEMM, routing, picks grouped by expert, the grouped
+// expert GEMMs (gate/up with SwiGLU, then down), the shared expert's GEMMs,
+// and the weighted sum into the residual pf_x.
+cudaError_t moe_chunk(hy_cache* c, const hy_layer_weights& L, int n, cudaStream_t st) {
+  hy_model* m = c->m;
+  const hy_config& cf = m->cfg;
+  const int H = cf.hidden, ka = c->pf_ka, E = cf.n_experts, K = cf.top_k, Fe = cf.expert_ffn,
+            Fs = cf.shared_ffn, P = n * K;
+  auto base = [&](int M, int N, int Kd, int epi) {
+    gemm::Params g;
+    memset(&g, 0, sizeof(g));
+    g.M = M;
+    g.N = N;
+    g.K = Kd;
+    g.epi = epi;
+    g.guard = c->guard;
+    return g;
+  };
+  gemm::Params g = base(n, E + 1, H, gemm::kEpiStore);  // router logits [n][E + 1]
+  g.y = c->pf_rlog;
+  g.ldy = E + 1;
+  cudaError_t e = gemm::launch(g, c->pf_ahi, c->pf_alo, ka, (const uint16_t*)L.router, nullptr, H, st);
+  if (e == cudaSuccess) e = moepf::route(c->pf_rlog, E + 1, n, E, K, c->pf_ids, c->pf_rw, st);
+  if (e == cudaSuccess)
+    e = moepf::bucket(c->pf_ids, n, E, K, c->pf_pos, c->pf_tok, c->pf_tiles, c->pf_ntiles, c->guard, st);
+  if (e == cudaSuccess) e = moepf::gather(c->pf_ahi, c->pf_alo, ka, H, c->pf_tok, P, c->pf_ghi, c->pf_glo, st);
+  const int mt = moepf::max_tiles(n, E, K);
+  if (e == cudaSuccess) {  // grouped gate/up + SwiGLU: [P][Fe] hi / lo
+    g = base(P, Fe, H, gemm::kEpiSwigluSplit);
+    g.h_hi = c->pf_ehi;
+    g.h_lo = c->pf_elo;
+    g.ldh = Fe;
+    g.tiles = c->pf_tiles;
+    g.ntiles = c->pf_ntiles;
+    g.max_tiles = mt;
+    g.w_group_rows = Fe;
+    g.n_groups = E;
+    e = gemm::launch(g, c->pf_ghi, c->pf_glo, H, (const uint16_t*)L.exp_gate.w, (const uint16_t*)L.exp_up.w, H, st);
+  }
+  if (e == cudaSuccess) {  // grouped down: [P][H] FP32
+    g = base(P, H, Fe, gemm::kEpiStore);
+    g.y = c->pf_ye;
+    g.ldy = H;
+    g.tiles = c->pf_tiles;
+    g.ntiles = c->pf_ntiles;
+    g.max_tiles = mt;
+    g.w_group_rows = H;
+    g.n_groups = E;
+    e = gemm::launch(g, c->pf_ehi, c->pf_elo, Fe, (const uint16_t*)L.exp_down.w, nullptr, Fe, st);
+  }
+  if (e == cudaSuccess) {  // shared expert gate/up + SwiGLU
+    g = base(n, Fs, H, gemm::kEpiSwigluSplit);
+    g.h_hi = c->pf_shi;
+    g.h_lo = c->pf_slo;
+    g.ldh = Fs;
+    e = gemm::launch(g, c->pf_ahi, c->pf_alo, ka, (const uint16_t*)L.sh_gate.w, (const uint16_t*)L.sh_up.w, H, st);
+  }
+  if (e == cudaSuccess) {  // shared expert down: [n][H] FP32
+    g = base(n, H, Fs, gemm::kEpiStore);
+    g.y = c->pf_ysh;
+    g.ldy = H;
+    e = gemm::launch(g, c->pf_shi, c->pf_slo, Fs, (const uint16_t*)L.sh_down.w, nullptr, Fs, st);
+  }
+  if (e == cudaSuccess) e = moepf::combine(c->pf_x, H, n, K, c->pf_rw, c->pf_pos, c->pf_ye, c->pf_ysh, st);
+  return e;
 }
 
 // One chunk of n prompt tokens of sequence `seq` at positions t0 .. t0+n-1
@@ -1158,10 +1250,21 @@ int prefill_chunk(hy_cache* c, int seq, const int* tok, int n, int t0, bool last
     }
     if (e == cudaSuccess) e = gemm_run(H, od, gemm::kEpiResid, c->pf_ahi, c->pf_alo, ka, L.w_o.w, nullptr, c->pf_x, H);
     if (e == cudaSuccess) e = gemm::norm_split(c->pf_x, H, L.norm2, cf.rms_eps, n, H, c->pf_ahi, c->pf_alo, ka, st);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && m->moe) {
+      e = moe_chunk(c, L, n, st);
+    } else if (e == cudaSuccess) {
       e = gemm_run(cf.ffn, H, gemm::kEpiSwigluSplit, c->pf_ahi, c->pf_alo, ka, L.w_gate.w, L.w_up.w, nullptr, 0);
-    if (e == cudaSuccess)
-      e = gemm_run(H, cf.ffn, gemm::kEpiResid, c->pf_hhi, c->pf_hlo, cf.ffn, L.w_down.w, nullptr, c->pf_x, H);
+      if (e == cudaSuccess)
+        e = gemm_run(H, cf.ffn, gemm::kEpiResid, c->pf_hhi, c->pf_hlo, cf.ffn, L.w_down.w, nullptr, c->pf_x, H);
+    }
+    if (e == cudaSuccess && last && m->debug && m->moe) {  // the last token's routing, as a decode step records it
+      const int K = cf.top_k, E = cf.n_experts;
+      e = cudaMemcpyAsync(c->dbg_rids + (size_t)l * K, c->pf_ids + (size_t)(n - 1) * K, sizeof(int) * K,
+                          cudaMemcpyDeviceToDevice, st);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(c->dbg_rlog + (size_t)l * (E + 1), c->pf_rlog + (size_t)(n - 1) * (E + 1),
+                            sizeof(float) * (E + 1), cudaMemcpyDeviceToDevice, st);
+    }
     if (e == cudaSuccess && last && m->debug)
       e = cudaMemcpyAsync(c->dbg_hidden + (size_t)l * H, c->pf_x + (size_t)(n - 1) * H, sizeof(float) * H,
                           cudaMemcpyDeviceToDevice, st);
@@ -1270,10 +1373,13 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
   m->graphs = !(c.flags & HY_FLAG_NO_GRAPH);
   m->debug = (c.flags & HY_FLAG_DEBUG) != 0;
   m->q4 = c.weight_format == 1;
-  {  // the chunked prompt path: bf16 dense models whose GEMM widths suit the tensor copies
+  {  // the chunked prompt path: bf16 models whose GEMM widths suit the tensor copies
     const int od = std::max(m->n_gdn ? c.gdn_heads * c.gdn_dv : 8, m->n_attn ? c.attn_q_heads * c.head_dim : 8);
-    m->chunk_prefill = !m->q4 && !m->moe && c.kv_format == 0 && !(c.flags & HY_FLAG_TOKEN_PREFILL) && H % 8 == 0 &&
-                       c.ffn % 8 == 0 && od % 8 == 0;
+    const bool ffn_ok = m->moe ? (c.expert_ffn % 8 == 0 && c.shared_ffn % 8 == 0 && c.shared_ffn > 0 &&
+                                  c.n_experts <= 512 && c.top_k <= 16)
+                               : c.ffn % 8 == 0;
+    m->chunk_prefill = !m->q4 && c.kv_format == 0 && !(c.flags & HY_FLAG_TOKEN_PREFILL) && H % 8 == 0 && ffn_ok &&
+                       od % 8 == 0;
   }
   *out = m;
   g_err.clear();

@@ -17,7 +17,10 @@
 //     with tcgen05.commit;
 //   * the epilogue reads the accumulator with tcgen05.ld and stores it, adds it
 //     to a residual, or applies SwiGLU and splits the result into the bf16
-//     hi/lo parts the next GEMM consumes.
+//     hi/lo parts the next GEMM consumes;
+//   * grouped form (the MoE experts of a prompt chunk): each row tile comes
+//     from a device-side table {first row of the gathered activations, rows,
+//     expert}, and the expert selects the block of weight rows it reads.
 // Rows past M or N and K past the end arrive as zeros from the tensor copies.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -73,7 +76,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Pa
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool pair = p.epi == kEpiSwigluSplit;
   const int BN = pair ? 128 : 256;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int n0 = blockIdx.x * BN;
+  int m0 = blockIdx.y * BM, mrows = p.M - m0, wr0 = n0;  // first A row, valid rows, first W row
+  if (p.tiles) {  // grouped: the tile table (written by an earlier kernel of the stream)
+    const int i = blockIdx.y;
+    if (i >= *p.ntiles) return;
+    m0 = p.tiles[3 * i];
+    mrows = p.tiles[3 * i + 1];
+    const int g = p.tiles[3 * i + 2];
+    if (g < 0 || g >= p.n_groups || m0 < 0 || mrows < 1 || mrows > BM || m0 + mrows > p.M) {
+      if (threadIdx.x == 0) set_guard(p.guard, kGuardBadIndex);
+      return;
+    }
+    wr0 = g * p.w_group_rows + n0;
+  }
   const int nk = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -104,10 +120,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Pa
         tc::tma_load_2d(st, &mp.a_hi, t * BK, m0, &full[s]);
         tc::tma_load_2d(st + kTileA, &mp.a_lo, t * BK, m0, &full[s]);
         if (!pair) {
-          tc::tma_load_2d(st + 2 * kTileA, &mp.b0, t * BK, n0, &full[s]);
+          tc::tma_load_2d(st + 2 * kTileA, &mp.b0, t * BK, wr0, &full[s]);
         } else {
-          tc::tma_load_2d(st + 2 * kTileA, &mp.b0, t * BK, n0, &full[s]);
-          tc::tma_load_2d(st + 2 * kTileA + kTileB / 2, &mp.b1, t * BK, n0, &full[s]);
+          tc::tma_load_2d(st + 2 * kTileA, &mp.b0, t * BK, wr0, &full[s]);
+          tc::tma_load_2d(st + 2 * kTileA + kTileB / 2, &mp.b1, t * BK, wr0, &full[s]);
         }
       }
       // the CTA must not retire while its copies are in flight
@@ -150,13 +166,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Pa
     if (!got && threadIdx.x == 0) set_guard(p.guard, kGuardWaitTimeout);
     tc::fence_after_sync();
     const int row = m0 + warp * 32 + lane;
+    const bool live = warp * 32 + lane < mrows;  // the tile's own rows (grouped: not the next group's)
     const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
     if (got) {
       if (!pair) {
         for (int c0 = 0; c0 < BN; c0 += 32) {
           float v[32];
           tc::tmem_ld32(tbase + c0, v);
-          if (row >= p.M) continue;
+          if (!live) continue;
           float* y = p.y + (long long)row * p.ldy + n0 + c0;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -170,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Pa
           float g[32], u[32];
           tc::tmem_ld32(tbase + c0, g);
           tc::tmem_ld32(tbase + 128 + c0, u);
-          if (row >= p.M) continue;
+          if (!live) continue;
           uint16_t* hh = p.h_hi + (long long)row * p.ldh + n0 + c0;
           uint16_t* hl = p.h_lo + (long long)row * p.ldh + n0 + c0;
 #pragma unroll
@@ -237,16 +254,19 @@ bool supported(int M, int N, int K) { return M > 0 && N > 0 && K > 0 && K % 8 ==
 cudaError_t launch(const Params& p, const uint16_t* a_hi, const uint16_t* a_lo, int lda, const uint16_t* w0,
                    const uint16_t* w1, int ldw, cudaStream_t st) {
   if (!g_encode || !supported(p.M, p.N, p.K) || lda < p.K || ldw < p.K) return cudaErrorInvalidValue;
+  const bool grouped = p.tiles != nullptr;
+  if (grouped && (!p.ntiles || p.max_tiles < 1 || p.n_groups < 1 || p.w_group_rows < p.N)) return cudaErrorInvalidValue;
   const bool pair = p.epi == kEpiSwigluSplit;
   if (pair && (!w1 || !p.h_hi || !p.h_lo)) return cudaErrorInvalidValue;
   if (!pair && !p.y) return cudaErrorInvalidValue;
   alignas(64) Maps mp;
   memset(&mp, 0, sizeof(mp));
   const int bn = pair ? 128 : 256;
+  const long long wrows = grouped ? (long long)p.n_groups * p.w_group_rows : p.N;
   if (!encode(&mp.a_hi, a_hi, p.M, p.K, lda, BM) || !encode(&mp.a_lo, a_lo, p.M, p.K, lda, BM) ||
-      !encode(&mp.b0, w0, p.N, p.K, ldw, bn) || (pair && !encode(&mp.b1, w1, p.N, p.K, ldw, bn)))
+      !encode(&mp.b0, w0, wrows, p.K, ldw, bn) || (pair && !encode(&mp.b1, w1, wrows, p.K, ldw, bn)))
     return cudaErrorInvalidValue;
-  const dim3 grid((p.N + bn - 1) / bn, (p.M + BM - 1) / BM);
+  const dim3 grid((p.N + bn - 1) / bn, grouped ? p.max_tiles : (p.M + BM - 1) / BM);
   return launch_k(k_gemm, grid, dim3(kThreads), (size_t)kSmem, st, false, p, mp);
 }
 

@@ -290,6 +290,12 @@ struct Params {
   uint16_t* h_lo;
   int ldh;
   unsigned* guard;
+  // grouped (tiles != null): row tile i of the grid is tiles[3i .. 3i+2] = {first A row, rows (<= 128),
+  // group g}; its W rows are g * w_group_rows + n (W holds n_groups * w_group_rows rows); output rows are
+  // A's; tiles i >= *ntiles do nothing.  M = rows of A (and of the output).
+  const int* tiles;
+  const int* ntiles;
+  int max_tiles, w_group_rows, n_groups;
 };
 cudaError_t init();
 bool supported(int M, int N, int K);
@@ -300,6 +306,30 @@ cudaError_t launch(const Params& p, const uint16_t* a_hi, const uint16_t* a_lo, 
 cudaError_t norm_split(const float* x, int ld_x, const float* g, float eps, int rows, int cols, uint16_t* hi,
                        uint16_t* lo, int ld_out, cudaStream_t st);
 }  // namespace gemm
+
+// ---------------------------------------------------------------- prompt MoE
+// The MoE FFN of a chunk of n prompt tokens (moe_prefill.cu), around the
+// router GEMM, the grouped expert GEMMs and the shared expert's GEMMs.
+namespace moepf {
+constexpr int kTileRows = 128;  // rows of a grouped GEMM tile
+// Routing of every token: logits [n][ldl] (E routed + the shared gate at E) ->
+// ids [n][K] (top K, descending, lowest index on ties) and weights [n][K+1]
+// (softmax over the picks; last: sigmoid of the shared gate).
+cudaError_t route(const float* logits, int ldl, int n, int E, int K, int* ids, float* w, cudaStream_t st);
+// Tokens grouped by expert, in token order (deterministic): pos_of[t*K+k] is
+// the gathered row of pick (t, k), tok_of[row] its token; tiles / ntiles: the
+// grouped GEMM's row tiles {first row, rows, expert} (at most
+// max_tiles(n, E, K)).  One CTA.
+int max_tiles(int n, int E, int K);
+cudaError_t bucket(const int* ids, int n, int E, int K, int* pos_of, int* tok_of, int* tiles, int* ntiles,
+                   unsigned* guard, cudaStream_t st);
+// Gathered activations: rows [n*K] of hi / lo (ld) = rows tok_of[r] of src_hi / src_lo.
+cudaError_t gather(const uint16_t* src_hi, const uint16_t* src_lo, int ld, int cols, const int* tok_of, int rows,
+                   uint16_t* dst_hi, uint16_t* dst_lo, cudaStream_t st);
+// x[t] += sum_k w[t][k] Ye[pos_of[t*K+k]] + w[t][K] Ysh[t], in that order.
+cudaError_t combine(float* x, int H, int n, int K, const float* w, const int* pos_of, const float* Ye,
+                    const float* Ysh, cudaStream_t st);
+}  // namespace moepf
 
 // ---------------------------------------------------------------- prompt mixers
 // The chunk of n prompt tokens at positions t0 .. t0+n-1 of one sequence

@@ -1,5 +1,5 @@
-"""The chunked prompt path (tensor-core GEMMs and the prompt mixer kernels)
-against the FP64 oracle and against the token-by-token prefill through the
+"""The chunked prompt path (tensor-core GEMMs, for MoE models the grouped
+expert GEMMs, and the prompt mixer kernels) against the FP64 oracle and against the token-by-token prefill through the
 decode step: several chunks with a ragged last one, a prompt continued by a
 second call (positions not starting at 0), a single-token prompt, and the
 decode steps that follow, which read the caches the prefill left.
@@ -50,7 +50,7 @@ def hidden_of(model, shape):
     return [to_np(model.debug_hidden(l)).copy() for l in range(shape.n_layers)]
 
 
-def run(shape, segments, n_decode, seed=1):
+def run(shape, segments, n_decode, seed=1, same_tol=SAME_TOL):
     """Prefill the prompt in `segments` (lengths of consecutive prefill calls),
     then decode n_decode greedy steps (the oracle's token), comparing the
     chunked model with the oracle and with the token-by-token model."""
@@ -72,15 +72,22 @@ def run(shape, segments, n_decode, seed=1):
         fast.prefill(0, toks, lf)
         slow.prefill(0, toks, ls)
         for t in prompt[i0:i0 + n]:
-            r = ref.forward(int(t))
+            r = ref.forward(int(t), want_router=shape.is_moe)
         i0 += n
         torch.cuda.synchronize()
         hf, hs = hidden_of(fast, shape), hidden_of(slow, shape)
         for l in range(shape.n_layers):
             assert rel_l2(hf[l], r["hidden"][l]) <= HIDDEN_TOL, f"prefill to {i0}: layer {l} vs oracle"
-            assert rel_l2(hf[l], hs[l]) <= SAME_TOL, f"prefill to {i0}: layer {l} chunked vs token by token"
+            assert rel_l2(hf[l], hs[l]) <= same_tol, f"prefill to {i0}: layer {l} chunked vs token by token"
+        if shape.is_moe:  # the last token picked the oracle's experts in every layer (or differs at a near-tie)
+            for l in range(shape.n_layers):
+                dev = sorted(to_np(fast.debug_router(l)[1]).tolist())
+                if dev != sorted(int(i) for i in r["router_ids"][l]):
+                    srt = np.sort(np.asarray(r["router_logits"][l][:shape.n_experts]))[::-1]
+                    gap = srt[shape.top_k - 1] - srt[shape.top_k]
+                    assert gap <= 1e-3 * max(1.0, abs(srt[0])), f"prefill to {i0}: layer {l} experts {dev}"
         assert rel_l2(to_np(lf), r["logits"]) <= LOGIT_TOL
-        assert rel_l2(to_np(lf), to_np(ls)) <= SAME_TOL
+        assert rel_l2(to_np(lf), to_np(ls)) <= same_tol
     assert fast.seq_len(0) == total and slow.seq_len(0) == total
     ids_f = torch.empty(1, dtype=torch.int32, device="cuda")
     ids_s = torch.empty(1, dtype=torch.int32, device="cuda")
@@ -93,7 +100,7 @@ def run(shape, segments, n_decode, seed=1):
         torch.cuda.synchronize()
         e = rel_l2(to_np(lf), r["logits"])
         assert e <= LOGIT_TOL, f"decode {s}: logits rel-L2 {e:.3g}"
-        assert rel_l2(to_np(lf), to_np(ls)) <= SAME_TOL, f"decode {s}: chunked vs token-by-token caches"
+        assert rel_l2(to_np(lf), to_np(ls)) <= same_tol, f"decode {s}: chunked vs token-by-token caches"
         hf = hidden_of(fast, shape)
         for l in range(shape.n_layers):
             assert rel_l2(hf[l], r["hidden"][l]) <= HIDDEN_TOL, f"decode {s} layer {l}"
@@ -126,6 +133,34 @@ def test_dense4b_full_widths_truncated_depth(built, chunk_rows):
     chunk_rows(128)
     shape = dataclasses.replace(workloads.DENSE4B, name="dense4b-l4-v4k", n_layers=4, attn_layers=(3,), vocab=4096)
     run(shape, [300], 2)
+
+
+# a tiny bf16 MoE hybrid whose widths suit the GEMM's tensor copies (multiples of 8)
+TINY_MOE = workloads.ModelShape("tiny-moe-bf16", n_layers=2, hidden=256, vocab=1024, ffn=0, gdn_heads=4, gdn_dk=64,
+                                gdn_dv=64, attn_q_heads=4, attn_kv_heads=2, head_dim=64, attn_layers=(1,),
+                                n_experts=16, top_k=4, expert_ffn=256, shared_ffn=256)
+
+
+def test_tiny_moe_prompt_in_ragged_chunks(built, chunk_rows):
+    """Tiny MoE hybrid (16 experts, top 4, shared expert), a 130-token prompt
+    in chunks of 48: router GEMM, routing, the grouped expert GEMMs, the
+    shared expert and the combine, against the oracle and the token-by-token
+    prefill; then decode steps on the caches it left."""
+    chunk_rows(48)
+    run(TINY_MOE, [130], 4)
+
+
+def test_moe_full_widths_truncated_depth(built, chunk_rows):
+    """Full widths of the MoE 35B-A3B-shaped model (hidden 2048, 256 experts
+    of 512, top 8, shared expert, 16x128 DeltaNet heads, 16/2x256 GQA), 4
+    layers, vocab cut to 4096; a 200-token prompt in chunks of 128, so that
+    experts take several grouped tiles or none."""
+    chunk_rows(128)
+    shape = dataclasses.replace(workloads.MOE35B, name="moe-l4-v4k", n_layers=4, attn_layers=(3,), vocab=4096)
+    # a MoE layer's output sums top_k + 1 = 9 expert outputs, each with the rounding of the bf16 hi / lo parts
+    # of its input and of its SwiGLU output; 9 such terms add about sqrt(9) = 3 times a dense FFN's rounding
+    # difference between the two paths (1e-4 at dense widths)
+    run(shape, [200], 2, same_tol=3 * SAME_TOL)
 
 
 def test_prefill_refuses_past_capacity_with_nothing_launched(built):
