@@ -573,9 +573,11 @@ def timed_prefill(model, toks, shape, logits):
     n = int(toks.numel())
     fl = acc.prefill_flops(shape, n)
     _, sustained, kind = load_tensor_peak()
-    chunked = shape.ffn > 0 and getattr(shape, "weight_format", 0) == 0 and getattr(shape, "kv_format", 0) == 0
+    chunked = getattr(shape, "weight_format", 0) == 0 and getattr(shape, "kv_format", 0) == 0
+    gemms = ("tcgen05 GEMMs (the experts as grouped GEMMs over the tokens that picked them)" if shape.is_moe
+             else "tcgen05 GEMMs")
     return {"tokens": n, "ttft_ms": t * 1e3, "tokens_per_s": n / t,
-            "path": "chunks of up to 2048 tokens: tcgen05 GEMMs + prompt mixer kernels" if chunked
+            "path": f"chunks of up to 2048 tokens: {gemms} + prompt mixer kernels" if chunked
             else "token by token through the decode step",
             "flops_total": fl["total"], "tflops_total": fl["total"] / t / 1e12,
             "tensor_tflops_executed": fl["tensor_executed"] / t / 1e12, "peak_tflops_sustained": sustained,
