@@ -5,7 +5,9 @@
 //   v rows; q, k L2-normalised (q also scaled by dk^-1/2); alpha =
 //   sigmoid(a_h), beta = sigmoid(b_h); then per value row i, in place
 //       u_i = S_i . k,   S_i <- alpha S_i + beta (v_i - alpha u_i) k,   o_i = S_i . q
-// which is S <- alpha S (I - beta k k^T) + beta v k^T, o = S q written per row
+// which is S <- alpha S (I - beta k k^T) + beta v k^T, o = S q written per row;
+// o_i of the updated row is formed as alpha (S_i . q) + d_i (k . q) with
+// d_i = beta (v_i - alpha u_i), so that u_i and S_i . q reduce in one pass
 // ("Beating llama.cpp from Scratch on Consumer AMD", "The Beast": a fixed FP32
 // state updated in place by a 1D convolution and a gated delta rule).  The
 // read row is the write row ("Fourteen hours to 100 tokens per second",
@@ -174,22 +176,40 @@ __device__ __forceinline__ void run_item(const Params& p, int h, int rc, Rows<EP
   }
   const float alpha = sigmoidf_(a_in);
   const float beta = sigmoidf_(b_in);
+  // o_i = S_i' . q = alpha (S_i . q) + d_i (k . q): both dots of a row reduce
+  // together, before its update
+  float kqd = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) kqd = fmaf(kq[e], qq[e], kqd);
+  float ur[RPW], qr[RPW];
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    ur[r] = 0.f;
+    qr[r] = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      ur[r] = fmaf(R.S[r][e], kq[e], ur[r]);
+      qr[r] = fmaf(R.S[r][e], qq[e], qr[r]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kqd += __shfl_xor_sync(0xffffffffu, kqd, o);
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+      ur[r] += __shfl_xor_sync(0xffffffffu, ur[r], o);
+      qr[r] += __shfl_xor_sync(0xffffffffu, qr[r], o);
+    }
+  }
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
     const int li = warp * RPW + r;
     const int i = rc * kRowsPerCta + li;
     if (i >= dv) continue;
-    float u = 0.f;
+    const float d = beta * (sh.v[li] - alpha * ur[r]);
+    const float o = fmaf(alpha, qr[r], d * kqd);
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) u = fmaf(R.S[r][e], kq[e], u);
-    u = warp_sum(u);
-    const float d = beta * (sh.v[li] - alpha * u);
-    float o = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      R.S[r][e] = fmaf(alpha, R.S[r][e], d * kq[e]);
-      o = fmaf(R.S[r][e], qq[e], o);
-    }
+    for (int e = 0; e < EPL; ++e) R.S[r][e] = fmaf(alpha, R.S[r][e], d * kq[e]);
     if (EPL >= 4) {
 #pragma unroll
       for (int e = 0; e < EPL; e += 4)
@@ -198,7 +218,6 @@ __device__ __forceinline__ void run_item(const Params& p, int h, int rc, Rows<EP
 #pragma unroll
       for (int e = 0; e < EPL; ++e) R.ptr[r][e] = R.S[r][e];
     }
-    o = warp_sum(o);
     if (lane == 0) p.o[h * dv + i] = o;
   }
   sync();  // the item's shared scratch may be reused after this

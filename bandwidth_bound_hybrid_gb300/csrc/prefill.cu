@@ -148,20 +148,36 @@ __global__ void __launch_bounds__(kScanThreads) k_gdn_scan(GdnArgs a) {
   for (int i = 0; i < a.n; ++i) {
     float kn[EPL], qn[EPL], vn[kScanRPW], aln = 0.f, ben = 0.f;
     if (i + 1 < a.n) load(i + 1, kn, qn, vn, aln, ben);
+    // the decode step's arithmetic: u_i = S_i . k and S_i . q reduce together,
+    // o_i = alpha (S_i . q) + d_i (k . q), then the row update
+    float kqd = 0.f, u[kScanRPW], sq[kScanRPW];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) kqd = fmaf(kq[e], qq[e], kqd);
 #pragma unroll
     for (int r = 0; r < kScanRPW; ++r) {
-      float u = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) u = fmaf(S[r][e], kq[e], u);
-      u = warp_sum(u);
-      const float d = be * (vr[r] - al * u);
-      float o = 0.f;
+      u[r] = 0.f;
+      sq[r] = 0.f;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
-        S[r][e] = fmaf(al, S[r][e], d * kq[e]);
-        o = fmaf(S[r][e], qq[e], o);
+        u[r] = fmaf(S[r][e], kq[e], u[r]);
+        sq[r] = fmaf(S[r][e], qq[e], sq[r]);
       }
-      o = warp_sum(o);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kqd += __shfl_xor_sync(0xffffffffu, kqd, o);
+#pragma unroll
+      for (int r = 0; r < kScanRPW; ++r) {
+        u[r] += __shfl_xor_sync(0xffffffffu, u[r], o);
+        sq[r] += __shfl_xor_sync(0xffffffffu, sq[r], o);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kScanRPW; ++r) {
+      const float d = be * (vr[r] - al * u[r]);
+      const float o = fmaf(al, sq[r], d * kqd);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) S[r][e] = fmaf(al, S[r][e], d * kq[e]);
       if (lane == 0 && row[r] < dv) {
         const long long off = (long long)i * a.ldo + h * dv + row[r];
         split_bf16(o, a.O_hi + off, a.O_lo + off);
