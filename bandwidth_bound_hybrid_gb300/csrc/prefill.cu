@@ -112,12 +112,37 @@ __global__ void __launch_bounds__(kPrepThreads) k_gdn_prep(GdnArgs a) {
 }
 
 constexpr int kScanRows = 16, kScanThreads = 128, kScanRPW = kScanRows / (kScanThreads / 32);
+constexpr int kScanTB = 32;  // tokens whose inputs are staged in shared memory at a time
 
+// Floats of one staged token: k [dk], q [dk], the CTA's v rows [16], alpha and
+// beta, padding to 16 bytes.
+__host__ __device__ constexpr int scan_tok_floats(int dk) { return 2 * dk + kScanRows + 4; }
+size_t scan_smem(int dk) { return (size_t)2 * kScanTB * scan_tok_floats(dk) * sizeof(float); }
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// The recurrence over the chunk's tokens for one head and 16 state rows: the
+// rows stay in registers for the whole chunk; the inputs of blocks of 32
+// tokens (k, q, the v rows, the gates) are staged in shared memory by the
+// whole CTA with asynchronous copies, the next block's while the current one
+// runs, so that a token's step waits on no global load.
 template <int EPL>
 __global__ void __launch_bounds__(kScanThreads) k_gdn_scan(GdnArgs a) {
+  extern __shared__ __align__(16) float stage[];
   const int h = blockIdx.x, rc = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int dk = EPL * 32;
+  constexpr int TF = scan_tok_floats(dk);
   const int nh = a.nh, dv = a.dv;
   float S[kScanRPW][EPL];
   float* ptr[kScanRPW];
@@ -129,71 +154,88 @@ __global__ void __launch_bounds__(kScanThreads) k_gdn_scan(GdnArgs a) {
 #pragma unroll
     for (int e = 0; e < EPL; ++e) S[r][e] = ptr[r][e];
   }
-  // inputs of token i, loaded one token ahead of their use
-  float kq[EPL], qq[EPL], vr[kScanRPW], al = 0.f, be = 0.f;
-  auto load = [&](int i, float* k_, float* q_, float* v_, float& al_, float& be_) {
-    const float* Kr = a.Kn + ((long long)i * nh + h) * dk + lane * EPL;
-    const float* Qr = a.Qn + ((long long)i * nh + h) * dk + lane * EPL;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      k_[e] = Kr[e];
-      q_[e] = Qr[e];
-    }
-#pragma unroll
-    for (int r = 0; r < kScanRPW; ++r) v_[r] = row[r] < dv ? a.V[((long long)i * nh + h) * dv + row[r]] : 0.f;
-    al_ = a.AB[((long long)i * nh + h) * 2];
-    be_ = a.AB[((long long)i * nh + h) * 2 + 1];
-  };
-  if (a.n > 0) load(0, kq, qq, vr, al, be);
-  for (int i = 0; i < a.n; ++i) {
-    float kn[EPL], qn[EPL], vn[kScanRPW], aln = 0.f, ben = 0.f;
-    if (i + 1 < a.n) load(i + 1, kn, qn, vn, aln, ben);
-    // the decode step's arithmetic: u_i = S_i . k and S_i . q reduce together,
-    // o_i = alpha (S_i . q) + d_i (k . q), then the row update
-    float kqd = 0.f, u[kScanRPW], sq[kScanRPW];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) kqd = fmaf(kq[e], qq[e], kqd);
-#pragma unroll
-    for (int r = 0; r < kScanRPW; ++r) {
-      u[r] = 0.f;
-      sq[r] = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        u[r] = fmaf(S[r][e], kq[e], u[r]);
-        sq[r] = fmaf(S[r][e], qq[e], sq[r]);
+  // block b's inputs into buffer b & 1: per token dk/4 + dk/4 + 4 16-byte pieces and the gates (8 bytes)
+  auto issue = [&](int b) {
+    float* buf = stage + (b & 1) * kScanTB * TF;
+    const int i0 = b * kScanTB, nt = (a.n - i0 < kScanTB) ? a.n - i0 : kScanTB;
+    constexpr int per = dk / 2 + kScanRows / 4 + 1;
+    for (int c = tid; c < nt * per; c += kScanThreads) {
+      const int j = c / per, q = c % per;
+      const long long i = i0 + j;
+      float* d = buf + j * TF;
+      if (q < dk / 4) {
+        cp_async16(d + 4 * q, a.Kn + (i * nh + h) * dk + 4 * q);
+      } else if (q < dk / 2) {
+        const int u = q - dk / 4;
+        cp_async16(d + dk + 4 * u, a.Qn + (i * nh + h) * dk + 4 * u);
+      } else if (q < dk / 2 + kScanRows / 4) {
+        const int u = q - dk / 2;
+        if (rc * kScanRows + 4 * u + 3 < dv) cp_async16(d + 2 * dk + 4 * u, a.V + (i * nh + h) * dv + rc * kScanRows + 4 * u);
+      } else {
+        cp_async8(d + 2 * dk + kScanRows, a.AB + (i * nh + h) * 2);
       }
     }
+    cp_async_commit();
+  };
+  const int nb = (a.n + kScanTB - 1) / kScanTB;
+  if (nb > 0) issue(0);
+  for (int b = 0; b < nb; ++b) {
+    if (b + 1 < nb) {
+      issue(b + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const float* buf = stage + (b & 1) * kScanTB * TF;
+    const int i0 = b * kScanTB, nt = (a.n - i0 < kScanTB) ? a.n - i0 : kScanTB;
+    for (int j = 0; j < nt; ++j) {
+      const float* tk = buf + j * TF;
+      float kq[EPL], qq[EPL];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      kqd += __shfl_xor_sync(0xffffffffu, kqd, o);
+      for (int e = 0; e < EPL; ++e) {
+        kq[e] = tk[lane * EPL + e];
+        qq[e] = tk[dk + lane * EPL + e];
+      }
+      const float al = tk[2 * dk + kScanRows], be = tk[2 * dk + kScanRows + 1];
+      // the decode step's arithmetic: u_i = S_i . k and S_i . q reduce together,
+      // o_i = alpha (S_i . q) + d_i (k . q), then the row update
+      float kqd = 0.f, u[kScanRPW], sq[kScanRPW];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) kqd = fmaf(kq[e], qq[e], kqd);
 #pragma unroll
       for (int r = 0; r < kScanRPW; ++r) {
-        u[r] += __shfl_xor_sync(0xffffffffu, u[r], o);
-        sq[r] += __shfl_xor_sync(0xffffffffu, sq[r], o);
-      }
-    }
+        u[r] = 0.f;
+        sq[r] = 0.f;
 #pragma unroll
-    for (int r = 0; r < kScanRPW; ++r) {
-      const float d = be * (vr[r] - al * u[r]);
-      const float o = fmaf(al, sq[r], d * kqd);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) S[r][e] = fmaf(al, S[r][e], d * kq[e]);
-      if (lane == 0 && row[r] < dv) {
-        const long long off = (long long)i * a.ldo + h * dv + row[r];
-        split_bf16(o, a.O_hi + off, a.O_lo + off);
-      }
-    }
-    if (i + 1 < a.n) {
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        kq[e] = kn[e];
-        qq[e] = qn[e];
+        for (int e = 0; e < EPL; ++e) {
+          u[r] = fmaf(S[r][e], kq[e], u[r]);
+          sq[r] = fmaf(S[r][e], qq[e], sq[r]);
+        }
       }
 #pragma unroll
-      for (int r = 0; r < kScanRPW; ++r) vr[r] = vn[r];
-      al = aln;
-      be = ben;
+      for (int o = 16; o > 0; o >>= 1) {
+        kqd += __shfl_xor_sync(0xffffffffu, kqd, o);
+#pragma unroll
+        for (int r = 0; r < kScanRPW; ++r) {
+          u[r] += __shfl_xor_sync(0xffffffffu, u[r], o);
+          sq[r] += __shfl_xor_sync(0xffffffffu, sq[r], o);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kScanRPW; ++r) {
+        const float vr = row[r] < dv ? tk[2 * dk + warp * kScanRPW + r] : 0.f;
+        const float d = be * (vr - al * u[r]);
+        const float o = fmaf(al, sq[r], d * kqd);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) S[r][e] = fmaf(al, S[r][e], d * kq[e]);
+        if (lane == 0 && row[r] < dv) {
+          const long long off = (long long)(i0 + j) * a.ldo + h * dv + row[r];
+          split_bf16(o, a.O_hi + off, a.O_lo + off);
+        }
+      }
     }
+    __syncthreads();  // buffer b & 1 is refilled with block b + 2 next
   }
 #pragma unroll
   for (int r = 0; r < kScanRPW; ++r)
@@ -419,6 +461,12 @@ cudaError_t init() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_attn_causal<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)CausalSmem<256>::total);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_gdn_scan<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem(64));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_gdn_scan<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem(128));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_gdn_scan<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem(256));
   return e;
 }
 
@@ -436,10 +484,12 @@ cudaError_t gdn(const GdnArgs& a, cudaStream_t st) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const dim3 grid(a.nh, (a.dv + kScanRows - 1) / kScanRows);
+  if (a.dv % 4) return cudaErrorInvalidValue;
+  const size_t sm = scan_smem(a.dk);
   switch (a.dk / 32) {
-    case 2: k_gdn_scan<2><<<grid, kScanThreads, 0, st>>>(a); break;
-    case 4: k_gdn_scan<4><<<grid, kScanThreads, 0, st>>>(a); break;
-    case 8: k_gdn_scan<8><<<grid, kScanThreads, 0, st>>>(a); break;
+    case 2: k_gdn_scan<2><<<grid, kScanThreads, sm, st>>>(a); break;
+    case 4: k_gdn_scan<4><<<grid, kScanThreads, sm, st>>>(a); break;
+    case 8: k_gdn_scan<8><<<grid, kScanThreads, sm, st>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
