@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_gdn_prep(GdnArgs a) {
   }
 }
 
-constexpr int kScanRows = 16, kScanThreads = 128, kScanRPW = kScanRows / (kScanThreads / 32);
+constexpr int kScanRows = 16, kScanThreads = 256, kScanRPW = kScanRows / (kScanThreads / 32);
 constexpr int kScanTB = 32;  // tokens whose inputs are staged in shared memory at a time
 
 // Floats of one staged token: k [dk], q [dk], the CTA's v rows [16], alpha and
@@ -147,10 +147,14 @@ __global__ void __launch_bounds__(kScanThreads) k_gdn_scan(GdnArgs a) {
   float S[kScanRPW][EPL];
   float* ptr[kScanRPW];
   int row[kScanRPW];
+  uint16_t* ohi[kScanRPW];  // the row's output at token 0; token i at + i * ldo
+  uint16_t* olo[kScanRPW];
 #pragma unroll
   for (int r = 0; r < kScanRPW; ++r) {
     row[r] = rc * kScanRows + warp * kScanRPW + r;
     ptr[r] = a.S + ((long long)h * dv + (row[r] < dv ? row[r] : 0)) * dk + lane * EPL;
+    ohi[r] = a.O_hi + h * dv + row[r];
+    olo[r] = a.O_lo + h * dv + row[r];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) S[r][e] = ptr[r][e];
   }
@@ -230,8 +234,9 @@ __global__ void __launch_bounds__(kScanThreads) k_gdn_scan(GdnArgs a) {
 #pragma unroll
         for (int e = 0; e < EPL; ++e) S[r][e] = fmaf(al, S[r][e], d * kq[e]);
         if (lane == 0 && row[r] < dv) {
-          const long long off = (long long)(i0 + j) * a.ldo + h * dv + row[r];
-          split_bf16(o, a.O_hi + off, a.O_lo + off);
+          split_bf16(o, ohi[r], olo[r]);
+          ohi[r] += a.ldo;
+          olo[r] += a.ldo;
         }
       }
     }
