@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_gdn_prep(GdnArgs a) {
   }
 }
 
-constexpr int kScanRows = 16, kScanThreads = 256, kScanRPW = kScanRows / (kScanThreads / 32);
+constexpr int kScanRows = 16, kScanThreads = 512, kScanRPW = kScanRows / (kScanThreads / 32);
 constexpr int kScanTB = 32;  // tokens whose inputs are staged in shared memory at a time
 
 // Floats of one staged token: k [dk], q [dk], the CTA's v rows [16], alpha and
