@@ -7,14 +7,16 @@
 // Prefill is the one place of the step where the work is a dense contraction
 // ("Beating llama.cpp from Scratch on Consumer AMD", Act 1: the prompt runs
 // through batched kernels, one launch per layer for all its tokens).  Design:
-//   * one CTA per 128-token x 256-row output tile (a SwiGLU pair: 128 rows of
-//     the gate and of the up matrix), 192 threads: warps 0-3 epilogue (TMEM
-//     lanes 0-127 = the tile's tokens), warp 4 copies, warp 5 issues MMAs;
+//   * 128-token x 256-row output tiles (a SwiGLU pair: 128 rows of the gate
+//     and of the up matrix); persistent CTAs (one per SM) take tiles in turn,
+//     192 threads: warps 0-3 epilogue (TMEM lanes 0-127 = the tile's tokens),
+//     warp 4 copies, warp 5 issues MMAs;
 //   * the copy lane stages 64-wide K slices of A_hi, A_lo and W with 2D
 //     tensor copies (TMA, 128-byte swizzle) into a 3-stage ring (64 KB each);
 //   * one thread issues tcgen05.mma (M = 128, N = 256 or 2 x 128, K = 16) into
-//     an FP32 accumulator of 256 TMEM columns and releases each ring stage
-//     with tcgen05.commit;
+//     one of two FP32 accumulators of 256 TMEM columns (alternating by tile,
+//     so that the epilogue of a tile overlaps the MMAs of the next) and
+//     releases each ring stage with tcgen05.commit;
 //   * the epilogue reads the accumulator with tcgen05.ld and stores it, adds it
 //     to a residual, or applies SwiGLU and splits the result into the bf16
 //     hi/lo parts the next GEMM consumes;
@@ -39,7 +41,7 @@ constexpr int kTileA = BM * BK * 2;               // 16 KB
 constexpr int kTileB = 256 * BK * 2;              // 32 KB
 constexpr int kStageBytes = 2 * kTileA + kTileB;  // 64 KB
 constexpr int kSmem = kStages * kStageBytes + 1024 + 128;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;  // two accumulators of 256 columns
 
 struct Maps {
   CUtensorMap a_hi, a_lo, b0, b1;
@@ -65,31 +67,54 @@ __device__ __forceinline__ void split_bf16(float v, uint16_t& hi, uint16_t& lo) 
   lo = f32_to_bf16_rne(v - bf16_to_f32(hi));
 }
 
+// Output tile t of the launch (t = m tile x n tiles + n tile): its first A row,
+// valid rows, first W row and first output column; false past the last tile
+// (grouped: also at a bad table entry, with the guard set; every role of the
+// CTA reads the same entries and stops at the same tile).
+struct TileInfo {
+  int m0, mrows, wr0, n0;
+};
+__device__ __forceinline__ bool tile_at(const Params& p, int t, int n_tiles, int BN, int total, TileInfo& ti) {
+  if (t >= total) return false;
+  const int mt = t / n_tiles;
+  ti.n0 = (t % n_tiles) * BN;
+  if (!p.tiles) {
+    ti.m0 = mt * BM;
+    ti.mrows = p.M - ti.m0;
+    ti.wr0 = ti.n0;
+    return true;
+  }
+  ti.m0 = p.tiles[3 * mt];
+  ti.mrows = p.tiles[3 * mt + 1];
+  const int g = p.tiles[3 * mt + 2];
+  if (g < 0 || g >= p.n_groups || ti.m0 < 0 || ti.mrows < 1 || ti.mrows > BM || ti.m0 + ti.mrows > p.M) {
+    if (threadIdx.x == 0) set_guard(p.guard, kGuardBadIndex);
+    return false;
+  }
+  ti.wr0 = g * p.w_group_rows + ti.n0;
+  return true;
+}
+
+// Persistent: CTA b takes output tiles b, b + grid, ... .  The ring of stages
+// runs on across tiles; the accumulator alternates between two 256-column
+// halves of TMEM, so the epilogue of one tile overlaps the MMAs of the next
+// (tfull: the MMAs of a tile are done; tempty: the epilogue has read it).
 __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Params p, const __grid_constant__ Maps mp) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* accum = empty + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool pair = p.epi == kEpiSwigluSplit;
   const int BN = pair ? 128 : 256;
-  const int n0 = blockIdx.x * BN;
-  int m0 = blockIdx.y * BM, mrows = p.M - m0, wr0 = n0;  // first A row, valid rows, first W row
-  if (p.tiles) {  // grouped: the tile table (written by an earlier kernel of the stream)
-    const int i = blockIdx.y;
-    if (i >= *p.ntiles) return;
-    m0 = p.tiles[3 * i];
-    mrows = p.tiles[3 * i + 1];
-    const int g = p.tiles[3 * i + 2];
-    if (g < 0 || g >= p.n_groups || m0 < 0 || mrows < 1 || mrows > BM || m0 + mrows > p.M) {
-      if (threadIdx.x == 0) set_guard(p.guard, kGuardBadIndex);
-      return;
-    }
-    wr0 = g * p.w_group_rows + n0;
-  }
+  const int n_tiles = (p.N + BN - 1) / BN;
+  const int total = n_tiles * (p.tiles ? *p.ntiles : (p.M + BM - 1) / BM);
+  if ((int)blockIdx.x >= total) return;
   const int nk = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -97,7 +122,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Pa
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(done, 1);
     fence_mbar_init();
   }
   if (warp == 5) tc::tmem_alloc(tmem_slot, kTmemCols);
@@ -105,79 +134,99 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Pa
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  TileInfo ti;
 
   if (warp == 4) {
     if (lane == 0) {
-      int t = 0;
-      for (; t < nk; ++t) {
-        const int s = t % kStages;
-        if (t >= kStages && !mbar_wait(&empty[s], ((t / kStages) - 1) & 1)) {
-          set_guard(p.guard, kGuardWaitTimeout);
-          break;
+      int q = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && tile_at(p, t, n_tiles, BN, total, ti); t += gridDim.x)
+        for (int kk = 0; kk < nk; ++kk, ++q) {
+          const int s = q % kStages;
+          if (q >= kStages && !mbar_wait(&empty[s], ((q / kStages) - 1) & 1)) {
+            set_guard(p.guard, kGuardWaitTimeout);
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * kStageBytes;
+          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          tc::tma_load_2d(st, &mp.a_hi, kk * BK, ti.m0, &full[s]);
+          tc::tma_load_2d(st + kTileA, &mp.a_lo, kk * BK, ti.m0, &full[s]);
+          tc::tma_load_2d(st + 2 * kTileA, &mp.b0, kk * BK, ti.wr0, &full[s]);
+          if (pair) tc::tma_load_2d(st + 2 * kTileA + kTileB / 2, &mp.b1, kk * BK, ti.wr0, &full[s]);
         }
-        uint8_t* st = smem + s * kStageBytes;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
-        tc::tma_load_2d(st, &mp.a_hi, t * BK, m0, &full[s]);
-        tc::tma_load_2d(st + kTileA, &mp.a_lo, t * BK, m0, &full[s]);
-        if (!pair) {
-          tc::tma_load_2d(st + 2 * kTileA, &mp.b0, t * BK, wr0, &full[s]);
-        } else {
-          tc::tma_load_2d(st + 2 * kTileA, &mp.b0, t * BK, wr0, &full[s]);
-          tc::tma_load_2d(st + 2 * kTileA + kTileB / 2, &mp.b1, t * BK, wr0, &full[s]);
-        }
-      }
       // the CTA must not retire while its copies are in flight
-      for (int u = (t > kStages ? t - kStages : 0); u < t; ++u)
+      for (int u = (q > kStages ? q - kStages : 0); u < q; ++u)
         if (!mbar_wait(&full[u % kStages], (u / kStages) & 1)) set_guard(p.guard, kGuardWaitTimeout);
     }
   } else if (warp == 5) {
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
-      for (int t = 0; t < nk; ++t) {
-        const int s = t % kStages;
-        if (!mbar_wait(&full[s], (t / kStages) & 1)) {
+      int q = 0, lt = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && tile_at(p, t, n_tiles, BN, total, ti); t += gridDim.x, ++lt) {
+        const int b = lt & 1, use = lt >> 1;
+        if (use > 0 && !mbar_wait(&tempty[b], (use - 1) & 1)) {
           set_guard(p.guard, kGuardWaitTimeout);
           break;
         }
         tc::fence_after_sync();
-        const uint32_t st = smem_addr(smem + s * kStageBytes);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ah = tc::sdesc_k128(st + kk * 32);
-          const uint64_t al = tc::sdesc_k128(st + kTileA + kk * 32);
-          const uint64_t b0 = tc::sdesc_k128(st + 2 * kTileA + kk * 32);
-          const bool acc = (t > 0 || kk > 0);
-          tc::mma_bf16(tmem, ah, b0, idesc, acc);
-          tc::mma_bf16(tmem, al, b0, idesc, true);
-          if (pair) {
-            const uint64_t b1 = tc::sdesc_k128(st + 2 * kTileA + kTileB / 2 + kk * 32);
-            tc::mma_bf16(tmem + 128, ah, b1, idesc, acc);
-            tc::mma_bf16(tmem + 128, al, b1, idesc, true);
+        const uint32_t acc = tmem + (uint32_t)(b * 256);
+        for (int kk = 0; kk < nk; ++kk, ++q) {
+          const int s = q % kStages;
+          if (!mbar_wait(&full[s], (q / kStages) & 1)) {
+            set_guard(p.guard, kGuardWaitTimeout);
+            ok = false;
+            break;
           }
+          tc::fence_after_sync();
+          const uint32_t st = smem_addr(smem + s * kStageBytes);
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16) {
+            const uint64_t ah = tc::sdesc_k128(st + k16 * 32);
+            const uint64_t al = tc::sdesc_k128(st + kTileA + k16 * 32);
+            const uint64_t b0 = tc::sdesc_k128(st + 2 * kTileA + k16 * 32);
+            const bool accum = (kk > 0 || k16 > 0);
+            tc::mma_bf16(acc, ah, b0, idesc, accum);
+            tc::mma_bf16(acc, al, b0, idesc, true);
+            if (pair) {
+              const uint64_t b1 = tc::sdesc_k128(st + 2 * kTileA + kTileB / 2 + k16 * 32);
+              tc::mma_bf16(acc + 128, ah, b1, idesc, accum);
+              tc::mma_bf16(acc + 128, al, b1, idesc, true);
+            }
+          }
+          tc::mma_commit(&empty[s]);
         }
-        tc::mma_commit(&empty[s]);
+        tc::mma_commit(&tfull[b]);  // also after a timeout: arrives once the issued MMAs have completed
       }
-      tc::mma_commit(accum);  // also after a timeout: arrives once the issued MMAs have completed
+      // every issued MMA has completed before TMEM is released
+      tc::mma_commit(done);
+      if (!mbar_wait(done, 0)) set_guard(p.guard, kGuardWaitTimeout);
     }
   } else {
-    // epilogue: thread (warp w, lane i) owns token row m0 + 32 w + i
-    // the TMEM loads are warp-collective: the whole warp takes the same branch
-    const bool got = __all_sync(0xffffffffu, mbar_wait(accum, 0));
-    if (!got && threadIdx.x == 0) set_guard(p.guard, kGuardWaitTimeout);
-    tc::fence_after_sync();
-    const int row = m0 + warp * 32 + lane;
-    const bool live = warp * 32 + lane < mrows;  // the tile's own rows (grouped: not the next group's)
-    const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
-    if (got) {
+    // epilogue: thread (warp w, lane i) owns token row m0 + 32 w + i of each tile; the TMEM loads are
+    // warp-collective, so the whole warp takes the same branches
+    int lt = 0;
+    for (int t = blockIdx.x; tile_at(p, t, n_tiles, BN, total, ti); t += gridDim.x, ++lt) {
+      const int b = lt & 1, use = lt >> 1;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&tfull[b], use & 1));
+      if (!got) {
+        if (lane == 0) set_guard(p.guard, kGuardWaitTimeout);
+        break;
+      }
+      tc::fence_after_sync();
+      const int row = ti.m0 + warp * 32 + lane;
+      const bool live = warp * 32 + lane < ti.mrows;  // the tile's own rows (grouped: not the next group's)
+      const uint32_t tbase = tmem + (uint32_t)(b * 256) + ((uint32_t)(warp * 32) << 16);
       if (!pair) {
         for (int c0 = 0; c0 < BN; c0 += 32) {
           float v[32];
           tc::tmem_ld32(tbase + c0, v);
           if (!live) continue;
-          float* y = p.y + (long long)row * p.ldy + n0 + c0;
+          float* y = p.y + (long long)row * p.ldy + ti.n0 + c0;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (n0 + c0 + j >= p.N) break;
+            if (ti.n0 + c0 + j >= p.N) break;
             if (p.epi == kEpiResid) y[j] += v[j];
             else y[j] = v[j];
           }
@@ -188,18 +237,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Pa
           tc::tmem_ld32(tbase + c0, g);
           tc::tmem_ld32(tbase + 128 + c0, u);
           if (!live) continue;
-          uint16_t* hh = p.h_hi + (long long)row * p.ldh + n0 + c0;
-          uint16_t* hl = p.h_lo + (long long)row * p.ldh + n0 + c0;
+          uint16_t* hh = p.h_hi + (long long)row * p.ldh + ti.n0 + c0;
+          uint16_t* hl = p.h_lo + (long long)row * p.ldh + ti.n0 + c0;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (n0 + c0 + j >= p.N) break;
-            uint16_t a, b;
-            split_bf16(siluf_(g[j]) * u[j], a, b);
+            if (ti.n0 + c0 + j >= p.N) break;
+            uint16_t a, c;
+            split_bf16(siluf_(g[j]) * u[j], a, c);
             hh[j] = a;
-            hl[j] = b;
+            hl[j] = c;
           }
         }
       }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
     }
   }
   tc::fence_before_sync();
@@ -266,7 +318,16 @@ cudaError_t launch(const Params& p, const uint16_t* a_hi, const uint16_t* a_lo, 
   if (!encode(&mp.a_hi, a_hi, p.M, p.K, lda, BM) || !encode(&mp.a_lo, a_lo, p.M, p.K, lda, BM) ||
       !encode(&mp.b0, w0, wrows, p.K, ldw, bn) || (pair && !encode(&mp.b1, w1, wrows, p.K, ldw, bn)))
     return cudaErrorInvalidValue;
-  const dim3 grid((p.N + bn - 1) / bn, grouped ? p.max_tiles : (p.M + BM - 1) / BM);
+  // persistent: at most one CTA per SM (its shared memory and all 512 TMEM columns)
+  static int nsm_of[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (nsm_of[dev] == 0 && (e = cudaDeviceGetAttribute(&nsm_of[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const long long tiles = (long long)((p.N + bn - 1) / bn) * (grouped ? p.max_tiles : (p.M + BM - 1) / BM);
+  const dim3 grid((unsigned)(tiles < nsm_of[dev] ? tiles : nsm_of[dev]));
   return launch_k(k_gemm, grid, dim3(kThreads), (size_t)kSmem, st, false, p, mp);
 }
 
