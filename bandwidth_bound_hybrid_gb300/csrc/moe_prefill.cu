@@ -3,9 +3,10 @@
 //   route    one warp per token: top K of the E routed logits (warp_topk:
 //            descending, lowest index on ties), softmax over the picks and
 //            the sigmoid of the shared expert's gate, as in the decode step;
-//   bucket   one CTA: the picks grouped by expert in token order (counts,
-//            offsets, then per expert a ballot scan over the tokens), the
-//            gathered row of every pick and the grouped GEMM's row tiles;
+//   bucket   one CTA: the picks grouped by expert in token order (a stable
+//            counting sort: per-warp counts over contiguous token ranges,
+//            prefix sums, placement), the gathered row of every pick and the
+//            grouped GEMM's row tiles;
 //   gather   the normalised activations (bf16 hi / lo parts) of every pick
 //            into its gathered row;
 //   combine  x[t] += sum_k w[t][k] y_e[row of (t, k)] + w[t][K] y_shared[t].
@@ -60,62 +61,85 @@ __device__ __forceinline__ int valid_id(int e, int E, unsigned* guard) {
   return e;
 }
 
-__global__ void __launch_bounds__(1024) k_bucket(const int* ids, int n, int E, int K, int* pos_of, int* tok_of,
-                                                 int* tiles, int* ntiles, unsigned* guard) {
-  __shared__ int cnt[kMaxE];
-  __shared__ int off[kMaxE];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+constexpr int kBucketWarps = 16;
+
+// A stable counting sort of the picks by expert: warp w owns tokens
+// [w n / 16, (w + 1) n / 16); (1) each warp counts its picks per expert (lane k
+// takes slot k of a token; a token's picks are distinct experts, so the lanes
+// never touch the same counter at once); (2) per expert, the prefix over the
+// experts before it and over the warps before w gives warp w's first row;
+// (3) each warp walks its tokens in order again and hands out rows.
+__global__ void __launch_bounds__(kBucketWarps * 32) k_bucket(const int* ids, int n, int E, int K, int* pos_of,
+                                                               int* tok_of, int* tiles, int* ntiles,
+                                                               unsigned* guard) {
+  __shared__ int hist[kBucketWarps][kMaxE];  // counts, then next free row
+  __shared__ int tot[kMaxE];
+  __shared__ int s_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kBucketWarps * kMaxE; i += blockDim.x) (&hist[0][0])[i] = 0;
   for (int i = tid; i < n * K; i += blockDim.x) {  // every row and pick names a valid row even if an id was bad
     tok_of[i] = 0;
     pos_of[i] = 0;
   }
   __syncthreads();
-  for (int i = tid; i < n * K; i += blockDim.x) atomicAdd(&cnt[valid_id(ids[i], E, guard)], 1);
+  const int t0 = (int)((long long)warp * n / kBucketWarps), t1 = (int)((long long)(warp + 1) * n / kBucketWarps);
+  for (int t = t0; t < t1; ++t) {
+    if (lane < K) ++hist[warp][valid_id(ids[(long long)t * K + lane], E, guard)];
+    __syncwarp();
+  }
   __syncthreads();
-  if (warp == 0) {  // exclusive prefix sum of the counts
+  for (int e = tid; e < E; e += blockDim.x) {  // per expert: warp offsets, total
+    int run = 0;
+    for (int w = 0; w < kBucketWarps; ++w) {
+      const int c = hist[w][e];
+      hist[w][e] = run;
+      run += c;
+    }
+    tot[e] = run;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive prefix over the experts, added to every warp's offsets
     int run = 0;
     for (int c0 = 0; c0 < E; c0 += 32) {
-      const int v = (c0 + lane < E) ? cnt[c0 + lane] : 0;
+      const int e = c0 + lane;
+      const int v = (e < E) ? tot[e] : 0;
       int incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += u;
       }
-      if (c0 + lane < E) off[c0 + lane] = run + incl - v;
+      if (e < E) {
+        const int base = run + incl - v;
+        for (int w = 0; w < kBucketWarps; ++w) hist[w][e] += base;
+        tot[e] = base;  // expert e's first row
+      }
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
+    if (lane == 0) s_total = run;
   }
   __syncthreads();
-  // expert e's picks take rows off[e] .. in token order
-  for (int e = warp; e < E; e += nw) {
-    int run = off[e];
-    for (int t0 = 0; t0 < n; t0 += 32) {
-      const int t = t0 + lane;
-      int hit = -1;
-      if (t < n)
-        for (int k = 0; k < K; ++k)
-          if (valid_id(ids[(long long)t * K + k], E, nullptr) == e) hit = k;
-      const unsigned b = __ballot_sync(0xffffffffu, hit >= 0);
-      if (hit >= 0) {
-        const int pos = run + __popc(b & ((1u << lane) - 1u));
-        tok_of[pos] = t;
-        pos_of[(long long)t * K + hit] = pos;
-      }
-      run += __popc(b);
+  for (int t = t0; t < t1; ++t) {
+    if (lane < K) {
+      const int e = valid_id(ids[(long long)t * K + lane], E, nullptr);
+      const int pos = hist[warp][e]++;
+      tok_of[pos] = t;
+      pos_of[(long long)t * K + lane] = pos;
     }
+    __syncwarp();
   }
   __syncthreads();
   if (tid == 0) {
     int nt = 0;
-    for (int e = 0; e < E; ++e)
-      for (int r = 0; r < cnt[e]; r += kTileRows) {
-        tiles[3 * nt] = off[e] + r;
-        tiles[3 * nt + 1] = (cnt[e] - r < kTileRows) ? cnt[e] - r : kTileRows;
+    for (int e = 0; e < E; ++e) {
+      const int cnt = (e + 1 < E ? tot[e + 1] : s_total) - tot[e];
+      for (int r = 0; r < cnt; r += kTileRows) {
+        tiles[3 * nt] = tot[e] + r;
+        tiles[3 * nt + 1] = (cnt - r < kTileRows) ? cnt - r : kTileRows;
         tiles[3 * nt + 2] = e;
         ++nt;
       }
+    }
     *ntiles = nt;
   }
 }
@@ -170,7 +194,7 @@ cudaError_t bucket(const int* ids, int n, int E, int K, int* pos_of, int* tok_of
                    unsigned* guard, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   if (E < 1 || E > kMaxE || K < 1 || K > kMaxK) return cudaErrorInvalidValue;
-  k_bucket<<<1, 1024, 0, st>>>(ids, n, E, K, pos_of, tok_of, tiles, ntiles, guard);
+  k_bucket<<<1, kBucketWarps * 32, 0, st>>>(ids, n, E, K, pos_of, tok_of, tiles, ntiles, guard);
   return cudaGetLastError();
 }
 
