@@ -116,6 +116,8 @@ cudaError_t launch(const Params& p, cudaStream_t st, bool pdl) {
   if (p.kv8 && (p.cap_s % 4 || p.cap_s < p.cap)) return cudaErrorInvalidValue;
   if (p.pages && (p.kv8 || p.page_tokens <= 0 || p.page_tokens % 128)) return cudaErrorInvalidValue;
   if (p.nb < 0 || p.nb > 8 || p.nsplit > 0xFFFF) return cudaErrorInvalidValue;
+  if (p.spread < 0 || (p.spread > 0 && (p.nb < 1 || p.spread < p.nb || p.spread > 0xFFFF)))
+    return cudaErrorInvalidValue;
   // Mergers per kv head: enough that each merges about 16 partial values
   // per thread; while they wait, at most (mergers - 1) CTAs per head and
   // token hold an SM, which must leave at least one SM for the CTAs they wait
@@ -131,20 +133,25 @@ cudaError_t launch(const Params& p, cudaStream_t st, bool pdl) {
     nsm_of[dev] = n;
   }
   // more CTAs than SMs: the CTA-pair variant where it exists
-  const long long grid = (long long)p.nkv * p.nsplit * (p.nb > 0 ? p.nb : 1);
+  // grid rows: splits of one token (z over the batch), or of the whole batch (spread)
+  const int rows = p.spread > 0 ? p.spread : p.nsplit, zs = (p.nb > 0 && p.spread == 0) ? p.nb : 1;
+  const long long grid = (long long)p.nkv * rows * zs;
   size_t smem = 0;
   void* k = grid > nsm_of[dev] ? pick_pair(p.hd, p.nq / p.nkv, &smem, p.kv8 != 0) : nullptr;
   if (!k) k = pick(p.hd, p.nq / p.nkv, &smem, p.kv8 != 0);
   if (!k) return cudaErrorInvalidValue;
   Params q = p;
-  const long long values = (long long)p.nq * p.hd * p.nsplit / p.nkv;  // partial o values of one kv head
+  // partial o values of one kv head (spread: of a token's average share; the
+  // kernel caps the mergers at each token's own split count)
+  const long long per = p.spread > 0 ? (p.spread + p.nb - 1) / p.nb : p.nsplit;
+  const long long values = (long long)p.nq * p.hd * per / p.nkv;
   long long K = (values + 16 * kCT - 1) / (16 * kCT);
   const long long groups = (long long)p.nkv * (p.nb > 0 ? p.nb : 1);
   const long long kmax = (nsm_of[dev] - 1) / groups + 1;
   if (K > kmax) K = kmax;
-  if (K > p.nsplit) K = p.nsplit;
+  if (K > per) K = per;
   q.mergers = K < 1 ? 1 : (int)K;
-  return launch_k(reinterpret_cast<void (*)(Params)>(k), dim3(p.nkv, p.nsplit, p.nb > 0 ? p.nb : 1), dim3(kThreads),
+  return launch_k(reinterpret_cast<void (*)(Params)>(k), dim3(p.nkv, rows, zs), dim3(kThreads),
                   smem, st, pdl, q);
 }
 

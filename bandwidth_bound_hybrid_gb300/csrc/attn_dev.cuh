@@ -86,6 +86,60 @@ __device__ __forceinline__ long long kv_row(const Params& p, int g, int r) {
   return ((long long)g * p.cap + r) * HD;
 }
 
+// Batch spread: grid row y of nkv x spread.  Token b of the batch owns n_b
+// consecutive rows, n_b = 1 + floor((spread - nb) L_b / sum L) plus one for
+// the tokens with the largest remainders (ties to the lower index) until the
+// rows are used up, L_b = cached rows + 1 (clamped to [1, cap_b]), so that every
+// CTA streams about the same number of cached rows whatever the mix of
+// lengths.  Every CTA works out the same shares from the same lengths.
+// Returns the token of row y, its split within the token (*sp) and the
+// token's split count (*ns).
+__device__ __forceinline__ int spread_row(const Params& p, int y, int* sp, int* ns) {
+  const int nb = p.nb;
+  long long Lb[8], tot = 0;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    long long L = 0;
+    if (b < nb) {
+      L = (long long)*p.len_b[b] + 1;
+      L = L < 1 ? 1 : (L > p.cap_b[b] ? p.cap_b[b] : L);
+      if (L < 1) L = 1;
+    }
+    Lb[b] = L;
+    tot += L;
+  }
+  const long long rest = p.spread - nb;
+  int n[8];
+  long long rem[8];
+  int left = (int)rest;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const long long q = rest * Lb[b];
+    n[b] = b < nb ? 1 + (int)(q / tot) : 0;
+    rem[b] = b < nb ? q % tot : -1;
+    left -= b < nb ? n[b] - 1 : 0;
+  }
+  int first = 0, z = nb - 1;
+  *sp = 0;
+  *ns = 1;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    if (b < nb) {
+      int rank = 0;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) rank += (rem[c] > rem[b] || (rem[c] == rem[b] && c < b)) ? 1 : 0;
+      const int nbb = n[b] + (rank < left ? 1 : 0);
+      if (y >= first && y < first + nbb) {
+        z = b;
+        *sp = y - first;
+        *ns = nbb;
+      }
+      first += nbb;
+    }
+  }
+  return z;
+}
+
 template <int HD>
 __device__ __forceinline__ Item item_of(const Params& p, int T, int sp) {
   Item it;

@@ -29,8 +29,13 @@ struct Smem {
 template <int HD, int G, bool KV8, bool PAIR>
 __global__ void __launch_bounds__(kThreads, Smem<HD, G, PAIR>::min_blocks) k_attn(const Params p0) {
   Params p = p0;
-  if (p0.nb > 0) {  // token blockIdx.z of a batch: its sequence's cache and scratch
-    const int z = blockIdx.z;
+  int sp = blockIdx.y;
+  if (p0.nb > 0) {  // token blockIdx.z of a batch (or of grid row y, spread): its sequence's cache and scratch
+    int z = blockIdx.z;
+    if (p0.spread > 0) {
+      z = spread_row(p0, blockIdx.y, &sp, &p.nsplit);
+      if (p.mergers > p.nsplit) p.mergers = p.nsplit;
+    }
     p.y = p0.y + (long long)z * p0.ld_y;
     p.o = p0.o + (long long)z * p0.ld_o;
     p.part = p0.part + (long long)z * p0.ld_part;
@@ -53,7 +58,7 @@ __global__ void __launch_bounds__(kThreads, Smem<HD, G, PAIR>::min_blocks) k_att
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S_::stages + ((S_::work + 15) & ~(size_t)15));
   uint64_t* empty = full + R_;
 
-  const int g = blockIdx.x, sp = blockIdx.y;
+  const int g = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = *p.len;  // written only by the previous step's last kernel
   if (T < 0 || T >= p.cap) {  // the host checks capacity first; never touch memory past it

@@ -142,6 +142,8 @@ struct hy_model {
   bool q4 = false;          // 4-bit linear weights: every step runs the batched path
   bool splits_auto = true;  // split-KV count chosen from the SM count (the batched step then scales it down)
   int splits_long = 0;      // splits of a single sequence whose cache holds attn::kLongContext positions or more
+  int batch_spread = -1;    // batched attention: -1 = the step's splits shared over the batch by length, 0 = off,
+                            //   > 0 = that many splits shared (HY_ATTN_BATCH_SPREAD)
   bool chunk_prefill = false;  // prompts run as chunks through the tensor-core GEMMs (else token by token)
 };
 
@@ -670,11 +672,16 @@ int record_batch(hy_cache* c, const std::vector<int>& seqs, float* logits, int* 
       a.nq = cf.attn_q_heads;
       a.nkv = cf.attn_kv_heads;
       a.hd = cf.head_dim;
-      // a batch already spreads over the SMs: fewer splits per sequence (the
-      // largest power of two <= 2 SMs / (kv heads x batch); measured at batch
-      // 8: 16 splits 1903, 32 splits 1884, 8 splits 1845 tokens/s)
+      // the step's splits (one CTA per SM over the kv heads) shared among the
+      // batch's sequences in proportion to their lengths, on the device
+      // (ragged contexts: every CTA streams about the same rows); with the
+      // spread off, each sequence takes the same count (the largest power of
+      // two <= 2 SMs / (kv heads x batch))
       a.nsplit = m->splits;
-      if (m->splits_auto) {
+      if (m->splits_auto && m->batch_spread != 0) {
+        a.spread = std::max(m->batch_spread > 0 ? m->batch_spread : m->splits, B);
+        a.spread = std::min(a.spread, std::max(m->splits, m->splits_long) + B - 1);  // scratch: ld_part splits
+      } else if (m->splits_auto) {
         int sb = 1;
         while (2 * sb <= std::max(1, 2 * m->nsm / (cf.attn_kv_heads * B))) sb *= 2;
         a.nsplit = std::min(m->splits, sb);
@@ -1369,6 +1376,9 @@ int hy_model_create(const hy_config* cfg, const hy_weights* w, hy_model** out) {
   m->splits = c.attn_splits > 0 ? c.attn_splits : attn::step_splits(c.attn_kv_heads, m->nsm);
   m->splits_auto = c.attn_splits <= 0;
   m->splits_long = m->splits_auto ? attn::long_context_splits(c.attn_q_heads, c.attn_kv_heads, m->nsm) : m->splits;
+  if (const char* v = getenv("HY_ATTN_BATCH_SPREAD")) {
+    if (*v) m->batch_spread = std::max(atoi(v), 0);
+  }
   m->pdl = !(c.flags & HY_FLAG_NO_PDL);
   m->graphs = !(c.flags & HY_FLAG_NO_GRAPH);
   m->debug = (c.flags & HY_FLAG_DEBUG) != 0;

@@ -168,6 +168,11 @@ struct Params {
   // batch (nb > 0): token z = blockIdx.z uses y + z*ld_y, o + z*ld_o,
   // part + z*ld_part, counter + z*nkv and its own sequence's cache
   int nb, ld_y, ld_o;
+  // batch spread (spread > 0, nb > 0): the grid is nkv x spread; its rows are
+  // the batch's splits, each token taking a share in proportion to its cache
+  // length, worked out on the device from len_b (nsplit is then per token);
+  // ld_part must hold spread - nb + 1 splits
+  int spread;
   long long ld_part;
   uint16_t* K_b[8];
   uint16_t* V_b[8];

@@ -50,11 +50,12 @@ def test_reference_arm_prints_one_contract_line(capsys):
 
 def test_traffic_lines_come_only_from_current_captures():
     """The roofline's DRAM traffic is read from profiles/traffic.txt: comment
-    lines are skipped, the dense and MoE GEMV captures are found, and the
-    batched GEMV, whose counters predate later changes to its kernel, has no
-    line (the bench reports null)."""
+    lines are skipped, the captures of the dense and MoE GEMVs and of the
+    batched 4-bit GEMV are found, an unknown workload has none (the bench
+    reports null)."""
     import bench
     assert bench.load_traffic("gemv_swiglu", "dense4b") == 94498560
     assert bench.load_traffic("gemv_in", "moe35b") == 25360128
-    assert bench.load_traffic("gemv_batch", "moe35b-q4-b8") is None
+    assert bench.load_traffic("moe_gateup", "moe35b") == 37838592
+    assert bench.load_traffic("gemv_batch", "moe35b-q4-b8") == 68662272
     assert bench.load_traffic("gemv_swiglu", "no-such-workload") is None

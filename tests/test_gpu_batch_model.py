@@ -109,6 +109,20 @@ def test_moe35b_q4_truncated_batch(built):
     run(shape, [3, 5, 2, 4], 2)
 
 
+@pytest.mark.parametrize("spread", ["", "0", "5"])
+def test_ragged_batch_attention_splits(built, monkeypatch, spread):
+    """Batched attention over strongly ragged contexts: the step's splits
+    shared among the sequences in proportion to their lengths on the device
+    (the default), one split count for every sequence (spread off), and 5
+    splits for 4 sequences (one each, the largest remainder a second): every
+    sequence against its own oracle."""
+    if spread:
+        monkeypatch.setenv("HY_ATTN_BATCH_SPREAD", spread)
+    else:
+        monkeypatch.delenv("HY_ATTN_BATCH_SPREAD", raising=False)
+    run(TINY_MOE_Q4, [1, 150, 2, 40], 3)
+
+
 def test_batch_rejects_repeated_and_full_sequences(built):
     import torch
 
