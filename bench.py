@@ -17,7 +17,10 @@ shapes:
 
 One JSON line on rank 0.  `--impl reference` times the FP64 CPU oracle on the
 same metric and config instead.  With torchrun (N > 1) every rank runs an
-independent replica (the decode step has no cross-GPU exchange).
+independent replica (the decode step has no cross-GPU exchange).  On one GPU,
+the default workload's line also carries `other_workloads`: the same
+measurement of dense4b-32k, moe35b and moe35b-q4-b8, each run after the main
+one in a process of its own (--no-other-workloads skips them).
 """
 from __future__ import annotations
 
@@ -62,7 +65,35 @@ def parse_args(argv=None):
                     help="time every decode kernel kind on its own (CUDA graphs over every layer's own buffers) and "
                          "print one JSON line of rows instead of the benchmark line")
     ap.add_argument("--paged", action="store_true", help="batch workloads: a paged KV cache sized to the contexts")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="default workload on one GPU: skip the runs of the other workloads")
     return ap.parse_args(argv)
+
+
+OTHER_WORKLOADS = ("dense4b-32k", "moe35b", "moe35b-q4-b8")
+OTHER_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline", "step_roofline", "timing",
+              "split_sweep_tokens_per_s", "prefill", "e2e", "gpu_launches", "kernels_per_step", "clocks")
+
+
+def other_workloads(args):
+    """The other decode workloads, each measured by this script in a process
+    of its own (same steps and warm-up, no CPU baseline), after the main run
+    has released the GPU; their lines, trimmed to the measurement keys."""
+    out = {}
+    for wl in OTHER_WORKLOADS:
+        cmd = [sys.executable, os.path.abspath(__file__), "--workload", wl, "--steps", str(args.steps),
+               "--warmup", str(args.warmup), "--no-cpu-baseline", "--no-other-workloads"]
+        try:
+            r = subprocess.run(cmd, capture_output=True, text=True, timeout=900, env=dict(os.environ))
+            lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+            if r.returncode != 0 or not lines:
+                out[wl] = {"error": f"exit {r.returncode}: {(r.stderr or '').strip().splitlines()[-1:]}"}
+                continue
+            d = json.loads(lines[-1])
+            out[wl] = {k: d[k] for k in OTHER_KEYS if k in d}
+        except (subprocess.TimeoutExpired, OSError, ValueError) as e:
+            out[wl] = {"error": f"{type(e).__name__}: {e}"}
+    return out
 
 
 def workload_of(args):
@@ -422,8 +453,14 @@ def run_ours(args):
             "graph_launches_per_token": 1,
             "clocks": clk,
         }
-        print(json.dumps(line), flush=True)
     model.close()
+    if rank == 0:
+        if ws == 1 and args.workload == "dense4b" and not args.no_other_workloads and not args.layers \
+                and args.prompt < 0:
+            del model, weights
+            torch.cuda.empty_cache()
+            line["other_workloads"] = other_workloads(args)
+        print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
