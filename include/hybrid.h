@@ -215,20 +215,23 @@ int32_t hy_step_kernels(const hy_cache* c);
  * uses: hy_config.attn_splits when set, else one CTA per SM across the kv
  * heads, or, for a cache of 16384 positions or more with up to 4 query heads
  * per kv head, 64 splits run as two CTAs per SM.  0 for a bad sequence index
- * or a model without attention layers. */
+ * or a model without attention layers.  (A step of several sequences with
+ * the automatic count shares the step's splits among them in proportion to
+ * their lengths, worked out on the device at every step.) */
 int32_t hy_step_splits(const hy_cache* c, int32_t seq);
 
 /* Run the n prompt tokens tokens_dev[0..n) of sequence `seq` through the
  * model at positions len .. len+n-1, filling its caches.  logits_dev
  * (nullable) receives the FP32 logits [V] of the last token.
- * HY_ERR_CAPACITY (nothing launched) if len + n > capacity.  bf16 dense
- * models run the prompt in chunks of up to 2048 tokens (HY_PREFILL_CHUNK in
- * the environment overrides) through tensor-core GEMMs (tcgen05, the
- * activations as bf16 hi + lo parts, FP32 accumulation) and prompt kernels
- * of the mixers, with buffers the library allocates at the first such call;
- * the caches it leaves equal those of a token-by-token prefill within
- * rounding.  MoE and 4-bit models, and models created with
- * HY_FLAG_TOKEN_PREFILL, run the prompt one position at a time through the
+ * HY_ERR_CAPACITY (nothing launched) if len + n > capacity.  bf16 models
+ * (dense and MoE) with the bf16 cache run the prompt in chunks of up to 2048
+ * tokens (HY_PREFILL_CHUNK in the environment overrides) through tensor-core
+ * GEMMs (tcgen05, the activations as bf16 hi + lo parts, FP32 accumulation;
+ * the MoE experts as grouped GEMMs over the chunk's picks) and prompt
+ * kernels of the mixers, with buffers the library allocates at the first
+ * such call; the caches it leaves equal those of a token-by-token prefill
+ * within rounding.  4-bit models, int8-cache models and models created with
+ * HY_FLAG_TOKEN_PREFILL run the prompt one position at a time through the
  * decode step.  [Strata] "Act 1" (batched chunk kernels: one launch per layer
  * for all prompt tokens). */
 int hy_prefill(hy_model* m, hy_cache* c, int32_t seq, const int32_t* tokens_dev, int32_t n, float* logits_dev,
