@@ -25,6 +25,10 @@
 //   by the last few CTAs of a kv head to finish, each a slice of the outputs
 //   (a ticket counter: earlier CTAs exit at once, the last ones wait for the
 //   very last, bounded, then merge together).
+// A batch of tokens (each its own sequence and cache) runs in one launch:
+// grid (kv_heads, splits, tokens), or (kv_heads, spread) with the spread's
+// rows shared among the tokens in proportion to their cache lengths, so that
+// ragged contexts give every CTA about the same number of rows.
 #include "attn_kernel.cuh"
 
 namespace hy {
