@@ -59,3 +59,38 @@ def test_traffic_lines_come_only_from_current_captures():
     assert bench.load_traffic("moe_gateup", "moe35b") == 37838592
     assert bench.load_traffic("gemv_batch", "moe35b-q4-b8") == 68662272
     assert bench.load_traffic("gemv_swiglu", "no-such-workload") is None
+
+
+def test_other_workloads_trim_lines_and_report_failures(monkeypatch):
+    """The default run's `other_workloads`: one child run per workload with the
+    parent's steps and warm-up and no CPU baseline; each child's last JSON
+    line trimmed to the measurement keys; a failing child gives an error
+    entry instead of breaking the line."""
+    import json
+    import subprocess
+    calls = []
+
+    class Done:
+        def __init__(self, rc, out, err=""):
+            self.returncode, self.stdout, self.stderr = rc, out, err
+
+    def fake_run(cmd, **kw):
+        calls.append(cmd)
+        wl = cmd[cmd.index("--workload") + 1]
+        if wl == "moe35b":
+            return Done(1, "", "Traceback\nRuntimeError: no GPU")
+        line = {"metric": "m", "value": 1.5, "unit": "tokens/s", "steps": 7, "warmup": 3, "cpu_baseline": None,
+                "config": {"workload": wl}, "clocks": {"sm_mhz": 1.0}, "depth_curve": [1, 2]}
+        return Done(0, "build log\n" + json.dumps(line) + "\n")
+
+    monkeypatch.setattr(subprocess, "run", fake_run)
+    args = bench.parse_args(["--steps", "7", "--warmup", "3"])
+    out = bench.other_workloads(args)
+    assert list(out) == list(bench.OTHER_WORKLOADS)
+    for cmd in calls:
+        assert cmd[cmd.index("--steps") + 1] == "7" and cmd[cmd.index("--warmup") + 1] == "3"
+        assert "--no-cpu-baseline" in cmd and "--no-other-workloads" in cmd
+    ok = out["dense4b-32k"]
+    assert ok["value"] == 1.5 and ok["config"]["workload"] == "dense4b-32k" and ok["clocks"] == {"sm_mhz": 1.0}
+    assert "depth_curve" not in ok and "cpu_baseline" not in ok and "metric" not in ok
+    assert "error" in out["moe35b"] and "no GPU" in out["moe35b"]["error"]
